@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Throughput of the chunked gated-delta-rule forward with FP8 E4M3 state and W QDQ.
+
+Workload: B=4, H=16 (q/k and v heads), T=4096, dk=dv=128, state QDQ + W QDQ, h0 ~ N(0, 0.1),
+synthetic seeded inputs (fp8_state_qat_gb300.workloads). One step = one gdn_chunk_fwd call
+over the whole batch; inputs resident in HBM (two alternating input sets of 346 MB each,
+larger than the 129 MB L2). Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+N > 1 (launched by torch.distributed.run): every rank runs its own replica of the workload on
+its own GPU (the path has no exchange step; weak scaling), timing is max over ranks.
+--impl reference times the fp64 CPU oracle instead (rank 0 only), on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gdn_b4_h16_t4096_d128"
+METRIC = "GDN chunked-prefill tokens/s (B4 H16 T4096 d128, FP8 state QDQ); % of roofline"
+UNIT = "tokens/s"
+PROFILE = os.path.join(ROOT, "profiles", "chunk_fwd_gdn_b4_h16_t4096_d128.md")
+
+
+def algorithmic(x):
+    """Counted bytes and FLOPs of one forward over the workload. Bytes: q, k (per q/k head),
+    v in bf16, g and beta in fp32, o in fp32, h0 read and hT write in fp32. FLOPs per
+    token-head: 2 [C dk (K K^T) + C dk (Q K^T) + C (dk + dv) (T [beta Gam K | beta V])
+    + 3 dk dv (W S, Q S, K^T Delta) + C dv (P Delta)] + C^2 / 3 (solve), C = 64."""
+    s = x.shape
+    tok = x.tokens()
+    C = 64
+    by = tok * (s["Hqk"] * 2 * s["dk"] * 2 + s["Hv"] * (2 * s["dv"] + 8 + 4 * s["dv"]))
+    by += 2 * s["N"] * s["Hv"] * s["dk"] * s["dv"] * 4
+    fl_th = 2 * (C * s["dk"] * 2 + C * (s["dk"] + s["dv"]) + 3 * s["dk"] * s["dv"] + C * s["dv"]) + C * C / 3
+    return by, fl_th * tok * s["Hv"]
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_state_qat_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel sources (else None)."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return None
+        inside = [r for t, r in self.rows if self.t0 and self.t1 and self.t0 - 0.15 <= t <= self.t1 + 0.15]
+        rows = inside or [r for _, r in self.rows]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "in_timed_region": bool(inside)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_inputs(x, t_tokens):
+    """The workload's first t_tokens tokens as contiguous fp32/fp64 numpy arrays (converted
+    once, outside any timed region)."""
+    import numpy as np
+
+    sl = slice(0, t_tokens)
+    f = lambda t: np.ascontiguousarray(t[:, sl].float().numpy())
+    return (f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta),
+            None if x.h0 is None else np.ascontiguousarray(x.h0.double().numpy()))
+
+
+def oracle_sample(x, arrays, units, threads):
+    """Chunked fp64 oracle (state + W QDQ) on the first `units` (sequence, head) units of the
+    prepared arrays. Returns (seconds, tokens in the metric's unit)."""
+    import numpy as np
+
+    import oracle
+
+    s = x.shape
+    mask = np.zeros((s["N"], s["Hv"]), np.uint8)
+    mask.reshape(-1)[:units] = 1
+    q, k, v, g, beta, h0 = arrays
+    t = time.perf_counter()
+    oracle.gdn_chunked(q, k, v, g, beta, h0, None, state_qdq=x.state_qdq, w_qdq=x.w_qdq, unit_mask=mask,
+                       threads=threads)
+    dt = time.perf_counter() - t
+    # a (sequence, head) unit over L tokens is 1/Hv of the work of L batch tokens
+    return dt, units * q.shape[1] / s["Hv"]
+
+
+def cpu_baseline(x, target_s=15.0):
+    """Time the oracle as it stands on all host cores on a bounded sample (~10-30 s of CPU work)."""
+    import oracle
+
+    oracle.build()
+    cores = cpu_cores()
+    s = x.shape
+    total_units = s["N"] * s["Hv"]
+    dt1, _ = oracle_sample(x, oracle_inputs(x, 512), 1, 1)      # calibrate: one unit, 512 tokens, one thread
+    per_unit_full = dt1 * s["T"] / 512
+    units = max(1, min(total_units, int(target_s / max(per_unit_full, 1e-6))))
+    dt, toks = oracle_sample(x, oracle_inputs(x, s["T"]), units, cores)
+    return {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{units} of {total_units} (sequence, head) units x all {s['T']} tokens, chunked fp64 "
+                      f"oracle with state+W QDQ, {cores} threads, {dt:.2f} s wall"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from fp8_state_qat_gb300 import workloads
+
+    oracle.build()
+    x = workloads.workload(WORKLOAD)
+    cores = cpu_cores()
+    s = x.shape
+    budget = 150.0 / max(1, args.steps + args.warmup)        # seconds per step: whole run in a few minutes
+    dt1, _ = oracle_sample(x, oracle_inputs(x, 64), 1, 1)
+    per_unit_tok = dt1 / 64
+    units = max(1, min(s["N"] * s["Hv"], cores))
+    t_tok = int(budget * cores / max(units * per_unit_tok, 1e-9)) // 64 * 64
+    t_tok = max(64, min(s["T"], t_tok))
+    arrays = oracle_inputs(x, t_tok)
+    for _ in range(args.warmup):
+        oracle_sample(x, arrays, units, cores)
+    secs, toks = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, tk = oracle_sample(x, arrays, units, cores)
+        secs += dt
+        toks += tk
+    value = toks / secs
+    sample = (f"per step {units} (sequence, head) units x first {t_tok} tokens of the workload, chunked fp64 "
+              f"oracle with state+W QDQ on {cores} host threads")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": 4, "H": 16, "T": 4096, "dk": 128, "dv": 128,
+                       "state_qdq": True, "w_qdq": True, "parallelism": "none (host threads)"},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import fp8_state_qat_gb300 as gdn
+    from fp8_state_qat_gb300 import workloads
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    gdn.load()
+    dev = torch.device("cuda", local)
+    x = workloads.workload(WORKLOAD)
+    s = x.shape
+    tokens = x.tokens()
+    bytes_alg, flops_alg = algorithmic(x)
+
+    def resident():
+        return dict(q=x.q.to(dev), k=x.k.to(dev), v=x.v.to(dev), g=x.g.to(dev), beta=x.beta.to(dev),
+                    h0=x.h0.to(dev), o=torch.empty((s["B"], s["T"], s["Hv"], s["dv"]), device=dev),
+                    hT=torch.empty((s["N"], s["Hv"], s["dk"], s["dv"]), device=dev))
+
+    sets = [resident(), resident()]
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        b = sets[i & 1]
+        gdn.gdn_chunk_fwd(b["q"], b["k"], b["v"], b["g"], b["beta"], b["h0"], None, state_qdq=x.state_qdq,
+                          w_qdq=x.w_qdq, o=b["o"], hT=b["hT"], workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    gdn.gdn_check_device_status(ws)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.2)
+    clocks.stop()
+    gdn.gdn_check_device_status(ws)
+    ms = t_start.elapsed_time(t_end)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: pinned host inputs -> device, forward, outputs -> host
+    host = {k: x_.pin_memory() for k, x_ in dict(q=x.q, k=x.k, v=x.v, g=x.g, beta=x.beta, h0=x.h0).items()}
+    dst = sets[0]
+    o_host = torch.empty(dst["o"].shape, dtype=torch.float32).pin_memory()
+    hT_host = torch.empty(dst["hT"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * 4 + hT_host.numel() * 4
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        for k_, t in host.items():
+            dst[k_].copy_(t, non_blocking=True)
+        gdn.gdn_chunk_fwd(dst["q"], dst["k"], dst["v"], dst["g"], dst["beta"], dst["h0"], None,
+                          state_qdq=x.state_qdq, w_qdq=x.w_qdq, o=dst["o"], hT=dst["hT"], workspace=ws, stream=stream)
+        o_host.copy_(dst["o"], non_blocking=True)
+        hT_host.copy_(dst["hT"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank == 0:
+        hbm, bf16, src = peaks()
+        achieved = bytes_alg / (launch_ms * 1e-3) / 1e9
+        value = world * tokens * args.steps / (ms * 1e-3)
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "B": s["B"], "H": s["Hv"], "T": s["T"], "dk": s["dk"], "dv": s["dv"],
+                           "state_qdq": x.state_qdq, "w_qdq": x.w_qdq, "h0": "N(0,0.1)",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                           "l2": "inputs larger than L2: two alternating 346 MB input sets"},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                             "frac": achieved / hbm, "traffic": profiled_traffic(), "peak_source": src,
+                             "bytes_per_launch": bytes_alg, "flops_per_launch": flops_alg,
+                             "tensor_frac": flops_alg / (launch_ms * 1e-3) / (bf16 * 1e12),
+                             "kernel_ms": launch_ms},
+                "e2e": {"value": world * tokens * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "gpu_launches": args.steps * 1,
+                "clocks": clocks.summary()}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(x)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,64 @@
+// common.cuh -- device helpers shared by the kernels of libgdnqat (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdnqat.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;          // chunk length fixed by the method ("GDN state/W QAT foundation")
+constexpr int kStateTileCols = 64;  // state QDQ tile: all dk rows x 64 value columns (same page)
+constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 (fn) magnitude
+
+// Scale of one QDQ tile from its amax: amax / 448 with the zero guard (0 -> 1), in fp32
+// with IEEE round-to-nearest division.
+__device__ __forceinline__ float qdq_scale(float amax) {
+  float s = __fdiv_rn(amax, kE4M3Max);
+  return s == 0.0f ? 1.0f : s;
+}
+
+// Two elements x -> E4M3(x / s) * s. The divide is IEEE round-to-nearest; the E4M3
+// conversion is the hardware round-to-nearest-even with saturation to +-448; the
+// product back is one fp32 multiply. The E4M3 value is exact in fp32.
+__device__ __forceinline__ float2 qdq2(float a, float b, float s) {
+  const float2 y = make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+  const __nv_fp8x2_e4m3 c(y);          // cvt.rn.satfinite.e4m3x2.f32
+  const float2 cf = static_cast<float2>(c);
+  return make_float2(__fmul_rn(cf.x, s), __fmul_rn(cf.y, s));
+}
+
+__device__ __forceinline__ float qdq1(float a, float s) {
+  return qdq2(a, 0.0f, s).x;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 8 bf16 (16 bytes) -> 8 fp32
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float* out) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+
+}  // namespace gdn

@@ -1,0 +1,215 @@
+"""ctypes binding of libgdnqat.so (include/gdnqat.h), same names as the C ABI.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels. torch supplies device memory (outputs are allocated here when not given) and the
+current CUDA stream. There is no fallback: if the library is missing or the device is not
+sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = 1
+GDN_ERR_UNSUPPORTED_ARCH = 2
+GDN_ERR_UNSUPPORTED_SHAPE = 3
+GDN_ERR_WORKSPACE_TOO_SMALL = 4
+GDN_ERR_CUDA = 5
+GDN_ERR_DEVICE_TIMEOUT = 6
+
+GDN_FLAG_STATE_QDQ = 1
+GDN_FLAG_W_QDQ = 2
+GDN_FLAG_KDA = 4
+
+# every extern "C" symbol of include/gdnqat.h
+EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "kda_chunk_fwd", "gdn_decode_step",
+            "fp8_tile_qdq", "gdn_status_string", "gdn_check_device_status")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+class ChunkArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
+                ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_host", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("hT", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("N", ctypes.c_int32), ("Hqk", ctypes.c_int32),
+                ("Hv", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load libgdnqat.so (building it in-tree if it is missing and nvcc is available)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB_PATH) or (build_if_missing and not _build.up_to_date()):
+            if not build_if_missing:
+                raise RuntimeError(f"CUDA library not built: {_build.LIB_PATH}")
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        P, I32, U32, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float
+        lib.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.gdn_chunk_fwd_workspace_size.argtypes = [ctypes.POINTER(ChunkArgs)]
+        for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
+            getattr(lib, fn).restype = ctypes.c_int
+            getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, ctypes.c_size_t, P]
+        lib.gdn_decode_step.restype = ctypes.c_int
+        lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, F, U32, P]
+        lib.fp8_tile_qdq.restype = ctypes.c_int
+        lib.fp8_tile_qdq.argtypes = [P, P, P, ctypes.c_int64, I32, I32, I32, P]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_status_string.argtypes = [ctypes.c_int]
+        lib.gdn_check_device_status.restype = ctypes.c_int
+        lib.gdn_check_device_status.argtypes = [P, P]
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().gdn_status_string(int(status)).decode()
+
+
+def _check(fn, st):
+    if st != GDN_OK:
+        raise GdnError(fn, st)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def workspace_bytes(args: ChunkArgs) -> int:
+    return int(load().gdn_chunk_fwd_workspace_size(ctypes.byref(args)))
+
+
+def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state,
+           workspace, stream):
+    lib = load()
+    q = _dev(q, torch.bfloat16, "q")
+    k = _dev(k, torch.bfloat16, "k")
+    v = _dev(v, torch.bfloat16, "v")
+    g = _dev(g, torch.float32, "g")
+    beta = _dev(beta, torch.float32, "beta")
+    h0 = _dev(h0, torch.float32, "h0")
+    B, T, Hqk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    dev = q.device
+    cu_dev = cu_host = None
+    if cu_seqlens is not None:
+        cu_host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+        cu_dev = cu_seqlens.to(dev, torch.int32).contiguous() if cu_seqlens.is_cuda else cu_host.to(dev)
+        N = cu_host.numel() - 1
+    else:
+        N = B
+    if o is None:
+        o = torch.empty((B, T, Hv, dv), dtype=torch.float32, device=dev)
+    if hT is None and output_final_state:
+        hT = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
+    flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_W_QDQ if w_qdq else 0)
+    a = ChunkArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_dev), _ptr(cu_host),
+                  _ptr(o), _ptr(hT), B, T, N, Hqk, Hv, dk, dv, float(scale), flags)
+    need = workspace_bytes(a)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = getattr(lib, fn_name)(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(fn_name, st)
+    return o, hT
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False, w_qdq=False, scale=1.0,
+                  o=None, hT=None, output_final_state=True, workspace=None, stream=None):
+    """Chunked GDN forward. q, k [B,T,Hqk,dk] bf16; v [B,T,Hv,dv] bf16; g, beta [B,T,Hv] fp32;
+    h0 [N,Hv,dk,dv] fp32 or None; cu_seqlens int32 [N+1] (CPU or CUDA) or None.
+    Returns (o [B,T,Hv,dv] fp32, hT [N,Hv,dk,dv] fp32 or None)."""
+    return _chunk("gdn_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
+                  output_final_state, workspace, stream)
+
+
+def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False, w_qdq=False, scale=1.0,
+                  o=None, hT=None, output_final_state=True, workspace=None, stream=None):
+    """KDA chunked forward: as gdn_chunk_fwd with g [B,T,Hv,dk] (one log-decay per key channel)."""
+    return _chunk("kda_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
+                  output_final_state, workspace, stream)
+
+
+def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale=1.0, o=None, stream=None):
+    """One decode token per sequence; `state` [N,Hv,dk,dv] fp32 is updated in place.
+    q, k [N,Hqk,dk] bf16; v [N,Hv,dv] bf16; g [N,Hv] (kda: [N,Hv,dk]) fp32; beta [N,Hv] fp32.
+    Returns o [N,Hv,dv] fp32."""
+    lib = load()
+    q = _dev(q, torch.bfloat16, "q")
+    k = _dev(k, torch.bfloat16, "k")
+    v = _dev(v, torch.bfloat16, "v")
+    g = _dev(g, torch.float32, "g")
+    beta = _dev(beta, torch.float32, "beta")
+    state = _dev(state, torch.float32, "state")
+    N, Hqk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    if o is None:
+        o = torch.empty((N, Hv, dv), dtype=torch.float32, device=q.device)
+    flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_KDA if kda else 0)
+    st = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o), N, Hqk, Hv,
+                             dk, dv, float(scale), flags, _stream(stream, q.device))
+    _check("gdn_decode_step", st)
+    return o
+
+
+def fp8_tile_qdq(x, tile_cols, *, y=None, scales=True, stream=None):
+    """Dynamic per-tile E4M3 QDQ of x [lead, rows, cols] fp32 (a tile = all rows x tile_cols
+    columns). Returns (y, scales [lead, ceil(cols/tile_cols)] or None). y may be x."""
+    lib = load()
+    x = _dev(x, torch.float32, "x")
+    if x.dim() == 2:
+        x = x.unsqueeze(0)
+    lead, rows, cols = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    sc = None
+    if scales:
+        sc = torch.empty((lead, (cols + tile_cols - 1) // tile_cols), dtype=torch.float32, device=x.device)
+    st = lib.fp8_tile_qdq(_ptr(x), _ptr(y), _ptr(sc), lead, rows, cols, int(tile_cols), _stream(stream, x.device))
+    _check("fp8_tile_qdq", st)
+    return y, sc
+
+
+def gdn_check_device_status(workspace, stream=None):
+    st = load().gdn_check_device_status(_ptr(workspace), _stream(stream, workspace.device))
+    _check("gdn_check_device_status", st)

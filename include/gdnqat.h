@@ -1,0 +1,132 @@
+/* gdnqat.h -- C ABI of the GB300 (sm_103a) chunked gated-delta-rule forward with dynamic
+ * FP8 E4M3 fake quantize-dequantize (QDQ) of the recurrent state and of the WY operand W.
+ *
+ * Sources (pages of the NVIDIA/Model-Optimizer pull requests on the method):
+ *  [F] "GDN state/W QAT foundation", "What does this PR do?": the fused path uses chunk
+ *      size 64; state QDQ at each 64-token boundary with amax recomputed over each
+ *      full-key x 64-value-column tile, per sequence and head, scale = amax / 448 with a
+ *      zero guard; a separate dynamic FP8 QDQ of the WY-transformed W; quantizers start
+ *      disabled; a supplied-scale QDQ helper; errors are raised before any launch.
+ *  [D] "Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD
+ *      workflow", step 3: a decode token reads the stored state, computes its output from
+ *      the updated working state, then applies QDQ before storing; state stays in
+ *      floating-point storage.
+ *  [K] "Add KDA prefill numerical emulation for QAT", "What does this PR do?": KDA uses
+ *      per-key-channel retention, with causal pairwise decays from prefix differences.
+ *  [R] "Add experimental GDN/KDA decode and replay QAT", "What does this PR do?":
+ *      per-token FP8 state writes.
+ *
+ * Recurrence (the pages name GatedDeltaNet but do not print it), per sequence n and
+ * value head h, state S in R^{dk x dv} (row = key channel):
+ *     S_t = a_t S_{t-1} + b_t k_t (v_t - a_t S_{t-1}^T k_t)^T,   o_t = scale * S_t^T q_t,
+ * a_t = exp(g_t); KDA: a_t S_{t-1} becomes Diag(exp(g_t)) S_{t-1}.
+ *
+ * Conventions for every call
+ *  - Every pointer named "device" is caller-owned device memory; the library allocates
+ *    nothing and keeps no state apart from a cached per-device capability probe.
+ *  - Each call validates its arguments and the device on the host and returns a status
+ *    BEFORE launching anything ([F]); a non-OK status means nothing was enqueued.
+ *  - Work is enqueued on the caller's stream (NULL = legacy default stream); calls return
+ *    without synchronizing. Outputs are valid once the stream reaches that point.
+ *  - Layouts are head-last and contiguous: q, k [B, T, Hqk, dk] bf16; v [B, T, Hv, dv]
+ *    bf16; g [B, T, Hv] fp32 (KDA [B, T, Hv, dk]); beta [B, T, Hv] fp32; states
+ *    [N, Hv, dk, dv] fp32 row-major; o [B, T, Hv, dv] fp32. GQA: value head h reads
+ *    q/k head h / (Hv / Hqk). Varlen: B == 1, sequence n owns tokens
+ *    [cu_seqlens[n], cu_seqlens[n+1]) of the T axis.
+ *  - Supported sizes: dk in {64, 128}; dv in {64, 128, 256}; chunk size 64 only ([F]).
+ *    Device pointers must be 16-byte aligned.
+ *  - The device must be sm_103 (GB300); the library is built for sm_103a only.
+ */
+#ifndef GDNQAT_H
+#define GDNQAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad dims, Hv % Hqk != 0, bad cu_seqlens */
+  GDN_ERR_UNSUPPORTED_ARCH = 2,     /* no CUDA device, or not sm_103 */
+  GDN_ERR_UNSUPPORTED_SHAPE = 3,    /* dk / dv outside the supported set */
+  GDN_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than gdn_chunk_fwd_workspace_size() */
+  GDN_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed */
+  GDN_ERR_DEVICE_TIMEOUT = 6        /* a kernel gave up a bounded wait (from gdn_check_device_status) */
+} gdn_status;
+
+/* Quantizer switches; all off by default, as the quantizers start disabled ([F]). */
+#define GDN_FLAG_STATE_QDQ 1u  /* E4M3 QDQ of S after every 64th token of a sequence ([F]) */
+#define GDN_FLAG_W_QDQ 2u      /* E4M3 QDQ of W, one scale per (sequence, head, chunk) ([F]) */
+#define GDN_FLAG_KDA 4u        /* decode only: g holds one log-decay per key channel ([K]) */
+
+typedef struct {
+  const void* q;               /* device bf16 [B, T, Hqk, dk] */
+  const void* k;               /* device bf16 [B, T, Hqk, dk] */
+  const void* v;               /* device bf16 [B, T, Hv, dv] */
+  const float* g;              /* device fp32 log-decay [B, T, Hv] (kda_chunk_fwd: [B, T, Hv, dk]) */
+  const float* beta;           /* device fp32 [B, T, Hv] */
+  const float* h0;             /* device fp32 [N, Hv, dk, dv]; NULL = zero initial state */
+  const int32_t* cu_seqlens;   /* device int32 [N + 1]; NULL = dense batch (N == B) */
+  const int32_t* cu_seqlens_host; /* host copy of cu_seqlens (required with it): validated before launch */
+  float* o;                    /* device fp32 [B, T, Hv, dv]; must not alias any input */
+  float* hT;                   /* device fp32 [N, Hv, dk, dv] or NULL; may alias h0 exactly */
+  int32_t B, T, N, Hqk, Hv, dk, dv;
+  float scale;                 /* multiplies o (1.0 = plain S^T q) */
+  uint32_t flags;              /* GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ */
+} gdn_chunk_args;
+
+/* Bytes of device workspace gdn_chunk_fwd / kda_chunk_fwd need for these arguments (a
+ * status word for bounded device waits plus any staging); 0 when the arguments are invalid. */
+size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args);
+
+/* Chunked GDN forward ([F]): per 64-token chunk, decay-weighted K.K^T, WY solve (W, U),
+ * optional W QDQ, state carry with state QDQ at every 64th token of each sequence; o for
+ * every token and hT per (sequence, head). hT is QDQ'd when a sequence's length is a
+ * positive multiple of 64 (its last token is then a 64th token). Empty sequences give
+ * hT = h0. workspace: device, >= gdn_chunk_fwd_workspace_size(args) bytes, 256-byte
+ * aligned; its contents need no initialization. */
+gdn_status gdn_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
+                         gdn_stream_t stream);
+
+/* KDA variant ([K]): same contract with g [B, T, Hv, dk], one log-decay per key channel;
+ * pairwise decays come from differences of prefix sums of g within a chunk. */
+gdn_status kda_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
+                         gdn_stream_t stream);
+
+/* One decode token per sequence ([D], [R]). q, k: device bf16 [N, Hqk, dk]; v: device
+ * bf16 [N, Hv, dv]; g: device fp32 [N, Hv] (GDN_FLAG_KDA: [N, Hv, dk]); beta: device fp32
+ * [N, Hv]; state: device fp32 [N, Hv, dk, dv], read and overwritten in place; o: device
+ * fp32 [N, Hv, dv]. Order per (sequence, head): read S, decay, delta update, o from the
+ * updated state, then (GDN_FLAG_STATE_QDQ) per-tile E4M3 QDQ, then store S. */
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state, float* o, int32_t N, int32_t Hqk,
+                           int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
+                           gdn_stream_t stream);
+
+/* Standalone dynamic tile QDQ ([F]: amax / 448 with a zero guard, E4M3). x, y: device fp32
+ * [lead, rows, cols] (y may equal x); a tile is all `rows` rows x `tile_cols` columns of one
+ * leading index (the last tile may be narrower). scales: device fp32 [lead, ceil(cols /
+ * tile_cols)] or NULL. Per tile, in fp32 with IEEE round-to-nearest: amax = max |x|,
+ * s = amax / 448 (s == 0 -> 1), c = E4M3 round-to-nearest-even with saturation (x / s),
+ * y = c * s. State tiles: rows = dk, tile_cols = 64. W tiles: rows = 64, tile_cols = dk. */
+gdn_status fp8_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int32_t rows,
+                        int32_t cols, int32_t tile_cols, gdn_stream_t stream);
+
+/* Static description of a status code. */
+const char* gdn_status_string(gdn_status status);
+
+/* Synchronizes `stream`, then reads the status word a chunk-forward call left in
+ * `workspace`: GDN_OK, or GDN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait. */
+gdn_status gdn_check_device_status(const void* workspace, gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDNQAT_H */

@@ -253,21 +253,23 @@ void chunked_unit(const Problem& p, int n, int h, int C, int state_qdq, int w_qd
         for (int c = 0; c < dk; ++c) acc += W[(size_t)r * dk + c] * S[(size_t)c * dv + j];
         Dl[(size_t)r * dv + j] = U[(size_t)r * dv + j] - acc;
       }
-    // outputs
+    // outputs (the row factors qg[c] = q_r[c] exp(gam_r[c]) and P[r][i] do not depend on the
+    // value column j, so they are formed once per row)
     if (o) {
       for (int r = 0; r < L; ++r) {
         const int64_t tok = u.t0 + c0 + r;
+        for (int c = 0; c < dk; ++c) X[c] = Q[(size_t)r * dk + c] * std::exp(gam[(size_t)r * dk + c]);
+        for (int i = 0; i <= r; ++i) {
+          double pri = 0.0;
+          for (int c = 0; c < dk; ++c)
+            pri += Q[(size_t)r * dk + c] * K[(size_t)i * dk + c] *
+                   std::exp(gam[(size_t)r * dk + c] - gam[(size_t)i * dk + c]);
+          A[i] = pri;   // A is free once Tm is formed: row r of P
+        }
         for (int j = 0; j < dv; ++j) {
           double acc = 0.0;
-          for (int c = 0; c < dk; ++c)
-            acc += Q[(size_t)r * dk + c] * std::exp(gam[(size_t)r * dk + c]) * S[(size_t)c * dv + j];
-          for (int i = 0; i <= r; ++i) {
-            double pri = 0.0;
-            for (int c = 0; c < dk; ++c)
-              pri += Q[(size_t)r * dk + c] * K[(size_t)i * dk + c] *
-                     std::exp(gam[(size_t)r * dk + c] - gam[(size_t)i * dk + c]);
-            acc += pri * Dl[(size_t)i * dv + j];
-          }
+          for (int c = 0; c < dk; ++c) acc += X[c] * S[(size_t)c * dv + j];
+          for (int i = 0; i <= r; ++i) acc += A[i] * Dl[(size_t)i * dv + j];
           o[(tok * p.Hv + h) * dv + j] = p.scale * acc;
         }
       }
@@ -275,10 +277,10 @@ void chunked_unit(const Problem& p, int n, int h, int C, int state_qdq, int w_qd
     // state carried to the next chunk
     for (int c = 0; c < dk; ++c) {
       const double gl = gam[(size_t)(L - 1) * dk + c];
+      for (int i = 0; i < L; ++i) X[i] = K[(size_t)i * dk + c] * std::exp(gl - gam[(size_t)i * dk + c]);
       for (int j = 0; j < dv; ++j) {
         double acc = std::exp(gl) * S[(size_t)c * dv + j];
-        for (int i = 0; i < L; ++i)
-          acc += K[(size_t)i * dk + c] * std::exp(gl - gam[(size_t)i * dk + c]) * Dl[(size_t)i * dv + j];
+        for (int i = 0; i < L; ++i) acc += X[i] * Dl[(size_t)i * dv + j];
         S1[(size_t)c * dv + j] = acc;
       }
     }

@@ -1,0 +1,82 @@
+"""Shared parity helpers for the GPU tests.
+
+Tolerances (relative L2 error, ||x - ref||_2 / ||ref||_2, separately for o and the final
+state): 1e-3 with every quantizer off, 2e-2 with state and/or W QDQ on. With QDQ on, an
+fp32 GPU value and the fp64 oracle value can sit on opposite sides of an E4M3 rounding
+boundary, so individual elements may differ by one E4M3 step; the bound absorbs that.
+The standalone QDQ on identical fp32 input is unique and compared bit for bit.
+"""
+import numpy as np
+import torch
+
+TOL_OFF = 1e-3
+TOL_QDQ = 2e-2
+
+
+def rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    n = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (n if n > 0 else 1.0))
+
+
+def to_cuda(x):
+    """PrefillInputs / DecodeInputs tensors -> dict of CUDA tensors."""
+    out = {}
+    for name in ("q", "k", "v", "g", "beta", "h0", "state"):
+        t = getattr(x, name, None)
+        out[name] = None if t is None else t.cuda()
+    return out
+
+
+def unit_rows(x, n):
+    """Token slice of sequence n in the [B, T] layout: (b, slice)."""
+    if x.cu_seqlens is not None:
+        cu = x.cu_seqlens.tolist()
+        return 0, slice(cu[n], cu[n + 1])
+    return n, slice(0, x.q.shape[1])
+
+
+def compare_units(x, units, o_gpu, hT_gpu, o_ref, hT_ref, tol):
+    """rel-L2 over the sampled (n, h) units, aggregated and per unit."""
+    o_gpu = o_gpu.detach().cpu().double().numpy()
+    hT_gpu = hT_gpu.detach().cpu().double().numpy()
+    og, orf, hg, hrf = [], [], [], []
+    worst = 0.0
+    for n, h in units:
+        b, s = unit_rows(x, n)
+        og.append(o_gpu[b, s, h].ravel())
+        orf.append(o_ref[b, s, h].ravel())
+        hg.append(hT_gpu[n, h].ravel())
+        hrf.append(hT_ref[n, h].ravel())
+        if og[-1].size:
+            worst = max(worst, rel(og[-1], orf[-1]))
+        worst = max(worst, rel(hg[-1], hrf[-1]))
+    eo = rel(np.concatenate(og), np.concatenate(orf)) if sum(a.size for a in og) else 0.0
+    eh = rel(np.concatenate(hg), np.concatenate(hrf))
+    assert eo <= tol, f"o rel-L2 {eo:.3e} > {tol}"
+    assert eh <= tol, f"hT rel-L2 {eh:.3e} > {tol}"
+    assert worst <= tol, f"worst unit rel-L2 {worst:.3e} > {tol}"
+    return eo, eh
+
+
+def mask_for(units, N, Hv):
+    m = np.zeros((N, Hv), np.uint8)
+    for n, h in units:
+        m[n, h] = 1
+    return m
+
+
+def sample_units(N, Hv, count, seed):
+    rng = np.random.default_rng(seed)
+    all_units = [(n, h) for n in range(N) for h in range(Hv)]
+    if count >= len(all_units):
+        return all_units
+    idx = rng.choice(len(all_units), count, replace=False)
+    return sorted(all_units[i] for i in idx)
+
+
+def bits(t):
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().numpy()
+    return np.ascontiguousarray(t, dtype=np.float32).view(np.uint32)

@@ -1,0 +1,109 @@
+"""The C ABI library (CPU-only checks): it builds, loads, exports every function that
+include/gdnqat.h declares, and its host-side validation returns the documented status
+before touching a device ("GDN state/W QAT foundation": errors are raised before any
+kernel launches). No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import fp8_state_qat_gb300 as lib
+from fp8_state_qat_gb300 import gdnqat as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gdnqat.h")
+
+
+@pytest.fixture(scope="module")
+def so():
+    return lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"defined"})
+
+
+def test_exports_every_declared_symbol(so):
+    names = declared_functions()
+    assert set(names) == set(B.EXPORTED), names
+    for n in names:
+        assert hasattr(so, n), n
+
+
+def test_status_strings(so):
+    for code in range(7):
+        assert lib.status_string(code)
+    assert lib.status_string(99) == "unknown status"
+
+
+FAKE = 1 << 40   # distinct, 256-byte aligned fake device addresses; validation never dereferences them
+
+
+def good_args(**over):
+    a = dict(q=FAKE, k=FAKE + (1 << 32), v=FAKE + (2 << 32), g=FAKE + (3 << 32), beta=FAKE + (4 << 32), h0=None,
+             cu_seqlens=None, cu_seqlens_host=None, o=FAKE + (5 << 32), hT=FAKE + (6 << 32),
+             B=2, T=128, N=2, Hqk=2, Hv=4, dk=128, dv=128, scale=1.0, flags=3)
+    a.update(over)
+    return B.ChunkArgs(**a)
+
+
+def call_chunk(so, args, ws=FAKE + (7 << 32), ws_bytes=1 << 20):
+    return so.gdn_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(dk=96), B.GDN_ERR_UNSUPPORTED_SHAPE),
+    (dict(dv=96), B.GDN_ERR_UNSUPPORTED_SHAPE),
+    (dict(dv=512), B.GDN_ERR_UNSUPPORTED_SHAPE),
+    (dict(Hv=3), B.GDN_ERR_INVALID_ARG),          # Hv % Hqk != 0
+    (dict(N=3), B.GDN_ERR_INVALID_ARG),           # dense needs N == B
+    (dict(q=None), B.GDN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), B.GDN_ERR_INVALID_ARG),    # misaligned
+    (dict(flags=8), B.GDN_ERR_INVALID_ARG),       # unknown flag
+    (dict(o=FAKE + (2 << 32) + 64), B.GDN_ERR_INVALID_ARG),   # o overlaps v
+    (dict(h0=FAKE + (8 << 32), hT=FAKE + (8 << 32) + 256), B.GDN_ERR_INVALID_ARG),  # partial alias
+])
+def test_chunk_validation(so, over, want):
+    assert call_chunk(so, good_args(**over)) == want
+
+
+def test_varlen_validation(so):
+    cu_bad = (ctypes.c_int32 * 4)(0, 50, 40, 128)   # non-monotone
+    a = good_args(B=1, N=3, cu_seqlens=FAKE + (9 << 32), cu_seqlens_host=ctypes.addressof(cu_bad))
+    assert call_chunk(so, a) == B.GDN_ERR_INVALID_ARG
+    cu_end = (ctypes.c_int32 * 4)(0, 50, 60, 127)   # does not end at T
+    a = good_args(B=1, N=3, cu_seqlens=FAKE + (9 << 32), cu_seqlens_host=ctypes.addressof(cu_end))
+    assert call_chunk(so, a) == B.GDN_ERR_INVALID_ARG
+    a = good_args(B=1, N=3, cu_seqlens=FAKE + (9 << 32), cu_seqlens_host=None)   # host copy required
+    assert call_chunk(so, a) == B.GDN_ERR_INVALID_ARG
+
+
+def test_workspace_checks(so):
+    a = good_args()
+    need = so.gdn_chunk_fwd_workspace_size(ctypes.byref(a))
+    assert need >= 4
+    assert call_chunk(so, a, ws_bytes=need - 1) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+    assert call_chunk(so, a, ws=0) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+    assert so.gdn_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=96))) == 0
+
+
+def test_decode_and_qdq_validation(so):
+    P = ctypes.c_void_p
+    ptrs = [P(FAKE + (i << 32)) for i in range(7)]
+    assert so.gdn_decode_step(*ptrs, 4, 2, 4, 96, 128, 1.0, 1, None) == B.GDN_ERR_UNSUPPORTED_SHAPE
+    assert so.gdn_decode_step(*ptrs, 4, 3, 4, 128, 128, 1.0, 1, None) == B.GDN_ERR_INVALID_ARG
+    assert so.gdn_decode_step(*ptrs, 4, 2, 4, 128, 128, 1.0, 16, None) == B.GDN_ERR_INVALID_ARG
+    assert so.fp8_tile_qdq(P(FAKE), P(FAKE), None, 2, 8, 64, 0, None) == B.GDN_ERR_INVALID_ARG
+    assert so.fp8_tile_qdq(P(FAKE), P(FAKE + 4), None, 2, 8, 64, 64, None) == B.GDN_ERR_INVALID_ARG  # overlap
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_args_without_device_report_arch(so):
+    assert call_chunk(so, good_args()) == B.GDN_ERR_UNSUPPORTED_ARCH
+    P = ctypes.c_void_p
+    ptrs = [P(FAKE + (i << 32)) for i in range(7)]
+    assert so.gdn_decode_step(*ptrs, 4, 2, 4, 128, 128, 1.0, 1, None) == B.GDN_ERR_UNSUPPORTED_ARCH
+    assert so.fp8_tile_qdq(P(FAKE), P(FAKE), None, 2, 8, 64, 64, None) == B.GDN_ERR_UNSUPPORTED_ARCH

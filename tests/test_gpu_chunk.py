@@ -1,0 +1,117 @@
+"""gdn_chunk_fwd / kda_chunk_fwd on the GPU against the fp64 oracle.
+
+State QDQ at every 64th token of a sequence with one scale per full-key x 64-value-column
+tile; W QDQ with one scale per (sequence, head, chunk) ("GDN state/W QAT foundation", "What
+does this PR do?"); KDA per-key-channel decay ("Add KDA prefill numerical emulation for QAT").
+With W QDQ off the oracle is the token-by-token recurrence, with W QDQ on the chunked form
+(W QDQ exists only there). Bounds: rel-L2 <= 1e-3 with QDQ off, <= 2e-2 with QDQ on.
+"""
+import numpy as np
+import pytest
+import torch
+
+from fp8_state_qat_gb300 import workloads
+from helpers import TOL_OFF, TOL_QDQ, compare_units, mask_for, sample_units, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(gdn, x, state_qdq, w_qdq, hT_alias=False):
+    c = to_cuda(x)
+    fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
+    hT = c["h0"] if (hT_alias and c["h0"] is not None) else None
+    o, hT = fn(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], x.cu_seqlens, state_qdq=state_qdq,
+               w_qdq=w_qdq, hT=hT)
+    torch.cuda.synchronize()
+    return o, hT
+
+
+def run_oracle(oracle_mod, x, state_qdq, w_qdq, units=None):
+    N, Hv = x.shape["N"], x.shape["Hv"]
+    m = None if units is None else mask_for(units, N, Hv)
+    if w_qdq:
+        return oracle_mod.gdn_chunked(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, kda=x.kda,
+                                      state_qdq=state_qdq, w_qdq=True, unit_mask=m)
+    return oracle_mod.gdn_recurrent(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, kda=x.kda,
+                                    state_qdq=state_qdq, unit_mask=m)
+
+
+def check(gdn, oracle_mod, x, state_qdq, w_qdq, units=None, hT_alias=False):
+    o, hT = run_gpu(gdn, x, state_qdq, w_qdq, hT_alias)
+    oref, href = run_oracle(oracle_mod, x, state_qdq, w_qdq, units)
+    if units is None:
+        units = [(n, h) for n in range(x.shape["N"]) for h in range(x.shape["Hv"])]
+    tol = TOL_QDQ if (state_qdq or w_qdq) else TOL_OFF
+    return compare_units(x, units, o, hT, oref, href, tol)
+
+
+QDQ_MODES = [(False, False), (True, False), (False, True), (True, True)]
+
+
+@pytest.mark.parametrize("state_qdq,w_qdq", QDQ_MODES)
+def test_small_workload(gdn, oracle_mod, state_qdq, w_qdq):
+    """B1 H2 T256 d64 (4 chunks of 64), h0 = 0, the small parity workload."""
+    x = workloads.workload("gdn_b1_h2_t256_d64")
+    check(gdn, oracle_mod, x, state_qdq, w_qdq)
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 200])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 256), (128, 64)])
+def test_lengths_and_shapes(gdn, oracle_mod, T, dk, dv):
+    x = workloads.prefill(2, T, 1, 2, dk, dv, seed=T + dk + dv, h0_std=0.1)
+    check(gdn, oracle_mod, x, True, False)
+    check(gdn, oracle_mod, x, False, False)
+
+
+@pytest.mark.parametrize("kda", [False, True])
+@pytest.mark.parametrize("state_qdq,w_qdq", QDQ_MODES)
+def test_varlen_gqa(gdn, oracle_mod, kda, state_qdq, w_qdq):
+    lens = [0, 1, 63, 64, 65, 129, 300]
+    x = workloads.prefill(1, 0, 2, 4, 128, 128, seed=31 + kda, h0_std=0.1, seqlens=lens, kda=kda)
+    check(gdn, oracle_mod, x, state_qdq, w_qdq)
+
+
+def test_final_state_aliases_h0(gdn, oracle_mod):
+    x = workloads.prefill(2, 150, 2, 2, 128, 128, seed=41, h0_std=0.1)
+    check(gdn, oracle_mod, x, True, True, hT_alias=True)
+
+
+def test_zero_initial_state_and_no_final_state(gdn, oracle_mod):
+    x = workloads.prefill(1, 100, 1, 1, 64, 64, seed=42, h0_std=None)
+    c = to_cuda(x)
+    o, hT = gdn.gdn_chunk_fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], None, None, state_qdq=True,
+                              output_final_state=False)
+    assert hT is None
+    oref, _ = run_oracle(oracle_mod, x, True, False)
+    torch.cuda.synchronize()
+    from helpers import rel
+    assert rel(o.cpu().double().numpy(), oref) <= TOL_QDQ
+
+
+def test_kda_small(gdn, oracle_mod):
+    x = workloads.prefill(2, 200, 2, 2, 128, 128, seed=43, kda=True, h0_std=0.1)
+    check(gdn, oracle_mod, x, False, False)
+    check(gdn, oracle_mod, x, True, True)
+
+
+# ---- full-size workloads, sampled (sequence, head) units ---------------------------------
+
+def test_gdn_b4_h16_t4096_d128_sampled(gdn, oracle_mod):
+    x = workloads.workload("gdn_b4_h16_t4096_d128")
+    units = sample_units(4, 16, 6, seed=1)
+    check(gdn, oracle_mod, x, True, True, units)        # the benchmarked configuration
+    check(gdn, oracle_mod, x, False, False, units)      # quantizers off: the 1e-3 bound
+
+
+def test_gdn_varlen8_hqk16_hv32_d128_sampled(gdn, oracle_mod):
+    x = workloads.workload("gdn_varlen8_hqk16_hv32_d128")
+    lens = np.diff(x.cu_seqlens.numpy())
+    longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
+    units = sorted(set(sample_units(8, 32, 6, seed=2) + [(longest, 31), (shortest, 0)]))
+    check(gdn, oracle_mod, x, True, False, units)
+
+
+def test_kda_b2_h32_t8192_d128_sampled(gdn, oracle_mod):
+    x = workloads.workload("kda_b2_h32_t8192_d128")
+    units = sample_units(2, 32, 4, seed=4)
+    check(gdn, oracle_mod, x, True, True, units)

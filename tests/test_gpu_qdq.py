@@ -1,0 +1,85 @@
+"""fp8_tile_qdq on the GPU is bit-for-bit the oracle's fp32 tile QDQ ("GDN state/W QAT
+foundation", "What does this PR do?": one scale per tile, amax / 448, zero guard, E4M3)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bits
+
+pytestmark = pytest.mark.gpu
+
+
+def wide_inputs(lead, rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    mag = np.exp2(rng.uniform(-20, 20, (lead, 1, 1)))
+    x = (rng.standard_normal((lead, rows, cols)) * mag).astype(np.float32)
+    if lead > 2:
+        x[1] = 0.0                              # all-zero tiles: scale 1, stay zero
+        x[2] = -0.0
+    return x
+
+
+@pytest.mark.parametrize("lead,rows,cols,tile", [
+    (64, 128, 128, 64),    # states [dk=128, dv=128]: two tiles each
+    (32, 64, 128, 128),    # W tiles [64 x dk]
+    (5, 33, 100, 64),      # ragged rows and a narrower last tile
+    (16, 128, 256, 64),
+    (3, 1, 1, 1),
+    (1, 64, 64, 64),
+])
+def test_qdq_bit_exact(gdn, oracle_mod, lead, rows, cols, tile):
+    x = wide_inputs(lead, rows, cols, seed=lead * 7 + cols)
+    y, s = gdn.fp8_tile_qdq(torch.from_numpy(x).cuda(), tile)
+    yo, so = oracle_mod.tile_qdq_f32(x, tile)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(y), bits(yo))
+    np.testing.assert_array_equal(bits(s), bits(so))
+
+
+def test_qdq_rounding_ties_and_saturation(gdn, oracle_mod):
+    """Scale exactly 1 (amax = 448): x / s = x, so every E4M3 midpoint is an exact tie; the
+    hardware conversion must round it to the even code as the oracle does."""
+    grid = [0.0]
+    for e in range(-6, 9):
+        for m in range(8):
+            v = (1 + m / 8) * 2.0 ** e
+            if v <= 448:
+                grid.append(v)
+    grid += [m / 8 * 2.0 ** -6 for m in range(1, 8)]
+    grid = np.array(sorted(set(grid)))
+    mids = (grid[:-1] + grid[1:]) / 2
+    vals = np.concatenate([mids, -mids, grid, np.nextafter(mids, 0), np.nextafter(mids, 1e9)]).astype(np.float32)
+    n = vals.size
+    cols = 64
+    rows = (n + cols - 1) // cols
+    x = np.zeros((1, rows, cols), np.float32)
+    x.reshape(-1)[:n] = vals
+    x[0, -1, -1] = 448.0
+    y, s = gdn.fp8_tile_qdq(torch.from_numpy(x).cuda(), cols * 1000)
+    yo, so = oracle_mod.tile_qdq_f32(x, cols * 1000)
+    assert so[0, 0] == 1.0
+    np.testing.assert_array_equal(bits(y), bits(yo))
+
+
+def test_qdq_denormals_and_in_place(gdn, oracle_mod):
+    x = np.zeros((4, 16, 64), np.float32)
+    rng = np.random.default_rng(5)
+    x[0] = rng.standard_normal((16, 64)) * 1e-39      # fp32 subnormal amax: scale underflows
+    x[1] = rng.standard_normal((16, 64)) * 1e-30
+    x[2] = rng.standard_normal((16, 64)) * 3e38       # near the fp32 maximum
+    x[3, 3, 7] = 1e-45
+    xt = torch.from_numpy(x).cuda()
+    y, s = gdn.fp8_tile_qdq(xt, 64, y=xt)             # in place
+    yo, so = oracle_mod.tile_qdq_f32(x, 64)
+    np.testing.assert_array_equal(bits(xt), bits(yo))
+    np.testing.assert_array_equal(bits(s), bits(so))
+
+
+def test_qdq_empty(gdn):
+    x = torch.zeros((0, 8, 64), device="cuda")
+    y, s = gdn.fp8_tile_qdq(x, 64)
+    assert y.shape == (0, 8, 64) and s.shape == (0, 1)
+    x = torch.zeros((2, 0, 64), device="cuda")
+    y, s = gdn.fp8_tile_qdq(x, 64)
+    torch.cuda.synchronize()
+    assert (s.cpu() == 1.0).all()
