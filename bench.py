@@ -231,6 +231,116 @@ def run_reference(args):
     return 0
 
 
+def decode_bytes(d):
+    """Counted bytes of one decode step: state read + write (fp32), q, k (per q/k head), v
+    (bf16), g, beta (fp32; KDA g per key channel), o (fp32)."""
+    _, N, Hqk, dk = d.q.shape
+    Hv, dv = d.v.shape[2], d.v.shape[3]
+    per_head = 2 * 4 * dk * dv + 2 * dv + 4 * (dk if d.kda else 1) + 4 + 4 * dv
+    return N * Hv * per_head + N * Hqk * 2 * 2 * dk
+
+
+class PrefillCase:
+    def __init__(self, x, dev, torch, gdn):
+        self.x, self.dev, self.torch, self.gdn = x, dev, torch, gdn
+        s = self.s = x.shape
+        self.tokens = x.tokens()
+        self.bytes, self.flops = algorithmic(x)
+        if x.kda:
+            self.bytes += self.tokens * s["Hv"] * 4 * (s["dk"] - 1)
+        self.fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
+        self.sets = [self.resident(), self.resident()]
+        self.cu = x.cu_seqlens
+
+    def resident(self):
+        x, s, dev, torch = self.x, self.s, self.dev, self.torch
+        return dict(q=x.q.to(dev), k=x.k.to(dev), v=x.v.to(dev), g=x.g.to(dev), beta=x.beta.to(dev),
+                    h0=None if x.h0 is None else x.h0.to(dev),
+                    o=torch.empty((s["B"], s["T"], s["Hv"], s["dv"]), device=dev),
+                    hT=torch.empty((s["N"], s["Hv"], s["dk"], s["dv"]), device=dev))
+
+    def step(self, i, ws, stream):
+        b = self.sets[i & 1]
+        self.fn(b["q"], b["k"], b["v"], b["g"], b["beta"], b["h0"], self.cu, state_qdq=self.x.state_qdq,
+                w_qdq=self.x.w_qdq, o=b["o"], hT=b["hT"], workspace=ws, stream=stream)
+
+    def host(self):
+        x = self.x
+        inp = dict(q=x.q, k=x.k, v=x.v, g=x.g, beta=x.beta)
+        if x.h0 is not None:
+            inp["h0"] = x.h0
+        self.h_in = {k: t.pin_memory() for k, t in inp.items()}
+        b = self.sets[0]
+        self.h_out = {k: self.torch.empty(b[k].shape, dtype=self.torch.float32).pin_memory() for k in ("o", "hT")}
+        return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
+                sum(t.numel() * 4 for t in self.h_out.values()))
+
+    def e2e_step(self, ws, stream):
+        b = self.sets[0]
+        for k, t in self.h_in.items():
+            b[k].copy_(t, non_blocking=True)
+        self.step(0, ws, stream)
+        for k, t in self.h_out.items():
+            t.copy_(b[k], non_blocking=True)
+
+    def config(self):
+        s, x = self.s, self.x
+        c = {"workload": x.name, "B": s["B"], "T": s["T"], "Hqk": s["Hqk"], "Hv": s["Hv"], "dk": s["dk"],
+             "dv": s["dv"], "state_qdq": x.state_qdq, "w_qdq": x.w_qdq, "kda": x.kda,
+             "h0": "N(0,0.1)" if x.h0 is not None else "zeros"}
+        if self.cu is not None:
+            c["seqlens"] = self.cu.diff().tolist()
+        return c
+
+
+class DecodeCase:
+    """One step = one decode token for every (sequence, head); the state stays resident and is
+    updated in place; the 64 token sets of the workload are cycled."""
+
+    def __init__(self, d, dev, torch, gdn):
+        self.d, self.dev, self.torch, self.gdn = d, dev, torch, gdn
+        self.steps_avail = d.q.shape[0]
+        self.tokens = d.q.shape[1]
+        self.bytes = decode_bytes(d)
+        _, N, Hqk, dk = d.q.shape
+        Hv, dv = d.v.shape[2], d.v.shape[3]
+        self.flops = N * Hv * 7 * dk * dv
+        self.state = d.state.to(dev)
+        self.tok = [dict(q=d.q[i].to(dev), k=d.k[i].to(dev), v=d.v[i].to(dev), g=d.g[i].to(dev),
+                         beta=d.beta[i].to(dev)) for i in range(self.steps_avail)]
+        self.o = torch.empty((N, Hv, dv), device=dev)
+
+    def step(self, i, ws, stream):
+        t = self.tok[i % self.steps_avail]
+        self.gdn.gdn_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], self.state, state_qdq=self.d.state_qdq,
+                                 kda=self.d.kda, o=self.o, stream=stream)
+
+    def host(self):
+        self.h_in = {k: getattr(self.d, k)[0].pin_memory() for k in ("q", "k", "v", "g", "beta")}
+        self.h_out = self.torch.empty(self.o.shape, dtype=self.torch.float32).pin_memory()
+        return sum(t.numel() * t.element_size() for t in self.h_in.values()), self.h_out.numel() * 4
+
+    def e2e_step(self, ws, stream):
+        for k, t in self.h_in.items():
+            self.tok[0][k].copy_(t, non_blocking=True)
+        self.step(0, ws, stream)
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    def config(self):
+        d = self.d
+        return {"workload": d.name, "N": d.q.shape[1], "H": d.v.shape[2], "dk": d.q.shape[3], "dv": d.v.shape[3],
+                "state_qdq": d.state_qdq, "kda": d.kda, "state": "N(0,0.05), updated in place across steps"}
+
+
+METRICS = {
+    "gdn_b4_h16_t4096_d128": METRIC,
+    "gdn_varlen8_hqk16_hv32_d128": "GDN varlen chunked-prefill tokens/s (8 seqs U[1,8192], GQA 16/32, d128, FP8 state QDQ)",
+    "kda_b2_h32_t8192_d128": "KDA chunked-prefill tokens/s (B2 H32 T8192 d128, FP8 state + W QDQ)",
+    "gdn_decode_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token FP8 state QDQ)",
+    "gdn_b1_h2_t256_d64": "GDN chunked-prefill tokens/s (B1 H2 T256 d64, FP8 state QDQ)",
+}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -244,27 +354,17 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     gdn.load()
     dev = torch.device("cuda", local)
-    x = workloads.workload(WORKLOAD)
-    s = x.shape
-    tokens = x.tokens()
-    bytes_alg, flops_alg = algorithmic(x)
-
-    def resident():
-        return dict(q=x.q.to(dev), k=x.k.to(dev), v=x.v.to(dev), g=x.g.to(dev), beta=x.beta.to(dev),
-                    h0=x.h0.to(dev), o=torch.empty((s["B"], s["T"], s["Hv"], s["dv"]), device=dev),
-                    hT=torch.empty((s["N"], s["Hv"], s["dk"], s["dv"]), device=dev))
-
-    sets = [resident(), resident()]
+    x = workloads.workload(args.workload)
+    if args.batch:   # profiling case of the same kernel: the first `batch` sequences
+        x = workloads.PrefillInputs(x.q[:args.batch], x.k[:args.batch], x.v[:args.batch], x.g[:args.batch],
+                                    x.beta[:args.batch], None if x.h0 is None else x.h0[:args.batch], None,
+                                    kda=x.kda, state_qdq=x.state_qdq, w_qdq=x.w_qdq, name=x.name)
+    case = (DecodeCase if isinstance(x, workloads.DecodeInputs) else PrefillCase)(x, dev, torch, gdn)
     ws = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
-        b = sets[i & 1]
-        gdn.gdn_chunk_fwd(b["q"], b["k"], b["v"], b["g"], b["beta"], b["h0"], None, state_qdq=x.state_qdq,
-                          w_qdq=x.w_qdq, o=b["o"], hT=b["hT"], workspace=ws, stream=stream)
-
     for i in range(args.warmup):
-        step(i)
+        case.step(i, ws, stream)
     torch.cuda.synchronize()
     gdn.gdn_check_device_status(ws)
 
@@ -280,7 +380,7 @@ def run_gpu(args):
     t_start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        step(i)
+        case.step(i, ws, stream)
         ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -297,32 +397,18 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # end to end through the public API: pinned host inputs -> device, forward, outputs -> host
-    host = {k: x_.pin_memory() for k, x_ in dict(q=x.q, k=x.k, v=x.v, g=x.g, beta=x.beta, h0=x.h0).items()}
-    dst = sets[0]
-    o_host = torch.empty(dst["o"].shape, dtype=torch.float32).pin_memory()
-    hT_host = torch.empty(dst["hT"].shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = o_host.numel() * 4 + hT_host.numel() * 4
+    # end to end through the public API: pinned host inputs -> device, call, outputs -> host
+    h2d, d2h = case.host()
     e2e_steps = max(1, min(args.steps, 50))
-
-    def e2e_step():
-        for k_, t in host.items():
-            dst[k_].copy_(t, non_blocking=True)
-        gdn.gdn_chunk_fwd(dst["q"], dst["k"], dst["v"], dst["g"], dst["beta"], dst["h0"], None,
-                          state_qdq=x.state_qdq, w_qdq=x.w_qdq, o=dst["o"], hT=dst["hT"], workspace=ws, stream=stream)
-        o_host.copy_(dst["o"], non_blocking=True)
-        hT_host.copy_(dst["hT"], non_blocking=True)
-
     for _ in range(2):
-        e2e_step()
+        case.e2e_step(ws, stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        case.e2e_step(ws, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -333,25 +419,24 @@ def run_gpu(args):
 
     if rank == 0:
         hbm, bf16, src = peaks()
-        achieved = bytes_alg / (launch_ms * 1e-3) / 1e9
-        value = world * tokens * args.steps / (ms * 1e-3)
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "B": s["B"], "H": s["Hv"], "T": s["T"], "dk": s["dk"], "dv": s["dv"],
-                           "state_qdq": x.state_qdq, "w_qdq": x.w_qdq, "h0": "N(0,0.1)",
-                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                           "l2": "inputs larger than L2: two alternating 346 MB input sets"},
+        achieved = case.bytes / (launch_ms * 1e-3) / 1e9
+        cfg = case.config()
+        cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+        cfg["l2"] = "inputs larger than L2 (129 MB); prefill alternates two resident input sets"
+        line = {"metric": METRICS.get(args.workload, args.workload), "value": world * case.tokens * args.steps / (ms * 1e-3),
+                "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic", "config": cfg,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                             "frac": achieved / hbm, "traffic": profiled_traffic(), "peak_source": src,
-                             "bytes_per_launch": bytes_alg, "flops_per_launch": flops_alg,
-                             "tensor_frac": flops_alg / (launch_ms * 1e-3) / (bf16 * 1e12),
-                             "kernel_ms": launch_ms},
-                "e2e": {"value": world * tokens * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+                             "frac": achieved / hbm,
+                             "traffic": profiled_traffic() if args.workload == WORKLOAD and not args.batch else None,
+                             "peak_source": src, "bytes_per_launch": case.bytes, "flops_per_launch": case.flops,
+                             "tensor_frac": case.flops / (launch_ms * 1e-3) / (bf16 * 1e12), "kernel_ms": launch_ms},
+                "e2e": {"value": world * case.tokens * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": args.steps * 1,
                 "clocks": clocks.summary()}
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and isinstance(case, PrefillCase) and args.workload == WORKLOAD:
             line["cpu_baseline"] = cpu_baseline(x)
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -367,6 +452,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(METRICS),
+                    help="the benchmark is the default; the others measure the remaining hot-path rows")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling only: keep the first B sequences (the line is then not the benchmark)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

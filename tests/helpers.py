@@ -5,12 +5,19 @@ state): 1e-3 with every quantizer off, 2e-2 with state and/or W QDQ on. With QDQ
 fp32 GPU value and the fp64 oracle value can sit on opposite sides of an E4M3 rounding
 boundary, so individual elements may differ by one E4M3 step; the bound absorbs that.
 The standalone QDQ on identical fp32 input is unique and compared bit for bit.
+
+The bound applies to the whole tensor (here: all sampled units together). A single
+(sequence, head) unit can drift further under QDQ: a flipped amax element changes the
+scale of its whole tile, and later QDQs carry that difference on ("Add experimental
+GDN/KDA decode and replay QAT": tiny arithmetic differences flip rounding ties and
+accumulate). Per unit we therefore only bound gross errors (UNIT_SANITY) when QDQ is on.
 """
 import numpy as np
 import torch
 
 TOL_OFF = 1e-3
 TOL_QDQ = 2e-2
+UNIT_SANITY = 0.1
 
 
 def rel(a, b):
@@ -56,7 +63,8 @@ def compare_units(x, units, o_gpu, hT_gpu, o_ref, hT_ref, tol):
     eh = rel(np.concatenate(hg), np.concatenate(hrf))
     assert eo <= tol, f"o rel-L2 {eo:.3e} > {tol}"
     assert eh <= tol, f"hT rel-L2 {eh:.3e} > {tol}"
-    assert worst <= tol, f"worst unit rel-L2 {worst:.3e} > {tol}"
+    unit_tol = tol if tol <= TOL_OFF else max(tol, UNIT_SANITY)
+    assert worst <= unit_tol, f"worst unit rel-L2 {worst:.3e} > {unit_tol}"
     return eo, eh
 
 

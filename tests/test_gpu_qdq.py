@@ -66,7 +66,7 @@ def test_qdq_denormals_and_in_place(gdn, oracle_mod):
     rng = np.random.default_rng(5)
     x[0] = rng.standard_normal((16, 64)) * 1e-39      # fp32 subnormal amax: scale underflows
     x[1] = rng.standard_normal((16, 64)) * 1e-30
-    x[2] = rng.standard_normal((16, 64)) * 3e38       # near the fp32 maximum
+    x[2] = np.clip(rng.standard_normal((16, 64)), -3, 3) * 1e38   # near the fp32 maximum, finite
     x[3, 3, 7] = 1e-45
     xt = torch.from_numpy(x).cuda()
     y, s = gdn.fp8_tile_qdq(xt, 64, y=xt)             # in place
