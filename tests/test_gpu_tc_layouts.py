@@ -1,0 +1,44 @@
+"""Hardware check of the tensor-core operand layouts the chunked forward relies on: a
+tcgen05 MMA on bf16 / tf32 operands staged in the 128-byte-swizzled K-major or MN-major
+shared-memory layout must reproduce a CPU matrix product of the same rounded operands."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def rounded(x, kind):
+    t = torch.from_numpy(x)
+    if kind == 0:
+        return t.to(torch.bfloat16).double().numpy()
+    u = t.view(torch.int32).numpy().astype(np.int64)
+    r = ((u + 0x1000) >> 13) << 13          # round to nearest, ties away, 10 mantissa bits
+    return r.astype(np.int32).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["bf16", "tf32"])
+@pytest.mark.parametrize("a_mn", [0, 1])
+@pytest.mark.parametrize("b_mn", [0, 1])
+@pytest.mark.parametrize("N,K", [(64, 64), (64, 128), (128, 64)])
+def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K):
+    lib = gdn.load()
+    fn = lib.gdnqat_internal_tc_selftest
+    fn.restype = ctypes.c_int
+    M = 128
+    rng = np.random.default_rng(kind * 8 + a_mn * 4 + b_mn * 2 + N + K)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dD = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = fn(ctypes.c_void_p(dA.data_ptr()), ctypes.c_void_p(dB.data_ptr()), ctypes.c_void_p(dD.data_ptr()), M, N, K,
+            kind, a_mn, b_mn, ctypes.c_void_p(st.data_ptr()), None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "bounded wait gave up"
+    want = rounded(A, kind) @ rounded(B, kind)
+    got = dD.cpu().double().numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-4, atol=1e-4 * np.abs(want).max())
