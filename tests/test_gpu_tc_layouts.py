@@ -19,15 +19,20 @@ def rounded(x, kind):
     return r.astype(np.int32).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("kind", [0, 1], ids=["bf16", "tf32"])
-@pytest.mark.parametrize("a_mn", [0, 1])
-@pytest.mark.parametrize("b_mn", [0, 1])
+# (kind, a_mn, b_mn): bf16 in every major combination, tf32 K-major only -- the chunked
+# forward stages tf32 operands K-major (an MN-major tf32 operand needs a different swizzle
+# mode than the 128-byte one staged here).
+COMBOS = [(0, 0, 0), (0, 0, 1), (0, 1, 0), (0, 1, 1), (1, 0, 0)]
+
+
+@pytest.mark.parametrize("kind,a_mn,b_mn", COMBOS)
 @pytest.mark.parametrize("N,K", [(64, 64), (64, 128), (128, 64)])
-def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K):
+@pytest.mark.parametrize("M", [128, 64])
+def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K, M):
+    """M = 128: row m of D in TMEM lane m. M = 64: row m in lane 32 (m / 16) + m % 16."""
     lib = gdn.load()
     fn = lib.gdnqat_internal_tc_selftest
     fn.restype = ctypes.c_int
-    M = 128
     rng = np.random.default_rng(kind * 8 + a_mn * 4 + b_mn * 2 + N + K)
     A = rng.standard_normal((M, K)).astype(np.float32)
     B = rng.standard_normal((K, N)).astype(np.float32)
@@ -41,4 +46,6 @@ def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K):
     assert int(st.item()) == 0, "bounded wait gave up"
     want = rounded(A, kind) @ rounded(B, kind)
     got = dD.cpu().double().numpy()
+    if M == 64:
+        got = got[[32 * (m // 16) + m % 16 for m in range(64)]]
     np.testing.assert_allclose(got, want, rtol=1e-4, atol=1e-4 * np.abs(want).max())
