@@ -1,0 +1,605 @@
+// chunk_tc.cu -- fused chunked gated-delta-rule forward on the sm_103a tensor cores (dk = 128).
+//
+// One CTA (256 threads) per (sequence n, value head h, 64-column value slab); the slab is one
+// state-QDQ tile (all 128 key rows x 64 value columns), so its amax is CTA-local ("GDN state/W
+// QAT foundation", "What does this PR do?"). The CTA walks the sequence's 64-token chunks; the
+// state S0 (fp32) lives in TMEM and, as the MMA operand, in shared memory as bf16 hi + lo
+// (or as exact E4M3 codes once it has been QDQ'd: codes are exact in bf16, the scale is
+// applied in the epilogue).
+//
+// Per chunk of L <= 64 tokens (rows r >= L carry beta = g = 0, so they drop out), gam = prefix
+// sums of g, Gam = exp(gam):
+//   TMA      Q, K [64 x 128] and V [64 x 64] bf16 tiles (128-byte swizzle), next chunk prefetched
+//   G1       [Q; K] K^T                         tcgen05 bf16, M=128 N=64 K=128 (exact products)
+//   A, P     A[r][i] = beta_r exp(gam_r - gam_i) (k_r.k_i), i < r;  P[r][i] = exp(gam_r - gam_i)(q_r.k_i), i <= r
+//   T        (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then block rows (CUDA cores)
+//   U        T'' V,  T'' = T diag(beta)         bf16 (T'' as hi + lo), M=64 N=64 K=64
+//   W^T      K^T T'^T, T' = T diag(beta Gam)    bf16 (T' as hi + lo), M=128 N=64 K=64
+//   W QDQ    one E4M3 scale over the chunk's W; the codes (exact in bf16) become the operand
+//   X, Y     W S0 and Q S0                      bf16, M=64 N=64 K=128
+//   Delta    U - X;   Dt = exp(gam_L - gam) Delta
+//   P Delta  tf32 (round-to-nearest operands), M=64 N=64 K=64
+//   C        K^T Dt                             bf16 (Dt as hi + lo), M=128 N=64 K=64
+//   o        scale (Gam Y + P Delta)            rows r < L to global
+//   S1       Gam_L S0 + C; QDQ(S1) when L == 64 (state QDQ); S1 -> TMEM and the operand
+// Decays are exponentials of non-positive prefix differences with the causal mask applied
+// before the exp ("Add KDA prefill numerical emulation for QAT", "What does this PR do?").
+//
+// Every mbarrier wait is bounded; a CTA whose wait gives up records it in the status word,
+// waits (bounded) for its own TMA in flight, frees its TMEM and exits.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr uint32_t KB = 1024;
+// shared memory map (byte offsets from a 1024-byte aligned base)
+constexpr uint32_t kStageBytes = 40 * KB;                                 // two stages
+constexpr uint32_t ST_V = 0, ST_Q0 = 8 * KB, ST_K0 = 16 * KB, ST_Q1 = 24 * KB, ST_K1 = 32 * KB;
+constexpr uint32_t OFF_SHI = 80 * KB, OFF_SLO = 96 * KB;                 // S0 bf16 [128 c][64 j], MN-major
+constexpr uint32_t OFF_TT = 112 * KB;   // T'' hi, lo, T' hi, lo (8 KB each) -> Delta^T tf32 (16 KB), Dt hi, lo
+constexpr uint32_t OFF_P = 144 * KB;    // P tf32 [64 r][64 i] K-major (two 8 KB atoms)
+constexpr uint32_t OFF_CW = 160 * KB;   // W codes (or W hi) bf16 [64 r][128 c] K-major; W lo at +16 KB
+constexpr uint32_t OFF_A = 192 * KB;    // fp32 A [64][65], solved into T in place
+constexpr uint32_t A_LD = 65;
+constexpr uint32_t OFF_SCR = OFF_A + 64 * A_LD * 4;   // solve scratch 16 x 48 fp32
+constexpr uint32_t OFF_VEC = OFF_SCR + 16 * 48 * 4;   // gam, Gam, decay-to-end, beta [64] each
+constexpr uint32_t OFF_RED = OFF_VEC + 4 * 64 * 4;    // 8 partial maxima
+constexpr uint32_t kSmemBytes = OFF_RED + 64 + 1024;  // + slack to align the base to 1024
+
+// TMEM columns (fp32 accumulators; M=64 results use lanes 32 q + (0..15))
+constexpr uint32_t TM_G1 = 0, TM_W = 64, TM_U = 128, TM_X = 192, TM_Y = 256, TM_C = 320, TM_S = 384;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t IDESC_G1 = tc::make_idesc(tc::kKindBF16, 128, 64, false, false);
+constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);
+constexpr uint32_t IDESC_W = tc::make_idesc(tc::kKindBF16, 128, 64, true, false);
+constexpr uint32_t IDESC_XY = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);
+constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindTF32, 64, 64, false, false);
+constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);
+
+struct TcParams {
+  const float* g;
+  const float* beta;
+  const float* h0;
+  const int32_t* cu;
+  float* o;
+  float* hT;
+  int* status;
+  int T, Hqk, Hv, dv;
+  float scale;
+  int state_qdq, w_qdq;
+};
+
+__device__ __forceinline__ void st_bf16(unsigned char* sm, uint32_t off, float x) {
+  *reinterpret_cast<__nv_bfloat16*>(sm + off) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ void st_f32(unsigned char* sm, uint32_t off, float x) {
+  *reinterpret_cast<float*>(sm + off) = x;
+}
+// E4M3 code of x / s (round-to-nearest-even, saturating), as an fp32 value
+__device__ __forceinline__ float e4m3_code(float x, float s) {
+  const __nv_fp8_e4m3 c(__fdiv_rn(x, s));
+  return static_cast<float>(c);
+}
+__device__ __forceinline__ void ld32(uint32_t tmem, uint32_t lane0, uint32_t col, float* v) {
+  tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col), v);
+  tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);
+  tc::tmem_ld_wait();
+}
+__device__ __forceinline__ void st32(uint32_t tmem, uint32_t lane0, uint32_t col, const float* v) {
+  tc::tmem_st16(tc::tmem_addr(tmem, lane0, col), v);
+  tc::tmem_st16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv, const TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[9];
+  __shared__ uint32_t tmem_slot;
+
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* sm = smem_raw + (sbase - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lt = tid & 31;
+  const int quad = warp & 3;          // TMEM lane quadrant this warp may access
+  const int col0 = (warp >> 2) * 32;  // accumulator columns handled by this warp
+  const int lane128 = quad * 32 + lt; // row of an M=128 accumulator
+  const int row64 = quad * 16 + lt;   // row of an M=64 accumulator (valid for lt < 16)
+
+  const int nslab = p.dv / 64;
+  const int slab = blockIdx.x % nslab;
+  const int h = (blockIdx.x / nslab) % p.Hv;
+  const int n = blockIdx.x / (nslab * p.Hv);
+  const int hq = h / (p.Hv / p.Hqk);
+  int64_t t0, len;
+  if (p.cu) {
+    t0 = p.cu[n];
+    len = (int64_t)p.cu[n + 1] - t0;
+  } else {
+    t0 = (int64_t)n * p.T;
+    len = p.T;
+  }
+  float* vgam = reinterpret_cast<float*>(sm + OFF_VEC);
+  float* vegam = vgam + 64;
+  float* vdec = vgam + 128;
+  float* vbeta = vgam + 192;
+  float* red = reinterpret_cast<float*>(sm + OFF_RED);
+  float* Am = reinterpret_cast<float*>(sm + OFF_A);
+  float* scr = reinterpret_cast<float*>(sm + OFF_SCR);
+  const uint32_t bar_tma0 = tc::smem_u32(&bars[0]), bar_g1 = tc::smem_u32(&bars[2]),
+                 bar_u = tc::smem_u32(&bars[3]), bar_w = tc::smem_u32(&bars[4]), bar_x = tc::smem_u32(&bars[5]),
+                 bar_y = tc::smem_u32(&bars[6]), bar_pd = tc::smem_u32(&bars[7]), bar_c = tc::smem_u32(&bars[8]);
+
+  if (tid == 0) {
+    for (int i = 0; i < 9; ++i) tc::mbar_init(tc::smem_u32(&bars[i]), 1);
+    tc::mbar_fence_init();
+    tc::tma_prefetch_desc(&tq);
+    tc::tma_prefetch_desc(&tk);
+    tc::tma_prefetch_desc(&tv);
+  }
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane0 = (uint32_t)quad * 32u;
+
+  // ---- initial state: h0 (or zeros) -> TMEM S and the bf16 hi/lo operand ----
+  const int64_t sb = ((int64_t)n * p.Hv + h) * 128 * p.dv + slab * 64;   // S[c][j] at sb + c dv + j
+  {
+    float s[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) s[j] = p.h0 ? p.h0[sb + (int64_t)lane128 * p.dv + col0 + j] : 0.f;
+    st32(tmem, lane0, TM_S + col0, s);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float hi = __bfloat162float(__float2bfloat16_rn(s[j]));
+      st_bf16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + j)), hi);
+      st_bf16(sm, OFF_SLO + tc::sw128(lane128, 2 * (col0 + j)), s[j] - hi);
+    }
+    tc::tmem_st_wait();
+  }
+  bool s_exact = false;   // S operand holds exact codes (one bf16 pass) with scale s_scale
+  float s_scale = 1.f;
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+
+  const int64_t nchunks = (len + 63) / 64;
+  auto issue_tma = [&](int64_t cj, int stg) {
+    const uint32_t base = sbase + (uint32_t)stg * kStageBytes, bar = bar_tma0 + 8u * (uint32_t)stg;
+    tc::mbar_expect_tx(bar, kStageBytes);
+    const int tok = (int)(t0 + cj * 64);
+    tc::tma_load_3d(base + ST_V, &tv, bar, slab * 64, h, tok);
+    tc::tma_load_3d(base + ST_Q0, &tq, bar, 0, hq, tok);
+    tc::tma_load_3d(base + ST_K0, &tk, bar, 0, hq, tok);
+    tc::tma_load_3d(base + ST_Q1, &tq, bar, 64, hq, tok);
+    tc::tma_load_3d(base + ST_K1, &tk, bar, 64, hq, tok);
+  };
+  if (tid == 0 && nchunks > 0) issue_tma(0, 0);
+  int64_t tma_issued = nchunks > 0 ? 1 : 0;   // chunks whose TMA has been issued
+
+  bool ok = true;
+  bool aborted = false;
+  // warp-uniform outcome: the TMEM loads that follow are warp-collective
+  auto wait = [&](uint32_t bar, uint32_t par) { ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(bar, par)); };
+  // warp 0 keeps the gates (g, beta) of the next chunk in registers: their loads overlap a chunk
+  float nga = 0.f, ngb = 0.f, nba = 0.f, nbb = 0.f;
+  auto load_gates = [&](int64_t cj) {
+    const int64_t cc0 = cj * 64;
+    const int Lj = (len - cc0) < 64 ? (int)(len - cc0) : 64;
+    const int64_t base = (t0 + cc0) * p.Hv + h;
+    nga = lt < Lj ? p.g[base + (int64_t)lt * p.Hv] : 0.f;
+    ngb = lt + 32 < Lj ? p.g[base + (int64_t)(lt + 32) * p.Hv] : 0.f;
+    nba = lt < Lj ? p.beta[base + (int64_t)lt * p.Hv] : 0.f;
+    nbb = lt + 32 < Lj ? p.beta[base + (int64_t)(lt + 32) * p.Hv] : 0.f;
+  };
+  if (warp == 0 && nchunks > 0) load_gates(0);
+
+  for (int64_t ci = 0; ci < nchunks; ++ci) {
+    const int st = (int)(ci & 1);
+    const uint32_t stg = sbase + (uint32_t)st * kStageBytes;
+    const int64_t c0 = ci * 64;
+    const int L = (len - c0) < 64 ? (int)(len - c0) : 64;
+    const uint32_t par = (uint32_t)(ci & 1);
+
+    wait(bar_tma0 + 8u * (uint32_t)st, (uint32_t)((ci >> 1) & 1));
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (tid == 0) {
+      tc::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t kb = ks >> 2, sub = ks & 3;
+        const uint64_t a = tc::make_sdesc(stg + (kb ? ST_Q1 : ST_Q0) + sub * 32, 16, 1024);
+        const uint64_t b = tc::make_sdesc(stg + (kb ? ST_K1 : ST_K0) + sub * 32, 16, 1024);
+        tc::mma_bf16(tmem + TM_G1, a, b, IDESC_G1, ks > 0);
+      }
+      tc::mma_commit(bar_g1);
+      if (ci + 1 < nchunks) issue_tma(ci + 1, st ^ 1);
+    }
+    if (ci + 1 < nchunks) tma_issued = ci + 2;
+
+    // ---- gates: prefix sums of g (in-chunk), Gam, decay to the chunk end, beta ----
+    if (warp == 0) {
+      const int r0 = lt, r1 = lt + 32;
+      float ga = nga, gb = ngb;
+      const float ba = nba, bb = nbb;
+      if (ci + 1 < nchunks) load_gates(ci + 1);
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float ya = __shfl_up_sync(0xffffffffu, ga, off);
+        const float yb = __shfl_up_sync(0xffffffffu, gb, off);
+        if (lt >= off) { ga += ya; gb += yb; }
+      }
+      gb += __shfl_sync(0xffffffffu, ga, 31);
+      const float gl = __shfl_sync(0xffffffffu, gb, 31);
+      vgam[r0] = ga; vgam[r1] = gb;
+      vegam[r0] = expf(ga); vegam[r1] = expf(gb);
+      vdec[r0] = expf(gl - ga); vdec[r1] = expf(gl - gb);
+      vbeta[r0] = ba; vbeta[r1] = bb;
+    }
+    __syncthreads();
+
+    // ---- A (rows of K K^T) and P (rows of Q K^T) from G1 ----
+    wait(bar_g1, par);
+    tc::tc_fence_after();
+    if (ok) {
+      float v[32];
+      ld32(tmem, lane0, TM_G1 + col0, v);
+      if (quad < 2) {   // G1 rows 0..63: Q K^T
+        const int r = lane128;
+        const float gr = vgam[r];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int i = col0 + j;
+          const float pv = i <= r ? __expf(gr - vgam[i]) * v[j] : 0.f;
+          st_f32(sm, OFF_P + (uint32_t)(i >> 5) * 8 * KB + tc::sw128(r, (i & 31) * 4), tc::to_tf32(pv));
+        }
+      } else {          // G1 rows 64..127: K K^T
+        const int r = lane128 - 64;
+        const float gr = vgam[r], br = vbeta[r];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int i = col0 + j;
+          Am[r * A_LD + i] = i < r ? br * __expf(gr - vgam[i]) * v[j] : 0.f;
+        }
+      }
+    }
+    tc::tc_fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+
+    // ---- T = (I + A)^{-1} in place: diagonal blocks, then block rows ----
+    {
+      float x[16];
+      const int b0 = (tid >> 4) * 16, jj = tid & 15;
+      if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float acc = (r == jj) ? 1.f : 0.f;
+#pragma unroll
+          for (int i = 0; i < r; ++i) acc = fmaf(-Am[(b0 + r) * A_LD + b0 + i], x[i], acc);
+          x[r] = r < jj ? 0.f : acc;
+        }
+      }
+      __syncthreads();
+      if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Am[(b0 + r) * A_LD + b0 + jj] = x[r];
+      }
+      __syncthreads();
+      const int rr = tid >> 4, cc = tid & 15;
+      for (int bi = 1; bi < 4; ++bi) {
+        for (int bj = 0; bj < bi; ++bj) {
+          float acc = 0.f;
+          for (int m = bj * 16; m < bi * 16; ++m) acc = fmaf(Am[(bi * 16 + rr) * A_LD + m], Am[m * A_LD + bj * 16 + cc], acc);
+          scr[rr * 48 + bj * 16 + cc] = acc;
+        }
+        __syncthreads();
+        for (int bj = 0; bj < bi; ++bj) {
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) acc = fmaf(Am[(bi * 16 + rr) * A_LD + bi * 16 + m], scr[m * 48 + bj * 16 + cc], acc);
+          Am[(bi * 16 + rr) * A_LD + bj * 16 + cc] = -acc;
+        }
+        __syncthreads();
+      }
+    }
+    // ---- T'' = T diag(beta), T' = T'' diag(Gam) as bf16 hi + lo, K-major [r][i] ----
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+      const int r = e >> 6, i = e & 63;
+      const float t2 = Am[r * A_LD + i] * vbeta[i];
+      const float t1 = t2 * vegam[i];
+      const uint32_t off = tc::sw128(r, 2 * i);
+      const float h2 = __bfloat162float(__float2bfloat16_rn(t2));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(t1));
+      st_bf16(sm, OFF_TT + off, h2);
+      st_bf16(sm, OFF_TT + 8 * KB + off, t2 - h2);
+      st_bf16(sm, OFF_TT + 16 * KB + off, h1);
+      st_bf16(sm, OFF_TT + 24 * KB + off, t1 - h1);
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::tc_fence_after();
+      // U = T'' V: A = T'' (K-major), B = V (MN-major)
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::make_sdesc(sbase + OFF_TT + part * 8 * KB + ks * 32, 16, 1024);
+          const uint64_t b = tc::make_sdesc(stg + ST_V + ks * 2048, 8 * KB, 1024);
+          tc::mma_bf16(tmem + TM_U, a, b, IDESC_U, (part | ks) != 0);
+        }
+      tc::mma_commit(bar_u);
+      // W^T = K^T T'^T: A = K^T (MN-major, the two 64-column K blocks 16 KB apart), B = T' (K-major)
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::make_sdesc(stg + ST_K0 + ks * 2048, 16 * KB, 1024);
+          const uint64_t b = tc::make_sdesc(sbase + OFF_TT + 16 * KB + part * 8 * KB + ks * 32, 16, 1024);
+          tc::mma_bf16(tmem + TM_W, a, b, IDESC_W, (part | ks) != 0);
+        }
+      tc::mma_commit(bar_w);
+    }
+
+    // ---- W QDQ (one scale per chunk) -> W operand for X ----
+    wait(bar_w, par);
+    tc::tc_fence_after();
+    float sW = 1.f;
+    {
+      float w[32];
+      if (ok) ld32(tmem, lane0, TM_W + col0, w);   // w[j] = W[r = col0 + j][c = lane128]
+      const int c = lane128;
+      const uint32_t cbase = OFF_CW + (uint32_t)(c >> 6) * 8 * KB;
+      if (p.w_qdq) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(w[j]));
+        m = warp_max(m);
+        if (lt == 0) red[warp] = m;
+        __syncthreads();
+        float amax = red[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+        sW = qdq_scale(amax);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_bf16(sm, cbase + tc::sw128(col0 + j, 2 * (c & 63)), e4m3_code(w[j], sW));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float hi = __bfloat162float(__float2bfloat16_rn(w[j]));
+          st_bf16(sm, cbase + tc::sw128(col0 + j, 2 * (c & 63)), hi);
+          st_bf16(sm, cbase + 16 * KB + tc::sw128(col0 + j, 2 * (c & 63)), w[j] - hi);
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (tid == 0) {
+      tc::tc_fence_after();
+      // X = W S0 (M=64, N=64, K=128): (codes or W hi) x (S hi or codes) [+ W hi x S lo] [+ W lo x S hi]
+      uint32_t aoff[3], boff[3];
+      int np = 0;
+      aoff[np] = OFF_CW; boff[np++] = OFF_SHI;
+      if (!s_exact) { aoff[np] = OFF_CW; boff[np++] = OFF_SLO; }
+      if (!p.w_qdq) { aoff[np] = OFF_CW + 16 * KB; boff[np++] = OFF_SHI; }
+      for (int q = 0; q < np; ++q)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t a = tc::make_sdesc(sbase + aoff[q] + (ks >> 2) * 8 * KB + (ks & 3) * 32, 16, 1024);
+          const uint64_t b = tc::make_sdesc(sbase + boff[q] + ks * 2048, 16 * KB, 1024);
+          tc::mma_bf16(tmem + TM_X, a, b, IDESC_XY, (q | ks) != 0);
+        }
+      tc::mma_commit(bar_x);
+      // Y = Q S0: A = Q (the 64 Q rows of each 128-byte K block), B = S operand
+      const int ny = s_exact ? 1 : 2;
+      for (int q = 0; q < ny; ++q)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t a = tc::make_sdesc(stg + ((ks >> 2) ? ST_Q1 : ST_Q0) + (ks & 3) * 32, 16, 1024);
+          const uint64_t b = tc::make_sdesc(sbase + (q ? OFF_SLO : OFF_SHI) + ks * 2048, 16 * KB, 1024);
+          tc::mma_bf16(tmem + TM_Y, a, b, IDESC_XY, (q | ks) != 0);
+        }
+      tc::mma_commit(bar_y);
+    }
+
+    // ---- Delta = U - W S0 -> Delta^T (tf32, for P Delta) and Dt = decay Delta (bf16 hi/lo) ----
+    wait(bar_u, par);
+    wait(bar_x, par);
+    tc::tc_fence_after();
+    if (ok) {
+      float xv[32], uv[32];
+      ld32(tmem, lane0, TM_X + col0, xv);
+      ld32(tmem, lane0, TM_U + col0, uv);
+      if (lt < 16) {
+        const int r = row64;
+        const float f = sW * s_scale, dr = vdec[r];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int jc = col0 + j;
+          const float d = uv[j] - f * xv[j];
+          st_f32(sm, OFF_TT + (uint32_t)(r >> 5) * 8 * KB + tc::sw128(jc, (r & 31) * 4), tc::to_tf32(d));
+          const float dt = dr * d;
+          const float hi = __bfloat162float(__float2bfloat16_rn(dt));
+          st_bf16(sm, OFF_TT + 16 * KB + tc::sw128(r, 2 * jc), hi);
+          st_bf16(sm, OFF_TT + 24 * KB + tc::sw128(r, 2 * jc), dt - hi);
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (tid == 0) {
+      tc::tc_fence_after();
+      // P Delta (tf32): A = P [r][i], B = Delta^T [j][i], both K-major
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t a = tc::make_sdesc(sbase + OFF_P + (ks >> 2) * 8 * KB + (ks & 3) * 32, 16, 1024);
+        const uint64_t b = tc::make_sdesc(sbase + OFF_TT + (ks >> 2) * 8 * KB + (ks & 3) * 32, 16, 1024);
+        tc::mma_tf32(tmem + TM_G1, a, b, IDESC_PD, ks != 0);
+      }
+      tc::mma_commit(bar_pd);
+      // C = K^T Dt: A = K^T (MN-major), B = Dt hi / lo (MN-major [i][j])
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::make_sdesc(stg + ST_K0 + ks * 2048, 16 * KB, 1024);
+          const uint64_t b = tc::make_sdesc(sbase + OFF_TT + 16 * KB + part * 8 * KB + ks * 2048, 8 * KB, 1024);
+          tc::mma_bf16(tmem + TM_C, a, b, IDESC_C, (part | ks) != 0);
+        }
+      tc::mma_commit(bar_c);
+    }
+
+    // ---- outputs: o = scale (Gam Y + P Delta) for rows r < L ----
+    wait(bar_y, par);
+    wait(bar_pd, par);
+    tc::tc_fence_after();
+    if (ok) {
+      float yv[32], pv[32];
+      ld32(tmem, lane0, TM_Y + col0, yv);
+      ld32(tmem, lane0, TM_G1 + col0, pv);
+      if (lt < 16 && row64 < L) {
+        const int r = row64;
+        const float er = vegam[r] * s_scale;
+        float4* out = reinterpret_cast<float4*>(p.o + ((t0 + c0 + r) * p.Hv + h) * (int64_t)p.dv + slab * 64 + col0);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          out[j >> 2] = make_float4(p.scale * fmaf(er, yv[j], pv[j]), p.scale * fmaf(er, yv[j + 1], pv[j + 1]),
+                                    p.scale * fmaf(er, yv[j + 2], pv[j + 2]), p.scale * fmaf(er, yv[j + 3], pv[j + 3]));
+      }
+    }
+
+    // ---- S1 = Gam_L S0 + C, state QDQ at the 64-token boundary ----
+    wait(bar_c, par);
+    tc::tc_fence_after();
+    {
+      float s0[32], cv[32];
+      if (ok) {
+        ld32(tmem, lane0, TM_S + col0, s0);
+        ld32(tmem, lane0, TM_C + col0, cv);
+      }
+      const float el = vegam[63];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) s0[j] = fmaf(el, s0[j], cv[j]);
+      const bool q = p.state_qdq && L == 64;
+      if (q) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(s0[j]));
+        m = warp_max(m);
+        __syncthreads();   // red[] from the W QDQ is no longer read
+        if (lt == 0) red[warp] = m;
+        __syncthreads();
+        float amax = red[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+        const float sS = qdq_scale(amax);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float code = e4m3_code(s0[j], sS);
+          s0[j] = __fmul_rn(code, sS);
+          st_bf16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + j)), code);
+        }
+        s_exact = true;
+        s_scale = sS;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float hi = __bfloat162float(__float2bfloat16_rn(s0[j]));
+          st_bf16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + j)), hi);
+          st_bf16(sm, OFF_SLO + tc::sw128(lane128, 2 * (col0 + j)), s0[j] - hi);
+        }
+        s_exact = false;
+        s_scale = 1.f;
+      }
+      if (ok) st32(tmem, lane0, TM_S + col0, s0);
+      tc::tmem_st_wait();
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    tc::tc_fence_after();
+  }
+
+  if (!aborted && p.hT) {
+    float s0[32];
+    ld32(tmem, lane0, TM_S + col0, s0);
+    float4* out = reinterpret_cast<float4*>(p.hT + sb + (int64_t)lane128 * p.dv + col0);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) out[j >> 2] = make_float4(s0[j], s0[j + 1], s0[j + 2], s0[j + 3]);
+  }
+  if (aborted) {
+    if (tid == 0) atomicExch(p.status, 1);
+    // the TMA of the last issued chunk may still be in flight: wait for it (bounded)
+    const int64_t last = tma_issued - 1;
+    if (last >= 0) tc::mbar_wait(bar_tma0 + 8u * (uint32_t)(last & 1), (uint32_t)((last >> 1) & 1), 1u << 16);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a head-last bf16 tensor [tokens, heads, D]: dims (D, heads, tokens), box 64 x 1 x 64
+bool make_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunk_tc_supported(const ChunkProblem& p) { return p.dk == 128 && !p.kda && p.dv % 64 == 0; }
+
+cudaError_t launch_chunk_tc(const ChunkProblem& p, int* status, cudaStream_t stream) {
+  const int64_t tokens = (int64_t)p.B * p.T;
+  const int64_t blocks = (int64_t)p.N * p.Hv * (p.dv / 64);
+  if (blocks == 0) return cudaSuccess;
+  CUtensorMap tq, tk, tv;
+  // an empty batch still needs valid maps: point them at a one-token view (never loaded)
+  const int64_t tmap = tokens > 0 ? tokens : 1;
+  if (!make_map(&tq, p.q, 128, p.Hqk, tmap) || !make_map(&tk, p.k, 128, p.Hqk, tmap) ||
+      !make_map(&tv, p.v, p.dv, p.Hv, tmap))
+    return cudaErrorInvalidValue;
+  TcParams tp{p.g, p.beta, p.h0, p.cu, p.o, p.hT, status, p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
+  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  chunk_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tp);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

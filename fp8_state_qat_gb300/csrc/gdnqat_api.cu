@@ -100,7 +100,9 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
   ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
                  (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
-  return gdn::launch_chunk_simt(p, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  const cudaError_t e = gdn::chunk_tc_supported(p) ? gdn::launch_chunk_tc(p, static_cast<int*>(ws), stream)
+                                                   : gdn::launch_chunk_simt(p, stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace

@@ -28,6 +28,11 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const flo
                           float* state, float* o, int N, int Hqk, int Hv, int dk, int dv, float scale,
                           int state_qdq, int kda, cudaStream_t stream);
 
+// Fused tensor-core chunked forward (tcgen05 + TMA), dk = 128, GDN. status: device int,
+// set to nonzero when a bounded wait gives up.
+bool chunk_tc_supported(const ChunkProblem& p);
+cudaError_t launch_chunk_tc(const ChunkProblem& p, int* status, cudaStream_t stream);
+
 // Per-CTA fp32 chunked forward on CUDA cores: one CTA per (sequence, head, 64-column
 // value slab). Used for shapes and variants the tensor-core path does not take.
 cudaError_t launch_chunk_simt(const ChunkProblem& p, cudaStream_t stream);
