@@ -28,8 +28,8 @@ def nvcc() -> str:
     return p
 
 
-def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+def _sources(csrc=CSRC):
+    return sorted(glob.glob(os.path.join(csrc, "*.cu")))
 
 
 def _deps():
@@ -44,11 +44,14 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, csrc: str = CSRC, out: str = LIB_PATH) -> str:
+    """Compile `csrc`/*.cu into the shared library `out` (defaults: this package's sources and
+    library)."""
+    if not force and csrc == CSRC and out == LIB_PATH and up_to_date():
         return LIB_PATH
-    os.makedirs(OBJ_DIR, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
+    obj_dir = os.path.join(os.path.dirname(out), "_obj_" + os.path.basename(out)) if out != LIB_PATH else OBJ_DIR
+    os.makedirs(obj_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(out), exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                     "-I", os.path.join(ROOT, "include")]
@@ -56,23 +59,23 @@ def build(force: bool = False, verbose: bool = False) -> str:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         r = subprocess.run([cc, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
-        results = list(ex.map(compile_one, _sources()))
+        results = list(ex.map(compile_one, _sources(csrc)))
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
