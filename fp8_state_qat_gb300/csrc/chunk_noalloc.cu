@@ -1,0 +1,63 @@
+// chunk_noalloc.cu -- gdn_chunk_fwd for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc or any allocating routine at the point where they run
+// the forward: code running inside a memory allocator's own hooks, latency-critical paths
+// where an allocation's implicit device synchronization is not allowed, or processes whose
+// device memory is fully handed out to a framework's pool. gdn_chunk_fwd needs a small
+// device workspace (the status word of the tensor-core kernel's bounded waits); this variant
+// takes that workspace from a fixed-size array that lives in the library itself, so the
+// caller passes only its inputs and outputs.
+//
+// The array is a file-scope __device__ object: every GPU that loads the library holds these
+// kNoAllocScratchBytes until the process exits, and all calls on a device share it. The host
+// symbol is only a stand-in; its device address is looked up once per device with
+// cudaGetSymbolAddress (on the first call made while that device is current).
+#include <mutex>
+
+#include "../../include/gdnqat.h"
+#include "common.cuh"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;   // the most the chunk forward asks for today
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch array on the current device (looked up once per device).
+gdn_status scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GDN_ERR_UNSUPPORTED_ARCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return GDN_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream) {
+  const size_t need = gdn_chunk_fwd_workspace_size(args);
+  if (need == 0) {
+    // invalid arguments: let the regular entry point report which check failed
+    return gdn_chunk_fwd(args, nullptr, 0, stream);
+  }
+  if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  const gdn_status s = scratch_for_current_device(&scratch);
+  if (s != GDN_OK) return s;
+  // gdn_chunk_fwd clears the status word on `stream` before its kernel runs
+  return gdn_chunk_fwd(args, scratch, kNoAllocScratchBytes, stream);
+}

@@ -28,8 +28,8 @@ GDN_FLAG_W_QDQ = 2
 GDN_FLAG_KDA = 4
 
 # every extern "C" symbol of include/gdnqat.h
-EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "kda_chunk_fwd", "gdn_decode_step",
-            "fp8_tile_qdq", "gdn_status_string", "gdn_check_device_status")
+EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc", "kda_chunk_fwd",
+            "gdn_decode_step", "fp8_tile_qdq", "gdn_status_string", "gdn_check_device_status")
 
 
 class GdnError(RuntimeError):
@@ -73,6 +73,8 @@ def load(build_if_missing: bool = True):
         for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
             getattr(lib, fn).restype = ctypes.c_int
             getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, ctypes.c_size_t, P]
+        lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.gdn_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkArgs), P]
         lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, F, U32, P]
         lib.fp8_tile_qdq.restype = ctypes.c_int

@@ -23,7 +23,8 @@
  *
  * Conventions for every call
  *  - Every pointer named "device" is caller-owned device memory; the library allocates
- *    nothing and keeps no state apart from a cached per-device capability probe.
+ *    nothing and keeps no state apart from a cached per-device capability probe (and the
+ *    fixed array behind gdn_chunk_fwd_noalloc).
  *  - Each call validates its arguments and the device on the host and returns a status
  *    BEFORE launching anything ([F]); a non-OK status means nothing was enqueued.
  *  - Work is enqueued on the caller's stream (NULL = legacy default stream); calls return
@@ -93,6 +94,25 @@ size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args);
  * aligned; its contents need no initialization. */
 gdn_status gdn_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
                          gdn_stream_t stream);
+
+/* gdn_chunk_fwd for callers that cannot allocate device memory: the pages have no
+ * counterpart for this call; it exists for callers that may not call cudaMalloc (for
+ * example code running inside a memory allocator's own hooks, latency-critical paths where
+ * an allocation's device synchronization is not allowed, or processes whose device memory
+ * is all handed to a framework's pool). Same arguments and
+ * results as gdn_chunk_fwd, minus the workspace: the workspace is a 256-byte array
+ * inside the library (static device memory, held by every GPU that loads the library until
+ * the process exits). No cudaMalloc, cudaFree or other allocating call is made.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current; make that first call before any stream capture.
+ *  - All calls on a device share the array (its status word is cleared at the start of
+ *    each call): calls that may run at the same time on the GPU, e.g. on different
+ *    streams, race on it. Serialize them, or use gdn_chunk_fwd with separate workspaces.
+ *  - Returns GDN_ERR_WORKSPACE_TOO_SMALL if these arguments would need more workspace than
+ *    the 256 bytes the array holds.
+ *  - A device-side timeout is recorded in the shared array and cannot be queried through
+ *    gdn_check_device_status. */
+gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream);
 
 /* KDA variant ([K]): same contract with g [B, T, Hv, dk], one log-decay per key channel;
  * pairwise decays come from differences of prefix sums of g within a chunk. */
