@@ -14,16 +14,19 @@
 //   A, P     A[r][i] = beta_r exp(gam_r - gam_i) (k_r.k_i), i < r;  P[r][i] = exp(gam_r - gam_i)(q_r.k_i), i <= r
 //   T        (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then block rows (CUDA cores)
 //   U        T'' V,  T'' = T diag(beta)         bf16 (T'' as hi + lo), M=64 N=64 K=64
-//   W^T      K^T T'^T, T' = T diag(beta Gam)    bf16 (T' as hi + lo), M=128 N=64 K=64
+//   W        T' K,   T' = T diag(beta Gam)      bf16 (T' as hi + lo), M=64 N=128 K=64
 //   W QDQ    one E4M3 scale over the chunk's W; the codes (exact in bf16) become the operand
 //   X, Y     W S0 and Q S0                      bf16, M=64 N=64 K=128
 //   Delta    U - X;   Dt = exp(gam_L - gam) Delta
-//   P Delta  tf32 (round-to-nearest operands), M=64 N=64 K=64
+//   P Delta  bf16 (P and Delta as hi + lo),     M=64 N=64 K=64
 //   C        K^T Dt                             bf16 (Dt as hi + lo), M=128 N=64 K=64
 //   o        scale (Gam Y + P Delta)            rows r < L to global
 //   S1       Gam_L S0 + C; QDQ(S1) when L == 64 (state QDQ); S1 -> TMEM and the operand
 // Decays are exponentials of non-positive prefix differences with the causal mask applied
 // before the exp ("Add KDA prefill numerical emulation for QAT", "What does this PR do?").
+// The fused QDQ epilogues multiply by a correctly rounded reciprocal of the tile scale; this
+// can differ from an exact divide by one ulp before the E4M3 rounding (the standalone
+// fp8_tile_qdq divides exactly).
 //
 // Every mbarrier wait is bounded; a CTA whose wait gives up records it in the status word,
 // waits (bounded) for its own TMA in flight, frees its TMEM and exits.
@@ -41,26 +44,26 @@ constexpr uint32_t KB = 1024;
 // shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t kStageBytes = 40 * KB;                                 // two stages
 constexpr uint32_t ST_V = 0, ST_Q0 = 8 * KB, ST_K0 = 16 * KB, ST_Q1 = 24 * KB, ST_K1 = 32 * KB;
-constexpr uint32_t OFF_SHI = 80 * KB, OFF_SLO = 96 * KB;                 // S0 bf16 [128 c][64 j], MN-major
-constexpr uint32_t OFF_TT = 112 * KB;   // T'' hi, lo, T' hi, lo (8 KB each) -> Delta^T tf32 (16 KB), Dt hi, lo
-constexpr uint32_t OFF_P = 144 * KB;    // P tf32 [64 r][64 i] K-major (two 8 KB atoms)
+constexpr uint32_t OFF_SHI = 80 * KB, OFF_SLO = 96 * KB;   // S0 bf16 [128 c][64 j], MN-major
+constexpr uint32_t OFF_TT = 112 * KB;   // T'' hi, lo, T' hi, lo (8 KB each, [r][i] K-major);
+                                        // later Delta hi, lo and Dt hi, lo ([i][j] MN-major)
+constexpr uint32_t OFF_P = 144 * KB;    // P hi, lo bf16 [64 r][64 i] K-major (8 KB each)
 constexpr uint32_t OFF_CW = 160 * KB;   // W codes (or W hi) bf16 [64 r][128 c] K-major; W lo at +16 KB
-constexpr uint32_t OFF_A = 192 * KB;    // fp32 A [64][65], solved into T in place
-constexpr uint32_t A_LD = 65;
+constexpr uint32_t OFF_A = 192 * KB;    // fp32 A [64][68], solved into T in place
+constexpr uint32_t A_LD = 68;
 constexpr uint32_t OFF_SCR = OFF_A + 64 * A_LD * 4;   // solve scratch 16 x 48 fp32
 constexpr uint32_t OFF_VEC = OFF_SCR + 16 * 48 * 4;   // gam, Gam, decay-to-end, beta [64] each
 constexpr uint32_t OFF_RED = OFF_VEC + 4 * 64 * 4;    // 8 partial maxima
 constexpr uint32_t kSmemBytes = OFF_RED + 64 + 1024;  // + slack to align the base to 1024
 
 // TMEM columns (fp32 accumulators; M=64 results use lanes 32 q + (0..15))
-constexpr uint32_t TM_G1 = 0, TM_W = 64, TM_U = 128, TM_X = 192, TM_Y = 256, TM_C = 320, TM_S = 384;
+constexpr uint32_t TM_G1 = 0, TM_W = 64, TM_U = 192, TM_X = 256, TM_Y = 320, TM_C = 384, TM_S = 448;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t IDESC_G1 = tc::make_idesc(tc::kKindBF16, 128, 64, false, false);
 constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);
-constexpr uint32_t IDESC_W = tc::make_idesc(tc::kKindBF16, 128, 64, true, false);
+constexpr uint32_t IDESC_W = tc::make_idesc(tc::kKindBF16, 64, 128, false, true);
 constexpr uint32_t IDESC_XY = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);
-constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindTF32, 64, 64, false, false);
 constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);
 
 struct TcParams {
@@ -76,16 +79,41 @@ struct TcParams {
   int state_qdq, w_qdq;
 };
 
-__device__ __forceinline__ void st_bf16(unsigned char* sm, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(sm + off) = __float2bfloat16_rn(x);
+// bf16 pair packed in 32 bits (low half = first element)
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ void st_f32(unsigned char* sm, uint32_t off, float x) {
-  *reinterpret_cast<float*>(sm + off) = x;
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
 }
-// E4M3 code of x / s (round-to-nearest-even, saturating), as an fp32 value
-__device__ __forceinline__ float e4m3_code(float x, float s) {
-  const __nv_fp8_e4m3 c(__fdiv_rn(x, s));
-  return static_cast<float>(c);
+// 8 consecutive values -> bf16 hi (exact rounding) and lo (residual), one 16-byte chunk each
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+    const float2 hf = unpack_bf16(h[i]);
+    l[i] = pack_bf16(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+__device__ __forceinline__ void st16(unsigned char* sm, uint32_t off, uint4 v) {
+  *reinterpret_cast<uint4*>(sm + off) = v;
+}
+// E4M3 QDQ of a pair with the reciprocal of the scale: codes (as fp32) and dequantized values
+__device__ __forceinline__ void qdq_pair(float a, float b, float rs, float s, float& ca, float& cb, float& qa,
+                                         float& qb) {
+  const __nv_fp8x2_e4m3 c(make_float2(__fmul_rn(a, rs), __fmul_rn(b, rs)));
+  const float2 cf = static_cast<float2>(c);
+  ca = cf.x;
+  cb = cf.y;
+  qa = __fmul_rn(cf.x, s);
+  qb = __fmul_rn(cf.y, s);
 }
 __device__ __forceinline__ void ld32(uint32_t tmem, uint32_t lane0, uint32_t col, float* v) {
   tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col), v);
@@ -96,6 +124,8 @@ __device__ __forceinline__ void st32(uint32_t tmem, uint32_t lane0, uint32_t col
   tc::tmem_st16(tc::tmem_addr(tmem, lane0, col), v);
   tc::tmem_st16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);
 }
+// descriptor for `addr` advanced by `off` bytes (the start field is the low 14 bits, in 16-byte units)
+__device__ __forceinline__ uint64_t dadv(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -109,7 +139,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   unsigned char* sm = smem_raw + (sbase - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lt = tid & 31;
   const int quad = warp & 3;          // TMEM lane quadrant this warp may access
-  const int col0 = (warp >> 2) * 32;  // accumulator columns handled by this warp
+  const int half = warp >> 2;         // which half of an accumulator's columns this warp handles
+  const int col0 = half * 32;         // 64-column accumulators: columns [col0, col0 + 32)
   const int lane128 = quad * 32 + lt; // row of an M=128 accumulator
   const int row64 = quad * 16 + lt;   // row of an M=64 accumulator (valid for lt < 16)
 
@@ -151,18 +182,40 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   const uint32_t tmem = tmem_slot;
   const uint32_t lane0 = (uint32_t)quad * 32u;
 
+  // operand descriptors (128-byte swizzle, 8-row groups 1024 bytes apart)
+  const uint64_t dS = tc::make_sdesc(sbase + OFF_SHI, 16 * KB, 1024);     // MN-major [c][j]; lo at +16 KB
+  const uint64_t dTT = tc::make_sdesc(sbase + OFF_TT, 16, 1024);          // K-major T''/T' hi, lo
+  const uint64_t dDl = tc::make_sdesc(sbase + OFF_TT, 8 * KB, 1024);      // MN-major Delta / Dt hi, lo
+  const uint64_t dP = tc::make_sdesc(sbase + OFF_P, 16, 1024);            // K-major P hi, lo
+  const uint64_t dCW = tc::make_sdesc(sbase + OFF_CW, 16, 1024);          // K-major W codes / hi, lo
+  const uint64_t dStgK[2] = {tc::make_sdesc(sbase + 0 * kStageBytes, 16, 1024),
+                             tc::make_sdesc(sbase + 1 * kStageBytes, 16, 1024)};
+  const uint64_t dStgM[2] = {tc::make_sdesc(sbase + 0 * kStageBytes, 16 * KB, 1024),   // MN-major K^T / V / K
+                             tc::make_sdesc(sbase + 1 * kStageBytes, 16 * KB, 1024)};
+
   // ---- initial state: h0 (or zeros) -> TMEM S and the bf16 hi/lo operand ----
   const int64_t sb = ((int64_t)n * p.Hv + h) * 128 * p.dv + slab * 64;   // S[c][j] at sb + c dv + j
   {
     float s[32];
+    if (p.h0) {
+      const float4* src = reinterpret_cast<const float4*>(p.h0 + sb + (int64_t)lane128 * p.dv + col0);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) s[j] = p.h0 ? p.h0[sb + (int64_t)lane128 * p.dv + col0 + j] : 0.f;
+      for (int j = 0; j < 8; ++j) {
+        const float4 f = src[j];
+        s[4 * j] = f.x; s[4 * j + 1] = f.y; s[4 * j + 2] = f.z; s[4 * j + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) s[j] = 0.f;
+    }
     st32(tmem, lane0, TM_S + col0, s);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float hi = __bfloat162float(__float2bfloat16_rn(s[j]));
-      st_bf16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + j)), hi);
-      st_bf16(sm, OFF_SLO + tc::sw128(lane128, 2 * (col0 + j)), s[j] - hi);
+    for (int q = 0; q < 4; ++q) {
+      uint4 hi, lo;
+      split8(s + 8 * q, hi, lo);
+      const uint32_t off = tc::sw128(lane128, 2 * (col0 + 8 * q));
+      st16(sm, OFF_SHI + off, hi);
+      st16(sm, OFF_SLO + off, lo);
     }
     tc::tmem_st_wait();
   }
@@ -215,12 +268,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     if (tid == 0) {
       tc::tc_fence_after();
+      // G1 = [Q; K] K^T
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t kb = ks >> 2, sub = ks & 3;
-        const uint64_t a = tc::make_sdesc(stg + (kb ? ST_Q1 : ST_Q0) + sub * 32, 16, 1024);
-        const uint64_t b = tc::make_sdesc(stg + (kb ? ST_K1 : ST_K0) + sub * 32, 16, 1024);
-        tc::mma_bf16(tmem + TM_G1, a, b, IDESC_G1, ks > 0);
+        const uint32_t kb = ks >> 2, sub = (ks & 3) * 32;
+        tc::mma_bf16(tmem + TM_G1, dadv(dStgK[st], (kb ? ST_Q1 : ST_Q0) + sub),
+                     dadv(dStgK[st], (kb ? ST_K1 : ST_K0) + sub), IDESC_G1, ks > 0);
       }
       tc::mma_commit(bar_g1);
       if (ci + 1 < nchunks) issue_tma(ci + 1, st ^ 1);
@@ -242,8 +295,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       gb += __shfl_sync(0xffffffffu, ga, 31);
       const float gl = __shfl_sync(0xffffffffu, gb, 31);
       vgam[r0] = ga; vgam[r1] = gb;
-      vegam[r0] = expf(ga); vegam[r1] = expf(gb);
-      vdec[r0] = expf(gl - ga); vdec[r1] = expf(gl - gb);
+      vegam[r0] = __expf(ga); vegam[r1] = __expf(gb);
+      vdec[r0] = __expf(gl - ga); vdec[r1] = __expf(gl - gb);
       vbeta[r0] = ba; vbeta[r1] = bb;
     }
     __syncthreads();
@@ -254,22 +307,35 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (ok) {
       float v[32];
       ld32(tmem, lane0, TM_G1 + col0, v);
-      if (quad < 2) {   // G1 rows 0..63: Q K^T
+      if (quad < 2) {   // G1 rows 0..63: Q K^T -> P (bf16 hi / lo, K-major [r][i])
         const int r = lane128;
         const float gr = vgam[r];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int i = col0 + j;
-          const float pv = i <= r ? __expf(gr - vgam[i]) * v[j] : 0.f;
-          st_f32(sm, OFF_P + (uint32_t)(i >> 5) * 8 * KB + tc::sw128(r, (i & 31) * 4), tc::to_tf32(pv));
+          v[j] = i <= r ? __expf(gr - vgam[i]) * v[j] : 0.f;
         }
-      } else {          // G1 rows 64..127: K K^T
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 hi, lo;
+          split8(v + 8 * q, hi, lo);
+          const uint32_t off = tc::sw128(r, 2 * (col0 + 8 * q));
+          st16(sm, OFF_P + off, hi);
+          st16(sm, OFF_P + 8 * KB + off, lo);
+        }
+      } else {          // G1 rows 64..127: K K^T -> A (fp32 rows)
         const int r = lane128 - 64;
         const float gr = vgam[r], br = vbeta[r];
+        float4* dst = reinterpret_cast<float4*>(Am + r * A_LD + col0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int i = col0 + j;
-          Am[r * A_LD + i] = i < r ? br * __expf(gr - vgam[i]) * v[j] : 0.f;
+        for (int j = 0; j < 32; j += 4) {
+          float a4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = col0 + j + u;
+            a4[u] = i < r ? br * __expf(gr - vgam[i]) * v[j + u] : 0.f;
+          }
+          dst[j >> 2] = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
       }
     }
@@ -283,9 +349,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       if (tid < 64) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float acc = (r == jj) ? 1.f : 0.f;
+          const float* arow = Am + (b0 + r) * A_LD + b0;
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;   // split accumulators: shorter chains
 #pragma unroll
-          for (int i = 0; i < r; ++i) acc = fmaf(-Am[(b0 + r) * A_LD + b0 + i], x[i], acc);
+          for (int i = 0; i < r; ++i) {
+            const float t = arow[i] * x[i];
+            if ((i & 3) == 0) a0 += t;
+            else if ((i & 3) == 1) a1 += t;
+            else if ((i & 3) == 2) a2 += t;
+            else a3 += t;
+          }
+          const float acc = ((r == jj) ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
           x[r] = r < jj ? 0.f : acc;
         }
       }
@@ -298,32 +372,49 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const int rr = tid >> 4, cc = tid & 15;
       for (int bi = 1; bi < 4; ++bi) {
         for (int bj = 0; bj < bi; ++bj) {
-          float acc = 0.f;
-          for (int m = bj * 16; m < bi * 16; ++m) acc = fmaf(Am[(bi * 16 + rr) * A_LD + m], Am[m * A_LD + bj * 16 + cc], acc);
-          scr[rr * 48 + bj * 16 + cc] = acc;
+          float s0 = 0.f, s1 = 0.f;
+          for (int m = bj * 16; m < bi * 16; m += 2) {
+            s0 = fmaf(Am[(bi * 16 + rr) * A_LD + m], Am[m * A_LD + bj * 16 + cc], s0);
+            s1 = fmaf(Am[(bi * 16 + rr) * A_LD + m + 1], Am[(m + 1) * A_LD + bj * 16 + cc], s1);
+          }
+          scr[rr * 48 + bj * 16 + cc] = s0 + s1;
         }
         __syncthreads();
         for (int bj = 0; bj < bi; ++bj) {
-          float acc = 0.f;
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) acc = fmaf(Am[(bi * 16 + rr) * A_LD + bi * 16 + m], scr[m * 48 + bj * 16 + cc], acc);
-          Am[(bi * 16 + rr) * A_LD + bj * 16 + cc] = -acc;
+          for (int m = 0; m < 16; m += 2) {
+            s0 = fmaf(Am[(bi * 16 + rr) * A_LD + bi * 16 + m], scr[m * 48 + bj * 16 + cc], s0);
+            s1 = fmaf(Am[(bi * 16 + rr) * A_LD + bi * 16 + m + 1], scr[(m + 1) * 48 + bj * 16 + cc], s1);
+          }
+          Am[(bi * 16 + rr) * A_LD + bj * 16 + cc] = -(s0 + s1);
         }
         __syncthreads();
       }
     }
     // ---- T'' = T diag(beta), T' = T'' diag(Gam) as bf16 hi + lo, K-major [r][i] ----
-    for (int e = tid; e < 64 * 64; e += kThreads) {
-      const int r = e >> 6, i = e & 63;
-      const float t2 = Am[r * A_LD + i] * vbeta[i];
-      const float t1 = t2 * vegam[i];
-      const uint32_t off = tc::sw128(r, 2 * i);
-      const float h2 = __bfloat162float(__float2bfloat16_rn(t2));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(t1));
-      st_bf16(sm, OFF_TT + off, h2);
-      st_bf16(sm, OFF_TT + 8 * KB + off, t2 - h2);
-      st_bf16(sm, OFF_TT + 16 * KB + off, h1);
-      st_bf16(sm, OFF_TT + 24 * KB + off, t1 - h1);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int task = tid + t * kThreads;   // 64 rows x 8 groups of 8 columns
+      const int r = task >> 3, i0 = (task & 7) * 8;
+      const float4 ta = *reinterpret_cast<const float4*>(Am + r * A_LD + i0);
+      const float4 tb = *reinterpret_cast<const float4*>(Am + r * A_LD + i0 + 4);
+      const float4 ba = *reinterpret_cast<const float4*>(vbeta + i0);
+      const float4 bb = *reinterpret_cast<const float4*>(vbeta + i0 + 4);
+      const float4 ea = *reinterpret_cast<const float4*>(vegam + i0);
+      const float4 eb = *reinterpret_cast<const float4*>(vegam + i0 + 4);
+      float t2[8] = {ta.x * ba.x, ta.y * ba.y, ta.z * ba.z, ta.w * ba.w,
+                     tb.x * bb.x, tb.y * bb.y, tb.z * bb.z, tb.w * bb.w};
+      float t1[8] = {t2[0] * ea.x, t2[1] * ea.y, t2[2] * ea.z, t2[3] * ea.w,
+                     t2[4] * eb.x, t2[5] * eb.y, t2[6] * eb.z, t2[7] * eb.w};
+      const uint32_t off = tc::sw128(r, 2 * i0);
+      uint4 hi, lo;
+      split8(t2, hi, lo);
+      st16(sm, OFF_TT + off, hi);
+      st16(sm, OFF_TT + 8 * KB + off, lo);
+      split8(t1, hi, lo);
+      st16(sm, OFF_TT + 16 * KB + off, hi);
+      st16(sm, OFF_TT + 24 * KB + off, lo);
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
@@ -333,37 +424,38 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::make_sdesc(sbase + OFF_TT + part * 8 * KB + ks * 32, 16, 1024);
-          const uint64_t b = tc::make_sdesc(stg + ST_V + ks * 2048, 8 * KB, 1024);
-          tc::mma_bf16(tmem + TM_U, a, b, IDESC_U, (part | ks) != 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_U, dadv(dTT, part * 8 * KB + ks * 32), dadv(dStgM[st], ST_V + ks * 2048), IDESC_U,
+                       (part | ks) != 0);
       tc::mma_commit(bar_u);
-      // W^T = K^T T'^T: A = K^T (MN-major, the two 64-column K blocks 16 KB apart), B = T' (K-major)
+      // W = T' K: A = T' (K-major), B = K (MN-major: the two 64-column blocks 16 KB apart)
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::make_sdesc(stg + ST_K0 + ks * 2048, 16 * KB, 1024);
-          const uint64_t b = tc::make_sdesc(sbase + OFF_TT + 16 * KB + part * 8 * KB + ks * 32, 16, 1024);
-          tc::mma_bf16(tmem + TM_W, a, b, IDESC_W, (part | ks) != 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_W, dadv(dTT, 16 * KB + part * 8 * KB + ks * 32), dadv(dStgM[st], ST_K0 + ks * 2048),
+                       IDESC_W, (part | ks) != 0);
       tc::mma_commit(bar_w);
     }
 
-    // ---- W QDQ (one scale per chunk) -> W operand for X ----
+    // ---- W QDQ (one scale per chunk) -> W operand [r][c] for X ----
     wait(bar_w, par);
     tc::tc_fence_after();
     float sW = 1.f;
     {
-      float w[32];
-      if (ok) ld32(tmem, lane0, TM_W + col0, w);   // w[j] = W[r = col0 + j][c = lane128]
-      const int c = lane128;
-      const uint32_t cbase = OFF_CW + (uint32_t)(c >> 6) * 8 * KB;
+      float w[64];   // row r = row64, columns [64 half, 64 half + 64)
+      if (ok) {
+        ld32(tmem, lane0, TM_W + half * 64, w);
+        ld32(tmem, lane0, TM_W + half * 64 + 32, w + 32);
+      }
+      const bool act = lt < 16;
+      const uint32_t abase = OFF_CW + (uint32_t)half * 8 * KB;
       if (p.w_qdq) {
         float m = 0.f;
+        if (act) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(w[j]));
+          for (int j = 0; j < 64; ++j) m = fmaxf(m, fabsf(w[j]));
+        }
         m = warp_max(m);
         if (lt == 0) red[warp] = m;
         __syncthreads();
@@ -371,14 +463,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
         for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
         sW = qdq_scale(amax);
+        const float rW = __frcp_rn(sW);
+        if (act) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) st_bf16(sm, cbase + tc::sw128(col0 + j, 2 * (c & 63)), e4m3_code(w[j], sW));
-      } else {
+          for (int q = 0; q < 8; ++q) {
+            float c[8], d[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float hi = __bfloat162float(__float2bfloat16_rn(w[j]));
-          st_bf16(sm, cbase + tc::sw128(col0 + j, 2 * (c & 63)), hi);
-          st_bf16(sm, cbase + 16 * KB + tc::sw128(col0 + j, 2 * (c & 63)), w[j] - hi);
+            for (int u = 0; u < 8; u += 2) qdq_pair(w[8 * q + u], w[8 * q + u + 1], rW, sW, c[u], c[u + 1], d[u], d[u + 1]);
+            st16(sm, abase + tc::sw128(row64, 16 * q), pack8(c));
+          }
+        }
+      } else if (act) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 hi, lo;
+          split8(w + 8 * q, hi, lo);
+          st16(sm, abase + tc::sw128(row64, 16 * q), hi);
+          st16(sm, abase + 16 * KB + tc::sw128(row64, 16 * q), lo);
         }
       }
     }
@@ -390,30 +491,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       // X = W S0 (M=64, N=64, K=128): (codes or W hi) x (S hi or codes) [+ W hi x S lo] [+ W lo x S hi]
       uint32_t aoff[3], boff[3];
       int np = 0;
-      aoff[np] = OFF_CW; boff[np++] = OFF_SHI;
-      if (!s_exact) { aoff[np] = OFF_CW; boff[np++] = OFF_SLO; }
-      if (!p.w_qdq) { aoff[np] = OFF_CW + 16 * KB; boff[np++] = OFF_SHI; }
+      aoff[np] = 0; boff[np++] = 0;
+      if (!s_exact) { aoff[np] = 0; boff[np++] = 16 * KB; }
+      if (!p.w_qdq) { aoff[np] = 16 * KB; boff[np++] = 0; }
       for (int q = 0; q < np; ++q)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = tc::make_sdesc(sbase + aoff[q] + (ks >> 2) * 8 * KB + (ks & 3) * 32, 16, 1024);
-          const uint64_t b = tc::make_sdesc(sbase + boff[q] + ks * 2048, 16 * KB, 1024);
-          tc::mma_bf16(tmem + TM_X, a, b, IDESC_XY, (q | ks) != 0);
-        }
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tmem + TM_X, dadv(dCW, aoff[q] + (ks >> 2) * 8 * KB + (ks & 3) * 32), dadv(dS, boff[q] + ks * 2048),
+                       IDESC_XY, (q | ks) != 0);
       tc::mma_commit(bar_x);
       // Y = Q S0: A = Q (the 64 Q rows of each 128-byte K block), B = S operand
       const int ny = s_exact ? 1 : 2;
       for (int q = 0; q < ny; ++q)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = tc::make_sdesc(stg + ((ks >> 2) ? ST_Q1 : ST_Q0) + (ks & 3) * 32, 16, 1024);
-          const uint64_t b = tc::make_sdesc(sbase + (q ? OFF_SLO : OFF_SHI) + ks * 2048, 16 * KB, 1024);
-          tc::mma_bf16(tmem + TM_Y, a, b, IDESC_XY, (q | ks) != 0);
-        }
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tmem + TM_Y, dadv(dStgK[st], ((ks >> 2) ? ST_Q1 : ST_Q0) + (ks & 3) * 32),
+                       dadv(dS, q * 16 * KB + ks * 2048), IDESC_XY, (q | ks) != 0);
       tc::mma_commit(bar_y);
     }
 
-    // ---- Delta = U - W S0 -> Delta^T (tf32, for P Delta) and Dt = decay Delta (bf16 hi/lo) ----
+    // ---- Delta = U - W S0 -> Delta (bf16 hi/lo, for P Delta) and Dt = decay Delta (hi/lo), MN-major [i][j] ----
     wait(bar_u, par);
     wait(bar_x, par);
     tc::tc_fence_after();
@@ -425,14 +522,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int r = row64;
         const float f = sW * s_scale, dr = vdec[r];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int jc = col0 + j;
-          const float d = uv[j] - f * xv[j];
-          st_f32(sm, OFF_TT + (uint32_t)(r >> 5) * 8 * KB + tc::sw128(jc, (r & 31) * 4), tc::to_tf32(d));
-          const float dt = dr * d;
-          const float hi = __bfloat162float(__float2bfloat16_rn(dt));
-          st_bf16(sm, OFF_TT + 16 * KB + tc::sw128(r, 2 * jc), hi);
-          st_bf16(sm, OFF_TT + 24 * KB + tc::sw128(r, 2 * jc), dt - hi);
+        for (int q = 0; q < 4; ++q) {
+          float d[8], dt[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            d[u] = fmaf(-f, xv[8 * q + u], uv[8 * q + u]);
+            dt[u] = dr * d[u];
+          }
+          const uint32_t off = tc::sw128(r, 2 * (col0 + 8 * q));
+          uint4 hi, lo;
+          split8(d, hi, lo);
+          st16(sm, OFF_TT + off, hi);
+          st16(sm, OFF_TT + 8 * KB + off, lo);
+          split8(dt, hi, lo);
+          st16(sm, OFF_TT + 16 * KB + off, hi);
+          st16(sm, OFF_TT + 24 * KB + off, lo);
         }
       }
     }
@@ -441,23 +545,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     if (tid == 0) {
       tc::tc_fence_after();
-      // P Delta (tf32): A = P [r][i], B = Delta^T [j][i], both K-major
+      // P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi: A = P (K-major [r][i]), B = Delta (MN-major [i][j])
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t a = tc::make_sdesc(sbase + OFF_P + (ks >> 2) * 8 * KB + (ks & 3) * 32, 16, 1024);
-        const uint64_t b = tc::make_sdesc(sbase + OFF_TT + (ks >> 2) * 8 * KB + (ks & 3) * 32, 16, 1024);
-        tc::mma_tf32(tmem + TM_G1, a, b, IDESC_PD, ks != 0);
-      }
+      for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_G1, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32), dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048),
+                       IDESC_XY, (q | ks) != 0);
       tc::mma_commit(bar_pd);
       // C = K^T Dt: A = K^T (MN-major), B = Dt hi / lo (MN-major [i][j])
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::make_sdesc(stg + ST_K0 + ks * 2048, 16 * KB, 1024);
-          const uint64_t b = tc::make_sdesc(sbase + OFF_TT + 16 * KB + part * 8 * KB + ks * 2048, 8 * KB, 1024);
-          tc::mma_bf16(tmem + TM_C, a, b, IDESC_C, (part | ks) != 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_C, dadv(dStgM[st], ST_K0 + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
+                       IDESC_C, (part | ks) != 0);
       tc::mma_commit(bar_c);
     }
 
@@ -504,21 +606,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         float amax = red[0];
 #pragma unroll
         for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-        const float sS = qdq_scale(amax);
+        const float sS = qdq_scale(amax), rS = __frcp_rn(sS);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float code = e4m3_code(s0[j], sS);
-          s0[j] = __fmul_rn(code, sS);
-          st_bf16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + j)), code);
+        for (int qq = 0; qq < 4; ++qq) {
+          float c[8];
+#pragma unroll
+          for (int u = 0; u < 8; u += 2)
+            qdq_pair(s0[8 * qq + u], s0[8 * qq + u + 1], rS, sS, c[u], c[u + 1], s0[8 * qq + u], s0[8 * qq + u + 1]);
+          st16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + 8 * qq)), pack8(c));
         }
         s_exact = true;
         s_scale = sS;
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float hi = __bfloat162float(__float2bfloat16_rn(s0[j]));
-          st_bf16(sm, OFF_SHI + tc::sw128(lane128, 2 * (col0 + j)), hi);
-          st_bf16(sm, OFF_SLO + tc::sw128(lane128, 2 * (col0 + j)), s0[j] - hi);
+        for (int qq = 0; qq < 4; ++qq) {
+          uint4 hi, lo;
+          split8(s0 + 8 * qq, hi, lo);
+          const uint32_t off = tc::sw128(lane128, 2 * (col0 + 8 * qq));
+          st16(sm, OFF_SHI + off, hi);
+          st16(sm, OFF_SLO + off, lo);
         }
         s_exact = false;
         s_scale = 1.f;
