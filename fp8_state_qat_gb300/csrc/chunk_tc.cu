@@ -12,7 +12,8 @@
 //   TMA      Q, K [64 x 128] and V [64 x 64] bf16 tiles (128-byte swizzle), next chunk prefetched
 //   G1       [Q; K] K^T                         tcgen05 bf16, M=128 N=64 K=128 (exact products)
 //   A, P     A[r][i] = beta_r exp(gam_r - gam_i) (k_r.k_i), i < r;  P[r][i] = exp(gam_r - gam_i)(q_r.k_i), i <= r
-//   T        (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then block rows (CUDA cores)
+//   T        (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then the off-diagonal
+//            blocks in three levels of the block recurrence (CUDA cores)
 //   U        T'' V,  T'' = T diag(beta)         bf16 (T'' as hi + lo), M=64 N=64 K=64
 //   W        T' K,   T' = T diag(beta Gam)      bf16 (T' as hi + lo), M=64 N=128 K=64
 //   W QDQ    one E4M3 scale over the chunk's W; the codes (exact in bf16) become the operand
@@ -49,9 +50,9 @@ constexpr uint32_t OFF_TT = 112 * KB;   // T'' hi, lo, T' hi, lo (8 KB each, [r]
                                         // later Delta hi, lo and Dt hi, lo ([i][j] MN-major)
 constexpr uint32_t OFF_P = 144 * KB;    // P hi, lo bf16 [64 r][64 i] K-major (8 KB each)
 constexpr uint32_t OFF_CW = 160 * KB;   // W codes (or W hi) bf16 [64 r][128 c] K-major; W lo at +16 KB
-constexpr uint32_t OFF_A = 192 * KB;    // fp32 A [64][68], solved into T in place
+constexpr uint32_t OFF_A = 192 * KB;    // fp32 A [64][68] (T is built in the OFF_TT region)
 constexpr uint32_t A_LD = 68;
-constexpr uint32_t OFF_SCR = OFF_A + 64 * A_LD * 4;   // solve scratch 16 x 48 fp32
+constexpr uint32_t OFF_SCR = OFF_A + 64 * A_LD * 4;   // solve scratch 3 x 16 x 16 fp32
 constexpr uint32_t OFF_VEC = OFF_SCR + 16 * 48 * 4;   // gam, Gam, decay-to-end, beta [64] each
 constexpr uint32_t OFF_RED = OFF_VEC + 4 * 64 * 4;    // 8 partial maxima
 constexpr uint32_t kSmemBytes = OFF_RED + 64 + 1024;  // + slack to align the base to 1024
@@ -257,6 +258,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   };
   if (warp == 0 && nchunks > 0) load_gates(0);
 
+  // wait for chunk cj's tiles, then issue its G1 = [Q; K] K^T and the TMA of chunk cj + 1
+  auto start_chunk = [&](int64_t cj) {
+    const int sj = (int)(cj & 1);
+    wait(bar_tma0 + 8u * (uint32_t)sj, (uint32_t)((cj >> 1) & 1));
+    if (__syncthreads_or(!ok)) return false;
+    if (tid == 0) {
+      tc::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t kb = ks >> 2, sub = (ks & 3) * 32;
+        tc::mma_bf16(tmem + TM_G1, dadv(dStgK[sj], (kb ? ST_Q1 : ST_Q0) + sub),
+                     dadv(dStgK[sj], (kb ? ST_K1 : ST_K0) + sub), IDESC_G1, ks > 0);
+      }
+      tc::mma_commit(bar_g1);
+      if (cj + 1 < nchunks) issue_tma(cj + 1, sj ^ 1);
+    }
+    if (cj + 1 < nchunks) tma_issued = cj + 2;
+    return true;
+  };
+
   for (int64_t ci = 0; ci < nchunks; ++ci) {
     const int st = (int)(ci & 1);
     const uint32_t stg = sbase + (uint32_t)st * kStageBytes;
@@ -264,22 +285,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     const int L = (len - c0) < 64 ? (int)(len - c0) : 64;
     const uint32_t par = (uint32_t)(ci & 1);
 
-    wait(bar_tma0 + 8u * (uint32_t)st, (uint32_t)((ci >> 1) & 1));
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-    if (tid == 0) {
-      tc::tc_fence_after();
-      // G1 = [Q; K] K^T
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t kb = ks >> 2, sub = (ks & 3) * 32;
-        tc::mma_bf16(tmem + TM_G1, dadv(dStgK[st], (kb ? ST_Q1 : ST_Q0) + sub),
-                     dadv(dStgK[st], (kb ? ST_K1 : ST_K0) + sub), IDESC_G1, ks > 0);
-      }
-      tc::mma_commit(bar_g1);
-      if (ci + 1 < nchunks) issue_tma(ci + 1, st ^ 1);
+    if (ci == 0) {
+      if (!start_chunk(0)) { aborted = true; break; }
     }
-    if (ci + 1 < nchunks) tma_issued = ci + 2;
 
+    const float y_scale = s_scale;   // scale of this chunk's S0 operand (Y = Q S0); s_scale moves on below
     // ---- gates: prefix sums of g (in-chunk), Gam, decay to the chunk end, beta ----
     if (warp == 0) {
       const int r0 = lt, r1 = lt + 32;
@@ -311,9 +321,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int r = lane128;
         const float gr = vgam[r];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 32; ++j) {   // the exponent is clamped so both select inputs are finite
           const int i = col0 + j;
-          v[j] = i <= r ? __expf(gr - vgam[i]) * v[j] : 0.f;
+          const float e = __expf(fminf(gr - vgam[i], 0.f)) * v[j];
+          v[j] = i <= r ? e : 0.f;
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -333,7 +344,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int i = col0 + j + u;
-            a4[u] = i < r ? br * __expf(gr - vgam[i]) * v[j + u] : 0.f;
+            const float e = br * __expf(fminf(gr - vgam[i], 0.f)) * v[j + u];
+            a4[u] = i < r ? e : 0.f;
           }
           dst[j >> 2] = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
@@ -342,11 +354,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc::tc_fence_before();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
 
-    // ---- T = (I + A)^{-1} in place: diagonal blocks, then block rows ----
+    // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution (into the T
+    // buffer), then the off-diagonal blocks by levels of the block recurrence
+    // T_ij = -T_ii sum_{j <= m < i} A_im T_mj  (level 1: i - j = 1, level 2: 2, level 3: 3)
+    float* Tm = reinterpret_cast<float*>(sm + OFF_TT);   // fp32 [64][A_LD]; T''/T' overwrite it below
     {
-      float x[16];
       const int b0 = (tid >> 4) * 16, jj = tid & 15;
       if (tid < 64) {
+        float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           const float* arow = Am + (b0 + r) * A_LD + b0;
@@ -362,59 +377,98 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           const float acc = ((r == jj) ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
           x[r] = r < jj ? 0.f : acc;
         }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tm[(b0 + r) * A_LD + b0 + jj] = x[r];
+        // the blocks above the diagonal are zero
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+#pragma unroll
+          for (int bb = 1; bb < 4; ++bb)
+            if (bb * 16 > b0) Tm[(b0 + r) * A_LD + bb * 16 + jj] = 0.f;
       }
       __syncthreads();
-      if (tid < 64) {
+      // level tasks: one 1 x 4 tile (row rr, columns 4 c4 .. 4 c4 + 3) of a 16 x 16 block per thread
+      const int blk = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+      // Y tile of block (bi, bj): sum_{m < 16 (bi - bj)} A[16 bi + rr][16 bj + m] T[16 bj + m][16 bj + c4 ..]
+      auto ytile = [&](int bi, int bj, float* y) {
+        y[0] = y[1] = y[2] = y[3] = 0.f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Am[(b0 + r) * A_LD + b0 + jj] = x[r];
-      }
+        for (int m = 0; m < 16 * (bi - bj); ++m) {
+          const float a = Am[(bi * 16 + rr) * A_LD + bj * 16 + m];
+          const float4 t = *reinterpret_cast<const float4*>(Tm + (bj * 16 + m) * A_LD + bj * 16 + c4);
+          y[0] = fmaf(a, t.x, y[0]); y[1] = fmaf(a, t.y, y[1]); y[2] = fmaf(a, t.z, y[2]); y[3] = fmaf(a, t.w, y[3]);
+        }
+      };
+      // T tile of block (bi, bj) = -T_ii Y, Y a 16 x 16 scratch block
+      auto ttile = [&](int bi, int bj, const float* Y) {
+        float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float a = Tm[(bi * 16 + rr) * A_LD + bi * 16 + m];
+          const float4 y = *reinterpret_cast<const float4*>(Y + m * 16 + c4);
+          t4[0] = fmaf(a, y.x, t4[0]); t4[1] = fmaf(a, y.y, t4[1]); t4[2] = fmaf(a, y.z, t4[2]); t4[3] = fmaf(a, y.w, t4[3]);
+        }
+        *reinterpret_cast<float4*>(Tm + (bi * 16 + rr) * A_LD + bj * 16 + c4) = make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
+      };
+      auto put = [&](float* Y, const float* y) {
+        *reinterpret_cast<float4*>(Y + rr * 16 + c4) = make_float4(y[0], y[1], y[2], y[3]);
+      };
+      float y[4];
+      // level 1: blocks (1,0) (2,1) (3,2), 64 threads each
+      if (blk < 3) { ytile(blk + 1, blk, y); put(scr + blk * 256, y); }
       __syncthreads();
-      const int rr = tid >> 4, cc = tid & 15;
-      for (int bi = 1; bi < 4; ++bi) {
-        for (int bj = 0; bj < bi; ++bj) {
-          float s0 = 0.f, s1 = 0.f;
-          for (int m = bj * 16; m < bi * 16; m += 2) {
-            s0 = fmaf(Am[(bi * 16 + rr) * A_LD + m], Am[m * A_LD + bj * 16 + cc], s0);
-            s1 = fmaf(Am[(bi * 16 + rr) * A_LD + m + 1], Am[(m + 1) * A_LD + bj * 16 + cc], s1);
-          }
-          scr[rr * 48 + bj * 16 + cc] = s0 + s1;
-        }
-        __syncthreads();
-        for (int bj = 0; bj < bi; ++bj) {
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; m += 2) {
-            s0 = fmaf(Am[(bi * 16 + rr) * A_LD + bi * 16 + m], scr[m * 48 + bj * 16 + cc], s0);
-            s1 = fmaf(Am[(bi * 16 + rr) * A_LD + bi * 16 + m + 1], scr[(m + 1) * 48 + bj * 16 + cc], s1);
-          }
-          Am[(bi * 16 + rr) * A_LD + bj * 16 + cc] = -(s0 + s1);
-        }
-        __syncthreads();
-      }
+      if (blk < 3) ttile(blk + 1, blk, scr + blk * 256);
+      __syncthreads();
+      // level 2: blocks (2,0) (3,1)
+      if (blk < 2) { ytile(blk + 2, blk, y); put(scr + blk * 256, y); }
+      __syncthreads();
+      if (blk < 2) ttile(blk + 2, blk, scr + blk * 256);
+      __syncthreads();
+      // level 3: block (3,0)
+      if (blk == 0) { ytile(3, 0, y); put(scr, y); }
+      __syncthreads();
+      if (blk == 0) ttile(3, 0, scr);
+      __syncthreads();
     }
     // ---- T'' = T diag(beta), T' = T'' diag(Gam) as bf16 hi + lo, K-major [r][i] ----
+    // (T is read into registers first: the outputs overwrite the T buffer)
+    {
+      float tv[2][8];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const int task = tid + t * kThreads;   // 64 rows x 8 groups of 8 columns
-      const int r = task >> 3, i0 = (task & 7) * 8;
-      const float4 ta = *reinterpret_cast<const float4*>(Am + r * A_LD + i0);
-      const float4 tb = *reinterpret_cast<const float4*>(Am + r * A_LD + i0 + 4);
-      const float4 ba = *reinterpret_cast<const float4*>(vbeta + i0);
-      const float4 bb = *reinterpret_cast<const float4*>(vbeta + i0 + 4);
-      const float4 ea = *reinterpret_cast<const float4*>(vegam + i0);
-      const float4 eb = *reinterpret_cast<const float4*>(vegam + i0 + 4);
-      float t2[8] = {ta.x * ba.x, ta.y * ba.y, ta.z * ba.z, ta.w * ba.w,
-                     tb.x * bb.x, tb.y * bb.y, tb.z * bb.z, tb.w * bb.w};
-      float t1[8] = {t2[0] * ea.x, t2[1] * ea.y, t2[2] * ea.z, t2[3] * ea.w,
-                     t2[4] * eb.x, t2[5] * eb.y, t2[6] * eb.z, t2[7] * eb.w};
-      const uint32_t off = tc::sw128(r, 2 * i0);
-      uint4 hi, lo;
-      split8(t2, hi, lo);
-      st16(sm, OFF_TT + off, hi);
-      st16(sm, OFF_TT + 8 * KB + off, lo);
-      split8(t1, hi, lo);
-      st16(sm, OFF_TT + 16 * KB + off, hi);
-      st16(sm, OFF_TT + 24 * KB + off, lo);
+      for (int t = 0; t < 2; ++t) {
+        const int task = tid + t * kThreads;   // 64 rows x 8 groups of 8 columns
+        const int r = task >> 3, i0 = (task & 7) * 8;
+        const float4 ta = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
+        const float4 tb = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
+        tv[t][0] = ta.x; tv[t][1] = ta.y; tv[t][2] = ta.z; tv[t][3] = ta.w;
+        tv[t][4] = tb.x; tv[t][5] = tb.y; tv[t][6] = tb.z; tv[t][7] = tb.w;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int task = tid + t * kThreads;
+        const int r = task >> 3, i0 = (task & 7) * 8;
+        const float4 ba = *reinterpret_cast<const float4*>(vbeta + i0);
+        const float4 bb = *reinterpret_cast<const float4*>(vbeta + i0 + 4);
+        const float4 ea = *reinterpret_cast<const float4*>(vegam + i0);
+        const float4 eb = *reinterpret_cast<const float4*>(vegam + i0 + 4);
+        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+        const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+        float t2[8], t1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          t2[u] = tv[t][u] * bv[u];
+          t1[u] = t2[u] * ev[u];
+        }
+        const uint32_t off = tc::sw128(r, 2 * i0);
+        uint4 hi, lo;
+        split8(t2, hi, lo);
+        st16(sm, OFF_TT + off, hi);
+        st16(sm, OFF_TT + 8 * KB + off, lo);
+        split8(t1, hi, lo);
+        st16(sm, OFF_TT + 16 * KB + off, hi);
+        st16(sm, OFF_TT + 24 * KB + off, lo);
+      }
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
@@ -550,7 +604,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       for (int q = 0; q < 3; ++q)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_G1, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32), dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048),
+          tc::mma_bf16(tmem + TM_X, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32), dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048),
                        IDESC_XY, (q | ks) != 0);
       tc::mma_commit(bar_pd);
       // C = K^T Dt: A = K^T (MN-major), B = Dt hi / lo (MN-major [i][j])
@@ -561,25 +615,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           tc::mma_bf16(tmem + TM_C, dadv(dStgM[st], ST_K0 + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
                        IDESC_C, (part | ks) != 0);
       tc::mma_commit(bar_c);
-    }
-
-    // ---- outputs: o = scale (Gam Y + P Delta) for rows r < L ----
-    wait(bar_y, par);
-    wait(bar_pd, par);
-    tc::tc_fence_after();
-    if (ok) {
-      float yv[32], pv[32];
-      ld32(tmem, lane0, TM_Y + col0, yv);
-      ld32(tmem, lane0, TM_G1 + col0, pv);
-      if (lt < 16 && row64 < L) {
-        const int r = row64;
-        const float er = vegam[r] * s_scale;
-        float4* out = reinterpret_cast<float4*>(p.o + ((t0 + c0 + r) * p.Hv + h) * (int64_t)p.dv + slab * 64 + col0);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          out[j >> 2] = make_float4(p.scale * fmaf(er, yv[j], pv[j]), p.scale * fmaf(er, yv[j + 1], pv[j + 1]),
-                                    p.scale * fmaf(er, yv[j + 2], pv[j + 2]), p.scale * fmaf(er, yv[j + 3], pv[j + 3]));
-      }
     }
 
     // ---- S1 = Gam_L S0 + C, state QDQ at the 64-token boundary ----
@@ -636,6 +671,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc::tc_fence_before();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     tc::tc_fence_after();
+    // the next chunk's G1 runs on the tensor cores while this chunk's outputs are written
+    if (ci + 1 < nchunks && !start_chunk(ci + 1)) { aborted = true; break; }
+    // ---- outputs: o = scale (Gam Y + P Delta) for rows r < L ----
+    wait(bar_y, par);
+    wait(bar_pd, par);
+    tc::tc_fence_after();
+    if (ok) {
+      float yv[32], pv[32];
+      ld32(tmem, lane0, TM_Y + col0, yv);
+      ld32(tmem, lane0, TM_X + col0, pv);
+      if (lt < 16 && row64 < L) {
+        const int r = row64;
+        const float er = vegam[r] * y_scale;
+        float4* out = reinterpret_cast<float4*>(p.o + ((t0 + c0 + r) * p.Hv + h) * (int64_t)p.dv + slab * 64 + col0);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          out[j >> 2] = make_float4(p.scale * fmaf(er, yv[j], pv[j]), p.scale * fmaf(er, yv[j + 1], pv[j + 1]),
+                                    p.scale * fmaf(er, yv[j + 2], pv[j + 2]), p.scale * fmaf(er, yv[j + 3], pv[j + 3]));
+      }
+    }
+
+    __syncthreads();   // the gate vectors are rewritten by the next chunk
   }
 
   if (!aborted && p.hT) {
