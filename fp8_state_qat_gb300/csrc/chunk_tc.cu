@@ -53,8 +53,8 @@ constexpr uint32_t OFF_CW = 160 * KB;   // W codes (or W hi) bf16 [64 r][128 c] 
 constexpr uint32_t OFF_A = 192 * KB;    // fp32 A [64][68] (T is built in the OFF_TT region)
 constexpr uint32_t A_LD = 68;
 constexpr uint32_t OFF_SCR = OFF_A + 64 * A_LD * 4;   // solve scratch 3 x 16 x 16 fp32
-constexpr uint32_t OFF_VEC = OFF_SCR + 16 * 48 * 4;   // gam, Gam, decay-to-end, beta [64] each
-constexpr uint32_t OFF_RED = OFF_VEC + 4 * 64 * 4;    // 8 partial maxima
+constexpr uint32_t OFF_VEC = OFF_SCR + 16 * 48 * 4;   // 2 x {gam, Gam, decay-to-end, beta} [64] (by chunk parity)
+constexpr uint32_t OFF_RED = OFF_VEC + 2 * 4 * 64 * 4;  // 8 partial maxima
 constexpr uint32_t kSmemBytes = OFF_RED + 64 + 1024;  // + slack to align the base to 1024
 
 // TMEM columns (fp32 accumulators; M=64 results use lanes 32 q + (0..15))
@@ -158,10 +158,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     t0 = (int64_t)n * p.T;
     len = p.T;
   }
-  float* vgam = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* vegam = vgam + 64;
-  float* vdec = vgam + 128;
-  float* vbeta = vgam + 192;
+  float* const vecs = reinterpret_cast<float*>(sm + OFF_VEC);
   float* red = reinterpret_cast<float*>(sm + OFF_RED);
   float* Am = reinterpret_cast<float*>(sm + OFF_A);
   float* scr = reinterpret_cast<float*>(sm + OFF_SCR);
@@ -257,6 +254,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     nbb = lt + 32 < Lj ? p.beta[base + (int64_t)(lt + 32) * p.Hv] : 0.f;
   };
   if (warp == 0 && nchunks > 0) load_gates(0);
+  // warp 0: prefix sums of g inside chunk cj, Gam, decay to the chunk end, beta -> vecs[cj & 1]
+  auto gates = [&](int64_t cj) {
+    float* vg = vecs + (cj & 1) * 256;
+    const int r0 = lt, r1 = lt + 32;
+    float ga = nga, gb = ngb;
+    const float ba = nba, bb = nbb;
+    if (cj + 1 < nchunks) load_gates(cj + 1);
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float ya = __shfl_up_sync(0xffffffffu, ga, off);
+      const float yb = __shfl_up_sync(0xffffffffu, gb, off);
+      if (lt >= off) { ga += ya; gb += yb; }
+    }
+    gb += __shfl_sync(0xffffffffu, ga, 31);
+    const float gl = __shfl_sync(0xffffffffu, gb, 31);
+    vg[r0] = ga; vg[r1] = gb;
+    vg[64 + r0] = __expf(ga); vg[64 + r1] = __expf(gb);
+    vg[128 + r0] = __expf(gl - ga); vg[128 + r1] = __expf(gl - gb);
+    vg[192 + r0] = ba; vg[192 + r1] = bb;
+  };
 
   // wait for chunk cj's tiles, then issue its G1 = [Q; K] K^T and the TMA of chunk cj + 1
   auto start_chunk = [&](int64_t cj) {
@@ -290,27 +307,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
 
     const float y_scale = s_scale;   // scale of this chunk's S0 operand (Y = Q S0); s_scale moves on below
-    // ---- gates: prefix sums of g (in-chunk), Gam, decay to the chunk end, beta ----
-    if (warp == 0) {
-      const int r0 = lt, r1 = lt + 32;
-      float ga = nga, gb = ngb;
-      const float ba = nba, bb = nbb;
-      if (ci + 1 < nchunks) load_gates(ci + 1);
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float ya = __shfl_up_sync(0xffffffffu, ga, off);
-        const float yb = __shfl_up_sync(0xffffffffu, gb, off);
-        if (lt >= off) { ga += ya; gb += yb; }
-      }
-      gb += __shfl_sync(0xffffffffu, ga, 31);
-      const float gl = __shfl_sync(0xffffffffu, gb, 31);
-      vgam[r0] = ga; vgam[r1] = gb;
-      vegam[r0] = __expf(ga); vegam[r1] = __expf(gb);
-      vdec[r0] = __expf(gl - ga); vdec[r1] = __expf(gl - gb);
-      vbeta[r0] = ba; vbeta[r1] = bb;
+    float* vgam = vecs + (ci & 1) * 256;   // this chunk's gate vectors
+    float* vegam = vgam + 64;
+    float* vdec = vgam + 128;
+    float* vbeta = vgam + 192;
+    if (ci == 0) {
+      if (warp == 0) gates(0);
+      __syncthreads();
     }
-    __syncthreads();
-
     // ---- A (rows of K K^T) and P (rows of Q K^T) from G1 ----
     wait(bar_g1, par);
     tc::tc_fence_after();
@@ -599,6 +603,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     if (tid == 0) {
       tc::tc_fence_after();
+      // C = K^T Dt first: it is on the path to the next chunk: A = K^T (MN-major), B = Dt hi / lo (MN-major [i][j])
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_C, dadv(dStgM[st], ST_K0 + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
+                       IDESC_C, (part | ks) != 0);
+      tc::mma_commit(bar_c);
       // P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi: A = P (K-major [r][i]), B = Delta (MN-major [i][j])
 #pragma unroll
       for (int q = 0; q < 3; ++q)
@@ -607,14 +619,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           tc::mma_bf16(tmem + TM_X, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32), dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048),
                        IDESC_XY, (q | ks) != 0);
       tc::mma_commit(bar_pd);
-      // C = K^T Dt: A = K^T (MN-major), B = Dt hi / lo (MN-major [i][j])
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_C, dadv(dStgM[st], ST_K0 + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
-                       IDESC_C, (part | ks) != 0);
-      tc::mma_commit(bar_c);
     }
 
     // ---- S1 = Gam_L S0 + C, state QDQ at the 64-token boundary ----
@@ -673,6 +677,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc::tc_fence_after();
     // the next chunk's G1 runs on the tensor cores while this chunk's outputs are written
     if (ci + 1 < nchunks && !start_chunk(ci + 1)) { aborted = true; break; }
+    if (warp == 0 && ci + 1 < nchunks) gates(ci + 1);   // other buffer: this chunk's vectors stay intact
     // ---- outputs: o = scale (Gam Y + P Delta) for rows r < L ----
     wait(bar_y, par);
     wait(bar_pd, par);
@@ -692,7 +697,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       }
     }
 
-    __syncthreads();   // the gate vectors are rewritten by the next chunk
+    __syncthreads();   // the next chunk's gate vectors are complete
   }
 
   if (!aborted && p.hT) {
