@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
+#include "tc_epilogue.cuh"
 
 namespace gdn {
 namespace {
@@ -79,54 +80,6 @@ struct TcParams {
   float scale;
   int state_qdq, w_qdq;
 };
-
-// bf16 pair packed in 32 bits (low half = first element)
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-}
-// 8 consecutive values -> bf16 hi (exact rounding) and lo (residual), one 16-byte chunk each
-__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
-    const float2 hf = unpack_bf16(h[i]);
-    l[i] = pack_bf16(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-__device__ __forceinline__ uint4 pack8(const float* x) {
-  return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-}
-__device__ __forceinline__ void st16(unsigned char* sm, uint32_t off, uint4 v) {
-  *reinterpret_cast<uint4*>(sm + off) = v;
-}
-// E4M3 QDQ of a pair with the reciprocal of the scale: codes (as fp32) and dequantized values
-__device__ __forceinline__ void qdq_pair(float a, float b, float rs, float s, float& ca, float& cb, float& qa,
-                                         float& qb) {
-  const __nv_fp8x2_e4m3 c(make_float2(__fmul_rn(a, rs), __fmul_rn(b, rs)));
-  const float2 cf = static_cast<float2>(c);
-  ca = cf.x;
-  cb = cf.y;
-  qa = __fmul_rn(cf.x, s);
-  qb = __fmul_rn(cf.y, s);
-}
-__device__ __forceinline__ void ld32(uint32_t tmem, uint32_t lane0, uint32_t col, float* v) {
-  tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col), v);
-  tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);
-  tc::tmem_ld_wait();
-}
-__device__ __forceinline__ void st32(uint32_t tmem, uint32_t lane0, uint32_t col, const float* v) {
-  tc::tmem_st16(tc::tmem_addr(tmem, lane0, col), v);
-  tc::tmem_st16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);
-}
-// descriptor for `addr` advanced by `off` bytes (the start field is the low 14 bits, in 16-byte units)
-__device__ __forceinline__ uint64_t dadv(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -718,6 +671,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+}  // namespace
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed)
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -737,7 +692,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D map over a head-last bf16 tensor [tokens, heads, D]: dims (D, heads, tokens), box 64 x 1 x 64
-bool make_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens) {
+bool make_bf16_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)tokens};
@@ -749,7 +704,6 @@ bool make_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
 
 bool chunk_tc_supported(const ChunkProblem& p) { return p.dk == 128 && !p.kda && p.dv % 64 == 0; }
 
@@ -760,8 +714,8 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, int* status, cudaStream_t str
   CUtensorMap tq, tk, tv;
   // an empty batch still needs valid maps: point them at a one-token view (never loaded)
   const int64_t tmap = tokens > 0 ? tokens : 1;
-  if (!make_map(&tq, p.q, 128, p.Hqk, tmap) || !make_map(&tk, p.k, 128, p.Hqk, tmap) ||
-      !make_map(&tv, p.v, p.dv, p.Hv, tmap))
+  if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap) ||
+      !make_bf16_map(&tv, p.v, p.dv, p.Hv, tmap))
     return cudaErrorInvalidValue;
   TcParams tp{p.g, p.beta, p.h0, p.cu, p.o, p.hT, status, p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

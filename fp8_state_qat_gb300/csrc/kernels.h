@@ -1,6 +1,7 @@
 // kernels.h -- internal launchers behind the C ABI (not part of the public header).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,6 +33,10 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const flo
 // set to nonzero when a bounded wait gives up.
 bool chunk_tc_supported(const ChunkProblem& p);
 cudaError_t launch_chunk_tc(const ChunkProblem& p, int* status, cudaStream_t stream);
+
+// TMA descriptor of a head-last bf16 tensor [tokens, heads, D] with 64 x 1 x 64 boxes
+// (128-byte swizzle). Host only; false when the driver entry point is unavailable.
+bool make_bf16_map(CUtensorMap* map, const void* base, int D, int heads, int64_t tokens);
 
 // Per-CTA fp32 chunked forward on CUDA cores: one CTA per (sequence, head, 64-column
 // value slab). Used for shapes and variants the tensor-core path does not take.
