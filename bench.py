@@ -251,6 +251,17 @@ class PrefillCase:
         self.fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
         self.sets = [self.resident(), self.resident()]
         self.cu = x.cu_seqlens
+        # dk = 128 GDN with the full workspace: a parallel prep kernel, then the state chain
+        self.launches = 2 if (not x.kda and s["dk"] == 128) else 1
+
+    def scope(self):
+        if self.launches == 2:
+            return "one step = chunk_prep_kernel + chunk_chain_kernel; achieved is over both"
+        return "one step = one kernel launch"
+
+    def workspace_bytes(self):
+        return self.gdn.chunk_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu, state_qdq=self.x.state_qdq,
+                                              w_qdq=self.x.w_qdq)
 
     def resident(self):
         x, s, dev, torch = self.x, self.s, self.dev, self.torch
@@ -309,6 +320,13 @@ class DecodeCase:
         self.tok = [dict(q=d.q[i].to(dev), k=d.k[i].to(dev), v=d.v[i].to(dev), g=d.g[i].to(dev),
                          beta=d.beta[i].to(dev)) for i in range(self.steps_avail)]
         self.o = torch.empty((N, Hv, dv), device=dev)
+        self.launches = 1
+
+    def workspace_bytes(self):
+        return 0
+
+    def scope(self):
+        return "one step = one kernel launch"
 
     def step(self, i, ws, stream):
         t = self.tok[i % self.steps_avail]
@@ -360,7 +378,7 @@ def run_gpu(args):
                                     x.beta[:args.batch], None if x.h0 is None else x.h0[:args.batch], None,
                                     kda=x.kda, state_qdq=x.state_qdq, w_qdq=x.w_qdq, name=x.name)
     case = (DecodeCase if isinstance(x, workloads.DecodeInputs) else PrefillCase)(x, dev, torch, gdn)
-    ws = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(case.workspace_bytes(), 1 << 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     for i in range(args.warmup):
@@ -430,11 +448,12 @@ def run_gpu(args):
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                              "frac": achieved / hbm,
                              "traffic": profiled_traffic() if args.workload == WORKLOAD and not args.batch else None,
-                             "peak_source": src, "bytes_per_launch": case.bytes, "flops_per_launch": case.flops,
+                             "peak_source": src, "scope": case.scope(), "bytes_per_launch": case.bytes,
+                             "flops_per_launch": case.flops,
                              "tensor_frac": case.flops / (launch_ms * 1e-3) / (bf16 * 1e12), "kernel_ms": launch_ms},
                 "e2e": {"value": world * case.tokens * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-                "gpu_launches": args.steps * 1,
+                "gpu_launches": args.steps * case.launches,
                 "clocks": clocks.summary()}
         if world == 1 and not args.no_cpu_baseline and isinstance(case, PrefillCase) and args.workload == WORKLOAD:
             line["cpu_baseline"] = cpu_baseline(x)

@@ -10,6 +10,7 @@ from .gdnqat import (  # noqa: F401
     GDN_FLAG_W_QDQ,
     ChunkArgs,
     GdnError,
+    chunk_workspace_bytes,
     fp8_tile_qdq,
     gdn_check_device_status,
     gdn_chunk_fwd,

@@ -3,10 +3,10 @@
 // Some callers cannot call cudaMalloc or any allocating routine at the point where they run
 // the forward: code running inside a memory allocator's own hooks, latency-critical paths
 // where an allocation's implicit device synchronization is not allowed, or processes whose
-// device memory is fully handed out to a framework's pool. gdn_chunk_fwd needs a small
-// device workspace (the status word of the tensor-core kernel's bounded waits); this variant
-// takes that workspace from a fixed-size array that lives in the library itself, so the
-// caller passes only its inputs and outputs.
+// device memory is fully handed out to a framework's pool. gdn_chunk_fwd needs at least a
+// small device workspace (the status word of the tensor-core kernels' bounded waits); this
+// variant takes that minimum from a fixed-size array that lives in the library itself, so
+// the caller passes only its inputs and outputs (and the forward runs its single-kernel path).
 //
 // The array is a file-scope __device__ object: every GPU that loads the library holds these
 // kNoAllocScratchBytes until the process exits, and all calls on a device share it. The host
@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 256;   // the most the chunk forward asks for today
+constexpr size_t kNoAllocScratchBytes = 256;   // the chunk forward's minimum workspace
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -49,12 +49,12 @@ gdn_status scratch_for_current_device(void** out) {
 }  // namespace
 
 extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream) {
-  const size_t need = gdn_chunk_fwd_workspace_size(args);
-  if (need == 0) {
+  if (gdn_chunk_fwd_workspace_size(args) == 0) {
     // invalid arguments: let the regular entry point report which check failed
     return gdn_chunk_fwd(args, nullptr, 0, stream);
   }
-  if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  // the smallest workspace gdn_chunk_fwd accepts (it then takes its single-kernel path)
+  if (GDN_CHUNK_MIN_WORKSPACE_BYTES > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const gdn_status s = scratch_for_current_device(&scratch);
   if (s != GDN_OK) return s;

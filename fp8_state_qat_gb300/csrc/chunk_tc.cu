@@ -31,8 +31,6 @@
 //
 // Every mbarrier wait is bounded; a CTA whose wait gives up records it in the status word,
 // waits (bounded) for its own TMA in flight, frees its TMEM and exits.
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -250,7 +248,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
   for (int64_t ci = 0; ci < nchunks; ++ci) {
     const int st = (int)(ci & 1);
-    const uint32_t stg = sbase + (uint32_t)st * kStageBytes;
     const int64_t c0 = ci * 64;
     const int L = (len - c0) < 64 ? (int)(len - c0) : 64;
     const uint32_t par = (uint32_t)(ci & 1);
@@ -672,38 +669,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 }
 
 }  // namespace
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed)
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// 3-D map over a head-last bf16 tensor [tokens, heads, D]: dims (D, heads, tokens), box 64 x 1 x 64
-bool make_bf16_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)tokens};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-  const cuuint32_t box[3] = {64, 1, 64};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 
 bool chunk_tc_supported(const ChunkProblem& p) { return p.dk == 128 && !p.kda && p.dv % 64 == 0; }
 

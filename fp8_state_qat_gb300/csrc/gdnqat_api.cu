@@ -49,7 +49,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 bool dk_ok(int dk) { return dk == 64 || dk == 128; }
 bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
 
-constexpr size_t kWorkspaceBytes = 256;   // device status word (+ padding to one 256-byte line)
+constexpr size_t kWorkspaceBytes = gdn::kStatusBytes;   // device status word (+ padding to one line)
+static_assert(kWorkspaceBytes == GDN_CHUNK_MIN_WORKSPACE_BYTES, "the header's minimum must match");
 
 gdn_status validate_chunk(const gdn_chunk_args* a, bool kda) {
   if (!a) return GDN_ERR_INVALID_ARG;
@@ -100,8 +101,15 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
   ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
                  (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
-  const cudaError_t e = gdn::chunk_tc_supported(p) ? gdn::launch_chunk_tc(p, static_cast<int*>(ws), stream)
-                                                   : gdn::launch_chunk_simt(p, stream);
+  // dk = 128 GDN: the two-kernel path (parallel prep, then the state chain) when the workspace
+  // holds its staging, else the single fused kernel; other shapes and KDA: CUDA cores
+  cudaError_t e;
+  if (gdn::chunk_split_supported(p) && ws_bytes >= gdn::chunk_split_layout(p).total)
+    e = gdn::launch_chunk_split(p, ws, stream);
+  else if (gdn::chunk_tc_supported(p))
+    e = gdn::launch_chunk_tc(p, static_cast<int*>(ws), stream);
+  else
+    e = gdn::launch_chunk_simt(p, stream);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -123,7 +131,14 @@ const char* gdn_status_string(gdn_status status) {
 }
 
 size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args) {
-  if (validate_chunk(args, false) != GDN_OK && validate_chunk(args, true) != GDN_OK) return 0;
+  const bool gdn_ok = validate_chunk(args, false) == GDN_OK;
+  if (!gdn_ok && validate_chunk(args, true) != GDN_OK) return 0;
+  if (gdn_ok) {
+    const gdn::ChunkProblem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                              args->B, args->T, args->N, args->Hqk, args->Hv, args->dk, args->dv, args->scale,
+                              (args->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 0};
+    if (gdn::chunk_split_supported(p)) return gdn::chunk_split_layout(p).total;
+  }
   return kWorkspaceBytes;
 }
 

@@ -33,8 +33,8 @@ __device__ void stage(unsigned char* base, const float* src, int rows, int cols,
 }
 
 __global__ void __launch_bounds__(128, 1)
-tc_selftest_kernel(const float* A, const float* B, float* D, int M, int N, int K, int kind, int a_mn, int b_mn,
-                   int* status) {
+tc_selftest_kernel(const float* A, const float* B, float* D, float* D2, int M, int N, int K, int kind, int a_mn,
+                   int b_mn, int* status) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ uint64_t mbar;
   __shared__ uint32_t tmem_base_slot;
@@ -81,6 +81,18 @@ tc_selftest_kernel(const float* A, const float* B, float* D, int M, int N, int K
 #pragma unroll
       for (int j = 0; j < 16; ++j) D[lane * N + c0 + j] = v[j];
     }
+    if (D2) {   // the same accumulator read with the 16-lane two-half shape (split = N / 2)
+      const int t = threadIdx.x & 31, row = warp * 32 + (t & 15);
+      for (int c0 = 0; c0 < N / 2; c0 += 16) {
+        float v[16];
+        if (N == 128) tc::tmem_ld16x2<64>(tc::tmem_addr(tmem, warp * 32, c0), v);
+        else tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, warp * 32, c0), v);
+        tc::tmem_ld_wait();
+        const int col = c0 + (t >> 4) * (N / 2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) D2[row * N + col + j] = v[j];
+      }
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -92,12 +104,13 @@ tc_selftest_kernel(const float* A, const float* B, float* D, int M, int N, int K
 
 // Internal: D [128 lanes x N] from A [M x K] and B [K x N] (device fp32, row-major) with the
 // requested operand kind (0 bf16, 1 tf32) and majors; status (device int) set on a timeout.
-extern "C" int gdnqat_internal_tc_selftest(const float* A, const float* B, float* D, int M, int N, int K, int kind,
-                                           int a_mn, int b_mn, int* status, cudaStream_t stream) {
+// D2 (nullable): the accumulator read again with the 16x32bx2 TMEM load shape.
+extern "C" int gdnqat_internal_tc_selftest(const float* A, const float* B, float* D, float* D2, int M, int N, int K,
+                                           int kind, int a_mn, int b_mn, int* status, cudaStream_t stream) {
   if ((M != 64 && M != 128) || (N != 64 && N != 128) || (K != 64 && K != 128)) return 1;
   cudaError_t e = cudaFuncSetAttribute(gdn::tc_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)gdn::kSmemBytes);
   if (e != cudaSuccess) return 2;
-  gdn::tc_selftest_kernel<<<1, 128, gdn::kSmemBytes, stream>>>(A, B, D, M, N, K, kind, a_mn, b_mn, status);
+  gdn::tc_selftest_kernel<<<1, 128, gdn::kSmemBytes, stream>>>(A, B, D, D2, M, N, K, kind, a_mn, b_mn, status);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

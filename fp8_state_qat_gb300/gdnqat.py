@@ -122,9 +122,24 @@ def workspace_bytes(args: ChunkArgs) -> int:
     return int(load().gdn_chunk_fwd_workspace_size(ctypes.byref(args)))
 
 
-def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state,
-           workspace, stream):
-    lib = load()
+def chunk_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False, w_qdq=False):
+    """gdn_chunk_fwd_workspace_size for q [B,T,Hqk,dk], v [B,T,Hv,dv] (shapes only): the
+    workspace of the fastest path. The size depends on shapes and flags only, so the query
+    passes distinct placeholder device addresses."""
+    B, T, Hqk, dk = q_shape
+    Hv, dv = v_shape[2], v_shape[3]
+    cu_host, N = None, B
+    if cu_seqlens is not None:
+        cu_host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+        N = cu_host.numel() - 1
+    fake = [ctypes.c_void_p((1 << 44) + (i << 38)) for i in range(10)]
+    flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_W_QDQ if w_qdq else 0)
+    a = ChunkArgs(fake[0], fake[1], fake[2], fake[3], fake[4], None, fake[6] if cu_host is not None else None,
+                  _ptr(cu_host), fake[8], fake[9], B, T, N, Hqk, Hv, dk, dv, 1.0, flags)
+    return workspace_bytes(a)
+
+
+def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state):
     q = _dev(q, torch.bfloat16, "q")
     k = _dev(k, torch.bfloat16, "k")
     v = _dev(v, torch.bfloat16, "v")
@@ -146,8 +161,18 @@ def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o
     if hT is None and output_final_state:
         hT = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
     flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_W_QDQ if w_qdq else 0)
+    # the host copy of cu_seqlens must outlive the call: it is returned with the args
     a = ChunkArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_dev), _ptr(cu_host),
                   _ptr(o), _ptr(hT), B, T, N, Hqk, Hv, dk, dv, float(scale), flags)
+    return a, (o, hT), (cu_host, cu_dev)
+
+
+def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state,
+           workspace, stream):
+    lib = load()
+    a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
+                                    output_final_state)
+    dev = o.device
     need = workspace_bytes(a)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)

@@ -82,16 +82,27 @@ typedef struct {
   uint32_t flags;              /* GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ */
 } gdn_chunk_args;
 
-/* Bytes of device workspace gdn_chunk_fwd / kda_chunk_fwd need for these arguments (a
- * status word for bounded device waits plus any staging); 0 when the arguments are invalid. */
+/* Smallest workspace gdn_chunk_fwd / kda_chunk_fwd accept: the device status word of the
+ * kernels' bounded waits, padded to one 256-byte line. */
+#define GDN_CHUNK_MIN_WORKSPACE_BYTES 256
+
+/* Bytes of device workspace for the fastest path with these arguments; 0 when the arguments
+ * are invalid. For dk = 128 (GDN) that is the status word plus the staging of the two-kernel
+ * path: per 64-token chunk slot and v-head, the chunk's W (transposed; E4M3 codes in bf16
+ * with GDN_FLAG_W_QDQ, else bf16 hi + lo), T diag(beta) as bf16 hi + lo and its gate vectors
+ * -- 33 KB (49 KB without W QDQ) for each of (B T / 64 + N) x Hv slots. Otherwise
+ * GDN_CHUNK_MIN_WORKSPACE_BYTES. */
 size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args);
 
 /* Chunked GDN forward ([F]): per 64-token chunk, decay-weighted K.K^T, WY solve (W, U),
  * optional W QDQ, state carry with state QDQ at every 64th token of each sequence; o for
  * every token and hT per (sequence, head). hT is QDQ'd when a sequence's length is a
  * positive multiple of 64 (its last token is then a 64th token). Empty sequences give
- * hT = h0. workspace: device, >= gdn_chunk_fwd_workspace_size(args) bytes, 256-byte
- * aligned; its contents need no initialization. */
+ * hT = h0. workspace: device, 256-byte aligned, at least GDN_CHUNK_MIN_WORKSPACE_BYTES;
+ * its contents need no initialization. With gdn_chunk_fwd_workspace_size(args) bytes or
+ * more, dk = 128 runs as two kernels (every chunk's state-independent work in parallel,
+ * then the state carry); with less, as one fused kernel that does both chunk by chunk
+ * (slower, same arithmetic). Returns GDN_ERR_WORKSPACE_TOO_SMALL below the minimum. */
 gdn_status gdn_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
                          gdn_stream_t stream);
 
@@ -108,8 +119,9 @@ gdn_status gdn_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t wor
  *  - All calls on a device share the array (its status word is cleared at the start of
  *    each call): calls that may run at the same time on the GPU, e.g. on different
  *    streams, race on it. Serialize them, or use gdn_chunk_fwd with separate workspaces.
- *  - Returns GDN_ERR_WORKSPACE_TOO_SMALL if these arguments would need more workspace than
- *    the 256 bytes the array holds.
+ *  - The array holds GDN_CHUNK_MIN_WORKSPACE_BYTES, so dk = 128 always takes the fused
+ *    single-kernel path. Returns GDN_ERR_WORKSPACE_TOO_SMALL if a path would need more
+ *    workspace than the array holds (none does today).
  *  - A device-side timeout is recorded in the shared array and cannot be queried through
  *    gdn_check_device_status. */
 gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream);

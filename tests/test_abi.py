@@ -81,13 +81,30 @@ def test_varlen_validation(so):
     assert call_chunk(so, a) == B.GDN_ERR_INVALID_ARG
 
 
+MIN_WS = 256   # GDN_CHUNK_MIN_WORKSPACE_BYTES
+
+
 def test_workspace_checks(so):
+    """Below the minimum (the status word) the call is refused before anything else; between
+    the minimum and gdn_chunk_fwd_workspace_size() it is accepted (single-kernel path)."""
     a = good_args()
-    need = so.gdn_chunk_fwd_workspace_size(ctypes.byref(a))
-    assert need >= 4
-    assert call_chunk(so, a, ws_bytes=need - 1) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+    assert call_chunk(so, a, ws_bytes=MIN_WS - 1) == B.GDN_ERR_WORKSPACE_TOO_SMALL
     assert call_chunk(so, a, ws=0) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+    # with enough workspace the next check is the device's (none here)
+    assert call_chunk(so, a, ws_bytes=MIN_WS) == B.GDN_ERR_UNSUPPORTED_ARCH
     assert so.gdn_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=96))) == 0
+
+
+def test_workspace_size_covers_the_two_kernel_staging(so):
+    """dk = 128: status word + per (chunk slot, v-head) W^T (16 KB with W QDQ, 32 KB without),
+    T'' hi + lo (16 KB) and the gate vectors (1 KB), slots = B T / 64 + N. dk = 64: the minimum."""
+    for flags, wt in ((B.GDN_FLAG_STATE_QDQ | B.GDN_FLAG_W_QDQ, 16), (B.GDN_FLAG_STATE_QDQ, 32)):
+        a = good_args(flags=flags)
+        items = (a.B * a.T // 64 + a.N) * a.Hv
+        need = so.gdn_chunk_fwd_workspace_size(ctypes.byref(a))
+        assert need >= MIN_WS + items * (wt + 16 + 1) * 1024
+        assert need <= MIN_WS + items * (wt + 16 + 1) * 1024 + 3 * 1024
+    assert so.gdn_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=64))) == MIN_WS
 
 
 def test_decode_and_qdq_validation(so):

@@ -16,12 +16,18 @@ from helpers import TOL_OFF, TOL_QDQ, compare_units, mask_for, sample_units, to_
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(gdn, x, state_qdq, w_qdq, hT_alias=False):
+# dk = 128 GDN has two paths: "split" (the workspace holds the per-chunk staging: a parallel
+# prep kernel, then the state chain) and "fused" (the minimum 256-byte workspace: one kernel)
+PATHS = ["split", "fused"]
+
+
+def run_gpu(gdn, x, state_qdq, w_qdq, hT_alias=False, path="split"):
     c = to_cuda(x)
     fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
     hT = c["h0"] if (hT_alias and c["h0"] is not None) else None
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda") if path == "fused" else None
     o, hT = fn(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], x.cu_seqlens, state_qdq=state_qdq,
-               w_qdq=w_qdq, hT=hT)
+               w_qdq=w_qdq, hT=hT, workspace=ws)
     torch.cuda.synchronize()
     return o, hT
 
@@ -36,8 +42,8 @@ def run_oracle(oracle_mod, x, state_qdq, w_qdq, units=None):
                                     state_qdq=state_qdq, unit_mask=m)
 
 
-def check(gdn, oracle_mod, x, state_qdq, w_qdq, units=None, hT_alias=False):
-    o, hT = run_gpu(gdn, x, state_qdq, w_qdq, hT_alias)
+def check(gdn, oracle_mod, x, state_qdq, w_qdq, units=None, hT_alias=False, path="split"):
+    o, hT = run_gpu(gdn, x, state_qdq, w_qdq, hT_alias, path)
     oref, href = run_oracle(oracle_mod, x, state_qdq, w_qdq, units)
     if units is None:
         units = [(n, h) for n in range(x.shape["N"]) for h in range(x.shape["Hv"])]
@@ -55,25 +61,45 @@ def test_small_workload(gdn, oracle_mod, state_qdq, w_qdq):
     check(gdn, oracle_mod, x, state_qdq, w_qdq)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 200])
-@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 256), (128, 64)])
-def test_lengths_and_shapes(gdn, oracle_mod, T, dk, dv):
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 256), (128, 64), (128, 256)])
+def test_lengths_and_shapes(gdn, oracle_mod, T, dk, dv, path):
+    if dk == 64 and path == "fused":
+        pytest.skip("dk = 64 has a single path")
     x = workloads.prefill(2, T, 1, 2, dk, dv, seed=T + dk + dv, h0_std=0.1)
-    check(gdn, oracle_mod, x, True, False)
-    check(gdn, oracle_mod, x, False, False)
+    check(gdn, oracle_mod, x, True, False, path=path)
+    check(gdn, oracle_mod, x, False, False, path=path)
+    if dk == 128:
+        check(gdn, oracle_mod, x, True, True, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("kda", [False, True])
 @pytest.mark.parametrize("state_qdq,w_qdq", QDQ_MODES)
-def test_varlen_gqa(gdn, oracle_mod, kda, state_qdq, w_qdq):
+def test_varlen_gqa(gdn, oracle_mod, kda, state_qdq, w_qdq, path):
+    if kda and path == "fused":
+        pytest.skip("KDA has a single path")
     lens = [0, 1, 63, 64, 65, 129, 300]
     x = workloads.prefill(1, 0, 2, 4, 128, 128, seed=31 + kda, h0_std=0.1, seqlens=lens, kda=kda)
-    check(gdn, oracle_mod, x, state_qdq, w_qdq)
+    check(gdn, oracle_mod, x, state_qdq, w_qdq, path=path)
 
 
-def test_final_state_aliases_h0(gdn, oracle_mod):
+@pytest.mark.parametrize("path", PATHS)
+def test_final_state_aliases_h0(gdn, oracle_mod, path):
     x = workloads.prefill(2, 150, 2, 2, 128, 128, seed=41, h0_std=0.1)
-    check(gdn, oracle_mod, x, True, True, hT_alias=True)
+    check(gdn, oracle_mod, x, True, True, hT_alias=True, path=path)
+
+
+def test_paths_agree_closely(gdn):
+    """The two dk = 128 paths compute the same arithmetic (operands split the same way, the same
+    QDQ epilogues); on a QDQ-off case their outputs agree far inside the oracle bound."""
+    x = workloads.prefill(2, 333, 2, 4, 128, 128, seed=44, h0_std=0.1)
+    o1, h1 = run_gpu(gdn, x, False, False, path="split")
+    o2, h2 = run_gpu(gdn, x, False, False, path="fused")
+    from helpers import rel
+    assert rel(o1.cpu().double().numpy(), o2.cpu().double().numpy()) <= 1e-5
+    assert rel(h1.cpu().double().numpy(), h2.cpu().double().numpy()) <= 1e-5
 
 
 def test_zero_initial_state_and_no_final_state(gdn, oracle_mod):
@@ -96,19 +122,21 @@ def test_kda_small(gdn, oracle_mod):
 
 # ---- full-size workloads, sampled (sequence, head) units ---------------------------------
 
-def test_gdn_b4_h16_t4096_d128_sampled(gdn, oracle_mod):
+@pytest.mark.parametrize("path", PATHS)
+def test_gdn_b4_h16_t4096_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("gdn_b4_h16_t4096_d128")
     units = sample_units(4, 16, 6, seed=1)
-    check(gdn, oracle_mod, x, True, True, units)        # the benchmarked configuration
-    check(gdn, oracle_mod, x, False, False, units)      # quantizers off: the 1e-3 bound
+    check(gdn, oracle_mod, x, True, True, units, path=path)        # the benchmarked configuration
+    check(gdn, oracle_mod, x, False, False, units, path=path)      # quantizers off: the 1e-3 bound
 
 
-def test_gdn_varlen8_hqk16_hv32_d128_sampled(gdn, oracle_mod):
+@pytest.mark.parametrize("path", PATHS)
+def test_gdn_varlen8_hqk16_hv32_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("gdn_varlen8_hqk16_hv32_d128")
     lens = np.diff(x.cu_seqlens.numpy())
     longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
     units = sorted(set(sample_units(8, 32, 6, seed=2) + [(longest, 31), (shortest, 0)]))
-    check(gdn, oracle_mod, x, True, False, units)
+    check(gdn, oracle_mod, x, True, False, units, path=path)
 
 
 def test_kda_b2_h32_t8192_d128_sampled(gdn, oracle_mod):

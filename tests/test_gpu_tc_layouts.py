@@ -39,8 +39,8 @@ def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K, M):
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dD = torch.full((128, N), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = fn(ctypes.c_void_p(dA.data_ptr()), ctypes.c_void_p(dB.data_ptr()), ctypes.c_void_p(dD.data_ptr()), M, N, K,
-            kind, a_mn, b_mn, ctypes.c_void_p(st.data_ptr()), None)
+    rc = fn(ctypes.c_void_p(dA.data_ptr()), ctypes.c_void_p(dB.data_ptr()), ctypes.c_void_p(dD.data_ptr()), None,
+            M, N, K, kind, a_mn, b_mn, ctypes.c_void_p(st.data_ptr()), None)
     assert rc == 0
     torch.cuda.synchronize()
     assert int(st.item()) == 0, "bounded wait gave up"
@@ -49,3 +49,32 @@ def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K, M):
     if M == 64:
         got = got[[32 * (m // 16) + m % 16 for m in range(64)]]
     np.testing.assert_allclose(got, want, rtol=1e-4, atol=1e-4 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_tmem_16x32bx2_reads_m64_rows(gdn, N):
+    """The 16-lane two-half TMEM load on an M = 64 accumulator: thread t of warp w reads row
+    16 w + t % 16, columns [c0 + (t / 16) N / 2, + 16). Every row of the product is recovered and
+    lanes 16-31 of each quadrant are never touched."""
+    lib = gdn.load()
+    fn = lib.gdnqat_internal_tc_selftest
+    fn.restype = ctypes.c_int
+    M, K = 64, 128
+    rng = np.random.default_rng(500 + N)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dD = torch.full((128, N), float("nan"), device="cuda")
+    dD2 = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = fn(ctypes.c_void_p(dA.data_ptr()), ctypes.c_void_p(dB.data_ptr()), ctypes.c_void_p(dD.data_ptr()),
+            ctypes.c_void_p(dD2.data_ptr()), M, N, K, 0, 0, 0, ctypes.c_void_p(st.data_ptr()), None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "bounded wait gave up"
+    want = rounded(A, 0) @ rounded(B, 0)
+    got = dD2.cpu().double().numpy()
+    rows = [32 * (m // 16) + m % 16 for m in range(64)]
+    np.testing.assert_allclose(got[rows], want, rtol=1e-4, atol=1e-4 * np.abs(want).max())
+    untouched = [l for l in range(128) if l not in rows]
+    assert np.isnan(got[untouched]).all()
