@@ -1,29 +1,27 @@
 // chunk_chain.cu -- the state-carrying half of the chunked gated-delta-rule forward (dk = 128) on
-// the sm_103a tensor cores, after chunk_prep.cu has staged every chunk's W^T, T'', P and gate
-// vectors in the workspace.
+// the sm_103a tensor cores, after chunk_prep.cu has staged every chunk's W^T, T'' and gate vectors
+// in the workspace.
 //
 // One CTA (256 threads) per (sequence n, v-head h, 64-column value slab); the slab is one
 // state-QDQ tile (all 128 key rows x 64 value columns), so its amax is CTA-local ("GDN state/W QAT
 // foundation", "What does this PR do?"). Two warpgroups split each 64-token chunk:
-//   chain  (warps 4-7)  X = W S0 (and Y = Q S0 right behind it) -> Delta = U - X,
-//                       Dt = exp(gam_63 - gam) Delta -> C = K^T Dt -> S1 = Gam_63 S0 + C, QDQ(S1) at
-//                       a 64-token boundary -> the next chunk. Only this loop is serial from chunk to
-//                       chunk. It also refills the W^T buffer and the Q/K stages.
-//   output (warps 0-3)  U = T'' V (one chunk ahead, with the next T'' / V load), P Delta, the next
-//                       P load, o = scale (Gam Y + P Delta).
+//   chain  (warps 4-7)  X = W S0 -> Delta = U - X, Dt = exp(gam_63 - gam) Delta -> C = K^T Dt ->
+//                       S1 = Gam_63 S0 + C, QDQ(S1) at a 64-token boundary -> the next chunk.
+//                       Only this loop is serial from chunk to chunk. It also refills the W^T
+//                       buffer and the Q/K stages once their last readers are done.
+//   output (warps 0-3)  U = T'' V (and the next T'' / V load), G = Q K^T -> P (exp(gam_r - gam_i)
+//                       G, i <= r), Y = Q S0, P Delta, o = scale (Gam Y + P Delta); U and G of the
+//                       next chunk are issued right after P Delta, ahead of the chain's next X.
 // The state S0 (fp32) lives in the chain's registers (one key row of the slab per thread) and, as
 // the MMA operand, in shared memory as bf16 hi + lo, or as exact E4M3 codes once QDQ'd (the scale
-// is applied in the epilogues). W arrives as codes (exact in bf16) with W QDQ, else as bf16 hi + lo;
-// T'' and P as hi + lo; Delta and Dt are split into hi + lo before their MMAs.
+// is applied in the epilogues). W arrives as codes
+// (exact in bf16) with W QDQ, else as bf16 hi + lo; T'' as hi + lo; Delta, Dt and P are split
+// into hi + lo before their MMAs.
 //
-// A tcgen05.mma costs about the same to issue at N = 64 as at N = 128, so products that share an
-// operand are issued as one N = 128 MMA: C = K^T [Dt_hi | Dt_lo] and P_hi [Delta_hi | Delta_lo]
-// (the two halves are added in the epilogues).
-//
-// Hand-offs are mbarriers: TMA transactions, MMA commits, and one-arrival signals ("U consumed",
-// "Delta stored" from the chain; "Y consumed" from the output side, one per TMEM Y buffer). Every
-// wait is bounded; a warp whose wait gives up raises a CTA-wide abort flag, both warpgroups leave
-// their loops at their next checked barrier, TMA in flight is waited for (bounded), TMEM is freed.
+// Hand-offs are mbarriers (TMA transactions, MMA commits, and three one-arrival signals from the
+// chain: "U consumed", "Delta stored", "S0 of the next chunk stored"). Every wait is bounded; a
+// warp whose wait gives up raises a CTA-wide abort flag, both warpgroups leave their loops at
+// their next checked barrier, TMA in flight is waited for (bounded), TMEM is freed.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -36,6 +34,16 @@ cudaError_t launch_chunk_prep(const ChunkProblem& p, const SplitLayout& lay, uns
 namespace {
 
 constexpr int kThreads = 256;
+// The threads that issue each warpgroup's MMAs and TMA loads. A tcgen05.mma issues slowly while other
+// warps on the same SM sub-partition (warp id mod 4) keep its FP32 pipes busy, so the two issuers
+// sit on different sub-partitions.
+#ifndef GDN_OUT_ISSUER
+#define GDN_OUT_ISSUER 64     // warp 2
+#endif
+#ifndef GDN_CHAIN_ISSUER
+#define GDN_CHAIN_ISSUER 32   // warp 5 (index within the chain warpgroup)
+#endif
+constexpr int kOutIssuer = GDN_OUT_ISSUER, kChainIssuer = GDN_CHAIN_ISSUER;
 constexpr uint32_t KB = 1024;
 // shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t kStage = 34 * KB;   // two stages: Q0 | K0 | Q1 | K1 (8 KB each, key columns 0-63 | 64-127) | vec
@@ -46,24 +54,21 @@ constexpr uint32_t OFF_WT = 92 * KB;    // W^T codes [128 c][64 r] (or hi | lo, 
 constexpr uint32_t OFF_SHI = 124 * KB;  // S0 operand [128 c][64 j] MN-major; lo at +16 KB
 constexpr uint32_t OFF_DL = 156 * KB;   // Delta hi, lo, Dt hi, lo ([i][j] MN-major, 8 KB each)
 constexpr uint32_t OFF_P = 188 * KB;    // P hi | lo ([r][i] K-major)
-constexpr uint32_t OFF_MISC = 204 * KB; // S0 scale [2], partial maxima [4], abort flag
+constexpr uint32_t OFF_MISC = 204 * KB; // S0 scale [2], S0-is-codes [2], partial maxima [4], abort flag
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + slack to align the base
 
 // TMEM columns (M = 64 results sit in lanes 16 w .. 16 w + 15 of quadrant w)
-constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128 /* two buffers */, TM_C = 256 /* hi | lo */,
-                   TM_PD = 384 /* hi | lo */;
+constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128, TM_C = 192, TM_GP = 256, TM_PD = 320;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);     // T'' (K) x V (MN)
-constexpr uint32_t IDESC_X = tc::make_idesc(tc::kKindBF16, 64, 64, true, true);      // W^T (MN) x S0 (MN)
-constexpr uint32_t IDESC_Y = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);     // Q (K) x S0 (MN)
-constexpr uint32_t IDESC_C2 = tc::make_idesc(tc::kKindBF16, 128, 128, true, true);   // K^T (MN) x [Dt_hi | Dt_lo] (MN)
-constexpr uint32_t IDESC_PD2 = tc::make_idesc(tc::kKindBF16, 64, 128, false, true);  // P_hi (K) x [D_hi | D_lo] (MN)
-constexpr uint32_t IDESC_PD1 = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);   // P_lo (K) x D_hi (MN)
+constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // T'' (K) x V (MN)
+constexpr uint32_t IDESC_X = tc::make_idesc(tc::kKindBF16, 64, 64, true, true);     // W^T (MN) x S0 (MN)
+constexpr uint32_t IDESC_Y = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // Q (K) x S0 (MN)
+constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);    // K^T (MN) x Dt (MN)
+constexpr uint32_t IDESC_GP = tc::make_idesc(tc::kKindBF16, 64, 64, false, false);  // Q (K) x K (K)
+constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);   // P (K) x Delta (MN)
 
-enum : int {
-  B_QK0 = 0, B_QK1, B_TV, B_WC, B_PL, B_U, B_X, B_Y0, B_Y1, B_C, B_PD, B_DRDY, B_UFREE, B_OF0, B_OF1, kNumBars
-};
+enum : int { B_QK0 = 0, B_QK1, B_TV, B_WC, B_U, B_GP, B_X, B_Y, B_C, B_PD, B_SRDY, B_DRDY, B_UFREE, kNumBars };
 
 struct ChainParams {
   const float* vec;
@@ -92,8 +97,7 @@ __device__ __forceinline__ bool wg_any(int id, bool pred) {
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap twt,
-                   const __grid_constant__ CUtensorMap ttt, const __grid_constant__ CUtensorMap tpp,
-                   const ChainParams p) {
+                   const __grid_constant__ CUtensorMap ttt, const ChainParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_slot;
@@ -128,6 +132,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   float* const misc = reinterpret_cast<float*>(sm + OFF_MISC);
   float* const s_scale_slot = misc;                                       // [2], by chunk parity
+  int* const s_exact_slot = reinterpret_cast<int*>(misc + 2);             // [2]
   float* const red = misc + 4;                                            // [4]
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 8);
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
@@ -141,7 +146,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tc::tma_prefetch_desc(&tv);
     tc::tma_prefetch_desc(&twt);
     tc::tma_prefetch_desc(&ttt);
-    tc::tma_prefetch_desc(&tpp);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
   tc::tc_fence_before();
@@ -150,14 +154,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t tmem = tmem_slot;
 
   // operand descriptors (128-byte swizzle, 8-row groups 1024 bytes apart)
-  const uint64_t dStgK = tc::make_sdesc(sbase, 16, 1024);        // K-major Q of stage 0
+  const uint64_t dStgK = tc::make_sdesc(sbase, 16, 1024);        // K-major Q / K of stage 0
   const uint64_t dStgM = tc::make_sdesc(sbase, 16 * KB, 1024);   // MN-major K^T of stage 0
   const uint64_t dTT = tc::make_sdesc(sbase + OFF_TT, 16, 1024);
   const uint64_t dV = tc::make_sdesc(sbase + OFF_V, 8 * KB, 1024);
   const uint64_t dWT = tc::make_sdesc(sbase + OFF_WT, 16 * KB, 1024);
   const uint64_t dS = tc::make_sdesc(sbase + OFF_SHI, 16 * KB, 1024);
-  const uint64_t dD2 = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);             // [Delta_hi | Delta_lo]
-  const uint64_t dDt2 = tc::make_sdesc(sbase + OFF_DL + 16 * KB, 8 * KB, 1024);  // [Dt_hi | Dt_lo]
+  const uint64_t dDl = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);
   const uint64_t dP = tc::make_sdesc(sbase + OFF_P, 16, 1024);
 
   auto tma_qk = [&](int64_t cj) {   // Q, K tiles and gate vectors of chunk cj into stage cj & 1
@@ -186,15 +189,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tc::tma_load_2d(sbase + OFF_WT + 16 * KB, &twt, bar(B_WC), 0, (int)(item(cj) * 256 + 128));
     }
   };
-  auto tma_p = [&](int64_t cj) {   // P hi | lo of chunk cj
-    tc::mbar_expect_tx(bar(B_PL), 16 * KB);
-    tc::tma_load_2d(sbase + OFF_P, &tpp, bar(B_PL), 0, (int)(item(cj) * 128));
-  };
   if (tid == 0 && nchunks > 0) {
     tma_qk(0);
     tma_tv(0);
     tma_wc(0);
-    tma_p(0);
     if (nchunks > 1) tma_qk(1);
   }
 
@@ -203,15 +201,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   // barrier (wg_any), where they stop together. Nothing is issued once live() is false.
   bool ok = true;
   auto live = [&]() { return ok && !*abort_flag; };
-  auto wait = [&](int b, uint32_t par) {
-    if (live()) {
+  auto wait = [&](int b, uint32_t par) {   // warp-collective; the decision to wait is warp-uniform
+    if (__all_sync(0xffffffffu, live())) {
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(b), par));
       if (!ok && lt == 0) *abort_flag = 1;
+    } else {
+      ok = false;
     }
   };
 
   if (warp < 4) {
     // ================================ output warpgroup ================================
+    // U and G of chunk c + 1 are issued right after P Delta of chunk c, so that they are through
+    // the tensor pipe before the chain issues its next X.
     auto issue_u = [&]() {   // U = T'' V (T'' hi + lo)
       tc::tc_fence_after();
 #pragma unroll
@@ -221,77 +223,117 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           tc::mma_bf16(tmem + TM_U, dadv(dTT, part * 8 * KB + ks * 32), dadv(dV, ks * 2048), IDESC_U, (part | ks) != 0);
       tc::mma_commit(bar(B_U));
     };
+    auto issue_gp = [&](uint32_t stg) {   // G = Q K^T
+      tc::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = stg + (ks >> 2) * 16 * KB + (ks & 3) * 32;
+        tc::mma_bf16(tmem + TM_GP, dadv(dStgK, SQ0 + koff), dadv(dStgK, SK0 + koff), IDESC_GP, ks > 0);
+      }
+      tc::mma_commit(bar(B_GP));
+    };
     if (nchunks > 0) {
       wait(B_TV, 0);
-      if (tid == 0 && live()) issue_u();
+      if (tid == kOutIssuer && live()) issue_u();
+      wait(B_QK0, 0);
+      if (tid == kOutIssuer && live()) issue_gp(0);
     }
     for (int64_t c = 0; c < nchunks; ++c) {
       const int s = (int)(c & 1);
       const int L = chunk_len(c);
       const uint32_t par = (uint32_t)(c & 1);
-      const float* vg = reinterpret_cast<const float*>(sm + (uint32_t)s * kStage + SVEC);
-      // this chunk's Gam_r: read before P Delta is issued (the chain refills the stage once P Delta is done)
-      wait(B_QK0 + s, (uint32_t)((c >> 1) & 1));
-      const float egam_r = vg[64 + row64];
-      if (wg_any(1, !live())) break;
+      const uint32_t stg = (uint32_t)s * kStage;
+      const float* vg = reinterpret_cast<const float*>(sm + stg + SVEC);
       // T'' / V are free once U has read them: fetch the next chunk's (a whole chunk ahead)
-      if (warp == 0) {
+      if (warp == kOutIssuer / 32) {
         wait(B_U, par);
-        if (tid == 0 && c + 1 < nchunks && live()) tma_tv(c + 1);
+        if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_tv(c + 1);
       }
-      // ---- P Delta = P_hi [D_hi | D_lo] + P_lo D_hi once the chain has stored Delta ----
+      // ---- P = exp(gam_r - gam_i) G for i <= r -> bf16 hi | lo, K-major [r][i] ----
+      float egam_r;
+      wait(B_GP, par);
+      tc::tc_fence_after();
+      {
+        float v[32];
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_GP), v);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_GP + 16), v + 16);
+        tc::tmem_ld_wait();
+        const float gr = vg[row64];
+        egam_r = vg[64 + row64];   // kept for the output epilogue: the stage is refilled once Y is done
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {   // the exponent is clamped so both select inputs are finite
+          const int i = half * 32 + j;
+          const float e = __expf(fminf(gr - vg[i], 0.f)) * v[j];
+          v[j] = i <= row64 ? e : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 h16, l16;
+          split8(v + 8 * q, h16, l16);
+          const uint32_t off = tc::sw128(row64, 2 * (half * 32 + 8 * q));
+          st16(sm, OFF_P + off, h16);
+          st16(sm, OFF_P + 8 * KB + off, l16);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      if (wg_any(1, !live())) break;
+      // ---- Y = Q S0 once the chain has stored S0 for this chunk ----
+      wait(B_SRDY, par);
+      const float y_scale = s_scale_slot[s];
+      if (tid == kOutIssuer && live()) {
+        tc::tc_fence_after();
+        const int ny = s_exact_slot[s] ? 1 : 2;
+        for (int q = 0; q < ny; ++q)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_bf16(tmem + TM_Y, dadv(dStgK, SQ0 + stg + (ks >> 2) * 16 * KB + (ks & 3) * 32),
+                         dadv(dS, q * 16 * KB + ks * 2048), IDESC_Y, (q | ks) != 0);
+        tc::mma_commit(bar(B_Y));
+      }
+      // ---- P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi once the chain has stored Delta ----
       wait(B_DRDY, par);
-      const float y_scale = s_scale_slot[s];   // the scale of this chunk's S0 (stored before Delta)
-      wait(B_PL, par);
-      if (tid == 0 && live()) {
+      if (tid == kOutIssuer && live()) {
         tc::tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_PD, dadv(dP, ks * 32), dadv(dD2, ks * 2048), IDESC_PD2, ks > 0);
+        for (int q = 0; q < 3; ++q)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_PD, dadv(dP, 8 * KB + ks * 32), dadv(dD2, ks * 2048), IDESC_PD1, 1);
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + TM_PD, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32),
+                         dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048), IDESC_PD, (q | ks) != 0);
         tc::mma_commit(bar(B_PD));
       }
-      // ---- the next chunk's U, once the chain has read this one ----
+      // ---- the next chunk's U (once the chain has read this one) and G ----
       if (c + 1 < nchunks) {
         wait(B_TV, par ^ 1u);
         wait(B_UFREE, par);
-        if (tid == 0 && live()) issue_u();
+        if (tid == kOutIssuer && live()) issue_u();
+        wait(B_QK0 + (s ^ 1), (uint32_t)(((c + 1) >> 1) & 1));
+        if (tid == kOutIssuer && live()) issue_gp(stg ^ kStage);
       }
       // ---- o = scale (Gam Y + P Delta), rows r < L ----
-      wait(B_Y0 + s, (uint32_t)((c >> 1) & 1));
+      wait(B_Y, par);
       wait(B_PD, par);
-      if (tid == 0 && c + 1 < nchunks && live()) tma_p(c + 1);   // P has been read
       tc::tc_fence_after();
       {
-        float yv[32], pv[32], pw[32];
-        const uint32_t ty = TM_Y + (uint32_t)s * 64;
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, ty), yv);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, ty + 16), yv + 16);
+        float yv[32], pv[32];
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_Y), yv);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_Y + 16), yv + 16);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD), pv);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 16), pv + 16);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 64), pw);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 80), pw + 16);
         tc::tmem_ld_wait();
         if (row64 < L) {
           const float e2 = egam_r * y_scale;
           float4* out = reinterpret_cast<float4*>(p.o + ((t0 + c * 64 + row64) * p.Hv + h) * (int64_t)p.dv +
                                                   slab * 64 + half * 32);
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float4 r4;
-            r4.x = p.scale * fmaf(e2, yv[j], pv[j] + pw[j]);
-            r4.y = p.scale * fmaf(e2, yv[j + 1], pv[j + 1] + pw[j + 1]);
-            r4.z = p.scale * fmaf(e2, yv[j + 2], pv[j + 2] + pw[j + 2]);
-            r4.w = p.scale * fmaf(e2, yv[j + 3], pv[j + 3] + pw[j + 3]);
-            out[j >> 2] = r4;
-          }
+          for (int j = 0; j < 32; j += 4)
+            out[j >> 2] = make_float4(p.scale * fmaf(e2, yv[j], pv[j]), p.scale * fmaf(e2, yv[j + 1], pv[j + 1]),
+                                      p.scale * fmaf(e2, yv[j + 2], pv[j + 2]), p.scale * fmaf(e2, yv[j + 3], pv[j + 3]));
         }
       }
       tc::tc_fence_before();
       if (wg_any(1, !live())) break;
-      if (tid == 0) tc::mbar_arrive(bar(B_OF0 + s));   // TMEM Y buffer s has been read
     }
   } else {
     // ================================ chain warpgroup ================================
@@ -318,10 +360,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       st16(sm, OFF_SHI + off, h16);
       st16(sm, OFF_SHI + 16 * KB + off, l16);
     }
-    if (ctid == 0) s_scale_slot[0] = 1.f;
+    if (ctid == 0) {
+      s_scale_slot[0] = 1.f;
+      s_exact_slot[0] = 0;
+    }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     wg_sync(2);
+    if (ctid == 0) tc::mbar_arrive(bar(B_SRDY));
     bool s_exact = false;   // S0 operand holds exact codes with scale s_scale
     float s_scale = 1.f;
     for (int64_t c = 0; c < nchunks; ++c) {
@@ -333,9 +379,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       wait(B_QK0 + s, (uint32_t)((c >> 1) & 1));
       const float dr = vg[128 + row64], el = vg[64 + 63];
       const float f = vg[192] * s_scale;   // X = W S0 holds codes x codes: W scale x S0 scale
-      // ---- X = W S0, then Y = Q S0 (into TMEM Y buffer s once the output side has read it) ----
+      // ---- X = W S0 ----
       wait(B_WC, par);
-      if (ctid == 0 && live()) {
+      if (ctid == kChainIssuer && live()) {
         tc::tc_fence_after();
         // (W codes or W hi) x (S codes or S hi) [+ W x S lo] [+ W lo x S hi]
 #pragma unroll
@@ -353,29 +399,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         tc::mma_commit(bar(B_X));
       }
-      if (c >= 2) wait(B_OF0 + s, (uint32_t)(((c - 2) >> 1) & 1));
-      if (ctid == 0 && live()) {
-        const uint32_t ty = TM_Y + (uint32_t)s * 64;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tmem + ty, dadv(dStgK, SQ0 + stg + (ks >> 2) * 16 * KB + (ks & 3) * 32), dadv(dS, ks * 2048),
-                       IDESC_Y, ks > 0);
-        if (!s_exact) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tmem + ty, dadv(dStgK, SQ0 + stg + (ks >> 2) * 16 * KB + (ks & 3) * 32),
-                         dadv(dS, 16 * KB + ks * 2048), IDESC_Y, 1);
-        }
-        tc::mma_commit(bar(B_Y0 + s));
-      }
       wait(B_X, par);
-      if (ctid == 0 && c + 1 < nchunks && live()) tma_wc(c + 1);   // W^T is free once X has read it
+      if (ctid == kChainIssuer && c + 1 < nchunks && live()) tma_wc(c + 1);   // W^T is free once X has read it
       // ---- Delta = U - f X, Dt = exp(gam_63 - gam_r) Delta ----
       wait(B_U, par);
       if (c > 0) wait(B_PD, (uint32_t)((c - 1) & 1));   // the previous P Delta has read Delta
-      // the previous chunk's stage is free (its C and Y are done, and the output side read its
-      // gate vectors before issuing that P Delta): fetch chunk c + 1 into it
-      if (ctid == 0 && c >= 1 && c + 1 < nchunks && live()) tma_qk(c + 1);
       tc::tc_fence_after();
       float d[32];
       {
@@ -403,13 +431,16 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
-      if (ctid == 0) {
-        tc::mbar_arrive(bar(B_UFREE));   // U has been read
+      if (ctid == 0) tc::mbar_arrive(bar(B_UFREE));   // U has been read
+      if (ctid == kChainIssuer) {
         tc::tc_fence_after();
-        // C = K^T [Dt_hi | Dt_lo]
+        // C = K^T Dt (Dt hi + lo)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_C, dadv(dStgM, stg + SK0 + ks * 2048), dadv(dDt2, ks * 2048), IDESC_C2, ks > 0);
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + TM_C, dadv(dStgM, stg + SK0 + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
+                         IDESC_C, (part | ks) != 0);
         tc::mma_commit(bar(B_C));
       }
       // Delta hi | lo for the output warpgroup's P Delta (while C runs)
@@ -424,22 +455,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tc::fence_proxy_async_smem();
       if (wg_any(2, !live())) break;
       if (ctid == 0) tc::mbar_arrive(bar(B_DRDY));
-      // ---- S1 = Gam_63 S0 + C_hi + C_lo; QDQ at the 64-token boundary (after Y has read S0) ----
+      // ---- S1 = Gam_63 S0 + C; QDQ at the 64-token boundary (after Y has read S0) ----
       wait(B_C, par);
-      wait(B_Y0 + s, (uint32_t)((c >> 1) & 1));
+      wait(B_Y, par);
       tc::tc_fence_after();
       {
         float* const s1 = S;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float ch[32], cl[32];
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + h2 * 32), ch);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + h2 * 32 + 16), ch + 16);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 64 + h2 * 32), cl);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 64 + h2 * 32 + 16), cl + 16);
+        {
+          float cv[64];
+          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C), cv);
+          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 16), cv + 16);
+          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 32), cv + 32);
+          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 48), cv + 48);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) s1[h2 * 32 + j] = fmaf(el, s1[h2 * 32 + j], ch[j] + cl[j]);
+          for (int j = 0; j < 64; ++j) s1[j] = fmaf(el, s1[j], cv[j]);
         }
         if (p.state_qdq && L == 64) {
           float m8[8];
@@ -476,10 +506,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           s_scale = 1.f;
         }
       }
-      if (ctid == 0) s_scale_slot[s ^ 1] = s_scale;
+      if (ctid == 0) {
+        s_scale_slot[s ^ 1] = s_scale;
+        s_exact_slot[s ^ 1] = s_exact ? 1 : 0;
+      }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
+      if (ctid == 0) {
+        tc::mbar_arrive(bar(B_SRDY));   // S0 of chunk c + 1 is stored
+      }
+      // stage s is free: C and Y (committed after G) have read it, and the output warpgroup read its
+      // gate vectors before issuing Y -- fetch chunk c + 2 into it
+      if (ctid == kChainIssuer && c + 2 < nchunks && live()) tma_qk(c + 2);
     }
     if (live() && p.hT) {
       float4* out = reinterpret_cast<float4*>(p.hT + sb + (int64_t)lane128 * p.dv);
@@ -494,8 +533,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       atomicExch(p.status, 1);
       // TMA loads may still be landing in this CTA's shared memory: wait for each barrier's
       // current phase (one of the two parities returns at once), bounded
-      const int tx_bars[5] = {B_QK0, B_QK1, B_TV, B_WC, B_PL};
-      for (int i = 0; i < 5; ++i) {
+      const int tx_bars[4] = {B_QK0, B_QK1, B_TV, B_WC};
+      for (int i = 0; i < 4; ++i) {
         tc::mbar_wait(bar(tx_bars[i]), 0, 1u << 14);
         tc::mbar_wait(bar(tx_bars[i]), 1, 1u << 14);
       }
@@ -520,8 +559,7 @@ SplitLayout chunk_split_layout(const ChunkProblem& p) {
   auto up = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
   l.off_wt = up(kStatusBytes);
   l.off_tt = up(l.off_wt + (size_t)l.items * l.wt_item_bytes);
-  l.off_p = up(l.off_tt + (size_t)l.items * 16 * KB);
-  l.off_vec = up(l.off_p + (size_t)l.items * 16 * KB);
+  l.off_vec = up(l.off_tt + (size_t)l.items * 16 * KB);
   l.total = l.off_vec + (size_t)l.items * 1024;
   return l;
 }
@@ -536,18 +574,17 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   if (blocks == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)p.B * p.T;
   const int64_t tmap = tokens > 0 ? tokens : 1;   // an empty batch still needs valid maps (never loaded)
-  CUtensorMap tq, tk, tv, twt, ttt, tpp;
+  CUtensorMap tq, tk, tv, twt, ttt;
   if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap) ||
       !make_bf16_map(&tv, p.v, p.dv, p.Hv, tmap) ||
       !make_bf16_rows_map(&twt, w + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 128) ||
-      !make_bf16_rows_map(&ttt, w + lay.off_tt, lay.items * 128, 128) ||
-      !make_bf16_rows_map(&tpp, w + lay.off_p, lay.items * 128, 128))
+      !make_bf16_rows_map(&ttt, w + lay.off_tt, lay.items * 128, 128))
     return cudaErrorInvalidValue;
   ChainParams cp{reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT, reinterpret_cast<int*>(ws),
                  p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, twt, ttt, tpp, cp);
+  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, twt, ttt, cp);
   return cudaGetLastError();
 }
 

@@ -3,9 +3,8 @@
 //
 // For chunk c of sequence n and v-head h (L <= 64 tokens; rows r >= L carry beta = g = 0 and so
 // drop out), with gam = prefix sums of g inside the chunk and Gam = exp(gam):
-//   G1     [Q; K] K^T                              tcgen05 bf16, M=128 N=64 K=128 (exact products)
+//   G      K K^T                                   tcgen05 bf16, M=64 N=64 K=128 (exact products)
 //   A      A[r][i] = beta_r exp(gam_r - gam_i) (k_r . k_i), i < r
-//   P      P[r][i] = exp(gam_r - gam_i) (q_r . k_i), i <= r    -> workspace as bf16 hi + lo
 //   T      (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then three levels of
 //          the off-diagonal block recurrence (CUDA cores, fp32)
 //   T''    T diag(beta)                 -> workspace as bf16 hi + lo (the chain forms U = T'' V)
@@ -33,21 +32,18 @@ constexpr int kThreads = 128;
 constexpr uint32_t KB = 1024;
 constexpr uint32_t A_LD = 68;
 // shared memory map (byte offsets from a 1024-byte aligned base)
-// Q0 | K0 | Q1 | K1: the Q and K tiles, key columns 0-63 | 64-127, [64 tok][64] bf16 each, so that
-// [Q; K] is one M = 128 operand per key block. After G1 the Q slots hold T' hi | lo (the B operand of
-// W^T), then the W^T codes (rows c 0-63 | 64-127); without W QDQ the W^T lo part goes to the K slots.
-constexpr uint32_t OFF_Q0 = 0, OFF_K0 = 8 * KB, OFF_Q1 = 16 * KB, OFF_K1 = 24 * KB;
-constexpr uint32_t OFF_A = 32 * KB;                    // A fp32 [64][68]; after the solve: T'' hi | lo
-constexpr uint32_t OFF_T = 49 * KB;                    // T fp32 [64][68]; after the solve: P hi | lo
+constexpr uint32_t OFF_K = 0;                          // K tile: key columns 0-63 | 64-127, [64 tok][64] bf16 each
+constexpr uint32_t OFF_A = 16 * KB;                    // A fp32 [64][68]; after the solve: T'' hi | lo
+constexpr uint32_t OFF_T = 34 * KB;                    // T fp32 [64][68]
 constexpr uint32_t OFF_SCR = OFF_T + 64 * A_LD * 4;    // solve scratch, 3 x 16 x 16 fp32
-constexpr uint32_t OFF_VEC = 69 * KB;                  // gam, Gam, decay-to-end, beta [64]; 4 partial maxima
+constexpr uint32_t OFF_W = 54 * KB;                    // T' hi | lo; after the W MMA: W^T codes (or hi)
+constexpr uint32_t OFF_VEC = 70 * KB;                  // gam, Gam, decay-to-end, beta [64]; 4 partial maxima
 constexpr uint32_t kSmemBytes = OFF_VEC + 4 * 256 + 64 + 1024;   // + slack to align the base
-static_assert(OFF_A + 64 * A_LD * 4 <= OFF_T, "A overlaps T");
-static_assert(OFF_SCR + 3 * 1024 <= OFF_VEC, "solve scratch overlaps the vectors");
+static_assert(OFF_SCR + 3 * 1024 <= OFF_W, "solve scratch overlaps the W region");
 
-constexpr uint32_t TM_G = 0, TM_WT = 64;   // G1 rows 0-63 = Q K^T (lanes 0-63), rows 64-127 = K K^T
+constexpr uint32_t TM_G = 0, TM_WT = 64;
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t IDESC_G = tc::make_idesc(tc::kKindBF16, 128, 64, false, false);
+constexpr uint32_t IDESC_G = tc::make_idesc(tc::kKindBF16, 64, 64, false, false);
 constexpr uint32_t IDESC_WT = tc::make_idesc(tc::kKindBF16, 128, 64, true, false);
 
 struct PrepParams {
@@ -65,9 +61,8 @@ __device__ __forceinline__ int64_t seq_start(const PrepParams& p, int n) {
 }
 
 __global__ void __launch_bounds__(kThreads, 3)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap twt, const __grid_constant__ CUtensorMap ttt,
-                  const __grid_constant__ CUtensorMap tpp, const PrepParams p) {
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap twt,
+                  const __grid_constant__ CUtensorMap ttt, const PrepParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[3];
   __shared__ uint32_t tmem_slot;
@@ -107,11 +102,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) tc::mbar_init(tc::smem_u32(&bars[i]), 1);
     tc::mbar_fence_init();
-    tc::mbar_expect_tx(bar_k, 32 * KB);
-    tc::tma_load_3d(sbase + OFF_Q0, &tq, bar_k, 0, hq, tok);
-    tc::tma_load_3d(sbase + OFF_K0, &tk, bar_k, 0, hq, tok);
-    tc::tma_load_3d(sbase + OFF_Q1, &tq, bar_k, 64, hq, tok);
-    tc::tma_load_3d(sbase + OFF_K1, &tk, bar_k, 64, hq, tok);
+    tc::mbar_expect_tx(bar_k, 16 * KB);
+    tc::tma_load_3d(sbase + OFF_K, &tk, bar_k, 0, hq, tok);
+    tc::tma_load_3d(sbase + OFF_K + 8 * KB, &tk, bar_k, 64, hq, tok);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
   if (warp == 1) {   // gates: prefix sums of g in the chunk, Gam, decay to the chunk end, beta
@@ -142,22 +135,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  const uint64_t dQK = tc::make_sdesc(sbase + OFF_Q0, 16, 1024);      // K-major [Q; K] rows, K tile at +8 KB
-  const uint64_t dKt = tc::make_sdesc(sbase + OFF_K0, 16 * KB, 1024);  // MN-major K^T (key blocks 16 KB apart)
-  const uint64_t dTp = tc::make_sdesc(sbase + OFF_Q0, 16, 1024);       // K-major T' [r][i]: hi in Q0, lo in Q1
+  const uint64_t dK = tc::make_sdesc(sbase + OFF_K, 16, 1024);         // K-major [tok][c]
+  const uint64_t dKt = tc::make_sdesc(sbase + OFF_K, 8 * KB, 1024);    // MN-major K^T
+  const uint64_t dTp = tc::make_sdesc(sbase + OFF_W, 16, 1024);        // K-major T' [r][i]
 
   bool ok = true;
   bool k_done = false;   // the K tile has landed (nothing left in flight on bar_k)
   float sW = 1.f;
   do {
-    // ---- G1 = [Q; K] K^T ----
+    // ---- G = K K^T ----
     if (warp == 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_k, 0));
     if (tid == 0 && ok) {
       tc::tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks >> 2) * 16 * KB + (ks & 3) * 32;
-        tc::mma_bf16(tmem + TM_G, dadv(dQK, koff), dadv(dQK, OFF_K0 + koff), IDESC_G, ks > 0);
+        const uint32_t koff = (ks >> 2) * 8 * KB + (ks & 3) * 32;
+        tc::mma_bf16(tmem + TM_G, dadv(dK, koff), dadv(dK, koff), IDESC_G, ks > 0);
       }
       tc::mma_commit(bar_g);
     }
@@ -167,26 +160,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (__syncthreads_or(!ok)) break;
     tc::tc_fence_after();
 
-    // ---- A from the K K^T rows of G1 (warps 2, 3: TMEM lanes 64-127) ----
-    if (warp >= 2) {
-      const int r = tid - 64;
+    // ---- A (M = 64 accumulator: row 16 w + t % 16, columns 32 (t / 16) .. + 31) ----
+    {
+      const int r = warp * 16 + (lt & 15), half = lt >> 4;
+      float v[32];
+      tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_G), v);
+      tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_G + 16), v + 16);
+      tc::tmem_ld_wait();
       const float gr = vgam[r], br = vbeta[r];
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float v[32];
-        ld32(tmem, lane0, TM_G + h2 * 32, v);
-        float4* dst = reinterpret_cast<float4*>(Am + r * A_LD + h2 * 32);
+      float4* dst = reinterpret_cast<float4*>(Am + r * A_LD + half * 32);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float a4[4];
+      for (int j = 0; j < 32; j += 4) {
+        float a4[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {   // the exponent is clamped so both select inputs are finite
-            const int i = h2 * 32 + j + u;
-            const float e = br * __expf(fminf(gr - vgam[i], 0.f)) * v[j + u];
-            a4[u] = i < r ? e : 0.f;
-          }
-          dst[j >> 2] = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        for (int u = 0; u < 4; ++u) {   // the exponent is clamped so both select inputs are finite
+          const int i = half * 32 + j + u;
+          const float e = br * __expf(fminf(gr - vgam[i], 0.f)) * v[j + u];
+          a4[u] = i < r ? e : 0.f;
         }
+        dst[j >> 2] = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
     }
     __syncthreads();
@@ -268,7 +260,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       __syncthreads();
     }
 
-    // ---- T'' = T diag(beta) -> the A region, T' = T'' diag(Gam) -> the Q slots (bf16 hi | lo, [r][i]) ----
+    // ---- T'' = T diag(beta) -> the A region, T' = T'' diag(Gam) -> the W region (bf16 hi | lo, [r][i]) ----
 #pragma unroll 1
     for (int t = 0; t < 4; ++t) {
       const int task = tid + t * kThreads, r = task >> 3, i0 = (task & 7) * 8;
@@ -287,58 +279,30 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       st16(sm, OFF_A + off, h16);
       st16(sm, OFF_A + 8 * KB + off, l16);
       split8(t1, h16, l16);
-      st16(sm, OFF_Q0 + off, h16);
-      st16(sm, OFF_Q1 + off, l16);
+      st16(sm, OFF_W + off, h16);
+      st16(sm, OFF_W + 8 * KB + off, l16);
     }
     tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
       tc::tma_store_2d(&ttt, sbase + OFF_A, 0, (int)(item * 128));   // T'' hi (rows 0-63) | lo (64-127)
       tc::bulk_commit();
       tc::tc_fence_after();
-      // W^T = K^T T'^T: A = K^T (MN-major, key blocks 16 KB apart), B = T' hi / lo (K-major [r][i])
+      // W^T = K^T T'^T: A = K^T (MN-major, key blocks 8 KB apart), B = T' hi / lo (K-major [r][i])
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_WT, dadv(dKt, ks * 2048), dadv(dTp, part * 16 * KB + ks * 32), IDESC_WT,
+          tc::mma_bf16(tmem + TM_WT, dadv(dKt, ks * 2048), dadv(dTp, part * 8 * KB + ks * 32), IDESC_WT,
                        (part | ks) != 0);
       tc::mma_commit(bar_w);
-    }
-    // ---- P from the Q K^T rows of G1 (warps 0, 1: TMEM lanes 0-63) -> the T region (T is consumed) ----
-    if (warp < 2) {
-      const int r = tid;
-      const float gr = vgam[r];
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float v[32];
-        ld32(tmem, lane0, TM_G + h2 * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {   // the exponent is clamped so both select inputs are finite
-          const int i = h2 * 32 + j;
-          const float e = __expf(fminf(gr - vgam[i], 0.f)) * v[j];
-          v[j] = i <= r ? e : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 h16, l16;
-          split8(v + 8 * q, h16, l16);
-          const uint32_t off = tc::sw128(r, 2 * (h2 * 32 + 8 * q));
-          st16(sm, OFF_T + off, h16);
-          st16(sm, OFF_T + 8 * KB + off, l16);
-        }
-      }
-      tc::fence_proxy_async_smem();
     }
     ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_w, 0));
     if (__syncthreads_or(!ok)) break;
     tc::tc_fence_after();
 
-    // ---- W QDQ: thread = key channel c (TMEM lane), its 64 values W[r][c]; row c of W^T goes to the
-    // Q0 slot (c < 64) or the Q1 slot (c >= 64) ----
+    // ---- W QDQ: thread = key channel c (TMEM lane), its 64 values W[r][c] ----
     {
-      const uint32_t wrow = tid < 64 ? OFF_Q0 : OFF_Q1;
       float w[64];
       ld32(tmem, lane0, TM_WT, w);
       ld32(tmem, lane0, TM_WT + 32, w + 32);
@@ -357,15 +321,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           float cd[8], dq[8];
 #pragma unroll
           for (int u = 0; u < 8; u += 2) qdq_pair(w[8 * q + u], w[8 * q + u + 1], rW, sW, cd[u], cd[u + 1], dq[u], dq[u + 1]);
-          st16(sm, wrow + tc::sw128(tid & 63, 16 * q), pack8(cd));
+          st16(sm, OFF_W + tc::sw128(tid, 16 * q), pack8(cd));
         }
-      } else {   // hi -> the Q slots, lo -> the K slots (the MMAs that read them are done)
+      } else {   // hi -> the W region, lo -> the K region (both MMAs that read them are done)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           uint4 h16, l16;
           split8(w + 8 * q, h16, l16);
-          st16(sm, wrow + tc::sw128(tid & 63, 16 * q), h16);
-          st16(sm, wrow + 8 * KB + tc::sw128(tid & 63, 16 * q), l16);
+          st16(sm, OFF_W + tc::sw128(tid, 16 * q), h16);
+          st16(sm, OFF_K + tc::sw128(tid, 16 * q), l16);
         }
       }
     }
@@ -373,15 +337,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-      tc::tma_store_2d(&tpp, sbase + OFF_T, 0, (int)(item * 128));   // P hi (rows 0-63) | lo (64-127)
       if (p.w_qdq) {
-        tc::tma_store_2d(&twt, sbase + OFF_Q0, 0, (int)(item * 128));
-        tc::tma_store_2d(&twt, sbase + OFF_Q1, 0, (int)(item * 128 + 64));
+        tc::tma_store_2d(&twt, sbase + OFF_W, 0, (int)(item * 128));
       } else {
-        tc::tma_store_2d(&twt, sbase + OFF_Q0, 0, (int)(item * 256));
-        tc::tma_store_2d(&twt, sbase + OFF_Q1, 0, (int)(item * 256 + 64));
-        tc::tma_store_2d(&twt, sbase + OFF_K0, 0, (int)(item * 256 + 128));
-        tc::tma_store_2d(&twt, sbase + OFF_K1, 0, (int)(item * 256 + 192));
+        tc::tma_store_2d(&twt, sbase + OFF_W, 0, (int)(item * 256));
+        tc::tma_store_2d(&twt, sbase + OFF_K, 0, (int)(item * 256 + 128));
       }
       tc::bulk_commit();
       p.vec[item * 256 + 192] = sW;
@@ -405,18 +365,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 cudaError_t launch_chunk_prep(const ChunkProblem& p, const SplitLayout& lay, unsigned char* ws, cudaStream_t stream) {
   if (lay.items == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)p.B * p.T;
-  CUtensorMap tq, tk, twt, ttt, tpp;
-  if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tokens > 0 ? tokens : 1) ||
-      !make_bf16_map(&tk, p.k, 128, p.Hqk, tokens > 0 ? tokens : 1) ||
-      !make_bf16_rows_map(&twt, ws + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 64) ||
-      !make_bf16_rows_map(&ttt, ws + lay.off_tt, lay.items * 128, 128) ||
-      !make_bf16_rows_map(&tpp, ws + lay.off_p, lay.items * 128, 128))
+  CUtensorMap tk, twt, ttt;
+  if (!make_bf16_map(&tk, p.k, 128, p.Hqk, tokens > 0 ? tokens : 1) ||
+      !make_bf16_rows_map(&twt, ws + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 128) ||
+      !make_bf16_rows_map(&ttt, ws + lay.off_tt, lay.items * 128, 128))
     return cudaErrorInvalidValue;
   PrepParams pp{p.g, p.beta, p.cu, reinterpret_cast<float*>(ws + lay.off_vec), reinterpret_cast<int*>(ws),
                 p.T, p.N, p.Hqk, p.Hv, p.w_qdq};
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_prep_kernel<<<(unsigned)lay.items, kThreads, kSmemBytes, stream>>>(tq, tk, twt, ttt, tpp, pp);
+  chunk_prep_kernel<<<(unsigned)lay.items, kThreads, kSmemBytes, stream>>>(tk, twt, ttt, pp);
   return cudaGetLastError();
 }
 

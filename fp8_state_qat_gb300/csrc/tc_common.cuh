@@ -55,6 +55,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 // Bounded wait: gives up after `limit` polls (each poll may itself suspend briefly) and
 // returns false; callers record the failure in the device status word and wind down.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint32_t limit = (1u << 22)) {
