@@ -251,17 +251,19 @@ class PrefillCase:
         self.fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
         self.sets = [self.resident(), self.resident()]
         self.cu = x.cu_seqlens
-        # dk = 128 GDN with the full workspace: a parallel prep kernel, then the state chain
-        self.launches = 2 if (not x.kda and s["dk"] == 128) else 1
+        # dk = 128 with the full workspace: a parallel prep kernel, then the state chain
+        self.launches = 2 if s["dk"] == 128 else 1
 
     def scope(self):
         if self.launches == 2:
-            return "one step = chunk_prep_kernel + chunk_chain_kernel; achieved is over both"
+            pre = "chunk_prep_kda_kernel + chunk_chain_kda_kernel" if self.x.kda else \
+                "chunk_prep_kernel + chunk_chain_kernel"
+            return f"one step = {pre}; achieved is over both"
         return "one step = one kernel launch"
 
     def workspace_bytes(self):
         return self.gdn.chunk_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu, state_qdq=self.x.state_qdq,
-                                              w_qdq=self.x.w_qdq)
+                                              w_qdq=self.x.w_qdq, kda=self.x.kda)
 
     def resident(self):
         x, s, dev, torch = self.x, self.s, self.dev, self.torch

@@ -101,10 +101,13 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
   ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
                  (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
-  // dk = 128 GDN: the two-kernel path (parallel prep, then the state chain) when the workspace
-  // holds its staging, else the single fused kernel; other shapes and KDA: CUDA cores
+  // dk = 128: the two-kernel path (parallel prep, then the state chain) when the workspace
+  // holds its staging, else (GDN) the single fused kernel; other shapes and KDA with a small
+  // workspace: CUDA cores
   cudaError_t e;
-  if (gdn::chunk_split_supported(p) && ws_bytes >= gdn::chunk_split_layout(p).total)
+  if (gdn::kda_split_supported(p) && ws_bytes >= gdn::kda_split_layout(p).total)
+    e = gdn::launch_kda_split(p, ws, stream);
+  else if (gdn::chunk_split_supported(p) && ws_bytes >= gdn::chunk_split_layout(p).total)
     e = gdn::launch_chunk_split(p, ws, stream);
   else if (gdn::chunk_tc_supported(p))
     e = gdn::launch_chunk_tc(p, static_cast<int*>(ws), stream);
@@ -139,6 +142,15 @@ size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args) {
                               (args->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 0};
     if (gdn::chunk_split_supported(p)) return gdn::chunk_split_layout(p).total;
   }
+  return kWorkspaceBytes;
+}
+
+size_t kda_chunk_fwd_workspace_size(const gdn_chunk_args* args) {
+  if (validate_chunk(args, true) != GDN_OK) return 0;
+  const gdn::ChunkProblem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                            args->B, args->T, args->N, args->Hqk, args->Hv, args->dk, args->dv, args->scale,
+                            (args->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 1};
+  if (gdn::kda_split_supported(p)) return gdn::kda_split_layout(p).total;
   return kWorkspaceBytes;
 }
 

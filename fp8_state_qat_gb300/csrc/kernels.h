@@ -60,6 +60,22 @@ SplitLayout chunk_split_layout(const ChunkProblem& p);
 // ws: the workspace (status word at offset 0), ws_bytes >= chunk_split_layout(p).total.
 cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t stream);
 
+// ---- the same split for KDA (per-key-channel decay), dk = 128 ----
+// Per item the KDA prep kernel stores W^T, T'' as for GDN, plus
+//   P    bf16 [2][64 r][64 i]: hi | lo of sum_c q_r[c] k_i[c] exp(gam_r[c] - gam_i[c]), i <= r;
+//   Qd   bf16 [2][2][64 r][64 c]: hi | lo of q_r[c] exp(gam_r[c]), key blocks c < 64 | c >= 64;
+//   Kd   bf16 [2][2][64 i][64 c]: hi | lo of k_i[c] exp(gam_63[c] - gam_i[c]), same blocks;
+//   vec  fp32 [256]: exp(gam_63[c]) for c < 128, W scale at index 192.
+struct KdaLayout {
+  int64_t slots, items;
+  size_t wt_item_bytes;
+  size_t off_wt, off_tt, off_p, off_qd, off_kd, off_vec;
+  size_t total;
+};
+bool kda_split_supported(const ChunkProblem& p);
+KdaLayout kda_split_layout(const ChunkProblem& p);
+cudaError_t launch_kda_split(const ChunkProblem& p, void* ws, cudaStream_t stream);
+
 // Per-CTA fp32 chunked forward on CUDA cores: one CTA per (sequence, head, 64-column
 // value slab). Used for shapes and variants the tensor-core path does not take.
 cudaError_t launch_chunk_simt(const ChunkProblem& p, cudaStream_t stream);

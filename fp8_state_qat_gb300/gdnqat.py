@@ -28,7 +28,8 @@ GDN_FLAG_W_QDQ = 2
 GDN_FLAG_KDA = 4
 
 # every extern "C" symbol of include/gdnqat.h
-EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc", "kda_chunk_fwd",
+EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
+            "kda_chunk_fwd_workspace_size", "kda_chunk_fwd",
             "gdn_decode_step", "fp8_tile_qdq", "gdn_status_string", "gdn_check_device_status")
 
 
@@ -68,8 +69,9 @@ def load(build_if_missing: bool = True):
             _build.build()
         lib = ctypes.CDLL(_build.LIB_PATH)
         P, I32, U32, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float
-        lib.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
-        lib.gdn_chunk_fwd_workspace_size.argtypes = [ctypes.POINTER(ChunkArgs)]
+        for fn in ("gdn_chunk_fwd_workspace_size", "kda_chunk_fwd_workspace_size"):
+            getattr(lib, fn).restype = ctypes.c_size_t
+            getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs)]
         for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
             getattr(lib, fn).restype = ctypes.c_int
             getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, ctypes.c_size_t, P]
@@ -118,14 +120,15 @@ def _dev(t, dtype, name):
     return t
 
 
-def workspace_bytes(args: ChunkArgs) -> int:
-    return int(load().gdn_chunk_fwd_workspace_size(ctypes.byref(args)))
+def workspace_bytes(args: ChunkArgs, kda: bool = False) -> int:
+    fn = "kda_chunk_fwd_workspace_size" if kda else "gdn_chunk_fwd_workspace_size"
+    return int(getattr(load(), fn)(ctypes.byref(args)))
 
 
-def chunk_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False, w_qdq=False):
-    """gdn_chunk_fwd_workspace_size for q [B,T,Hqk,dk], v [B,T,Hv,dv] (shapes only): the
-    workspace of the fastest path. The size depends on shapes and flags only, so the query
-    passes distinct placeholder device addresses."""
+def chunk_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False, w_qdq=False, kda=False):
+    """gdn_chunk_fwd_workspace_size (kda: kda_chunk_fwd_workspace_size) for q [B,T,Hqk,dk],
+    v [B,T,Hv,dv] (shapes only): the workspace of the fastest path. The size depends on shapes
+    and flags only, so the query passes distinct placeholder device addresses."""
     B, T, Hqk, dk = q_shape
     Hv, dv = v_shape[2], v_shape[3]
     cu_host, N = None, B
@@ -136,7 +139,7 @@ def chunk_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False,
     flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_W_QDQ if w_qdq else 0)
     a = ChunkArgs(fake[0], fake[1], fake[2], fake[3], fake[4], None, fake[6] if cu_host is not None else None,
                   _ptr(cu_host), fake[8], fake[9], B, T, N, Hqk, Hv, dk, dv, 1.0, flags)
-    return workspace_bytes(a)
+    return workspace_bytes(a, kda)
 
 
 def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state):
@@ -173,7 +176,7 @@ def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o
     a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
                                     output_final_state)
     dev = o.device
-    need = workspace_bytes(a)
+    need = workspace_bytes(a, fn_name == "kda_chunk_fwd")
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     st = getattr(lib, fn_name)(ctypes.byref(a), _ptr(workspace), workspace.numel(), _stream(stream, dev))

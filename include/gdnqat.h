@@ -126,8 +126,20 @@ gdn_status gdn_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t wor
  *    gdn_check_device_status. */
 gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream);
 
+/* Bytes of device workspace for the fastest kda_chunk_fwd path with these arguments; 0 when
+ * the arguments are invalid. For dk = 128 that is the status word plus the staging of the
+ * two-kernel path: per 64-token chunk slot and v-head, W (transposed, as for
+ * gdn_chunk_fwd_workspace_size), T diag(beta), the intra-chunk P = decay-weighted Q K^T, Q and
+ * K scaled by their per-channel decays (all bf16 hi + lo) and the chunk's per-channel total
+ * decay -- 113 KB (129 KB without W QDQ) for each of (B T / 64 + N) x Hv slots. Otherwise
+ * GDN_CHUNK_MIN_WORKSPACE_BYTES. */
+size_t kda_chunk_fwd_workspace_size(const gdn_chunk_args* args);
+
 /* KDA variant ([K]): same contract with g [B, T, Hv, dk], one log-decay per key channel;
- * pairwise decays come from differences of prefix sums of g within a chunk. */
+ * pairwise decays come from differences of prefix sums of g within a chunk. With
+ * kda_chunk_fwd_workspace_size(args) bytes or more (and g 16-byte aligned), dk = 128 runs as
+ * two tensor-core kernels (every chunk's state-independent work in parallel, then the state
+ * carry); otherwise on CUDA cores, chunk by chunk (slower, same arithmetic). */
 gdn_status kda_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
                          gdn_stream_t stream);
 

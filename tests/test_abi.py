@@ -107,6 +107,25 @@ def test_workspace_size_covers_the_two_kernel_staging(so):
     assert so.gdn_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=64))) == MIN_WS
 
 
+def test_kda_workspace_size_covers_the_two_kernel_staging(so):
+    """KDA, dk = 128: status word + per (chunk slot, v-head) W^T (16 / 32 KB), T'' (16 KB), P
+    (16 KB), Q and K times their per-channel decays (32 KB each, bf16 hi + lo) and the decay
+    vectors (1 KB). dk = 64: the minimum (CUDA-core path); invalid arguments: 0."""
+    for flags, wt in ((B.GDN_FLAG_STATE_QDQ | B.GDN_FLAG_W_QDQ, 16), (B.GDN_FLAG_STATE_QDQ, 32)):
+        a = good_args(flags=flags)
+        items = (a.B * a.T // 64 + a.N) * a.Hv
+        need = so.kda_chunk_fwd_workspace_size(ctypes.byref(a))
+        per = (wt + 16 + 16 + 32 + 32 + 1) * 1024
+        assert MIN_WS + items * per <= need <= MIN_WS + items * per + 8 * 1024
+    assert so.kda_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=64))) == MIN_WS
+    assert so.kda_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=96))) == 0
+    # the binding's shape-only query agrees with the C call
+    a = good_args(flags=B.GDN_FLAG_STATE_QDQ)
+    q_shape, v_shape = (a.B, a.T, a.Hqk, a.dk), (a.B, a.T, a.Hv, a.dv)
+    assert B.chunk_workspace_bytes(q_shape, v_shape, state_qdq=True, kda=True) == \
+        so.kda_chunk_fwd_workspace_size(ctypes.byref(a))
+
+
 def test_decode_and_qdq_validation(so):
     P = ctypes.c_void_p
     ptrs = [P(FAKE + (i << 32)) for i in range(7)]

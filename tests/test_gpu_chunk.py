@@ -16,8 +16,9 @@ from helpers import TOL_OFF, TOL_QDQ, compare_units, mask_for, sample_units, to_
 pytestmark = pytest.mark.gpu
 
 
-# dk = 128 GDN has two paths: "split" (the workspace holds the per-chunk staging: a parallel
-# prep kernel, then the state chain) and "fused" (the minimum 256-byte workspace: one kernel)
+# dk = 128 has two paths: "split" (the workspace holds the per-chunk staging: a parallel prep
+# kernel, then the state chain, both on tensor cores) and "fused" (the minimum 256-byte
+# workspace: one kernel; for KDA the CUDA-core kernel)
 PATHS = ["split", "fused"]
 
 
@@ -78,8 +79,6 @@ def test_lengths_and_shapes(gdn, oracle_mod, T, dk, dv, path):
 @pytest.mark.parametrize("kda", [False, True])
 @pytest.mark.parametrize("state_qdq,w_qdq", QDQ_MODES)
 def test_varlen_gqa(gdn, oracle_mod, kda, state_qdq, w_qdq, path):
-    if kda and path == "fused":
-        pytest.skip("KDA has a single path")
     lens = [0, 1, 63, 64, 65, 129, 300]
     x = workloads.prefill(1, 0, 2, 4, 128, 128, seed=31 + kda, h0_std=0.1, seqlens=lens, kda=kda)
     check(gdn, oracle_mod, x, state_qdq, w_qdq, path=path)
@@ -114,10 +113,39 @@ def test_zero_initial_state_and_no_final_state(gdn, oracle_mod):
     assert rel(o.cpu().double().numpy(), oref) <= TOL_QDQ
 
 
-def test_kda_small(gdn, oracle_mod):
+@pytest.mark.parametrize("path", PATHS)
+def test_kda_small(gdn, oracle_mod, path):
     x = workloads.prefill(2, 200, 2, 2, 128, 128, seed=43, kda=True, h0_std=0.1)
-    check(gdn, oracle_mod, x, False, False)
-    check(gdn, oracle_mod, x, True, True)
+    check(gdn, oracle_mod, x, False, False, path=path)
+    check(gdn, oracle_mod, x, True, True, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 200])
+@pytest.mark.parametrize("dv", [64, 128, 256])
+def test_kda_lengths_and_shapes(gdn, oracle_mod, T, dv, path):
+    x = workloads.prefill(2, T, 1, 2, 128, dv, seed=7 * T + dv, h0_std=0.1, kda=True)
+    check(gdn, oracle_mod, x, True, False, path=path)
+    check(gdn, oracle_mod, x, False, False, path=path)
+    check(gdn, oracle_mod, x, True, True, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_kda_final_state_aliases_h0(gdn, oracle_mod, path):
+    x = workloads.prefill(2, 150, 2, 2, 128, 128, seed=45, h0_std=0.1, kda=True)
+    check(gdn, oracle_mod, x, True, True, hT_alias=True, path=path)
+
+
+def test_kda_paths_agree_closely(gdn):
+    """The tensor-core KDA path splits every fp32 operand into bf16 hi + lo (products keep
+    about 16 mantissa bits) and the CUDA-core path multiplies in fp32: on a QDQ-off case their
+    outputs agree far inside the oracle bound."""
+    x = workloads.prefill(2, 333, 2, 4, 128, 128, seed=46, h0_std=0.1, kda=True)
+    o1, h1 = run_gpu(gdn, x, False, False, path="split")
+    o2, h2 = run_gpu(gdn, x, False, False, path="fused")
+    from helpers import rel
+    assert rel(o1.cpu().double().numpy(), o2.cpu().double().numpy()) <= 1e-4
+    assert rel(h1.cpu().double().numpy(), h2.cpu().double().numpy()) <= 1e-4
 
 
 # ---- full-size workloads, sampled (sequence, head) units ---------------------------------
@@ -139,7 +167,8 @@ def test_gdn_varlen8_hqk16_hv32_d128_sampled(gdn, oracle_mod, path):
     check(gdn, oracle_mod, x, True, False, units, path=path)
 
 
-def test_kda_b2_h32_t8192_d128_sampled(gdn, oracle_mod):
+@pytest.mark.parametrize("path", PATHS)
+def test_kda_b2_h32_t8192_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("kda_b2_h32_t8192_d128")
     units = sample_units(2, 32, 4, seed=4)
-    check(gdn, oracle_mod, x, True, True, units)
+    check(gdn, oracle_mod, x, True, True, units, path=path)
