@@ -12,11 +12,14 @@
 // so that the state chain needs no per-channel exponentials: Y = Qd S0, C = Kd^T Delta,
 // S1 = diag(exp(gam_63)) S0 + C.
 //
-// The pairwise decays are never formed as a ratio of exponentials. For the 16 x 16 blocks below
-// the diagonal (row block b, columns i < a = 16 b) they factor exactly through the block's first
-// token a: exp(gam_r - gam_i) = exp(gam_r - gam_a) exp(gam_a - gam_i), both exponents <= 0 for
-// log-decays g <= 0, so A and P there are plain dot products of decayed rows; the four diagonal
-// blocks take the pairwise exponentials directly. The WY products run on tcgen05 (bf16 hi + lo);
+// The pairwise decays factor through the first token a = 16 b of each 16-row block b:
+// exp(gam_r - gam_i) = exp(gam_r - gam_a) exp(gam_a - gam_i), so A and P for rows of block b are
+// plain dot products of rows decayed to a. Below the diagonal block both exponents are <= 0 for
+// log-decays g <= 0 (no overflow; a factor that underflows bounds a product that is as small).
+// Inside the diagonal block exp(gam_a - gam_i) >= 1; the factored form is used there when every
+// channel's |gam_i - gam_a| over the block stays <= kDiagRange (both factors normal fp32, each
+// exponential's relative error a few 1e-6), else that block takes the pairwise exponentials
+// directly. The WY products run on tcgen05 (bf16 hi + lo);
 // the rest on CUDA cores. Every mbarrier wait is bounded; a CTA that gives up records it in the
 // status word, waits (bounded) for its TMA load in flight, frees its TMEM and exits.
 #include "common.cuh"
@@ -31,6 +34,7 @@ constexpr int kThreads = 256;
 constexpr uint32_t KB = 1024;
 constexpr int GLD = 132;   // row stride (floats) of gam and of the decayed-row scratch
 constexpr int A_LD = 68;
+constexpr float kDiagRange = 40.f;
 // shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0, OFF_K = 16 * KB;           // Q0 | Q1, K0 | K1 (TMA, 128-byte swizzle); later W^T
 constexpr uint32_t OFF_G = 32 * KB;                      // gam fp32 [64][GLD]
@@ -43,7 +47,7 @@ constexpr uint32_t OFF_VEC = 196 * KB;                   // beta [64], partial m
 constexpr uint32_t kSmemBytes = OFF_VEC + 1024 + 1024;   // + slack to align the base
 static_assert(OFF_G + 64 * GLD * 4 <= OFF_A && OFF_A + 64 * A_LD * 4 <= OFF_T && OFF_T + 64 * A_LD * 4 <= OFF_SCR,
               "regions overlap");
-static_assert((16 + 16 + 48) * GLD * 4 <= 64 * KB, "decayed-row scratch exceeds its region");
+static_assert((16 + 16 + 64) * GLD * 4 <= 64 * KB, "decayed-row scratch exceeds its region");
 
 constexpr uint32_t TM_WT = 0;
 constexpr uint32_t kTmemCols = 64;
@@ -166,10 +170,17 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     // ---- A and P, one 16-row block b at a time ----
     float* const Rk = scr;                 // [16][GLD]: k_r exp(gam_r - gam_a), rows of block b
     float* const Rq = scr + 16 * GLD;      // [16][GLD]: q_r exp(gam_r - gam_a)
-    float* const Ki = scr + 32 * GLD;      // [48][GLD]: k_i exp(gam_a - gam_i), i < a
+    float* const Ki = scr + 32 * GLD;      // [64][GLD]: k_i exp(gam_a - gam_i), i < a (+ 16 when factored)
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
       const int a = 16 * b;
+      float dev = 0.f;   // largest |gam_i - gam_a| over the block's rows and channels
+      for (int e = tid; e < 16 * 128; e += kThreads) {
+        const int i = a + (e >> 7), c = e & 127;
+        dev = fmaxf(dev, fabsf(gam[i * GLD + c] - gam[a * GLD + c]));
+      }
+      const bool pairwise = __syncthreads_or(!(dev <= kDiagRange));   // uniform across the CTA
+      const int nblk = pairwise ? b : b + 1;                          // column blocks as dot products
       {   // decayed rows of block b (one 8-column group per thread)
         const int rr = tid >> 4, c8 = (tid & 15) * 8;
         float kf[8], qf[8];
@@ -186,7 +197,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
               make_float4(qf[u] * e[u], qf[u + 1] * e[u + 1], qf[u + 2] * e[u + 2], qf[u + 3] * e[u + 3]);
         }
       }
-      for (int t = tid; t < a * 16; t += kThreads) {   // decayed earlier rows i < a
+      for (int t = tid; t < nblk * 256; t += kThreads) {   // decayed columns i < 16 nblk
         const int i = t >> 4, c8 = (t & 15) * 8;
         float kf[8];
         tile8(Kt, i, c8, kf);
@@ -201,16 +212,16 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         }
       }
       __syncthreads();
-      if (b > 0) {   // blocks below the diagonal: dot products of decayed rows
+      if (nblk > 0) {   // dot products of decayed rows: row a + rr, columns ii + 16 m, m < nblk
         const int rr = tid >> 4, ii = tid & 15;
-        float accA[3] = {0.f, 0.f, 0.f}, accP[3] = {0.f, 0.f, 0.f};
+        float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
         for (int c4 = 0; c4 < 128; c4 += 4) {
           const float4 rk = *reinterpret_cast<const float4*>(Rk + rr * GLD + c4);
           const float4 rq = *reinterpret_cast<const float4*>(Rq + rr * GLD + c4);
 #pragma unroll
-          for (int m = 0; m < 3; ++m) {
-            if (m < b) {
+          for (int m = 0; m < 4; ++m) {
+            if (m < nblk) {
               const float4 ki = *reinterpret_cast<const float4*>(Ki + (ii + 16 * m) * GLD + c4);
               accA[m] = fmaf(rk.x, ki.x, fmaf(rk.y, ki.y, fmaf(rk.z, ki.z, fmaf(rk.w, ki.w, accA[m]))));
               accP[m] = fmaf(rq.x, ki.x, fmaf(rq.y, ki.y, fmaf(rq.z, ki.z, fmaf(rq.w, ki.w, accP[m]))));
@@ -218,37 +229,38 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           }
         }
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {
-          if (m < b) {
+        for (int m = 0; m < 4; ++m) {
+          if (m < nblk) {
             const int r = a + rr, i = ii + 16 * m;
-            Am[r * A_LD + i] = vbeta[r] * accA[m];
-            Tm[r * A_LD + i] = accP[m];
+            if (i < r) Am[r * A_LD + i] = vbeta[r] * accA[m];   // A is strictly lower, P includes i = r
+            if (i <= r) Tm[r * A_LD + i] = accP[m];
           }
         }
       }
-      // diagonal block: pairs i <= r inside it, exponentials taken pairwise (lanes split c)
+      if (pairwise) {   // diagonal block with a steep decay: pairs i <= r, exponentials taken pairwise
 #pragma unroll 1
-      for (int pr = warp; pr < 136; pr += kThreads / 32) {
-        int ri = 0;
-        while ((ri + 1) * (ri + 2) / 2 <= pr) ++ri;   // pair pr -> (ri, ii) with ii <= ri
-        const int ii = pr - ri * (ri + 1) / 2;
-        const int r = a + ri, i = a + ii, c4 = lt * 4;
-        float kr[4], ki[4], qr[4];
-        tile4(Kt, r, c4, kr);
-        tile4(Kt, i, c4, ki);
-        tile4(Qt, r, c4, qr);
-        float sA = 0.f, sP = 0.f;
+        for (int pr = warp; pr < 136; pr += kThreads / 32) {
+          int ri = 0;
+          while ((ri + 1) * (ri + 2) / 2 <= pr) ++ri;   // pair pr -> (ri, ii) with ii <= ri
+          const int ii = pr - ri * (ri + 1) / 2;
+          const int r = a + ri, i = a + ii, c4 = lt * 4;
+          float kr[4], ki[4], qr[4];
+          tile4(Kt, r, c4, kr);
+          tile4(Kt, i, c4, ki);
+          tile4(Qt, r, c4, qr);
+          float sA = 0.f, sP = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float e = __expf(gam[r * GLD + c4 + u] - gam[i * GLD + c4 + u]);
-          sA = fmaf(kr[u] * ki[u], e, sA);
-          sP = fmaf(qr[u] * ki[u], e, sP);
-        }
-        sA = warp_sum(sA);
-        sP = warp_sum(sP);
-        if (lt == 0) {
-          Am[r * A_LD + i] = ii < ri ? vbeta[r] * sA : 0.f;
-          Tm[r * A_LD + i] = sP;
+          for (int u = 0; u < 4; ++u) {
+            const float e = __expf(gam[r * GLD + c4 + u] - gam[i * GLD + c4 + u]);
+            sA = fmaf(kr[u] * ki[u], e, sA);
+            sP = fmaf(qr[u] * ki[u], e, sP);
+          }
+          sA = warp_sum(sA);
+          sP = warp_sum(sP);
+          if (lt == 0) {
+            Am[r * A_LD + i] = ii < ri ? vbeta[r] * sA : 0.f;
+            Tm[r * A_LD + i] = sP;
+          }
         }
       }
       __syncthreads();

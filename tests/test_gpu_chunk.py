@@ -136,6 +136,22 @@ def test_kda_final_state_aliases_h0(gdn, oracle_mod, path):
     check(gdn, oracle_mod, x, True, True, hT_alias=True, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("g_steep", [-1.5, -2.5, -6.0])
+def test_kda_steep_decays(gdn, oracle_mod, g_steep, path):
+    """Some key channels decay steeply: over a 16-token block the log-decay then spans 22.5
+    (-1.5), 37.5 (-2.5) or 90 (-6.0). The tensor-core prep factors a diagonal block's pairwise
+    decays through the block's first token while that span is <= 40 and takes them pairwise
+    beyond, so this covers both forms, with exponentials near the factored form's limit."""
+    x = workloads.prefill(2, 150, 2, 2, 128, 128, seed=47, h0_std=0.1, kda=True)
+    g = x.g.clone()
+    g[..., 5::9] = g_steep                # every ninth channel, from channel 5
+    g[:, 70:90, :, 100:] = g_steep        # and a token range of the upper channels
+    x.g = g.contiguous()
+    check(gdn, oracle_mod, x, False, False, path=path)
+    check(gdn, oracle_mod, x, True, True, path=path)
+
+
 def test_kda_paths_agree_closely(gdn):
     """The tensor-core KDA path splits every fp32 operand into bf16 hi + lo (products keep
     about 16 mantissa bits) and the CUDA-core path multiplies in fp32: on a QDQ-off case their
