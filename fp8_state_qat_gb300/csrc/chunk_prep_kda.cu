@@ -12,7 +12,12 @@
 // so that the state chain needs no per-channel exponentials: Y = Qd S0, C = Kd^T Delta,
 // S1 = diag(exp(gam_63)) S0 + C.
 //
-// The pairwise decays factor through the first token a = 16 b of each 16-row block b:
+// The pairwise decays factor through a per-channel anchor: exp(gam_r - gam_i) = exp(gam_r - m)
+// exp(m - gam_i). When every channel's gam spans at most kChunkSpan over the chunk, m is the
+// midpoint of its range, both factors stay within exp(+-kChunkSpan / 2) (normal in fp32 and bf16),
+// and A and P are one tcgen05 product, [K o e^(gam - m) ; Q o e^(gam - m)] (K o e^(m - gam))^T, on
+// bf16 hi + lo operands, masked to i < r (A) and i <= r (P). Steeper chunks take CUDA cores:
+// the pairwise decays factor through the first token a = 16 b of each 16-row block b:
 // exp(gam_r - gam_i) = exp(gam_r - gam_a) exp(gam_a - gam_i), so A and P for rows of block b are
 // plain dot products of rows decayed to a. Below the diagonal block both exponents are <= 0 for
 // log-decays g <= 0 (no overflow; a factor that underflows bounds a product that is as small).
@@ -35,6 +40,7 @@ constexpr uint32_t KB = 1024;
 constexpr int GLD = 132;   // row stride (floats) of gam and of the decayed-row scratch
 constexpr int A_LD = 68;
 constexpr float kDiagRange = 40.f;
+constexpr float kChunkSpan = 64.f;
 // shared memory map (byte offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0, OFF_K = 16 * KB;           // Q0 | Q1, K0 | K1 (TMA, 128-byte swizzle); later W^T
 constexpr uint32_t OFF_G = 32 * KB;                      // gam fp32 [64][GLD]
@@ -43,15 +49,21 @@ constexpr uint32_t OFF_T = 83 * KB;                      // P fp32 [64][A_LD] (b
 constexpr uint32_t OFF_SCR = 100 * KB;                   // 64 KB: decayed rows; solve scratch; Qd | Kd; Kt
 constexpr uint32_t OFF_TT = 164 * KB;                    // T'' hi | lo [64 r][64 i] K-major
 constexpr uint32_t OFF_P = 180 * KB;                     // P hi | lo [64 r][64 i] K-major
-constexpr uint32_t OFF_VEC = 196 * KB;                   // beta [64], partial maxima [8]
+constexpr uint32_t OFF_VEC = 196 * KB;                   // beta [64], partial maxima [8], anchor m [128] at 128
+// tensor-core A / P operands (bf16 hi, lo): [K o e^(gam - m) ; Q o e^(gam - m)] (128 rows, k blocks 16 KB
+// apart), K o e^(m - gam) (64 rows, k blocks 8 KB apart); they overlay the scratch, T'' and P regions
+constexpr uint32_t OFF_LQ = OFF_SCR, OFF_LQ_LO = OFF_SCR + 32 * KB, OFF_KR = OFF_SCR + 64 * KB, OFF_KR_LO = OFF_KR + 16 * KB;
 constexpr uint32_t kSmemBytes = OFF_VEC + 1024 + 1024;   // + slack to align the base
 static_assert(OFF_G + 64 * GLD * 4 <= OFF_A && OFF_A + 64 * A_LD * 4 <= OFF_T && OFF_T + 64 * A_LD * 4 <= OFF_SCR,
               "regions overlap");
 static_assert((16 + 16 + 64) * GLD * 4 <= 64 * KB, "decayed-row scratch exceeds its region");
+static_assert(OFF_KR_LO + 16 * KB <= OFF_VEC && OFF_TT >= OFF_KR && OFF_P >= OFF_KR_LO, "operand overlay");
+static_assert(kThreads == 256, "the thread mappings below assume 256 threads");
 
 constexpr uint32_t TM_WT = 0;
 constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t IDESC_WT = tc::make_idesc(tc::kKindBF16, 128, 64, true, false);   // Kt^T (MN) x T''^T (K)
+constexpr uint32_t IDESC_AP = tc::make_idesc(tc::kKindBF16, 128, 64, false, false);  // [Kl ; Ql] (K) x Kr (K)
 
 struct KdaPrepParams {
   const float* g;      // [tokens, Hv, 128]
@@ -122,6 +134,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   float* const scr = reinterpret_cast<float*>(sm + OFF_SCR);
   float* const vbeta = reinterpret_cast<float*>(sm + OFF_VEC);
   float* const red = vbeta + 64;
+  float* const gmid = vbeta + 128;
   const uint32_t bar_k = tc::smem_u32(&bars[0]), bar_w = tc::smem_u32(&bars[1]);
 
   if (tid == 0) {
@@ -135,12 +148,19 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     tc::tma_load_3d(sbase + OFF_K + 8 * KB, &tk, bar_k, 64, hq, tok);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
-  // g of the chunk (rows beyond L are zero), beta
-  for (int e = tid; e < 64 * 32; e += kThreads) {
-    const int r = e >> 5, c4 = (e & 31) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < L) v = *reinterpret_cast<const float4*>(p.g + ((int64_t)(tok + r) * p.Hv + h) * 128 + c4);
-    *reinterpret_cast<float4*>(gam + r * GLD + c4) = v;
+  {   // g of the chunk (rows beyond L are zero; all loads in flight before the first store), beta
+    float4 gv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = tid + j * kThreads, r = e >> 5, c4 = (e & 31) * 4;
+      gv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < L) gv[j] = __ldcs(reinterpret_cast<const float4*>(p.g + ((int64_t)(tok + r) * p.Hv + h) * 128 + c4));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = tid + j * kThreads, r = e >> 5, c4 = (e & 31) * 4;
+      *reinterpret_cast<float4*>(gam + r * GLD + c4) = gv[j];
+    }
   }
   if (tid < 64) vbeta[tid] = tid < L ? p.beta[(int64_t)(tok + tid) * p.Hv + h] : 0.f;
   for (int e = tid; e < 2 * 64 * A_LD; e += kThreads) (e < 64 * A_LD ? Am : Tm)[e % (64 * A_LD)] = 0.f;
@@ -148,17 +168,24 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // prefix sums per key channel, in token order; exp(gam_63) for the chain
+  // prefix sums per key channel, in token order; exp(gam_63) for the chain; the range of each
+  // channel's gam over the chunk: its midpoint is the anchor, its width picks the A / P form
+  bool steep = false;
   if (tid < 128) {
-    float acc = 0.f;
+    float acc = 0.f, mx = -INFINITY, mn = INFINITY;
 #pragma unroll 8
     for (int r = 0; r < 64; ++r) {
       acc += gam[r * GLD + tid];
       gam[r * GLD + tid] = acc;
+      mx = fmaxf(mx, acc);
+      mn = fminf(mn, acc);
     }
     p.vec[item * 256 + tid] = __expf(acc);
+    gmid[tid] = 0.5f * (mx + mn);
+    steep = !(mx - mn <= kChunkSpan);
   }
-  __syncthreads();
+  const bool tc_ap = !__syncthreads_or(steep);   // uniform across the CTA
+  uint32_t w_phase = 0;                           // bar_w completions waited for so far
 
   bool ok = true, k_done = false;
   float sW = 1.f;
@@ -167,119 +194,200 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     if (__syncthreads_or(!ok)) break;
     k_done = true;
 
-    // ---- A and P, one 16-row block b at a time ----
-    float* const Rk = scr;                 // [16][GLD]: k_r exp(gam_r - gam_a), rows of block b
-    float* const Rq = scr + 16 * GLD;      // [16][GLD]: q_r exp(gam_r - gam_a)
-    float* const Ki = scr + 32 * GLD;      // [64][GLD]: k_i exp(gam_a - gam_i), i < a (+ 16 when factored)
-#pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
-      const int a = 16 * b;
-      float dev = 0.f;   // largest |gam_i - gam_a| over the block's rows and channels
-      for (int e = tid; e < 16 * 128; e += kThreads) {
-        const int i = a + (e >> 7), c = e & 127;
-        dev = fmaxf(dev, fabsf(gam[i * GLD + c] - gam[a * GLD + c]));
-      }
-      const bool pairwise = __syncthreads_or(!(dev <= kDiagRange));   // uniform across the CTA
-      const int nblk = pairwise ? b : b + 1;                          // column blocks as dot products
-      {   // decayed rows of block b (one 8-column group per thread)
-        const int rr = tid >> 4, c8 = (tid & 15) * 8;
-        float kf[8], qf[8];
-        tile8(Kt, a + rr, c8, kf);
-        tile8(Qt, a + rr, c8, qf);
-        float e[8];
+    if (tc_ap) {
+      // ---- A and P on tcgen05 ----
+      for (int t = tid; t < 64 * 16; t += kThreads) {
+        const int r = t >> 4, c8 = (t & 15) * 8;
+        float kf[8], qf[8], kl[8], ql[8], kr[8];
+        tile8(Kt, r, c8, kf);
+        tile8(Qt, r, c8, qf);
+        const float4 g0 = *reinterpret_cast<const float4*>(gam + r * GLD + c8);
+        const float4 g1 = *reinterpret_cast<const float4*>(gam + r * GLD + c8 + 4);
+        const float4 m0 = *reinterpret_cast<const float4*>(gmid + c8);
+        const float4 m1 = *reinterpret_cast<const float4*>(gmid + c8 + 4);
+        const float x[8] = {g0.x - m0.x, g0.y - m0.y, g0.z - m0.z, g0.w - m0.w,
+                            g1.x - m1.x, g1.y - m1.y, g1.z - m1.z, g1.w - m1.w};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) e[u] = __expf(gam[(a + rr) * GLD + c8 + u] - gam[a * GLD + c8 + u]);
-#pragma unroll
-        for (int u = 0; u < 8; u += 4) {
-          *reinterpret_cast<float4*>(Rk + rr * GLD + c8 + u) =
-              make_float4(kf[u] * e[u], kf[u + 1] * e[u + 1], kf[u + 2] * e[u + 2], kf[u + 3] * e[u + 3]);
-          *reinterpret_cast<float4*>(Rq + rr * GLD + c8 + u) =
-              make_float4(qf[u] * e[u], qf[u + 1] * e[u + 1], qf[u + 2] * e[u + 2], qf[u + 3] * e[u + 3]);
+        for (int u = 0; u < 8; ++u) {
+          const float el = __expf(x[u]), er = __expf(-x[u]);
+          kl[u] = kf[u] * el;
+          ql[u] = qf[u] * el;
+          kr[u] = kf[u] * er;
         }
+        const uint32_t kb = (uint32_t)(c8 >> 6), col = 2 * (c8 & 63);
+        const uint32_t sk = tc::sw128(r, col), sq = tc::sw128(64 + r, col);
+        uint4 h16, l16;
+        split8(kl, h16, l16);
+        st16(sm, OFF_LQ + kb * 16 * KB + sk, h16);
+        st16(sm, OFF_LQ_LO + kb * 16 * KB + sk, l16);
+        split8(ql, h16, l16);
+        st16(sm, OFF_LQ + kb * 16 * KB + sq, h16);
+        st16(sm, OFF_LQ_LO + kb * 16 * KB + sq, l16);
+        split8(kr, h16, l16);
+        st16(sm, OFF_KR + kb * 8 * KB + sk, h16);
+        st16(sm, OFF_KR_LO + kb * 8 * KB + sk, l16);
       }
-      for (int t = tid; t < nblk * 256; t += kThreads) {   // decayed columns i < 16 nblk
-        const int i = t >> 4, c8 = (t & 15) * 8;
-        float kf[8];
-        tile8(Kt, i, c8, kf);
-#pragma unroll
-        for (int u = 0; u < 8; u += 4) {
-          float4 v;
-          v.x = kf[u] * __expf(gam[a * GLD + c8 + u] - gam[i * GLD + c8 + u]);
-          v.y = kf[u + 1] * __expf(gam[a * GLD + c8 + u + 1] - gam[i * GLD + c8 + u + 1]);
-          v.z = kf[u + 2] * __expf(gam[a * GLD + c8 + u + 2] - gam[i * GLD + c8 + u + 2]);
-          v.w = kf[u + 3] * __expf(gam[a * GLD + c8 + u + 3] - gam[i * GLD + c8 + u + 3]);
-          *reinterpret_cast<float4*>(Ki + i * GLD + c8 + u) = v;
-        }
-      }
+      tc::fence_proxy_async_smem();
       __syncthreads();
-      if (nblk > 0) {   // dot products of decayed rows: row a + rr, columns ii + 16 m, m < nblk
-        const int rr = tid >> 4, ii = tid & 15;
-        float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
+      if (tid == 0) {
+        tc::tc_fence_after();
+        const uint64_t dA = tc::make_sdesc(sbase + OFF_LQ, 16, 1024);
+        const uint64_t dB = tc::make_sdesc(sbase + OFF_KR, 16, 1024);
+        // hi x hi + hi x lo + lo x hi
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_bf16(tmem + TM_WT, dadv(dA, (q == 2 ? 32 * KB : 0) + (ks >> 2) * 16 * KB + (ks & 3) * 32),
+                         dadv(dB, (q == 1 ? 16 * KB : 0) + (ks >> 2) * 8 * KB + (ks & 3) * 32), IDESC_AP, (q | ks) != 0);
+        tc::mma_commit(bar_w);
+      }
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_w, w_phase & 1));
+      ++w_phase;
+      if (__syncthreads_or(!ok)) break;
+      tc::tc_fence_after();
+      if (warp < 4) {   // TMEM lane = tid: rows 0-63 give A, rows 64-127 give P
+        float d[64];
+        ld32(tmem, (uint32_t)warp * 32u, TM_WT, d);
+        ld32(tmem, (uint32_t)warp * 32u, TM_WT + 32, d + 32);
+        if (tid < 64) {
+          const float br = vbeta[tid];
+#pragma unroll
+          for (int i = 0; i < 64; i += 4)
+            *reinterpret_cast<float4*>(Am + tid * A_LD + i) =
+                make_float4(i < tid ? br * d[i] : 0.f, i + 1 < tid ? br * d[i + 1] : 0.f,
+                            i + 2 < tid ? br * d[i + 2] : 0.f, i + 3 < tid ? br * d[i + 3] : 0.f);
+        } else {
+          const int r = tid - 64;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float pv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pv[u] = 8 * q + u <= r ? d[8 * q + u] : 0.f;
+            uint4 h16, l16;
+            split8(pv, h16, l16);
+            st16(sm, OFF_P + tc::sw128(r, 16 * q), h16);
+            st16(sm, OFF_P + 8 * KB + tc::sw128(r, 16 * q), l16);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncthreads();
+    } else {
+      // ---- A and P, one 16-row block b at a time ----
+      float* const Rk = scr;                 // [16][GLD]: k_r exp(gam_r - gam_a), rows of block b
+      float* const Rq = scr + 16 * GLD;      // [16][GLD]: q_r exp(gam_r - gam_a)
+      float* const Ki = scr + 32 * GLD;      // [64][GLD]: k_i exp(gam_a - gam_i), i < a (+ 16 when factored)
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        const int a = 16 * b;
+        float dev = 0.f;   // largest |gam_i - gam_a| over the block's rows and channels
+        for (int e = tid; e < 16 * 128; e += kThreads) {
+          const int i = a + (e >> 7), c = e & 127;
+          dev = fmaxf(dev, fabsf(gam[i * GLD + c] - gam[a * GLD + c]));
+        }
+        const bool pairwise = __syncthreads_or(!(dev <= kDiagRange));   // uniform across the CTA
+        const int nblk = pairwise ? b : b + 1;                          // column blocks as dot products
+        {   // decayed rows of block b (one 8-column group per thread)
+          const int rr = tid >> 4, c8 = (tid & 15) * 8;
+          float kf[8], qf[8];
+          tile8(Kt, a + rr, c8, kf);
+          tile8(Qt, a + rr, c8, qf);
+          float e[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) e[u] = __expf(gam[(a + rr) * GLD + c8 + u] - gam[a * GLD + c8 + u]);
+#pragma unroll
+          for (int u = 0; u < 8; u += 4) {
+            *reinterpret_cast<float4*>(Rk + rr * GLD + c8 + u) =
+                make_float4(kf[u] * e[u], kf[u + 1] * e[u + 1], kf[u + 2] * e[u + 2], kf[u + 3] * e[u + 3]);
+            *reinterpret_cast<float4*>(Rq + rr * GLD + c8 + u) =
+                make_float4(qf[u] * e[u], qf[u + 1] * e[u + 1], qf[u + 2] * e[u + 2], qf[u + 3] * e[u + 3]);
+          }
+        }
+        for (int t = tid; t < nblk * 256; t += kThreads) {   // decayed columns i < 16 nblk
+          const int i = t >> 4, c8 = (t & 15) * 8;
+          float kf[8];
+          tile8(Kt, i, c8, kf);
+#pragma unroll
+          for (int u = 0; u < 8; u += 4) {
+            float4 v;
+            v.x = kf[u] * __expf(gam[a * GLD + c8 + u] - gam[i * GLD + c8 + u]);
+            v.y = kf[u + 1] * __expf(gam[a * GLD + c8 + u + 1] - gam[i * GLD + c8 + u + 1]);
+            v.z = kf[u + 2] * __expf(gam[a * GLD + c8 + u + 2] - gam[i * GLD + c8 + u + 2]);
+            v.w = kf[u + 3] * __expf(gam[a * GLD + c8 + u + 3] - gam[i * GLD + c8 + u + 3]);
+            *reinterpret_cast<float4*>(Ki + i * GLD + c8 + u) = v;
+          }
+        }
+        __syncthreads();
+        if (nblk > 0) {   // dot products of decayed rows: row a + rr, columns ii + 16 m, m < nblk
+          const int rr = tid >> 4, ii = tid & 15;
+          float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-        for (int c4 = 0; c4 < 128; c4 += 4) {
-          const float4 rk = *reinterpret_cast<const float4*>(Rk + rr * GLD + c4);
-          const float4 rq = *reinterpret_cast<const float4*>(Rq + rr * GLD + c4);
+          for (int c4 = 0; c4 < 128; c4 += 4) {
+            const float4 rk = *reinterpret_cast<const float4*>(Rk + rr * GLD + c4);
+            const float4 rq = *reinterpret_cast<const float4*>(Rq + rr * GLD + c4);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              if (m < nblk) {
+                const float4 ki = *reinterpret_cast<const float4*>(Ki + (ii + 16 * m) * GLD + c4);
+                accA[m] = fmaf(rk.x, ki.x, fmaf(rk.y, ki.y, fmaf(rk.z, ki.z, fmaf(rk.w, ki.w, accA[m]))));
+                accP[m] = fmaf(rq.x, ki.x, fmaf(rq.y, ki.y, fmaf(rq.z, ki.z, fmaf(rq.w, ki.w, accP[m]))));
+              }
+            }
+          }
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             if (m < nblk) {
-              const float4 ki = *reinterpret_cast<const float4*>(Ki + (ii + 16 * m) * GLD + c4);
-              accA[m] = fmaf(rk.x, ki.x, fmaf(rk.y, ki.y, fmaf(rk.z, ki.z, fmaf(rk.w, ki.w, accA[m]))));
-              accP[m] = fmaf(rq.x, ki.x, fmaf(rq.y, ki.y, fmaf(rq.z, ki.z, fmaf(rq.w, ki.w, accP[m]))));
+              const int r = a + rr, i = ii + 16 * m;
+              if (i < r) Am[r * A_LD + i] = vbeta[r] * accA[m];   // A is strictly lower, P includes i = r
+              if (i <= r) Tm[r * A_LD + i] = accP[m];
             }
           }
         }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          if (m < nblk) {
-            const int r = a + rr, i = ii + 16 * m;
-            if (i < r) Am[r * A_LD + i] = vbeta[r] * accA[m];   // A is strictly lower, P includes i = r
-            if (i <= r) Tm[r * A_LD + i] = accP[m];
-          }
-        }
-      }
-      if (pairwise) {   // diagonal block with a steep decay: pairs i <= r, exponentials taken pairwise
+        if (pairwise) {   // diagonal block with a steep decay: pairs i <= r, exponentials taken pairwise
 #pragma unroll 1
-        for (int pr = warp; pr < 136; pr += kThreads / 32) {
-          int ri = 0;
-          while ((ri + 1) * (ri + 2) / 2 <= pr) ++ri;   // pair pr -> (ri, ii) with ii <= ri
-          const int ii = pr - ri * (ri + 1) / 2;
-          const int r = a + ri, i = a + ii, c4 = lt * 4;
-          float kr[4], ki[4], qr[4];
-          tile4(Kt, r, c4, kr);
-          tile4(Kt, i, c4, ki);
-          tile4(Qt, r, c4, qr);
-          float sA = 0.f, sP = 0.f;
+          for (int pr = warp; pr < 136; pr += kThreads / 32) {
+            int ri = 0;
+            while ((ri + 1) * (ri + 2) / 2 <= pr) ++ri;   // pair pr -> (ri, ii) with ii <= ri
+            const int ii = pr - ri * (ri + 1) / 2;
+            const int r = a + ri, i = a + ii, c4 = lt * 4;
+            float kr[4], ki[4], qr[4];
+            tile4(Kt, r, c4, kr);
+            tile4(Kt, i, c4, ki);
+            tile4(Qt, r, c4, qr);
+            float sA = 0.f, sP = 0.f;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float e = __expf(gam[r * GLD + c4 + u] - gam[i * GLD + c4 + u]);
-            sA = fmaf(kr[u] * ki[u], e, sA);
-            sP = fmaf(qr[u] * ki[u], e, sP);
-          }
-          sA = warp_sum(sA);
-          sP = warp_sum(sP);
-          if (lt == 0) {
-            Am[r * A_LD + i] = ii < ri ? vbeta[r] * sA : 0.f;
-            Tm[r * A_LD + i] = sP;
+            for (int u = 0; u < 4; ++u) {
+              const float e = __expf(gam[r * GLD + c4 + u] - gam[i * GLD + c4 + u]);
+              sA = fmaf(kr[u] * ki[u], e, sA);
+              sP = fmaf(qr[u] * ki[u], e, sP);
+            }
+            sA = warp_sum(sA);
+            sP = warp_sum(sP);
+            if (lt == 0) {
+              Am[r * A_LD + i] = ii < ri ? vbeta[r] * sA : 0.f;
+              Tm[r * A_LD + i] = sP;
+            }
           }
         }
+        __syncthreads();
+      }
+      // P -> bf16 hi | lo, K-major [r][i] (P is read from the T region, which the solve reuses)
+      for (int t = tid; t < 512; t += kThreads) {
+        const int r = t >> 3, i0 = (t & 7) * 8;
+        const float4 pa = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
+        const float4 pb = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
+        const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        uint4 h16, l16;
+        split8(pv, h16, l16);
+        const uint32_t off = tc::sw128(r, 2 * i0);
+        st16(sm, OFF_P + off, h16);
+        st16(sm, OFF_P + 8 * KB + off, l16);
       }
       __syncthreads();
+      for (int e = tid; e < 64 * A_LD; e += kThreads) Tm[e] = 0.f;
+      __syncthreads();
     }
-    // P -> bf16 hi | lo, K-major [r][i] (P is read from the T region, which the solve reuses)
-    for (int t = tid; t < 512; t += kThreads) {
-      const int r = t >> 3, i0 = (t & 7) * 8;
-      const float4 pa = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
-      const float4 pb = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
-      const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-      uint4 h16, l16;
-      split8(pv, h16, l16);
-      const uint32_t off = tc::sw128(r, 2 * i0);
-      st16(sm, OFF_P + off, h16);
-      st16(sm, OFF_P + 8 * KB + off, l16);
-    }
-    __syncthreads();
-    for (int e = tid; e < 64 * A_LD; e += kThreads) Tm[e] = 0.f;
-    __syncthreads();
 
     // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then the blocks below
     // the diagonal by levels of T_ij = -T_ii sum_{j <= m < i} A_im T_mj ----
@@ -419,7 +527,8 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                        IDESC_WT, (q | ks) != 0);
       tc::mma_commit(bar_w);
     }
-    ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_w, 0));
+    ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_w, w_phase & 1));
+    ++w_phase;
     if (__syncthreads_or(!ok)) break;
     tc::tc_fence_after();
 

@@ -137,12 +137,14 @@ def test_kda_final_state_aliases_h0(gdn, oracle_mod, path):
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("g_steep", [-1.5, -2.5, -6.0])
+@pytest.mark.parametrize("g_steep", [-0.9, -1.5, -2.5, -6.0])
 def test_kda_steep_decays(gdn, oracle_mod, g_steep, path):
-    """Some key channels decay steeply: over a 16-token block the log-decay then spans 22.5
-    (-1.5), 37.5 (-2.5) or 90 (-6.0). The tensor-core prep factors a diagonal block's pairwise
-    decays through the block's first token while that span is <= 40 and takes them pairwise
-    beyond, so this covers both forms, with exponentials near the factored form's limit."""
+    """Some key channels decay steeply. The tensor-core prep computes A and P as one product of
+    rows decayed to a per-channel anchor while every channel's log-decay spans <= 64 over the
+    chunk (-0.9: up to 57.6, exponentials up to e^28.8); steeper chunks anchor at each 16-token
+    block's first token while the block spans <= 40 (-1.5: 22.5, -2.5: 37.5) and take the
+    diagonal blocks' decays pairwise beyond (-6.0: 90). So this covers every form, each near
+    its limit."""
     x = workloads.prefill(2, 150, 2, 2, 128, 128, seed=47, h0_std=0.1, kda=True)
     g = x.g.clone()
     g[..., 5::9] = g_steep                # every ninth channel, from channel 5
