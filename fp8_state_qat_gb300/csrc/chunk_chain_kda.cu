@@ -7,16 +7,22 @@
 // per-key-channel retention ("Add KDA prefill numerical emulation for QAT", "What does this PR
 // do?") the chunk step is
 //   X = W S0,  Delta = U - X,  U = T'' V
-//   C = Kd^T Delta,  Kd = K o exp(gam_63 - gam)         (N = 128: Kd_hi^T [D_hi | D_lo] + Kd_lo^T D_hi)
-//   S1 = diag(exp(gam_63)) S0 + C;  QDQ(S1) at a 64-token boundary
+//   S1 = diag(exp(gam_63)) S0 + Kd^T Delta,  Kd = K o exp(gam_63 - gam);  QDQ(S1) at a 64-token boundary
 //   o = scale (Qd S0 + P Delta),  Qd = Q o exp(gam)
-// Roles as in the GDN chain kernel: the chain warpgroup (warps 4-7) runs X -> Delta -> C -> state
-// update, the only part that is serial from chunk to chunk; the output warpgroup (warps 0-3) issues
-// U, Y = Qd S0 and P Delta, refills their buffers and writes o. Each warpgroup issues its own MMAs
-// from a thread on its own SM sub-partition. Every staged operand has one buffer, refilled as soon
-// as its last reader is done (a chunk ahead of its next use). Every wait is bounded; a warp whose
-// wait gives up raises a CTA-wide abort flag, both warpgroups leave their loops together at their
-// next checked barrier, TMA in flight is waited for (bounded), TMEM is freed.
+// The state lives in TMEM as the accumulator of Kd^T Delta: the chain stores diag(exp(gam_63)) S0
+// there and the MMAs add Kd_hi^T D_hi + Kd_hi^T D_lo + Kd_lo^T D_hi on top. S0 as an MMA operand
+// (codes after a QDQ, else bf16 hi + lo) is double-buffered in shared memory, so Y = Qd S0 of one
+// chunk never holds up the next state.
+//
+// Roles: the chain warpgroup (warps 4-7) runs X -> Delta -> C -> state epilogue, the only part that
+// is serial from chunk to chunk; the output warpgroup (warps 0-3) issues Y, P Delta and the next U
+// and writes o. The tensor pipe runs MMAs in issue order, so the output issuer places its MMAs
+// behind the chain's: Y(c) after X(c) is issued (it runs while the chain computes Delta), P Delta
+// and the next U after C(c) (they run while the chain updates the state). Each warpgroup issues
+// from a thread on its own SM sub-partition. Every staged operand has one buffer, refilled once its
+// last reader is done. Every wait is bounded; a warp whose wait gives up raises a CTA-wide abort
+// flag, both warpgroups leave their loops together at their next checked barrier, TMA in flight
+// is waited for (bounded), TMEM is freed.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -37,23 +43,24 @@ constexpr uint32_t OFF_KD = 32 * KB;     // Kd hi | lo, same block layout (the M
 constexpr uint32_t OFF_TT = 64 * KB;     // T'' hi | lo [64 r][64 i] K-major
 constexpr uint32_t OFF_V = 80 * KB;      // V slab [64 tok][64 j]
 constexpr uint32_t OFF_WT = 88 * KB;     // W^T codes [128 c][64 r] (or hi | lo, 16 KB apart)
-constexpr uint32_t OFF_S = 120 * KB;     // S0 operand [128 c][64 j] MN-major; lo at +16 KB
-constexpr uint32_t OFF_DL = 152 * KB;    // Delta hi | lo ([i][j] MN-major, 8 KB each)
-constexpr uint32_t OFF_P = 168 * KB;     // P hi | lo ([r][i] K-major)
-constexpr uint32_t OFF_MISC = 184 * KB;  // S0 scale [2], S0-is-codes [2], partial maxima [4], abort flag
-constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;
+constexpr uint32_t OFF_S = 120 * KB;     // two S0 operand buffers [128 c][64 j] MN-major: codes or hi, lo at +16 KB
+constexpr uint32_t OFF_DL = 184 * KB;    // Delta hi | lo ([i][j] MN-major, 8 KB each)
+constexpr uint32_t OFF_P = 200 * KB;     // P hi | lo ([r][i] K-major)
+constexpr uint32_t OFF_MISC = 216 * KB;  // S0 scale [4], S0-is-codes [4], partial maxima [4], flags
+constexpr uint32_t kSmemBytes = OFF_MISC + 128 + 1024;
 
-constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128, TM_C = 192 /* [0, 64) + [64, 128) */, TM_PD = 320;
+constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128, TM_S = 192, TM_PD = 256;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);     // T'' (K) x V (MN)
 constexpr uint32_t IDESC_X = tc::make_idesc(tc::kKindBF16, 64, 64, true, true);      // W^T (MN) x S0 (MN)
 constexpr uint32_t IDESC_Y = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);     // Qd (K) x S0 (MN)
-constexpr uint32_t IDESC_C2 = tc::make_idesc(tc::kKindBF16, 128, 128, true, true);   // Kd_hi^T x [D_hi | D_lo]
-constexpr uint32_t IDESC_C1 = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);    // Kd_lo^T x D_hi
+constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);     // Kd^T (MN) x Delta (MN)
 constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // P (K) x Delta (MN)
 
-enum : int { B_QD = 0, B_KD, B_TV, B_WC, B_PL, B_U, B_X, B_Y, B_C, B_PD, B_SRDY, B_DRDY, kNumBars };
+enum : int {
+  B_QD = 0, B_KD, B_TV, B_WC, B_PL, B_U, B_X, B_Y0, B_Y1, B_C, B_PD, B_SRDY0, B_SRDY1, B_DRDY, kNumBars
+};
 
 struct KdaChainParams {
   const float* vec;
@@ -115,15 +122,19 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
   auto chunk_len = [&](int64_t cj) { return (len - cj * 64) < 64 ? (int)(len - cj * 64) : 64; };
 
   float* const misc = reinterpret_cast<float*>(sm + OFF_MISC);
-  float* const s_scale_slot = misc;
-  int* const s_exact_slot = reinterpret_cast<int*>(misc + 2);
-  float* const red = misc + 4;
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 8);
+  float* const s_scale_slot = misc;                                   // [4], by chunk & 3
+  int* const s_exact_slot = reinterpret_cast<int*>(misc + 4);         // [4]
+  float* const red = misc + 8;                                        // [4]
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 12);
+  volatile int* const x_issued = reinterpret_cast<volatile int*>(misc + 13);   // chunks whose X is issued
+  volatile int* const c_issued = reinterpret_cast<volatile int*>(misc + 14);   // chunks whose C is issued
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), 1);
     *abort_flag = 0;
+    *x_issued = 0;
+    *c_issued = 0;
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&tv);
     tc::tma_prefetch_desc(&twt);
@@ -144,7 +155,7 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
   const uint64_t dV = tc::make_sdesc(sbase + OFF_V, 8 * KB, 1024);
   const uint64_t dWT = tc::make_sdesc(sbase + OFF_WT, 16 * KB, 1024);
   const uint64_t dS = tc::make_sdesc(sbase + OFF_S, 16 * KB, 1024);
-  const uint64_t dD = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);     // [Delta_hi | Delta_lo]
+  const uint64_t dD = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);     // Delta_hi, Delta_lo 8 KB apart
   const uint64_t dP = tc::make_sdesc(sbase + OFF_P, 16, 1024);
 
   auto tma_qd = [&](int64_t cj) {
@@ -194,6 +205,20 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
       ok = false;
     }
   };
+  // warp-collective bounded wait until a chunk counter of the other warpgroup reaches `target`
+  auto wait_count = [&](volatile int* ctr, int target) {
+    if (__all_sync(0xffffffffu, live())) {
+      bool reached = false;
+      for (uint32_t it = 0; it < (1u << 22) && !reached; ++it) {
+        reached = __all_sync(0xffffffffu, *ctr >= target);
+        if (!reached && (it & 1023u) == 1023u && *abort_flag) break;
+      }
+      ok = reached;
+      if (!ok && lt == 0) *abort_flag = 1;
+    } else {
+      ok = false;
+    }
+  };
 
   if (warp < 4) {
     // ================================ output warpgroup ================================
@@ -207,9 +232,10 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
       tc::mma_commit(bar(B_U));
     };
     // Only the issuing warp waits on the barriers that gate an issue or a refill: a refill of a
-    // buffer follows its reader's completion, which follows that warp's wait on the fill, so no
-    // barrier can run a phase ahead of a warp still waiting on it. Every warp waits on Y and
-    // P Delta, whose accumulators it reads.
+    // buffer follows its reader's completion, which follows that warp's wait on the fill, and
+    // S0-ready / Y alternate between two barriers by chunk parity, so no barrier can run a phase
+    // ahead of a warp still waiting on it. Every warp waits on Y and P Delta, whose accumulators
+    // it reads.
     const bool issuer_warp = warp == kOutIssuer / 32;
     if (nchunks > 0 && issuer_warp) {
       wait(B_TV, 0);
@@ -217,35 +243,38 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
     }
     for (int64_t c = 0; c < nchunks; ++c) {
       const int L = chunk_len(c);
-      const uint32_t par = (uint32_t)(c & 1);
-      // T'' / V are free once U has read them
+      const uint32_t par = (uint32_t)(c & 1), par2 = (uint32_t)((c >> 1) & 1);
       if (issuer_warp) {
+        // T'' / V are free once U has read them
         wait(B_U, par);
         if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_tv(c + 1);
-        // ---- Y = Qd S0 once the chain has stored S0 ----
-        wait(B_SRDY, par);
+        // ---- Y = Qd S0 once S0 is stored and X(c) is ahead of it in the tensor pipe ----
+        wait(par ? B_SRDY1 : B_SRDY0, par2);
         wait(B_QD, par);
+        wait_count(x_issued, (int)c + 1);
       }
       if (tid == kOutIssuer && live()) {
-        const bool s_exact = s_exact_slot[c & 1] != 0;
+        const bool s_exact = s_exact_slot[c & 3] != 0;
+        const uint32_t sb = par * 32 * KB;
         tc::tc_fence_after();
         // Qd_hi x S (codes or hi) + Qd_lo x S [+ Qd_hi x S_lo]; the two 64-column key blocks of Qd
         // are 8 KB apart, each 16-key step of S is 2 KB
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           if (q == 2 && s_exact) break;
-          const uint32_t aoff = q == 1 ? 16 * KB : 0, boff = q == 2 ? 16 * KB : 0;
+          const uint32_t aoff = q == 1 ? 16 * KB : 0, boff = sb + (q == 2 ? 16 * KB : 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             tc::mma_bf16(tmem + TM_Y, dadv(dQd, aoff + (ks >> 2) * 8 * KB + (ks & 3) * 32), dadv(dS, boff + ks * 2048),
                          IDESC_Y, (q | ks) != 0);
         }
-        tc::mma_commit(bar(B_Y));
+        tc::mma_commit(bar(par ? B_Y1 : B_Y0));
       }
-      // ---- P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi once the chain has stored Delta ----
+      // ---- P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi and the next U, behind C(c) ----
       if (issuer_warp) {
         wait(B_DRDY, par);
         wait(B_PL, par);
+        wait_count(c_issued, (int)c + 1);
       }
       if (tid == kOutIssuer && live()) {
         tc::tc_fence_after();
@@ -257,21 +286,19 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
                          IDESC_PD, (q | ks) != 0);
         tc::mma_commit(bar(B_PD));
       }
-      // ---- the next chunk's U (the chain stored Delta, so it has read U) ----
-      if (c + 1 < nchunks && issuer_warp) {
+      if (c + 1 < nchunks && issuer_warp) {   // the chain stored Delta, so it has read U
         wait(B_TV, par ^ 1u);
         if (tid == kOutIssuer && live()) issue_u();
       }
-      // ---- refills once their readers are done: Qd after Y (the chain saw this Qd before it
-      // stored Delta), P after P Delta ----
-      wait(B_Y, par);
+      // ---- refills once their readers are done: Qd after Y, P after P Delta ----
+      wait(par ? B_Y1 : B_Y0, par2);
       if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_qd(c + 1);
       wait(B_PD, par);
       if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_p(c + 1);
-      // ---- o = scale (Y + P Delta), rows r < L; S0's scale slot is rewritten only after Y(c + 1) ----
+      // ---- o = scale (Y + P Delta), rows r < L; the scale slot is rewritten only after Y(c + 2) ----
       tc::tc_fence_after();
       {
-        const float y_scale = s_scale_slot[c & 1];
+        const float y_scale = s_scale_slot[c & 3];
         float yv[32], pv[32];
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_Y), yv);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_Y + 16), yv + 16);
@@ -293,26 +320,44 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
   } else {
     // ================================ chain warpgroup ================================
     const int ctid = tid - 128;
-    const int64_t sb = ((int64_t)n * p.Hv + h) * 128 * p.dv + slab * 64;   // S[c][j] at sb + c dv + j
-    float S[64];   // state row lane128 of the slab
-    if (p.h0) {
-      const float4* src = reinterpret_cast<const float4*>(p.h0 + sb + (int64_t)lane128 * p.dv);
+    const bool issuer_warp = warp == 4 + kChainIssuer / 32;
+    const int64_t sbg = ((int64_t)n * p.Hv + h) * 128 * p.dv + slab * 64;   // S[c][j] at sbg + c dv + j
+    // the W scale of the current chunk (read from global one chunk ahead)
+    float sw_next = 1.f;
+    {   // S0: operand buffer 0 (bf16 hi + lo) and diag(exp(gam_63)) S0 into the TMEM state
+      float s0[64];
+      if (p.h0) {
+        const float4* src = reinterpret_cast<const float4*>(p.h0 + sbg + (int64_t)lane128 * p.dv);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 f = src[j];
-        S[4 * j] = f.x; S[4 * j + 1] = f.y; S[4 * j + 2] = f.z; S[4 * j + 3] = f.w;
+        for (int j = 0; j < 16; ++j) {
+          const float4 f = src[j];
+          s0[4 * j] = f.x; s0[4 * j + 1] = f.y; s0[4 * j + 2] = f.z; s0[4 * j + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s0[j] = 0.f;
       }
-    } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) S[j] = 0.f;
-    }
+      for (int q = 0; q < 8; ++q) {
+        uint4 h16, l16;
+        split8(s0 + 8 * q, h16, l16);
+        const uint32_t off = tc::sw128(lane128, 16 * q);
+        st16(sm, OFF_S + off, h16);
+        st16(sm, OFF_S + 16 * KB + off, l16);
+      }
+      if (nchunks > 0) {
+        const float el0 = p.vec[item(0) * 256 + lane128];
+        sw_next = p.vec[item(0) * 256 + 192];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      uint4 h16, l16;
-      split8(S + 8 * q, h16, l16);
-      const uint32_t off = tc::sw128(lane128, 16 * q);
-      st16(sm, OFF_S + off, h16);
-      st16(sm, OFF_S + 16 * KB + off, l16);
+        for (int j = 0; j < 64; ++j) s0[j] *= el0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tmem_st16(tc::tmem_addr(tmem, lane0, TM_S + 16 * q), s0 + 16 * q);
+        tc::tmem_st_wait();
+      } else if (p.hT) {   // an empty sequence: hT = h0
+        float4* out = reinterpret_cast<float4*>(p.hT + sbg + (int64_t)lane128 * p.dv);
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) out[j >> 2] = make_float4(s0[j], s0[j + 1], s0[j + 2], s0[j + 3]);
+      }
     }
     if (ctid == 0) {
       s_scale_slot[0] = 1.f;
@@ -321,43 +366,35 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     wg_sync(2);
-    if (ctid == 0) tc::mbar_arrive(bar(B_SRDY));
+    if (ctid == 0) tc::mbar_arrive(bar(B_SRDY0));
     bool s_exact = false;
     float s_scale = 1.f;
-    const bool issuer_warp = warp == 4 + kChainIssuer / 32;
-    // exp(gam_63) of this thread's key row and the W scale, read from global one chunk ahead
-    float el_next = 1.f, sw_next = 1.f;
-    if (nchunks > 0) {
-      el_next = p.vec[item(0) * 256 + lane128];
-      sw_next = p.vec[item(0) * 256 + 192];
-    }
     for (int64_t c = 0; c < nchunks; ++c) {
       const int L = chunk_len(c);
       const uint32_t par = (uint32_t)(c & 1);
-      const float el = el_next;
-      const float f = sw_next * s_scale;         // X holds codes x codes: W scale x S0 scale
-      if (c + 1 < nchunks) {
-        el_next = p.vec[item(c + 1) * 256 + lane128];
-        sw_next = p.vec[item(c + 1) * 256 + 192];
-      }
+      const uint32_t sb = par * 32 * KB;          // this chunk's S0 operand buffer
+      const float f = sw_next * s_scale;          // X holds codes x codes: W scale x S0 scale
+      const float el1 = (c + 1 < nchunks) ? p.vec[item(c + 1) * 256 + lane128] : 1.f;   // the next chunk's decay
+      if (c + 1 < nchunks) sw_next = p.vec[item(c + 1) * 256 + 192];
       // ---- X = W S0 ----
       if (issuer_warp) wait(B_WC, par);
       if (ctid == kChainIssuer && live()) {
         tc::tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tmem + TM_X, dadv(dWT, ks * 2048), dadv(dS, ks * 2048), IDESC_X, ks > 0);
+          tc::mma_bf16(tmem + TM_X, dadv(dWT, ks * 2048), dadv(dS, sb + ks * 2048), IDESC_X, ks > 0);
         if (!s_exact) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tmem + TM_X, dadv(dWT, ks * 2048), dadv(dS, 16 * KB + ks * 2048), IDESC_X, 1);
+            tc::mma_bf16(tmem + TM_X, dadv(dWT, ks * 2048), dadv(dS, sb + 16 * KB + ks * 2048), IDESC_X, 1);
         }
         if (!p.w_qdq) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tmem + TM_X, dadv(dWT, 16 * KB + ks * 2048), dadv(dS, ks * 2048), IDESC_X, 1);
+            tc::mma_bf16(tmem + TM_X, dadv(dWT, 16 * KB + ks * 2048), dadv(dS, sb + ks * 2048), IDESC_X, 1);
         }
         tc::mma_commit(bar(B_X));
+        *x_issued = (int)c + 1;
       }
       wait(B_X, par);
       if (ctid == kChainIssuer && c + 1 < nchunks && live()) tma_wc(c + 1);
@@ -388,82 +425,86 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
       if (ctid == 0) tc::mbar_arrive(bar(B_DRDY));   // Delta stored; U and X read
-      // ---- C = Kd_hi^T [D_hi | D_lo] + Kd_lo^T D_hi ----
+      // ---- state += Kd_hi^T D_hi + Kd_hi^T D_lo + Kd_lo^T D_hi ----
       if (issuer_warp) wait(B_KD, par);
       if (ctid == kChainIssuer && live()) {
         tc::tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_C, dadv(dKd, ks * 2048), dadv(dD, ks * 2048), IDESC_C2, ks > 0);
+        for (int q = 0; q < 3; ++q)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_C, dadv(dKd, 16 * KB + ks * 2048), dadv(dD, ks * 2048), IDESC_C1, 1);
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + TM_S, dadv(dKd, (q == 2 ? 16 * KB : 0) + ks * 2048), dadv(dD, (q == 1 ? 8 * KB : 0) + ks * 2048),
+                         IDESC_C, 1);
         tc::mma_commit(bar(B_C));
+        *c_issued = (int)c + 1;
       }
       wait(B_C, par);
       if (ctid == kChainIssuer && c + 1 < nchunks && live()) tma_kd(c + 1);   // Kd is free once C has read it
-      // ---- S1 = exp(gam_63) S0 + C; QDQ at the 64-token boundary (after Y has read S0) ----
-      wait(B_Y, par);
+      // ---- S1 from TMEM; QDQ at the 64-token boundary; into the other operand buffer once
+      // Y(c - 1) has read it; diag(exp(gam_63)) S1 back into TMEM for the next chunk ----
       tc::tc_fence_after();
-      {
-        float* const s1 = S;
+      float s1[64];
 #pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {
-          float ca[16], cb[16];
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + h4 * 16), ca);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 64 + h4 * 16), cb);
-          tc::tmem_ld_wait();
+      for (int q = 0; q < 4; ++q) tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_S + 16 * q), s1 + 16 * q);
+      tc::tmem_ld_wait();
+      const uint32_t nb = (par ^ 1u) * 32 * KB;
+      if (c > 0) wait(par ? B_Y0 : B_Y1, (uint32_t)(((c - 1) >> 1) & 1));
+      if (p.state_qdq && L == 64) {
+        float m8[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) s1[h4 * 16 + j] = fmaf(el, s1[h4 * 16 + j], ca[j] + cb[j]);
+        for (int u = 0; u < 8; ++u) m8[u] = fabsf(s1[u]);
+#pragma unroll
+        for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], fabsf(s1[j]));
+        const float mm = warp_absmax(fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
+        if (lt == 0) red[quad] = mm;
+        wg_sync(2);
+        const float amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        const float sS = qdq_scale(amax), rS = __frcp_rn(sS);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float cd[8];
+#pragma unroll
+          for (int u = 0; u < 8; u += 2)
+            qdq_pair(s1[8 * q + u], s1[8 * q + u + 1], rS, sS, cd[u], cd[u + 1], s1[8 * q + u], s1[8 * q + u + 1]);
+          st16(sm, OFF_S + nb + tc::sw128(lane128, 16 * q), pack8(cd));
         }
-        if (p.state_qdq && L == 64) {
-          float m8[8];
+        s_exact = true;
+        s_scale = sS;
+      } else {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) m8[u] = fabsf(s1[u]);
-#pragma unroll
-          for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], fabsf(s1[j]));
-          float mm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          mm = warp_max(mm);
-          if (lt == 0) red[quad] = mm;
-          wg_sync(2);
-          const float amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-          const float sS = qdq_scale(amax), rS = __frcp_rn(sS);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float cd[8];
-#pragma unroll
-            for (int u = 0; u < 8; u += 2)
-              qdq_pair(s1[8 * q + u], s1[8 * q + u + 1], rS, sS, cd[u], cd[u + 1], s1[8 * q + u], s1[8 * q + u + 1]);
-            st16(sm, OFF_S + tc::sw128(lane128, 16 * q), pack8(cd));
-          }
-          s_exact = true;
-          s_scale = sS;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint4 h16, l16;
-            split8(s1 + 8 * q, h16, l16);
-            const uint32_t off = tc::sw128(lane128, 16 * q);
-            st16(sm, OFF_S + off, h16);
-            st16(sm, OFF_S + 16 * KB + off, l16);
-          }
-          s_exact = false;
-          s_scale = 1.f;
+        for (int q = 0; q < 8; ++q) {
+          uint4 h16, l16;
+          split8(s1 + 8 * q, h16, l16);
+          const uint32_t off = tc::sw128(lane128, 16 * q);
+          st16(sm, OFF_S + nb + off, h16);
+          st16(sm, OFF_S + nb + 16 * KB + off, l16);
         }
+        s_exact = false;
+        s_scale = 1.f;
+      }
+      if (c + 1 < nchunks) {
+        float e[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) e[u] = el1 * s1[16 * q + u];
+          tc::tmem_st16(tc::tmem_addr(tmem, lane0, TM_S + 16 * q), e);
+        }
+        tc::tmem_st_wait();
+      } else if (live() && p.hT) {
+        float4* out = reinterpret_cast<float4*>(p.hT + sbg + (int64_t)lane128 * p.dv);
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) out[j >> 2] = make_float4(s1[j], s1[j + 1], s1[j + 2], s1[j + 3]);
       }
       if (ctid == 0) {
-        s_scale_slot[(c + 1) & 1] = s_scale;
-        s_exact_slot[(c + 1) & 1] = s_exact ? 1 : 0;
+        s_scale_slot[(c + 1) & 3] = s_scale;
+        s_exact_slot[(c + 1) & 3] = s_exact ? 1 : 0;
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
-      if (ctid == 0) tc::mbar_arrive(bar(B_SRDY));   // S0 of chunk c + 1 is stored
-    }
-    if (live() && p.hT) {
-      float4* out = reinterpret_cast<float4*>(p.hT + sb + (int64_t)lane128 * p.dv);
-#pragma unroll
-      for (int j = 0; j < 64; j += 4) out[j >> 2] = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      if (ctid == 0) tc::mbar_arrive(bar(par ? B_SRDY0 : B_SRDY1));   // S0 of chunk c + 1 is stored
     }
   }
 

@@ -10,23 +10,25 @@
 //   Qd = Q o exp(gam),  Kd = K o exp(gam_63 - gam)                              -> workspace, hi + lo
 //   exp(gam_63[c])                                                               -> workspace
 // so that the state chain needs no per-channel exponentials: Y = Qd S0, C = Kd^T Delta,
-// S1 = diag(exp(gam_63)) S0 + C.
+// S1 = diag(exp(gam_63)) S0 + C. Every output goes from registers straight to global memory, in
+// the row-major bf16 layout the chain kernel's TMA loads read.
 //
 // The pairwise decays factor through a per-channel anchor: exp(gam_r - gam_i) = exp(gam_r - m)
 // exp(m - gam_i). When every channel's gam spans at most kChunkSpan over the chunk, m is the
 // midpoint of its range, both factors stay within exp(+-kChunkSpan / 2) (normal in fp32 and bf16),
 // and A and P are one tcgen05 product, [K o e^(gam - m) ; Q o e^(gam - m)] (K o e^(m - gam))^T, on
-// bf16 hi + lo operands, masked to i < r (A) and i <= r (P). Steeper chunks take CUDA cores:
-// the pairwise decays factor through the first token a = 16 b of each 16-row block b:
-// exp(gam_r - gam_i) = exp(gam_r - gam_a) exp(gam_a - gam_i), so A and P for rows of block b are
-// plain dot products of rows decayed to a. Below the diagonal block both exponents are <= 0 for
-// log-decays g <= 0 (no overflow; a factor that underflows bounds a product that is as small).
-// Inside the diagonal block exp(gam_a - gam_i) >= 1; the factored form is used there when every
-// channel's |gam_i - gam_a| over the block stays <= kDiagRange (both factors normal fp32, each
-// exponential's relative error a few 1e-6), else that block takes the pairwise exponentials
-// directly. The WY products run on tcgen05 (bf16 hi + lo);
-// the rest on CUDA cores. Every mbarrier wait is bounded; a CTA that gives up records it in the
-// status word, waits (bounded) for its TMA load in flight, frees its TMEM and exits.
+// bf16 hi + lo operands, masked to i < r (A) and i <= r (P); Qd, Kd and K o exp(gam) then follow
+// from the same two exponentials and the per-channel factors e^m, e^(gam_63 - m). Steeper chunks
+// take CUDA cores: the pairwise decays factor through the first token a = 16 b of each 16-row
+// block b: exp(gam_r - gam_i) = exp(gam_r - gam_a) exp(gam_a - gam_i), so A and P for rows of
+// block b are plain dot products of rows decayed to a. Below the diagonal block both exponents are
+// <= 0 for log-decays g <= 0 (no overflow; a factor that underflows bounds a product that is as
+// small). Inside the diagonal block exp(gam_a - gam_i) >= 1; the factored form is used there when
+// every channel's |gam_i - gam_a| over the block stays <= kDiagRange (both factors normal fp32,
+// each exponential's relative error a few 1e-6), else that block takes the pairwise exponentials
+// directly. The WY products run on tcgen05 (bf16 hi + lo); the rest on CUDA cores. Every mbarrier
+// wait is bounded; a CTA that gives up records it in the status word, waits (bounded) for its TMA
+// load in flight, frees its TMEM and exits.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -42,22 +44,21 @@ constexpr int A_LD = 68;
 constexpr float kDiagRange = 40.f;
 constexpr float kChunkSpan = 64.f;
 // shared memory map (byte offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0, OFF_K = 16 * KB;           // Q0 | Q1, K0 | K1 (TMA, 128-byte swizzle); later W^T
-constexpr uint32_t OFF_G = 32 * KB;                      // gam fp32 [64][GLD]
-constexpr uint32_t OFF_A = 66 * KB;                      // A fp32 [64][A_LD]
-constexpr uint32_t OFF_T = 83 * KB;                      // P fp32 [64][A_LD] (before the solve), then T
-constexpr uint32_t OFF_SCR = 100 * KB;                   // 64 KB: decayed rows; solve scratch; Qd | Kd; Kt
-constexpr uint32_t OFF_TT = 164 * KB;                    // T'' hi | lo [64 r][64 i] K-major
-constexpr uint32_t OFF_P = 180 * KB;                     // P hi | lo [64 r][64 i] K-major
-constexpr uint32_t OFF_VEC = 196 * KB;                   // beta [64], partial maxima [8], anchor m [128] at 128
+constexpr uint32_t OFF_Q = 0, OFF_K = 16 * KB;   // Q0 | Q1, K0 | K1 (TMA, 128-byte swizzle); then K o exp(gam) hi | lo
+constexpr uint32_t OFF_G = 32 * KB;              // gam fp32 [64][GLD]
+constexpr uint32_t OFF_A = 66 * KB;              // A fp32 [64][A_LD]
+constexpr uint32_t OFF_T = 83 * KB;              // P fp32 [64][A_LD] (CUDA-core form, before the solve), then T
+constexpr uint32_t OFF_SCR = 100 * KB;           // 64 KB: decayed rows (CUDA-core form); solve scratch
+constexpr uint32_t OFF_TT = 164 * KB;            // T'' hi | lo [64 r][64 i] K-major
+constexpr uint32_t OFF_VEC = 196 * KB;           // beta [64], partial maxima [8], then [128] each: m, e^m, e^(gam_63 - m)
 // tensor-core A / P operands (bf16 hi, lo): [K o e^(gam - m) ; Q o e^(gam - m)] (128 rows, k blocks 16 KB
-// apart), K o e^(m - gam) (64 rows, k blocks 8 KB apart); they overlay the scratch, T'' and P regions
+// apart), K o e^(m - gam) (64 rows, k blocks 8 KB apart); they overlay the scratch and T'' regions
 constexpr uint32_t OFF_LQ = OFF_SCR, OFF_LQ_LO = OFF_SCR + 32 * KB, OFF_KR = OFF_SCR + 64 * KB, OFF_KR_LO = OFF_KR + 16 * KB;
-constexpr uint32_t kSmemBytes = OFF_VEC + 1024 + 1024;   // + slack to align the base
+constexpr uint32_t kSmemBytes = OFF_VEC + 2 * KB + 1024;   // + slack to align the base
 static_assert(OFF_G + 64 * GLD * 4 <= OFF_A && OFF_A + 64 * A_LD * 4 <= OFF_T && OFF_T + 64 * A_LD * 4 <= OFF_SCR,
               "regions overlap");
 static_assert((16 + 16 + 64) * GLD * 4 <= 64 * KB, "decayed-row scratch exceeds its region");
-static_assert(OFF_KR_LO + 16 * KB <= OFF_VEC && OFF_TT >= OFF_KR && OFF_P >= OFF_KR_LO, "operand overlay");
+static_assert(OFF_KR_LO + 16 * KB <= OFF_VEC && OFF_TT + 16 * KB <= OFF_VEC, "operand overlay");
 static_assert(kThreads == 256, "the thread mappings below assume 256 threads");
 
 constexpr uint32_t TM_WT = 0;
@@ -69,11 +70,26 @@ struct KdaPrepParams {
   const float* g;      // [tokens, Hv, 128]
   const float* beta;   // [tokens, Hv]
   const int32_t* cu;
-  float* vec;
+  float* vec;          // per item: exp(gam_63) [128], W scale at 192
+  unsigned char* wt;   // per item 128 (W QDQ) or 256 rows of 128 bytes: W^T codes, or hi then lo
+  unsigned char* tt;   // per item 128 rows: T'' hi [64 r], lo [64 r]
+  unsigned char* pp;   // per item 128 rows: P hi, lo
+  unsigned char* qd;   // per item 256 rows: Qd hi [c < 64: 64 r | c >= 64: 64 r], lo (same)
+  unsigned char* kd;   // per item 256 rows: Kd, same layout
   int* status;
   int T, N, Hqk, Hv;
   int w_qdq;
 };
+
+// 8 consecutive floats from shared memory (16-byte aligned)
+__device__ __forceinline__ void ld8(const float* src, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+// 16 bytes into column group col8 (0..7) of a 128-byte row of a workspace array
+__device__ __forceinline__ void stg16(unsigned char* base, int64_t row, int col8, uint4 v) {
+  *reinterpret_cast<uint4*>(base + row * 128 + col8 * 16) = v;
+}
 
 __device__ __forceinline__ int64_t seq_start(const KdaPrepParams& p, int n) {
   return p.cu ? (int64_t)p.cu[n] : (int64_t)n * p.T;
@@ -98,9 +114,7 @@ __device__ __forceinline__ void tile4(const unsigned char* tile, int r, int c4, 
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap twt, const __grid_constant__ CUtensorMap ttt,
-                      const __grid_constant__ CUtensorMap tpp, const __grid_constant__ CUtensorMap tqd,
-                      const __grid_constant__ CUtensorMap tkd, const KdaPrepParams p) {
+                      const KdaPrepParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ uint32_t tmem_slot;
@@ -135,6 +149,8 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   float* const vbeta = reinterpret_cast<float*>(sm + OFF_VEC);
   float* const red = vbeta + 64;
   float* const gmid = vbeta + 128;
+  float* const gem = vbeta + 256;
+  float* const ge63m = vbeta + 384;
   const uint32_t bar_k = tc::smem_u32(&bars[0]), bar_w = tc::smem_u32(&bars[1]);
 
   if (tid == 0) {
@@ -180,12 +196,78 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mx = fmaxf(mx, acc);
       mn = fminf(mn, acc);
     }
+    const float m = 0.5f * (mx + mn);
     p.vec[item * 256 + tid] = __expf(acc);
-    gmid[tid] = 0.5f * (mx + mn);
+    gmid[tid] = m;
+    gem[tid] = __expf(m);
+    ge63m[tid] = __expf(acc - m);
     steep = !(mx - mn <= kChunkSpan);
   }
   const bool tc_ap = !__syncthreads_or(steep);   // uniform across the CTA
   uint32_t w_phase = 0;                           // bar_w completions waited for so far
+
+  // Qd, Kd (hi | lo) -> global; K o exp(gam) (hi | lo) -> smem over the Q / K tiles (each thread
+  // overwrites only the tile bytes it has read); with the anchor, also the A / P operands
+  auto produce = [&](bool anchored) {
+    for (int t = tid; t < 64 * 16; t += kThreads) {
+      const int r = t >> 4, c8 = (t & 15) * 8;
+      float kf[8], qf[8], gv[8], qd[8], kd[8], kt[8];
+      tile8(Qt, r, c8, qf);
+      tile8(Kt, r, c8, kf);
+      ld8(gam + r * GLD + c8, gv);
+      const uint32_t kb = (uint32_t)(c8 >> 6), col = 2 * (c8 & 63);
+      const uint32_t sk = tc::sw128(r, col);
+      uint4 h16, l16;
+      if (anchored) {
+        float mv[8], em[8], e63[8], kl[8], ql[8], kr[8];
+        ld8(gmid + c8, mv);
+        ld8(gem + c8, em);
+        ld8(ge63m + c8, e63);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float x = gv[u] - mv[u];
+          const float el = __expf(x), er = __expf(-x);
+          kl[u] = kf[u] * el;
+          ql[u] = qf[u] * el;
+          kr[u] = kf[u] * er;
+          qd[u] = ql[u] * em[u];
+          kt[u] = kl[u] * em[u];
+          kd[u] = kr[u] * e63[u];
+        }
+        const uint32_t sq = tc::sw128(64 + r, col);
+        split8(kl, h16, l16);
+        st16(sm, OFF_LQ + kb * 16 * KB + sk, h16);
+        st16(sm, OFF_LQ_LO + kb * 16 * KB + sk, l16);
+        split8(ql, h16, l16);
+        st16(sm, OFF_LQ + kb * 16 * KB + sq, h16);
+        st16(sm, OFF_LQ_LO + kb * 16 * KB + sq, l16);
+        split8(kr, h16, l16);
+        st16(sm, OFF_KR + kb * 8 * KB + sk, h16);
+        st16(sm, OFF_KR_LO + kb * 8 * KB + sk, l16);
+      } else {
+        float g63[8];
+        ld8(gam + 63 * GLD + c8, g63);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float e1 = __expf(gv[u]), e2 = __expf(g63[u] - gv[u]);
+          qd[u] = qf[u] * e1;
+          kt[u] = kf[u] * e1;
+          kd[u] = kf[u] * e2;
+        }
+      }
+      const int64_t row = item * 256 + kb * 64 + r;
+      const int c16 = (c8 & 63) >> 3;
+      split8(qd, h16, l16);
+      stg16(p.qd, row, c16, h16);
+      stg16(p.qd, row + 128, c16, l16);
+      split8(kd, h16, l16);
+      stg16(p.kd, row, c16, h16);
+      stg16(p.kd, row + 128, c16, l16);
+      split8(kt, h16, l16);
+      st16(sm, OFF_Q + kb * 8 * KB + sk, h16);
+      st16(sm, OFF_K + kb * 8 * KB + sk, l16);
+    }
+  };
 
   bool ok = true, k_done = false;
   float sW = 1.f;
@@ -196,37 +278,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 
     if (tc_ap) {
       // ---- A and P on tcgen05 ----
-      for (int t = tid; t < 64 * 16; t += kThreads) {
-        const int r = t >> 4, c8 = (t & 15) * 8;
-        float kf[8], qf[8], kl[8], ql[8], kr[8];
-        tile8(Kt, r, c8, kf);
-        tile8(Qt, r, c8, qf);
-        const float4 g0 = *reinterpret_cast<const float4*>(gam + r * GLD + c8);
-        const float4 g1 = *reinterpret_cast<const float4*>(gam + r * GLD + c8 + 4);
-        const float4 m0 = *reinterpret_cast<const float4*>(gmid + c8);
-        const float4 m1 = *reinterpret_cast<const float4*>(gmid + c8 + 4);
-        const float x[8] = {g0.x - m0.x, g0.y - m0.y, g0.z - m0.z, g0.w - m0.w,
-                            g1.x - m1.x, g1.y - m1.y, g1.z - m1.z, g1.w - m1.w};
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float el = __expf(x[u]), er = __expf(-x[u]);
-          kl[u] = kf[u] * el;
-          ql[u] = qf[u] * el;
-          kr[u] = kf[u] * er;
-        }
-        const uint32_t kb = (uint32_t)(c8 >> 6), col = 2 * (c8 & 63);
-        const uint32_t sk = tc::sw128(r, col), sq = tc::sw128(64 + r, col);
-        uint4 h16, l16;
-        split8(kl, h16, l16);
-        st16(sm, OFF_LQ + kb * 16 * KB + sk, h16);
-        st16(sm, OFF_LQ_LO + kb * 16 * KB + sk, l16);
-        split8(ql, h16, l16);
-        st16(sm, OFF_LQ + kb * 16 * KB + sq, h16);
-        st16(sm, OFF_LQ_LO + kb * 16 * KB + sq, l16);
-        split8(kr, h16, l16);
-        st16(sm, OFF_KR + kb * 8 * KB + sk, h16);
-        st16(sm, OFF_KR_LO + kb * 8 * KB + sk, l16);
-      }
+      produce(true);
       tc::fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) {
@@ -266,8 +318,8 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             for (int u = 0; u < 8; ++u) pv[u] = 8 * q + u <= r ? d[8 * q + u] : 0.f;
             uint4 h16, l16;
             split8(pv, h16, l16);
-            st16(sm, OFF_P + tc::sw128(r, 16 * q), h16);
-            st16(sm, OFF_P + 8 * KB + tc::sw128(r, 16 * q), l16);
+            stg16(p.pp, item * 128 + r, q, h16);
+            stg16(p.pp, item * 128 + 64 + r, q, l16);
           }
         }
       }
@@ -372,20 +424,20 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         }
         __syncthreads();
       }
-      // P -> bf16 hi | lo, K-major [r][i] (P is read from the T region, which the solve reuses)
+      // P -> global, hi | lo (P is read from the T region, which the solve reuses)
       for (int t = tid; t < 512; t += kThreads) {
         const int r = t >> 3, i0 = (t & 7) * 8;
-        const float4 pa = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
-        const float4 pb = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
-        const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        float pv[8];
+        ld8(Tm + r * A_LD + i0, pv);
         uint4 h16, l16;
         split8(pv, h16, l16);
-        const uint32_t off = tc::sw128(r, 2 * i0);
-        st16(sm, OFF_P + off, h16);
-        st16(sm, OFF_P + 8 * KB + off, l16);
+        stg16(p.pp, item * 128 + r, i0 >> 3, h16);
+        stg16(p.pp, item * 128 + 64 + r, i0 >> 3, l16);
       }
       __syncthreads();
       for (int e = tid; e < 64 * A_LD; e += kThreads) Tm[e] = 0.f;
+      produce(false);   // the Q / K tiles have been read by A and P
+      tc::fence_proxy_async_smem();
       __syncthreads();
     }
 
@@ -451,73 +503,28 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       __syncthreads();
     }
 
-    // ---- T'' = T diag(beta) (hi | lo, K-major [r][i]); Qd, Kd (hi | lo, [row][c] in 64-column blocks) ----
+    // ---- T'' = T diag(beta): hi | lo, K-major [r][i], to smem (the W product) and global ----
     for (int t = tid; t < 512; t += kThreads) {
       const int r = t >> 3, i0 = (t & 7) * 8;
-      const float4 ta = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
-      const float4 tb = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
-      const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-      float t2[8];
+      float tv[8], bv[8], t2[8];
+      ld8(Tm + r * A_LD + i0, tv);
+      ld8(vbeta + i0, bv);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) t2[u] = tv[u] * vbeta[i0 + u];
+      for (int u = 0; u < 8; ++u) t2[u] = tv[u] * bv[u];
       uint4 h16, l16;
       split8(t2, h16, l16);
       const uint32_t off = tc::sw128(r, 2 * i0);
       st16(sm, OFF_TT + off, h16);
       st16(sm, OFF_TT + 8 * KB + off, l16);
-    }
-    for (int t = tid; t < 64 * 16; t += kThreads) {
-      const int r = t >> 4, c8 = (t & 15) * 8;
-      float qf[8], kf[8], xq[8], xk[8];
-      tile8(Qt, r, c8, qf);
-      tile8(Kt, r, c8, kf);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float gr = gam[r * GLD + c8 + u];
-        xq[u] = qf[u] * __expf(gr);
-        xk[u] = kf[u] * __expf(gam[63 * GLD + c8 + u] - gr);
-      }
-      const uint32_t off = (c8 >> 6) * 8 * KB + tc::sw128(r, 2 * (c8 & 63));
-      uint4 h16, l16;
-      split8(xq, h16, l16);
-      st16(sm, OFF_SCR + off, h16);
-      st16(sm, OFF_SCR + 16 * KB + off, l16);
-      split8(xk, h16, l16);
-      st16(sm, OFF_SCR + 32 * KB + off, h16);
-      st16(sm, OFF_SCR + 48 * KB + off, l16);
-    }
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc::tma_store_2d(&ttt, sbase + OFF_TT, 0, (int)(item * 128));
-      tc::tma_store_2d(&tpp, sbase + OFF_P, 0, (int)(item * 128));
-      tc::tma_store_2d(&tqd, sbase + OFF_SCR, 0, (int)(item * 256));
-      tc::tma_store_2d(&tqd, sbase + OFF_SCR + 16 * KB, 0, (int)(item * 256 + 128));
-      tc::tma_store_2d(&tkd, sbase + OFF_SCR + 32 * KB, 0, (int)(item * 256));
-      tc::tma_store_2d(&tkd, sbase + OFF_SCR + 48 * KB, 0, (int)(item * 256 + 128));
-      tc::bulk_commit();
-      tc::bulk_wait_read();   // the scratch is rewritten below
-    }
-    __syncthreads();
-    // K o exp(gam) (hi | lo): the MN-major operand of W^T = (K o exp(gam))^T T''^T
-    for (int t = tid; t < 64 * 16; t += kThreads) {
-      const int r = t >> 4, c8 = (t & 15) * 8;
-      float kf[8], xk[8];
-      tile8(Kt, r, c8, kf);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) xk[u] = kf[u] * __expf(gam[r * GLD + c8 + u]);
-      const uint32_t off = (c8 >> 6) * 8 * KB + tc::sw128(r, 2 * (c8 & 63));
-      uint4 h16, l16;
-      split8(xk, h16, l16);
-      st16(sm, OFF_SCR + off, h16);
-      st16(sm, OFF_SCR + 16 * KB + off, l16);
+      stg16(p.tt, item * 128 + r, i0 >> 3, h16);
+      stg16(p.tt, item * 128 + 64 + r, i0 >> 3, l16);
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
       tc::tc_fence_after();
-      const uint64_t dA = tc::make_sdesc(sbase + OFF_SCR, 8 * KB, 1024);   // MN-major, key blocks 8 KB apart
-      const uint64_t dB = tc::make_sdesc(sbase + OFF_TT, 16, 1024);        // K-major T'' [r][i]
+      const uint64_t dA = tc::make_sdesc(sbase + OFF_Q, 8 * KB, 1024);    // MN-major K o exp(gam), key blocks 8 KB apart
+      const uint64_t dB = tc::make_sdesc(sbase + OFF_TT, 16, 1024);       // K-major T'' [r][i]
       // Kt_hi T''_hi + Kt_hi T''_lo + Kt_lo T''_hi
 #pragma unroll
       for (int q = 0; q < 3; ++q)
@@ -532,14 +539,12 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     if (__syncthreads_or(!ok)) break;
     tc::tc_fence_after();
 
-    // ---- W QDQ: warps 0-3, thread = key channel c (TMEM lane), its 64 values W[r][c]; row c of W^T
-    // goes to the Q0 slot (c < 64) or the Q1 slot ----
+    // ---- W QDQ: warps 0-3, thread = key channel c (TMEM lane), its 64 values W[r][c] = row c of W^T ----
     float w[64];
     if (warp < 4) {
       ld32(tmem, (uint32_t)warp * 32u, TM_WT, w);
       ld32(tmem, (uint32_t)warp * 32u, TM_WT + 32, w + 32);
     }
-    const uint32_t wrow = OFF_Q + (tid < 64 ? 0u : 8 * KB);
     if (p.w_qdq) {
       if (warp < 4) {
         float m = 0.f;
@@ -558,41 +563,25 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           float cd[8], dq[8];
 #pragma unroll
           for (int u = 0; u < 8; u += 2) qdq_pair(w[8 * q + u], w[8 * q + u + 1], rW, sW, cd[u], cd[u + 1], dq[u], dq[u + 1]);
-          st16(sm, wrow + tc::sw128(tid & 63, 16 * q), pack8(cd));
+          stg16(p.wt, item * 128 + tid, q, pack8(cd));
         }
       }
-    } else if (warp < 4) {   // hi -> the Q slots, lo -> the K slots
+    } else if (warp < 4) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         uint4 h16, l16;
         split8(w + 8 * q, h16, l16);
-        st16(sm, wrow + tc::sw128(tid & 63, 16 * q), h16);
-        st16(sm, wrow + 16 * KB + tc::sw128(tid & 63, 16 * q), l16);
+        stg16(p.wt, item * 256 + tid, q, h16);
+        stg16(p.wt, item * 256 + 128 + tid, q, l16);
       }
     }
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      if (p.w_qdq) {
-        tc::tma_store_2d(&twt, sbase + OFF_Q, 0, (int)(item * 128));
-        tc::tma_store_2d(&twt, sbase + OFF_Q + 8 * KB, 0, (int)(item * 128 + 64));
-      } else {
-        tc::tma_store_2d(&twt, sbase + OFF_Q, 0, (int)(item * 256));
-        tc::tma_store_2d(&twt, sbase + OFF_Q + 8 * KB, 0, (int)(item * 256 + 64));
-        tc::tma_store_2d(&twt, sbase + OFF_K, 0, (int)(item * 256 + 128));
-        tc::tma_store_2d(&twt, sbase + OFF_K + 8 * KB, 0, (int)(item * 256 + 192));
-      }
-      tc::bulk_commit();
-      p.vec[item * 256 + 192] = sW;
-    }
+    if (tid == 0) p.vec[item * 256 + 192] = sW;
   } while (0);
 
   if (!ok && tid == 0) {
     atomicExch(p.status, 1);
     if (!k_done) tc::mbar_wait(bar_k, 0, 1u << 16);   // the Q/K tiles may still be landing
   }
-  if (tid == 0) tc::bulk_wait_read();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -604,19 +593,15 @@ cudaError_t launch_kda_prep(const ChunkProblem& p, const KdaLayout& lay, unsigne
   if (lay.items == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)p.B * p.T;
   const int64_t tmap = tokens > 0 ? tokens : 1;
-  CUtensorMap tq, tk, twt, ttt, tpp, tqd, tkd;
-  if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap) ||
-      !make_bf16_rows_map(&twt, ws + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 64) ||
-      !make_bf16_rows_map(&ttt, ws + lay.off_tt, lay.items * 128, 128) ||
-      !make_bf16_rows_map(&tpp, ws + lay.off_p, lay.items * 128, 128) ||
-      !make_bf16_rows_map(&tqd, ws + lay.off_qd, lay.items * 256, 128) ||
-      !make_bf16_rows_map(&tkd, ws + lay.off_kd, lay.items * 256, 128))
+  CUtensorMap tq, tk;
+  if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap))
     return cudaErrorInvalidValue;
-  KdaPrepParams pp{p.g, p.beta, p.cu, reinterpret_cast<float*>(ws + lay.off_vec), reinterpret_cast<int*>(ws),
+  KdaPrepParams pp{p.g, p.beta, p.cu, reinterpret_cast<float*>(ws + lay.off_vec), ws + lay.off_wt, ws + lay.off_tt,
+                   ws + lay.off_p, ws + lay.off_qd, ws + lay.off_kd, reinterpret_cast<int*>(ws),
                    p.T, p.N, p.Hqk, p.Hv, p.w_qdq};
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_prep_kda_kernel<<<(unsigned)lay.items, kThreads, kSmemBytes, stream>>>(tq, tk, twt, ttt, tpp, tqd, tkd, pp);
+  chunk_prep_kda_kernel<<<(unsigned)lay.items, kThreads, kSmemBytes, stream>>>(tq, tk, pp);
   return cudaGetLastError();
 }
 

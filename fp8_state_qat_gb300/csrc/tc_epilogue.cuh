@@ -51,6 +51,12 @@ __device__ __forceinline__ void st32(uint32_t tmem, uint32_t lane0, uint32_t col
   tc::tmem_st16(tc::tmem_addr(tmem, lane0, col), v);
   tc::tmem_st16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);
 }
+// max |v| over the 32 lanes of a warp (redux.sync, sm_100 family); NaN inputs do not win, as with fmaxf
+__device__ __forceinline__ float warp_absmax(float v) {
+  float r;
+  asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 // descriptor for `addr` advanced by `off` bytes (the start field is the low 14 bits, in 16-byte units)
 __device__ __forceinline__ uint64_t dadv(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
 
