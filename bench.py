@@ -57,10 +57,15 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# the sources that build the benchmark step's two kernels (and the host code that launches them)
+PREFILL_SOURCES = ("chunk_prep.cu", "chunk_chain.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh", "tc_common.cuh",
+                   "tc_epilogue.cuh", "kernels.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_state_qat_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(PREFILL_SOURCES):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
