@@ -31,7 +31,6 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "gdn_b4_h16_t4096_d128"
 METRIC = "GDN chunked-prefill tokens/s (B4 H16 T4096 d128, FP8 state QDQ); % of roofline"
 UNIT = "tokens/s"
-PROFILE = os.path.join(ROOT, "profiles", "chunk_fwd_gdn_b4_h16_t4096_d128.md")
 
 
 def algorithmic(x):
@@ -60,27 +59,36 @@ def peaks():
 # the sources that build the benchmark step's two kernels (and the host code that launches them)
 PREFILL_SOURCES = ("chunk_prep.cu", "chunk_chain.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh", "tc_common.cuh",
                    "tc_epilogue.cuh", "kernels.h")
+# per workload: its ncu summary and the sources of the kernels a step launches
+PROFILES = {
+    "gdn_b4_h16_t4096_d128": ("chunk_fwd_gdn_b4_h16_t4096_d128.md", PREFILL_SOURCES),
+    "gdn_decode_n512_h32_d128_s64": ("decode_gdn_decode_n512_h32_d128_s64.md",
+                                     ("decode.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
+}
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=PREFILL_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_state_qat_gb300", "csrc")
-    for name in sorted(PREFILL_SOURCES):
+    for name in sorted(sources):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    kernel sources (else None)."""
+def profiled_traffic(workload=WORKLOAD):
+    """DRAM bytes per launch from the workload's committed ncu summary, if it was taken on the
+    current sources of its kernels (else None)."""
+    if workload not in PROFILES:
+        return None
+    name, sources = PROFILES[workload]
     try:
-        text = open(PROFILE).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    if not m or not h or h.group(1) != kernel_source_hash(sources):
         return None
     return float(m.group(1))
 
@@ -454,7 +462,7 @@ def run_gpu(args):
                 "dtype": "f32", "data": "synthetic", "config": cfg,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                              "frac": achieved / hbm,
-                             "traffic": profiled_traffic() if args.workload == WORKLOAD and not args.batch else None,
+                             "traffic": profiled_traffic(args.workload) if not args.batch else None,
                              "peak_source": src, "scope": case.scope(), "bytes_per_launch": case.bytes,
                              "flops_per_launch": case.flops,
                              "tensor_frac": case.flops / (launch_ms * 1e-3) / (bf16 * 1e12), "kernel_ms": launch_ms},
