@@ -64,6 +64,7 @@ PROFILES = {
     "gdn_b4_h16_t4096_d128": ("chunk_fwd_gdn_b4_h16_t4096_d128.md", PREFILL_SOURCES),
     "gdn_decode_n512_h32_d128_s64": ("decode_gdn_decode_n512_h32_d128_s64.md",
                                      ("decode.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
+    "qdq_state_n512_h32_d128": ("tile_qdq_qdq_state_n512_h32_d128.md", ("qdq.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
 }
 
 
@@ -365,11 +366,57 @@ class DecodeCase:
                 "state_qdq": d.state_qdq, "kda": d.kda, "state": "N(0,0.05), updated in place across steps"}
 
 
+class QdqCase:
+    """One step = one fp8_tile_qdq call over the whole tensor (out of place: x read, y and the
+    tile scales written); two resident input sets alternate."""
+
+    def __init__(self, d, dev, torch, gdn):
+        self.d, self.dev, self.torch, self.gdn = d, dev, torch, gdn
+        lead, rows, cols = d.x.shape
+        ntiles = (cols + d.tile_cols - 1) // d.tile_cols
+        self.tokens = lead * rows * cols                      # elements
+        self.bytes = 8 * self.tokens + 4 * lead * ntiles
+        self.flops = 0
+        self.unit = "elements/s"
+        self.xs = [d.x.to(dev), d.x.to(dev).neg_()]
+        self.y = torch.empty_like(self.xs[0])
+        self.launches = 1
+
+    def workspace_bytes(self):
+        return 0
+
+    def scope(self):
+        return "one step = one kernel launch"
+
+    def _call(self, x, stream):
+        self.gdn.fp8_tile_qdq(x, self.d.tile_cols, y=self.y, stream=stream)
+
+    def step(self, i, ws, stream):
+        self._call(self.xs[i & 1], stream)
+
+    def host(self):
+        self.h_in = self.d.x.pin_memory()
+        self.h_out = self.torch.empty(self.y.shape, dtype=self.torch.float32).pin_memory()
+        return self.h_in.numel() * 4, self.h_out.numel() * 4
+
+    def e2e_step(self, ws, stream):
+        self.xs[0].copy_(self.h_in, non_blocking=True)
+        self._call(self.xs[0], stream)
+        self.h_out.copy_(self.y, non_blocking=True)
+
+    def config(self):
+        d = self.d
+        lead, rows, cols = d.x.shape
+        return {"workload": d.name, "lead": lead, "rows": rows, "cols": cols, "tile_cols": d.tile_cols,
+                "x": "N(0,0.05) fp32, out of place"}
+
+
 METRICS = {
     "gdn_b4_h16_t4096_d128": METRIC,
     "gdn_varlen8_hqk16_hv32_d128": "GDN varlen chunked-prefill tokens/s (8 seqs U[1,8192], GQA 16/32, d128, FP8 state QDQ)",
     "kda_b2_h32_t8192_d128": "KDA chunked-prefill tokens/s (B2 H32 T8192 d128, FP8 state + W QDQ)",
     "gdn_decode_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token FP8 state QDQ)",
+    "qdq_state_n512_h32_d128": "standalone FP8 tile QDQ elements/s (16384 x [128 x 128] fp32, 64-column tiles)",
     "gdn_b1_h2_t256_d64": "GDN chunked-prefill tokens/s (B1 H2 T256 d64, FP8 state QDQ)",
 }
 
@@ -392,7 +439,12 @@ def run_gpu(args):
         x = workloads.PrefillInputs(x.q[:args.batch], x.k[:args.batch], x.v[:args.batch], x.g[:args.batch],
                                     x.beta[:args.batch], None if x.h0 is None else x.h0[:args.batch], None,
                                     kda=x.kda, state_qdq=x.state_qdq, w_qdq=x.w_qdq, name=x.name)
-    case = (DecodeCase if isinstance(x, workloads.DecodeInputs) else PrefillCase)(x, dev, torch, gdn)
+    if isinstance(x, workloads.DecodeInputs):
+        case = DecodeCase(x, dev, torch, gdn)
+    elif isinstance(x, workloads.QdqInputs):
+        case = QdqCase(x, dev, torch, gdn)
+    else:
+        case = PrefillCase(x, dev, torch, gdn)
     ws = torch.empty(max(case.workspace_bytes(), 1 << 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -456,8 +508,9 @@ def run_gpu(args):
         cfg = case.config()
         cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
         cfg["l2"] = "inputs larger than L2 (129 MB); prefill alternates two resident input sets"
+        unit = getattr(case, "unit", UNIT)
         line = {"metric": METRICS.get(args.workload, args.workload), "value": world * case.tokens * args.steps / (ms * 1e-3),
-                "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic", "config": cfg,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -466,7 +519,7 @@ def run_gpu(args):
                              "peak_source": src, "scope": case.scope(), "bytes_per_launch": case.bytes,
                              "flops_per_launch": case.flops,
                              "tensor_frac": case.flops / (launch_ms * 1e-3) / (bf16 * 1e12), "kernel_ms": launch_ms},
-                "e2e": {"value": world * case.tokens * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+                "e2e": {"value": world * case.tokens * e2e_steps / (e2e_ms * 1e-3), "unit": unit,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": args.steps * case.launches,
                 "clocks": clocks.summary()}

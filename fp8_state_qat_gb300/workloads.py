@@ -47,6 +47,13 @@ class PrefillInputs:
 
 
 @dataclass
+class QdqInputs:
+    x: torch.Tensor      # [lead, rows, cols] fp32
+    tile_cols: int
+    name: str = ""
+
+
+@dataclass
 class DecodeInputs:
     q: torch.Tensor      # [steps, N, Hqk, dk] bf16
     k: torch.Tensor      # [steps, N, Hqk, dk] bf16
@@ -113,7 +120,13 @@ def decode(steps, N, H, dk, dv, *, seed, kda=False, state_std=0.05, state_qdq=Tr
                         state_qdq=state_qdq, name=name)
 
 
-# --- the five named workloads -------------------------------------------------------
+def qdq(lead, rows, cols, tile_cols, *, seed, std=0.05, name="") -> QdqInputs:
+    """Standalone tile QDQ input: a state-shaped fp32 tensor."""
+    gen = torch.Generator().manual_seed(seed)
+    return QdqInputs(_normal(gen, (lead, rows, cols), std=std), tile_cols, name=name)
+
+
+# --- the named workloads --------------------------------------------------------------
 
 WORKLOADS = {
     # small parity case: 4 chunks of 64, state QDQ on, W QDQ off, h0 = 0
@@ -129,6 +142,8 @@ WORKLOADS = {
     # decode: 512 sequences x 32 heads, 64 single-token steps, QDQ on every write
     "gdn_decode_n512_h32_d128_s64": lambda: decode(64, 512, 32, 128, 128, seed=3, state_std=0.05,
                                                    name="gdn_decode_n512_h32_d128_s64"),
+    # standalone tile QDQ over a decode-sized state tensor: 16384 x [128 x 128], 64-column tiles
+    "qdq_state_n512_h32_d128": lambda: qdq(512 * 32, 128, 128, 64, seed=5, name="qdq_state_n512_h32_d128"),
     # KDA: per-key-channel decay, state + W QDQ, h0 = 0
     "kda_b2_h32_t8192_d128": lambda: prefill(2, 8192, 32, 32, 128, 128, seed=4, kda=True, state_qdq=True,
                                              w_qdq=True, name="kda_b2_h32_t8192_d128"),
