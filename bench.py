@@ -298,17 +298,21 @@ class PrefillCase:
             inp["h0"] = x.h0
         self.h_in = {k: t.pin_memory() for k, t in inp.items()}
         b = self.sets[0]
-        self.h_out = {k: self.torch.empty(b[k].shape, dtype=self.torch.float32).pin_memory() for k in ("o", "hT")}
+        self.h_out = [{k: self.torch.empty(b[k].shape, dtype=self.torch.float32).pin_memory() for k in ("o", "hT")}
+                      for _ in range(2)]
         return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
-                sum(t.numel() * 4 for t in self.h_out.values()))
+                sum(t.numel() * 4 for t in self.h_out[0].values()))
 
-    def e2e_step(self, ws, stream):
-        b = self.sets[0]
+    def h2d(self, slot):   # on the current stream
         for k, t in self.h_in.items():
-            b[k].copy_(t, non_blocking=True)
-        self.step(0, ws, stream)
-        for k, t in self.h_out.items():
-            t.copy_(b[k], non_blocking=True)
+            self.sets[slot][k].copy_(t, non_blocking=True)
+
+    def run(self, slot, ws, stream):
+        self.step(slot, ws, stream)
+
+    def d2h(self, slot):
+        for k, t in self.h_out[slot].items():
+            t.copy_(self.sets[slot][k], non_blocking=True)
 
     def config(self):
         s, x = self.s, self.x
@@ -351,14 +355,21 @@ class DecodeCase:
 
     def host(self):
         self.h_in = {k: getattr(self.d, k)[0].pin_memory() for k in ("q", "k", "v", "g", "beta")}
-        self.h_out = self.torch.empty(self.o.shape, dtype=self.torch.float32).pin_memory()
-        return sum(t.numel() * t.element_size() for t in self.h_in.values()), self.h_out.numel() * 4
+        self.h_out = [self.torch.empty(self.o.shape, dtype=self.torch.float32).pin_memory() for _ in range(2)]
+        self.o_slots = [self.o, self.torch.empty_like(self.o)]
+        return sum(t.numel() * t.element_size() for t in self.h_in.values()), self.h_out[0].numel() * 4
 
-    def e2e_step(self, ws, stream):
+    def h2d(self, slot):   # token inputs into the first two resident token sets
         for k, t in self.h_in.items():
-            self.tok[0][k].copy_(t, non_blocking=True)
-        self.step(0, ws, stream)
-        self.h_out.copy_(self.o, non_blocking=True)
+            self.tok[slot][k].copy_(t, non_blocking=True)
+
+    def run(self, slot, ws, stream):
+        t = self.tok[slot]
+        self.gdn.gdn_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], self.state, state_qdq=self.d.state_qdq,
+                                 kda=self.d.kda, o=self.o_slots[slot], stream=stream)
+
+    def d2h(self, slot):
+        self.h_out[slot].copy_(self.o_slots[slot], non_blocking=True)
 
     def config(self):
         d = self.d
@@ -396,13 +407,18 @@ class QdqCase:
 
     def host(self):
         self.h_in = self.d.x.pin_memory()
-        self.h_out = self.torch.empty(self.y.shape, dtype=self.torch.float32).pin_memory()
-        return self.h_in.numel() * 4, self.h_out.numel() * 4
+        self.h_out = [self.torch.empty(self.y.shape, dtype=self.torch.float32).pin_memory() for _ in range(2)]
+        self.y_slots = [self.y, self.torch.empty_like(self.y)]
+        return self.h_in.numel() * 4, self.h_out[0].numel() * 4
 
-    def e2e_step(self, ws, stream):
-        self.xs[0].copy_(self.h_in, non_blocking=True)
-        self._call(self.xs[0], stream)
-        self.h_out.copy_(self.y, non_blocking=True)
+    def h2d(self, slot):
+        self.xs[slot].copy_(self.h_in, non_blocking=True)
+
+    def run(self, slot, ws, stream):
+        self.gdn.fp8_tile_qdq(self.xs[slot], self.d.tile_cols, y=self.y_slots[slot], stream=stream)
+
+    def d2h(self, slot):
+        self.h_out[slot].copy_(self.y_slots[slot], non_blocking=True)
 
     def config(self):
         d = self.d
@@ -482,19 +498,46 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # end to end through the public API: pinned host inputs -> device, call, outputs -> host
+    # end to end through the public API: every step copies its inputs from pinned host memory,
+    # calls the library and copies its result back to pinned host memory. Copies in, calls and
+    # copies out run on three streams with two buffer slots, so step i's call overlaps step i+1's
+    # input copy and step i-1's output copy (the order a serving or training loop uses).
     h2d, d2h = case.host()
     e2e_steps = max(1, min(args.steps, 50))
-    for _ in range(2):
-        case.e2e_step(ws, stream)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_run = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_pipeline(steps):
+        for i in range(steps):
+            slot = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_run[slot])        # step i-2's call has read this slot's inputs
+                case.h2d(slot)
+                ev_in[slot].record(s_in)
+            stream.wait_event(ev_in[slot])
+            if i >= 2:
+                stream.wait_event(ev_out[slot])          # step i-2's outputs have left this slot
+            case.run(slot, ws, stream)
+            ev_run[slot].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[slot])
+                case.d2h(slot)
+                ev_out[slot].record(s_out)
+
+    e2e_pipeline(2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        case.e2e_step(ws, stream)
-    e1.record(stream)
+    e0.record(s_in)
+    stream.wait_event(e0)
+    s_out.wait_event(e0)
+    e2e_pipeline(e2e_steps)
+    s_out.wait_event(ev_run[(e2e_steps - 1) & 1])
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
