@@ -22,6 +22,9 @@
 // chain: "U consumed", "Delta stored", "S0 of the next chunk stored"). Every wait is bounded; a
 // warp whose wait gives up raises a CTA-wide abort flag, both warpgroups leave their loops at
 // their next checked barrier, TMA in flight is waited for (bounded), TMEM is freed.
+#include <algorithm>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -71,6 +74,7 @@ constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true)
 enum : int { B_QK0 = 0, B_QK1, B_TV, B_WC, B_U, B_GP, B_X, B_Y, B_C, B_PD, B_SRDY, B_DRDY, B_UFREE, kNumBars };
 
 struct ChainParams {
+  const int32_t* order;   // chain order of the sequences, or null (natural order)
   const float* vec;
   const float* h0;
   const int32_t* cu;
@@ -115,7 +119,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const int nslab = p.dv / 64;
   const int slab = blockIdx.x % nslab;
   const int h = (blockIdx.x / nslab) % p.Hv;
-  const int n = blockIdx.x / (nslab * p.Hv);
+  const int n = p.order ? p.order[blockIdx.x / (nslab * p.Hv)] : (int)(blockIdx.x / (nslab * p.Hv));
   const int hq = h / (p.Hv / p.Hqk);
   int64_t t0, len;
   if (p.cu) {
@@ -560,8 +564,22 @@ SplitLayout chunk_split_layout(const ChunkProblem& p) {
   l.off_wt = up(kStatusBytes);
   l.off_tt = up(l.off_wt + (size_t)l.items * l.wt_item_bytes);
   l.off_vec = up(l.off_tt + (size_t)l.items * 16 * KB);
-  l.total = l.off_vec + (size_t)l.items * 1024;
+  l.off_order = up(l.off_vec + (size_t)l.items * 1024);
+  l.total = l.off_order + (size_t)p.N * 4;
   return l;
+}
+
+const int32_t* stage_chain_order(const ChunkProblem& p, unsigned char* ws, size_t off_order, cudaStream_t stream,
+                                 cudaError_t* err) {
+  *err = cudaSuccess;
+  if (!p.cu || !p.cu_host || p.N < 2) return nullptr;
+  std::vector<int32_t> order(p.N);
+  for (int n = 0; n < p.N; ++n) order[n] = n;
+  const int32_t* c = p.cu_host;
+  std::stable_sort(order.begin(), order.end(), [c](int32_t a, int32_t b) { return c[a + 1] - c[a] > c[b + 1] - c[b]; });
+  // pageable source: the copy is staged before the call returns, so the vector may go
+  *err = cudaMemcpyAsync(ws + off_order, order.data(), (size_t)p.N * 4, cudaMemcpyHostToDevice, stream);
+  return *err == cudaSuccess ? reinterpret_cast<const int32_t*>(ws + off_order) : nullptr;
 }
 
 cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t stream) {
@@ -580,7 +598,9 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
       !make_bf16_rows_map(&twt, w + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 128) ||
       !make_bf16_rows_map(&ttt, w + lay.off_tt, lay.items * 128, 128))
     return cudaErrorInvalidValue;
-  ChainParams cp{reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT, reinterpret_cast<int*>(ws),
+  const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
+  if (e != cudaSuccess) return e;
+  ChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT, reinterpret_cast<int*>(ws),
                  p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -63,6 +63,7 @@ enum : int {
 };
 
 struct KdaChainParams {
+  const int32_t* order;   // chain order of the sequences, or null (natural order)
   const float* vec;
   const float* h0;
   const int32_t* cu;
@@ -107,7 +108,7 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
   const int nslab = p.dv / 64;
   const int slab = blockIdx.x % nslab;
   const int h = (blockIdx.x / nslab) % p.Hv;
-  const int n = blockIdx.x / (nslab * p.Hv);
+  const int n = p.order ? p.order[blockIdx.x / (nslab * p.Hv)] : (int)(blockIdx.x / (nslab * p.Hv));
   int64_t t0, len;
   if (p.cu) {
     t0 = p.cu[n];
@@ -544,7 +545,8 @@ KdaLayout kda_split_layout(const ChunkProblem& p) {
   l.off_qd = up(l.off_p + (size_t)l.items * 16 * KB);
   l.off_kd = up(l.off_qd + (size_t)l.items * 32 * KB);
   l.off_vec = up(l.off_kd + (size_t)l.items * 32 * KB);
-  l.total = l.off_vec + (size_t)l.items * 1024;
+  l.off_order = up(l.off_vec + (size_t)l.items * 1024);
+  l.total = l.off_order + (size_t)p.N * 4;
   return l;
 }
 
@@ -565,7 +567,9 @@ cudaError_t launch_kda_split(const ChunkProblem& p, void* ws, cudaStream_t strea
       !make_bf16_rows_map(&tqd, w + lay.off_qd, lay.items * 256, 128) ||
       !make_bf16_rows_map(&tkd, w + lay.off_kd, lay.items * 256, 128))
     return cudaErrorInvalidValue;
-  KdaChainParams cp{reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT,
+  const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
+  if (e != cudaSuccess) return e;
+  KdaChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT,
                     reinterpret_cast<int*>(ws), p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   e = cudaFuncSetAttribute(chunk_chain_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;

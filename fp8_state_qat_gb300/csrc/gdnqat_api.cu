@@ -101,6 +101,7 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
   ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
                  (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
+  p.cu_host = a->cu_seqlens ? a->cu_seqlens_host : nullptr;
   // dk = 128: the two-kernel path (parallel prep, then the state chain) when the workspace
   // holds its staging, else (GDN) the single fused kernel; other shapes and KDA with a small
   // workspace: CUDA cores

@@ -20,6 +20,7 @@ struct ChunkProblem {
   int B, T, N, Hqk, Hv, dk, dv;
   float scale;
   int state_qdq, w_qdq, kda;
+  const int32_t* cu_host = nullptr;   // host copy of cu_seqlens (when known): orders the chain CTAs
 };
 
 cudaError_t launch_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int rows, int cols,
@@ -52,6 +53,7 @@ struct SplitLayout {
   int64_t slots, items;
   size_t wt_item_bytes;            // 16 KB with W QDQ, 32 KB without
   size_t off_wt, off_tt, off_vec;  // byte offsets inside the workspace
+  size_t off_order;                // N int32: sequences by decreasing length (varlen chain order)
   size_t total;                    // workspace bytes, status word included
 };
 constexpr size_t kStatusBytes = 256;   // the device status word, padded to one line
@@ -59,6 +61,12 @@ bool chunk_split_supported(const ChunkProblem& p);
 SplitLayout chunk_split_layout(const ChunkProblem& p);
 // ws: the workspace (status word at offset 0), ws_bytes >= chunk_split_layout(p).total.
 cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t stream);
+// Chain CTAs of the longest sequences first: with more (sequence, head, slab) chains than SMs the
+// makespan is then close to total work / SMs. Writes the order into ws + off_order (N int32,
+// staged from host memory) and returns its device address, or null for one sequence, dense
+// batches (equal lengths) or no host copy of cu_seqlens.
+const int32_t* stage_chain_order(const ChunkProblem& p, unsigned char* ws, size_t off_order, cudaStream_t stream,
+                                 cudaError_t* err);
 
 // ---- the same split for KDA (per-key-channel decay), dk = 128 ----
 // Per item the KDA prep kernel stores W^T, T'' as for GDN, plus
@@ -69,7 +77,7 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
 struct KdaLayout {
   int64_t slots, items;
   size_t wt_item_bytes;
-  size_t off_wt, off_tt, off_p, off_qd, off_kd, off_vec;
+  size_t off_wt, off_tt, off_p, off_qd, off_kd, off_vec, off_order;
   size_t total;
 };
 bool kda_split_supported(const ChunkProblem& p);
