@@ -50,11 +50,11 @@ constexpr uint32_t OFF_A = 66 * KB;              // A fp32 [64][A_LD]
 constexpr uint32_t OFF_T = 83 * KB;              // P fp32 [64][A_LD] (CUDA-core form, before the solve), then T
 constexpr uint32_t OFF_SCR = 100 * KB;           // 64 KB: decayed rows (CUDA-core form); solve scratch
 constexpr uint32_t OFF_TT = 164 * KB;            // T'' hi | lo [64 r][64 i] K-major
-constexpr uint32_t OFF_VEC = 196 * KB;           // beta [64], partial maxima [8], then [128] each: m, e^m, e^(gam_63 - m)
+constexpr uint32_t OFF_VEC = 196 * KB;           // beta [64], partial maxima [8], then [128] each: m, e^m, e^(gam_63 - m); beta of the next item at 512
 // tensor-core A / P operands (bf16 hi, lo): [K o e^(gam - m) ; Q o e^(gam - m)] (128 rows, k blocks 16 KB
 // apart), K o e^(m - gam) (64 rows, k blocks 8 KB apart); they overlay the scratch and T'' regions
 constexpr uint32_t OFF_LQ = OFF_SCR, OFF_LQ_LO = OFF_SCR + 32 * KB, OFF_KR = OFF_SCR + 64 * KB, OFF_KR_LO = OFF_KR + 16 * KB;
-constexpr uint32_t kSmemBytes = OFF_VEC + 2 * KB + 1024;   // + slack to align the base
+constexpr uint32_t kSmemBytes = OFF_VEC + 3 * KB + 1024;   // + slack to align the base
 static_assert(OFF_G + 64 * GLD * 4 <= OFF_A && OFF_A + 64 * A_LD * 4 <= OFF_T && OFF_T + 64 * A_LD * 4 <= OFF_SCR,
               "regions overlap");
 static_assert((16 + 16 + 64) * GLD * 4 <= 64 * KB, "decayed-row scratch exceeds its region");
@@ -77,9 +77,25 @@ struct KdaPrepParams {
   unsigned char* qd;   // per item 256 rows: Qd hi [c < 64: 64 r | c >= 64: 64 r], lo (same)
   unsigned char* kd;   // per item 256 rows: Kd, same layout
   int* status;
+  int64_t items;
   int T, N, Hqk, Hv;
   int w_qdq;
 };
+
+// cp.async of `bytes` (4 or 16) with zero fill: src_bytes = 0 reads nothing and writes zeros
+__device__ __forceinline__ void cp_async_zfill16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_zfill4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
 
 // 8 consecutive floats from shared memory (16-byte aligned)
 __device__ __forceinline__ void ld8(const float* src, float* f) {
@@ -119,23 +135,6 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ uint32_t tmem_slot;
 
-  const int64_t item = blockIdx.x;
-  const int h = (int)(item % p.Hv);
-  const int64_t slot = item / p.Hv;
-  int lo = 0, hi = p.N - 1;   // the sequence owning this slot: the last n with floor(cu[n] / 64) + n <= slot
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (seq_start(p, mid) / 64 + mid <= slot) lo = mid;
-    else hi = mid - 1;
-  }
-  const int n = lo;
-  const int64_t t0 = seq_start(p, n), len = seq_start(p, n + 1) - t0;
-  const int64_t c = slot - (t0 / 64 + n);
-  if (c < 0 || c * 64 >= len) return;   // no chunk uses this slot (uniform across the CTA)
-  const int L = (int)(len - c * 64 < 64 ? len - c * 64 : 64);
-  const int hq = h / (p.Hv / p.Hqk);
-  const int tok = (int)(t0 + c * 64);
-
   const uint32_t raw = tc::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   unsigned char* sm = smem_raw + (sbase - raw);
@@ -146,44 +145,89 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   float* const Am = reinterpret_cast<float*>(sm + OFF_A);
   float* const Tm = reinterpret_cast<float*>(sm + OFF_T);
   float* const scr = reinterpret_cast<float*>(sm + OFF_SCR);
-  float* const vbeta = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* const red = vbeta + 64;
-  float* const gmid = vbeta + 128;
-  float* const gem = vbeta + 256;
-  float* const ge63m = vbeta + 384;
+  float* const vec_s = reinterpret_cast<float*>(sm + OFF_VEC);
+  float* const red = vec_s + 64;
+  float* const gmid = vec_s + 128;
+  float* const gem = vec_s + 256;
+  float* const ge63m = vec_s + 384;
   const uint32_t bar_k = tc::smem_u32(&bars[0]), bar_w = tc::smem_u32(&bars[1]);
+
+  // Persistent: this CTA takes items blockIdx.x, + gridDim.x, ... that own a chunk. While one
+  // item is processed, the next one's g and beta (cp.async, zero past the sequence end) and, once
+  // the W product has read the K o exp(gam) tiles, its Q / K tiles (TMA) are already loading.
+  struct Item { int64_t item; int h, hq, L, tok; };
+  auto decode = [&](int64_t it, Item& f) -> bool {
+    f.item = it;
+    f.h = (int)(it % p.Hv);
+    const int64_t slot = it / p.Hv;
+    int lo = 0, hi = p.N - 1;   // the sequence owning this slot: the last n with floor(cu[n] / 64) + n <= slot
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (seq_start(p, mid) / 64 + mid <= slot) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t t0 = seq_start(p, lo), len = seq_start(p, lo + 1) - t0;
+    const int64_t c = slot - (t0 / 64 + lo);
+    if (c < 0 || c * 64 >= len) return false;   // no chunk uses this slot
+    f.L = (int)(len - c * 64 < 64 ? len - c * 64 : 64);
+    f.hq = f.h / (p.Hv / p.Hqk);
+    f.tok = (int)(t0 + c * 64);
+    return true;
+  };
+  auto next_item = [&](int64_t from, Item& f) -> bool {
+    for (int64_t it = from; it < p.items; it += gridDim.x)
+      if (decode(it, f)) return true;
+    return false;
+  };
+  auto issue_qk = [&](const Item& f) {   // thread 0
+    tc::mbar_expect_tx(bar_k, 32 * KB);
+    tc::tma_load_3d(sbase + OFF_Q, &tq, bar_k, 0, f.hq, f.tok);
+    tc::tma_load_3d(sbase + OFF_Q + 8 * KB, &tq, bar_k, 64, f.hq, f.tok);
+    tc::tma_load_3d(sbase + OFF_K, &tk, bar_k, 0, f.hq, f.tok);
+    tc::tma_load_3d(sbase + OFF_K + 8 * KB, &tk, bar_k, 64, f.hq, f.tok);
+  };
+  auto issue_g = [&](const Item& f, float* beta_dst) {   // all threads: g rows (zero past L) and beta
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = tid + j * kThreads, r = e >> 5, c4 = (e & 31) * 4;
+      const bool in = r < f.L;
+      const float* src = in ? p.g + ((int64_t)(f.tok + r) * p.Hv + f.h) * 128 + c4 : p.g;
+      cp_async_zfill16(gam + r * GLD + c4, src, in ? 16u : 0u);
+    }
+    if (tid < 64) {
+      const bool in = tid < f.L;
+      cp_async_zfill4(beta_dst + tid, in ? p.beta + (int64_t)(f.tok + tid) * p.Hv + f.h : p.beta, in ? 4u : 0u);
+    }
+  };
 
   if (tid == 0) {
     tc::mbar_init(bar_k, 1);
     tc::mbar_init(bar_w, 1);
     tc::mbar_fence_init();
-    tc::mbar_expect_tx(bar_k, 32 * KB);
-    tc::tma_load_3d(sbase + OFF_Q, &tq, bar_k, 0, hq, tok);
-    tc::tma_load_3d(sbase + OFF_Q + 8 * KB, &tq, bar_k, 64, hq, tok);
-    tc::tma_load_3d(sbase + OFF_K, &tk, bar_k, 0, hq, tok);
-    tc::tma_load_3d(sbase + OFF_K + 8 * KB, &tk, bar_k, 64, hq, tok);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
-  {   // g of the chunk (rows beyond L are zero; all loads in flight before the first store), beta
-    float4 gv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = tid + j * kThreads, r = e >> 5, c4 = (e & 31) * 4;
-      gv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < L) gv[j] = __ldcs(reinterpret_cast<const float4*>(p.g + ((int64_t)(tok + r) * p.Hv + h) * 128 + c4));
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = tid + j * kThreads, r = e >> 5, c4 = (e & 31) * 4;
-      *reinterpret_cast<float4*>(gam + r * GLD + c4) = gv[j];
-    }
-  }
-  if (tid < 64) vbeta[tid] = tid < L ? p.beta[(int64_t)(tok + tid) * p.Hv + h] : 0.f;
-  for (int e = tid; e < 2 * 64 * A_LD; e += kThreads) (e < 64 * A_LD ? Am : Tm)[e % (64 * A_LD)] = 0.f;
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
+
+  Item cur;
+  bool have = next_item(blockIdx.x, cur);
+  if (have) {
+    if (tid == 0) issue_qk(cur);
+    issue_g(cur, vec_s + 512);
+  }
+  bool ok = true, k_pending = have;
+  uint32_t k_phase = 0, w_phase = 0;   // completions of bar_k / bar_w waited for so far
+  int vb = 1;                          // beta of the current item: vec_s + 512 vb
+  while (have && ok) {
+  const int64_t item = cur.item;
+  float* const vbeta = vb ? vec_s + 512 : vec_s;
+  Item nxt;
+  const bool more = next_item(item + gridDim.x, nxt);
+  cp_async_commit_wait_all();   // this item's g and beta (issued during the previous item)
+  for (int e = tid; e < 2 * 64 * A_LD; e += kThreads) (e < 64 * A_LD ? Am : Tm)[e % (64 * A_LD)] = 0.f;
+  __syncthreads();
   // prefix sums per key channel, in token order; exp(gam_63) for the chain; the range of each
   // channel's gam over the chunk: its midpoint is the anchor, its width picks the A / P form
   bool steep = false;
@@ -204,7 +248,6 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     steep = !(mx - mn <= kChunkSpan);
   }
   const bool tc_ap = !__syncthreads_or(steep);   // uniform across the CTA
-  uint32_t w_phase = 0;                           // bar_w completions waited for so far
 
   // Qd, Kd (hi | lo) -> global; K o exp(gam) (hi | lo) -> smem over the Q / K tiles (each thread
   // overwrites only the tile bytes it has read); with the anchor, also the A / P operands
@@ -269,18 +312,19 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     }
   };
 
-  bool ok = true, k_done = false;
   float sW = 1.f;
   do {
-    if (warp == 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_k, 0));
-    if (__syncthreads_or(!ok)) break;
-    k_done = true;
+    if (warp == 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_k, k_phase & 1));
+    if (__syncthreads_or(!ok)) { ok = false; break; }
+    k_pending = false;
+    ++k_phase;
 
     if (tc_ap) {
       // ---- A and P on tcgen05 ----
       produce(true);
       tc::fence_proxy_async_smem();
       __syncthreads();
+      if (more) issue_g(nxt, vb ? vec_s : vec_s + 512);   // gam and the other beta buffer are free now
       if (tid == 0) {
         tc::tc_fence_after();
         const uint64_t dA = tc::make_sdesc(sbase + OFF_LQ, 16, 1024);
@@ -296,7 +340,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_w, w_phase & 1));
       ++w_phase;
-      if (__syncthreads_or(!ok)) break;
+      if (__syncthreads_or(!ok)) { ok = false; break; }
       tc::tc_fence_after();
       if (warp < 4) {   // TMEM lane = tid: rows 0-63 give A, rows 64-127 give P
         float d[64];
@@ -439,6 +483,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       produce(false);   // the Q / K tiles have been read by A and P
       tc::fence_proxy_async_smem();
       __syncthreads();
+      if (more) issue_g(nxt, vb ? vec_s : vec_s + 512);
     }
 
     // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then the blocks below
@@ -536,8 +581,12 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     }
     ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_w, w_phase & 1));
     ++w_phase;
-    if (__syncthreads_or(!ok)) break;
+    if (__syncthreads_or(!ok)) { ok = false; break; }
     tc::tc_fence_after();
+    if (more) {   // the K o exp(gam) tiles are read: the next item's Q / K can land there
+      if (tid == 0) issue_qk(nxt);
+      k_pending = true;
+    }
 
     // ---- W QDQ: warps 0-3, thread = key channel c (TMEM lane), its 64 values W[r][c] = row c of W^T ----
     float w[64];
@@ -577,11 +626,20 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     }
     if (tid == 0) p.vec[item * 256 + 192] = sW;
   } while (0);
+  if (!ok) break;
+  tc::tc_fence_before();
+  __syncthreads();   // the next item rewrites smem this one still reads
+  tc::tc_fence_after();
+  cur = nxt;
+  have = more;
+  vb ^= 1;
+  }
 
   if (!ok && tid == 0) {
     atomicExch(p.status, 1);
-    if (!k_done) tc::mbar_wait(bar_k, 0, 1u << 16);   // the Q/K tiles may still be landing
+    if (k_pending) tc::mbar_wait(bar_k, k_phase & 1, 1u << 16);   // Q / K tiles may still be landing
   }
+  cp_async_commit_wait_all();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -597,11 +655,17 @@ cudaError_t launch_kda_prep(const ChunkProblem& p, const KdaLayout& lay, unsigne
   if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap))
     return cudaErrorInvalidValue;
   KdaPrepParams pp{p.g, p.beta, p.cu, reinterpret_cast<float*>(ws + lay.off_vec), ws + lay.off_wt, ws + lay.off_tt,
-                   ws + lay.off_p, ws + lay.off_qd, ws + lay.off_kd, reinterpret_cast<int*>(ws),
+                   ws + lay.off_p, ws + lay.off_qd, ws + lay.off_kd, reinterpret_cast<int*>(ws), lay.items,
                    p.T, p.N, p.Hqk, p.Hv, p.w_qdq};
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_prep_kda_kernel<<<(unsigned)lay.items, kThreads, kSmemBytes, stream>>>(tq, tk, pp);
+  int sms = 0, dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = lay.items < sms ? lay.items : sms;   // one resident CTA per SM, each walking items
+  chunk_prep_kda_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(tq, tk, pp);
   return cudaGetLastError();
 }
 
