@@ -65,6 +65,10 @@ PROFILES = {
     "gdn_decode_n512_h32_d128_s64": ("decode_gdn_decode_n512_h32_d128_s64.md",
                                      ("decode.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
     "qdq_state_n512_h32_d128": ("tile_qdq_qdq_state_n512_h32_d128.md", ("qdq.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
+    "gdn_varlen8_hqk16_hv32_d128": ("chunk_fwd_gdn_varlen8_hqk16_hv32_d128.md", PREFILL_SOURCES),
+    "kda_b2_h32_t8192_d128": ("chunk_fwd_kda_b2_h32_t8192_d128.md",
+                              ("chunk_prep_kda.cu", "chunk_chain_kda.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh",
+                               "tc_common.cuh", "tc_epilogue.cuh", "kernels.h")),
 }
 
 
