@@ -65,6 +65,8 @@ def _load():
             lib.oracle_gdn_chunked.argtypes = [P] * 7 + [I] * 11 + [D, P, I, P, P]
             lib.oracle_gdn_decode.restype = I
             lib.oracle_gdn_decode.argtypes = [P] * 5 + [I] * 8 + [D, P, I, P, P]
+            lib.oracle_gdn_prefill_decode.restype = I
+            lib.oracle_gdn_prefill_decode.argtypes = [P] * 8 + [I] * 10 + [D, P, I, P, P]
             _lib = lib
     return _lib
 
@@ -200,3 +202,21 @@ def gdn_decode(q, k, v, g, beta, state, *, kda=False, state_qdq=True, scale=1.0,
     if rc:
         raise ValueError("oracle_gdn_decode: bad arguments")
     return o, st
+
+
+def gdn_prefill_decode(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, kda=False,
+                       state_qdq=False, w_qdq=False, scale=1.0, unit_mask=None, threads=None):
+    """Prefill -> decode handoff: per sequence the first prefill_lengths[n] tokens chunked with no
+    state QDQ, QDQ at the handoff when tokens remain, then one decode step (with state QDQ) per
+    remaining token. Returns (o, hT) fp64."""
+    q, k, v, g, beta, h0, cu, B, T, N, Hqk, Hv, dk, dv = _prefill_args(q, k, v, g, beta, h0, cu_seqlens, kda)
+    pl = np.ascontiguousarray(np.asarray(prefill_lengths, dtype=np.int32).reshape(N))
+    o = np.zeros((B, T, Hv, dv), np.float64)
+    hT = np.zeros((N, Hv, dk, dv), np.float64)
+    m = _mask(unit_mask, N, Hv)
+    rc = _load().oracle_gdn_prefill_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu),
+                                           _ptr(pl), B, T, N, Hqk, Hv, dk, dv, int(kda), int(state_qdq), int(w_qdq),
+                                           float(scale), _ptr(m), _threads(threads), _ptr(o), _ptr(hT))
+    if rc:
+        raise ValueError("oracle_gdn_prefill_decode: bad arguments")
+    return o, hT

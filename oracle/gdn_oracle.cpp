@@ -20,6 +20,12 @@
 //        exponentials come from prefix differences of the log decay.
 //   [R]  "Add experimental GDN/KDA decode and replay QAT" (#2509), section "What does
 //        this PR do?": per-token FP8 state writes in decode.
+//   [H]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519), section
+//        "Megatron-Core QAT/QAD workflow", steps 2-3 and the "Ordinary state-QDQ path"
+//        flowchart: a sequence's first prefill_lengths tokens run as chunked prefill that
+//        produces a state without internal state QDQ; for a nonempty suffix QDQ is applied
+//        at the handoff, then each suffix token (teacher forced, the sequence's own tokens)
+//        is a decode step that QDQs the state before storing it.
 // The pages name GatedDeltaNet but never print its recurrence. The oracle uses the
 // standard gated delta rule for a state S in R^{dk x dv}:
 //     S_t = a_t S_{t-1} + b_t k_t (v_t - a_t S_{t-1}^T k_t)^T,   o_t = S_t^T q_t,
@@ -32,6 +38,8 @@
 //   oracle_gdn_recurrent     O1: token-by-token recurrence (the definition)
 //   oracle_gdn_chunked       O2: chunked / WY form (the only form in which W QDQ exists)
 //   oracle_gdn_decode        single-token decode steps with per-token state QDQ
+//   oracle_gdn_prefill_decode  [H]: chunked prefix (no state QDQ), QDQ at the handoff,
+//                            recurrent suffix with per-token state QDQ
 // Every function is pinned by tests/test_oracle_*.py against closed forms, invariants,
 // hand-worked examples and brute force.
 
@@ -132,43 +140,50 @@ void load_h0(const Problem& p, int n, int h, double* S) {
   }
 }
 
+// One token of the recurrence for head h at packed token index tok, on the state S
+// (steps 1-5; the caller decides on the QDQ of step 6).
+void recurrent_step(const Problem& p, int64_t tok, int h, double* S, double* o) {
+  const int dk = p.dk, dv = p.dv, hq = h / (p.Hv / p.Hqk);
+  std::vector<double> d(dv), kv(dk), qv(dk);
+  for (int c = 0; c < dk; ++c) {
+    kv[c] = (double)p.k[(tok * p.Hqk + hq) * dk + c];
+    qv[c] = (double)p.q[(tok * p.Hqk + hq) * dk + c];
+  }
+  const double b = (double)p.beta[tok * p.Hv + h];
+  // 1. S' = alpha S (KDA: row c scaled by alpha[c])
+  for (int c = 0; c < dk; ++c) {
+    const double a = std::exp(logdecay(p, tok, h, c));
+    for (int j = 0; j < dv; ++j) S[(size_t)c * dv + j] *= a;
+  }
+  // 2. p = S'^T k ; 3. delta = beta (v - p)
+  for (int j = 0; j < dv; ++j) {
+    double acc = 0.0;
+    for (int c = 0; c < dk; ++c) acc += S[(size_t)c * dv + j] * kv[c];
+    d[j] = b * ((double)p.v[(tok * p.Hv + h) * dv + j] - acc);
+  }
+  // 4. S = S' + k delta^T
+  for (int c = 0; c < dk; ++c)
+    for (int j = 0; j < dv; ++j) S[(size_t)c * dv + j] += kv[c] * d[j];
+  // 5. o = scale * S^T q  (from the updated, not yet quantized state)
+  if (o) {
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int c = 0; c < dk; ++c) acc += S[(size_t)c * dv + j] * qv[c];
+      o[(tok * p.Hv + h) * dv + j] = p.scale * acc;
+    }
+  }
+}
+
 // O1: the recurrence itself, one token at a time. QDQ of S after every token whose
 // sequence-local count is a multiple of qdq_period (64 for prefill per [F]).
 void recurrent_unit(const Problem& p, int n, int h, int state_qdq, int qdq_period,
                     double* o, double* hT) {
-  const int dk = p.dk, dv = p.dv, hq = h / (p.Hv / p.Hqk);
+  const int dk = p.dk, dv = p.dv;
   const UnitRange u = unit_range(p, n);
-  std::vector<double> S((size_t)dk * dv), d(dv), kv(dk), qv(dk);
+  std::vector<double> S((size_t)dk * dv);
   load_h0(p, n, h, S.data());
   for (int64_t t = 0; t < u.len; ++t) {
-    const int64_t tok = u.t0 + t;
-    for (int c = 0; c < dk; ++c) {
-      kv[c] = (double)p.k[(tok * p.Hqk + hq) * dk + c];
-      qv[c] = (double)p.q[(tok * p.Hqk + hq) * dk + c];
-    }
-    const double b = (double)p.beta[tok * p.Hv + h];
-    // 1. S' = alpha S (KDA: row c scaled by alpha[c])
-    for (int c = 0; c < dk; ++c) {
-      const double a = std::exp(logdecay(p, tok, h, c));
-      for (int j = 0; j < dv; ++j) S[(size_t)c * dv + j] *= a;
-    }
-    // 2. p = S'^T k ; 3. delta = beta (v - p)
-    for (int j = 0; j < dv; ++j) {
-      double acc = 0.0;
-      for (int c = 0; c < dk; ++c) acc += S[(size_t)c * dv + j] * kv[c];
-      d[j] = b * ((double)p.v[(tok * p.Hv + h) * dv + j] - acc);
-    }
-    // 4. S = S' + k delta^T
-    for (int c = 0; c < dk; ++c)
-      for (int j = 0; j < dv; ++j) S[(size_t)c * dv + j] += kv[c] * d[j];
-    // 5. o = scale * S^T q  (from the updated, not yet quantized state)
-    if (o) {
-      for (int j = 0; j < dv; ++j) {
-        double acc = 0.0;
-        for (int c = 0; c < dk; ++c) acc += S[(size_t)c * dv + j] * qv[c];
-        o[(tok * p.Hv + h) * dv + j] = p.scale * acc;
-      }
-    }
+    recurrent_step(p, u.t0 + t, h, S.data(), o);
     // 6. state QDQ at the boundary
     if (state_qdq && ((t + 1) % qdq_period) == 0) qdq_state(S.data(), dk, dv);
   }
@@ -190,15 +205,15 @@ void recurrent_unit(const Problem& p, int n, int h, int state_qdq, int qdq_perio
 // Unrolling the recurrence over a chunk gives S_r = Gam_r S0 + sum_{i<=r} (Gam_r/Gam_i)
 // k_i d_i^T; putting that into d_r = b_r (v_r - a_r S_{r-1}^T k_r) gives
 // (I + A) Delta = beta V - (beta Gam K) S0, i.e. Delta = U - W S0.
-void chunked_unit(const Problem& p, int n, int h, int C, int state_qdq, int w_qdq,
-                  double* o, double* hT) {
+// Runs the chunks of tokens [u.t0, u.t0 + u.len) of head h on the state S (in / out); chunk
+// and boundary positions count from u.t0, the sequence's first token.
+void chunked_range(const Problem& p, UnitRange u, int h, int C, int state_qdq, int w_qdq,
+                   double* o, std::vector<double>& S) {
   const int dk = p.dk, dv = p.dv, hq = h / (p.Hv / p.Hqk);
-  const UnitRange u = unit_range(p, n);
-  std::vector<double> S((size_t)dk * dv), S1((size_t)dk * dv);
+  std::vector<double> S1((size_t)dk * dv);
   std::vector<double> K((size_t)C * dk), Q((size_t)C * dk), V((size_t)C * dv), bt(C);
   std::vector<double> gam((size_t)C * dk), A((size_t)C * C), Tm((size_t)C * C);
   std::vector<double> X((size_t)C * dk), W((size_t)C * dk), U((size_t)C * dv), Dl((size_t)C * dv);
-  load_h0(p, n, h, S.data());
   for (int64_t c0 = 0; c0 < u.len; c0 += C) {
     const int L = (int)std::min<int64_t>(C, u.len - c0);
     for (int r = 0; r < L; ++r) {
@@ -287,7 +302,33 @@ void chunked_unit(const Problem& p, int n, int h, int C, int state_qdq, int w_qd
     S.swap(S1);
     if (state_qdq && ((c0 + L) % 64) == 0) qdq_state(S.data(), dk, dv);
   }
-  if (hT) std::copy(S.begin(), S.end(), hT + ((int64_t)n * p.Hv + h) * (int64_t)dk * dv);
+}
+
+void chunked_unit(const Problem& p, int n, int h, int C, int state_qdq, int w_qdq,
+                  double* o, double* hT) {
+  std::vector<double> S((size_t)p.dk * p.dv);
+  load_h0(p, n, h, S.data());
+  chunked_range(p, unit_range(p, n), h, C, state_qdq, w_qdq, o, S);
+  if (hT) std::copy(S.begin(), S.end(), hT + ((int64_t)n * p.Hv + h) * (int64_t)p.dk * p.dv);
+}
+
+// [H] for one (sequence, head): the first P tokens as chunked prefill (chunk 64) with no
+// state QDQ (W QDQ as asked), then -- if tokens remain -- QDQ of the handed-off state and
+// the remaining tokens one by one, each followed by a state QDQ (state_qdq on).
+void prefill_decode_unit(const Problem& p, int n, int h, int64_t P, int state_qdq, int w_qdq,
+                         double* o, double* hT) {
+  const UnitRange u = unit_range(p, n);
+  std::vector<double> S((size_t)p.dk * p.dv);
+  load_h0(p, n, h, S.data());
+  chunked_range(p, UnitRange{u.t0, P}, h, 64, 0, w_qdq, o, S);
+  if (P < u.len) {
+    if (state_qdq) qdq_state(S.data(), p.dk, p.dv);
+    for (int64_t t = P; t < u.len; ++t) {
+      recurrent_step(p, u.t0 + t, h, S.data(), o);
+      if (state_qdq) qdq_state(S.data(), p.dk, p.dv);
+    }
+  }
+  if (hT) std::copy(S.begin(), S.end(), hT + ((int64_t)n * p.Hv + h) * (int64_t)p.dk * p.dv);
 }
 
 // Run fn(n, h) for every selected (n, h) unit on `threads` std::threads.
@@ -384,6 +425,22 @@ int oracle_gdn_chunked(const float* q, const float* k, const float* v, const flo
   if (check_problem(p) || chunk <= 0) return 1;
   for_units(N, Hv, unit_mask, threads, [&](int n, int h) {
     chunked_unit(p, n, h, chunk, state_qdq, w_qdq, o, hT);
+  });
+  return 0;
+}
+
+// [H]. Same arguments as O2 (chunk fixed at 64) plus prefill_lengths [N]: 0 <= P_n <= L_n.
+int oracle_gdn_prefill_decode(const float* q, const float* k, const float* v, const float* g,
+                              const float* beta, const double* h0, const int32_t* cu_seqlens,
+                              const int32_t* prefill_lengths, int B, int T, int N, int Hqk, int Hv,
+                              int dk, int dv, int kda, int state_qdq, int w_qdq, double scale,
+                              const uint8_t* unit_mask, int threads, double* o, double* hT) {
+  Problem p{q, k, v, g, beta, h0, cu_seqlens, B, T, N, Hqk, Hv, dk, dv, kda, scale};
+  if (check_problem(p) || !prefill_lengths) return 1;
+  for (int n = 0; n < N; ++n)
+    if (prefill_lengths[n] < 0 || prefill_lengths[n] > unit_range(p, n).len) return 1;
+  for_units(N, Hv, unit_mask, threads, [&](int n, int h) {
+    prefill_decode_unit(p, n, h, prefill_lengths[n], state_qdq, w_qdq, o, hT);
   });
   return 0;
 }
