@@ -15,9 +15,12 @@ from .gdnqat import (  # noqa: F401
     gdn_check_device_status,
     gdn_chunk_fwd,
     gdn_decode_step,
+    gdn_prefill_decode_fwd,
     kda_chunk_fwd,
+    kda_prefill_decode_fwd,
     lib_path,
     load,
+    prefill_decode_workspace_bytes,
     status_string,
     workspace_bytes,
 )

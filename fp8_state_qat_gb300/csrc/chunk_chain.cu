@@ -78,6 +78,7 @@ struct ChainParams {
   const float* vec;
   const float* h0;
   const int32_t* cu;
+  const int32_t* lens;    // tokens run per sequence, or null (whole sequences)
   float* o;
   float* hT;
   int* status;
@@ -129,6 +130,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     t0 = (int64_t)n * p.T;
     len = p.T;
   }
+  if (p.lens) len = p.lens[n];
   const int64_t nchunks = (len + 63) / 64;
   const int64_t slot0 = t0 / 64 + n;   // workspace slot of chunk 0
   auto item = [&](int64_t cj) { return (slot0 + cj) * p.Hv + h; };
@@ -572,11 +574,14 @@ SplitLayout chunk_split_layout(const ChunkProblem& p) {
 const int32_t* stage_chain_order(const ChunkProblem& p, unsigned char* ws, size_t off_order, cudaStream_t stream,
                                  cudaError_t* err) {
   *err = cudaSuccess;
-  if (!p.cu || !p.cu_host || p.N < 2) return nullptr;
-  std::vector<int32_t> order(p.N);
-  for (int n = 0; n < p.N; ++n) order[n] = n;
-  const int32_t* c = p.cu_host;
-  std::stable_sort(order.begin(), order.end(), [c](int32_t a, int32_t b) { return c[a + 1] - c[a] > c[b + 1] - c[b]; });
+  if (p.N < 2 || !(p.lens ? p.lens_host != nullptr : (p.cu && p.cu_host))) return nullptr;
+  std::vector<int32_t> order(p.N), len(p.N);
+  for (int n = 0; n < p.N; ++n) {
+    order[n] = n;
+    len[n] = p.lens ? p.lens_host[n] : p.cu_host[n + 1] - p.cu_host[n];
+  }
+  const int32_t* l = len.data();
+  std::stable_sort(order.begin(), order.end(), [l](int32_t a, int32_t b) { return l[a] > l[b]; });
   // pageable source: the copy is staged before the call returns, so the vector may go
   *err = cudaMemcpyAsync(ws + off_order, order.data(), (size_t)p.N * 4, cudaMemcpyHostToDevice, stream);
   return *err == cudaSuccess ? reinterpret_cast<const int32_t*>(ws + off_order) : nullptr;
@@ -600,7 +605,7 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
     return cudaErrorInvalidValue;
   const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
   if (e != cudaSuccess) return e;
-  ChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT, reinterpret_cast<int*>(ws),
+  ChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.lens, p.o, p.hT, reinterpret_cast<int*>(ws),
                  p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -67,6 +67,7 @@ struct KdaChainParams {
   const float* vec;
   const float* h0;
   const int32_t* cu;
+  const int32_t* lens;    // tokens run per sequence, or null (whole sequences)
   float* o;
   float* hT;
   int* status;
@@ -117,6 +118,7 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
     t0 = (int64_t)n * p.T;
     len = p.T;
   }
+  if (p.lens) len = p.lens[n];
   const int64_t nchunks = (len + 63) / 64;
   const int64_t slot0 = t0 / 64 + n;
   auto item = [&](int64_t cj) { return (slot0 + cj) * p.Hv + h; };
@@ -569,7 +571,7 @@ cudaError_t launch_kda_split(const ChunkProblem& p, void* ws, cudaStream_t strea
     return cudaErrorInvalidValue;
   const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
   if (e != cudaSuccess) return e;
-  KdaChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.o, p.hT,
+  KdaChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.lens, p.o, p.hT,
                     reinterpret_cast<int*>(ws), p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   e = cudaFuncSetAttribute(chunk_chain_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;

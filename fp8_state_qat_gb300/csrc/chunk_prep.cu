@@ -50,6 +50,7 @@ struct PrepParams {
   const float* g;
   const float* beta;
   const int32_t* cu;
+  const int32_t* lens;   // tokens run per sequence, or null (whole sequences)
   float* vec;
   int* status;
   int T, N, Hqk, Hv;
@@ -78,7 +79,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     else hi = mid - 1;
   }
   const int n = lo;
-  const int64_t t0 = seq_start(p, n), len = seq_start(p, n + 1) - t0;
+  const int64_t t0 = seq_start(p, n), len = p.lens ? (int64_t)p.lens[n] : seq_start(p, n + 1) - t0;
   const int64_t c = slot - (t0 / 64 + n);
   if (c < 0 || c * 64 >= len) return;   // no chunk uses this slot (uniform across the CTA)
   const int L = (int)(len - c * 64 < 64 ? len - c * 64 : 64);
@@ -370,7 +371,7 @@ cudaError_t launch_chunk_prep(const ChunkProblem& p, const SplitLayout& lay, uns
       !make_bf16_rows_map(&twt, ws + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 128) ||
       !make_bf16_rows_map(&ttt, ws + lay.off_tt, lay.items * 128, 128))
     return cudaErrorInvalidValue;
-  PrepParams pp{p.g, p.beta, p.cu, reinterpret_cast<float*>(ws + lay.off_vec), reinterpret_cast<int*>(ws),
+  PrepParams pp{p.g, p.beta, p.cu, p.lens, reinterpret_cast<float*>(ws + lay.off_vec), reinterpret_cast<int*>(ws),
                 p.T, p.N, p.Hqk, p.Hv, p.w_qdq};
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -70,6 +70,7 @@ struct KdaPrepParams {
   const float* g;      // [tokens, Hv, 128]
   const float* beta;   // [tokens, Hv]
   const int32_t* cu;
+  const int32_t* lens; // tokens run per sequence, or null (whole sequences)
   float* vec;          // per item: exp(gam_63) [128], W scale at 192
   unsigned char* wt;   // per item 128 (W QDQ) or 256 rows of 128 bytes: W^T codes, or hi then lo
   unsigned char* tt;   // per item 128 rows: T'' hi [64 r], lo [64 r]
@@ -166,7 +167,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       if (seq_start(p, mid) / 64 + mid <= slot) lo = mid;
       else hi = mid - 1;
     }
-    const int64_t t0 = seq_start(p, lo), len = seq_start(p, lo + 1) - t0;
+    const int64_t t0 = seq_start(p, lo), len = p.lens ? (int64_t)p.lens[lo] : seq_start(p, lo + 1) - t0;
     const int64_t c = slot - (t0 / 64 + lo);
     if (c < 0 || c * 64 >= len) return false;   // no chunk uses this slot
     f.L = (int)(len - c * 64 < 64 ? len - c * 64 : 64);
@@ -654,7 +655,7 @@ cudaError_t launch_kda_prep(const ChunkProblem& p, const KdaLayout& lay, unsigne
   CUtensorMap tq, tk;
   if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap))
     return cudaErrorInvalidValue;
-  KdaPrepParams pp{p.g, p.beta, p.cu, reinterpret_cast<float*>(ws + lay.off_vec), ws + lay.off_wt, ws + lay.off_tt,
+  KdaPrepParams pp{p.g, p.beta, p.cu, p.lens, reinterpret_cast<float*>(ws + lay.off_vec), ws + lay.off_wt, ws + lay.off_tt,
                    ws + lay.off_p, ws + lay.off_qd, ws + lay.off_kd, reinterpret_cast<int*>(ws), lay.items,
                    p.T, p.N, p.Hqk, p.Hv, p.w_qdq};
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
     t0 = (int64_t)n * p.T;
     len = p.T;
   }
+  if (p.lens) len = p.lens[n];
   const __nv_bfloat16* qg = (const __nv_bfloat16*)p.q;
   const __nv_bfloat16* kg = (const __nv_bfloat16*)p.k;
   const __nv_bfloat16* vg = (const __nv_bfloat16*)p.v;

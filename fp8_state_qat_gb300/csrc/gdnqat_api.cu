@@ -117,9 +117,87 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// The prefill part of a prefill -> decode handoff runs the two-kernel tensor-core paths (or CUDA
+// cores for the shapes they do not take); the device copy of the prefill lengths follows the
+// chunk workspace.
+size_t handoff_chunk_bytes(const ChunkProblem& p) {
+  if (gdn::kda_split_supported(p)) return gdn::kda_split_layout(p).total;
+  if (gdn::chunk_split_supported(p)) return gdn::chunk_split_layout(p).total;
+  return kWorkspaceBytes;
+}
+size_t handoff_lens_offset(const ChunkProblem& p) { return (handoff_chunk_bytes(p) + 255) & ~(size_t)255; }
+size_t handoff_bytes(const ChunkProblem& p) { return handoff_lens_offset(p) + (size_t)p.N * 4; }
+
+ChunkProblem problem_of(const gdn_chunk_args* a, bool kda) {
+  ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
+                 a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
+                 (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
+  p.cu_host = a->cu_seqlens ? a->cu_seqlens_host : nullptr;
+  return p;
+}
+
+gdn_status prefill_decode(const gdn_chunk_args* a, const int32_t* plens, void* ws, size_t ws_bytes,
+                          cudaStream_t stream, bool kda) {
+  gdn_status s = validate_chunk(a, kda);
+  if (s != GDN_OK) return s;
+  if (!a->hT) return GDN_ERR_INVALID_ARG;   // the handed-off state lives in hT
+  if (a->N > 0 && !plens) return GDN_ERR_INVALID_ARG;
+  for (int n = 0; n < a->N; ++n) {
+    const int64_t L = a->cu_seqlens ? (int64_t)a->cu_seqlens_host[n + 1] - a->cu_seqlens_host[n] : (int64_t)a->T;
+    if (plens[n] < 0 || plens[n] > L) return GDN_ERR_INVALID_ARG;
+  }
+  ChunkProblem p = problem_of(a, kda);
+  if (!ws || ws_bytes < handoff_bytes(p)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return GDN_ERR_INVALID_ARG;
+  s = check_device();
+  if (s != GDN_OK) return s;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return GDN_ERR_CUDA;
+  if ((int64_t)a->N * a->Hv == 0) return GDN_OK;
+  int32_t* lens = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + handoff_lens_offset(p));
+  // pageable source: the copy is staged before the call returns
+  if (cudaMemcpyAsync(lens, plens, (size_t)p.N * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  // the prefix: chunked, W QDQ as asked, no state QDQ
+  const int state_qdq = p.state_qdq;
+  p.state_qdq = 0;
+  p.lens = lens;
+  p.lens_host = plens;
+  cudaError_t e;
+  if (gdn::kda_split_supported(p))
+    e = gdn::launch_kda_split(p, ws, stream);
+  else if (gdn::chunk_split_supported(p))
+    e = gdn::launch_chunk_split(p, ws, stream);
+  else
+    e = gdn::launch_chunk_simt(p, stream);
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
+  // the handoff and the decode tokens
+  p.state_qdq = state_qdq;
+  return gdn::launch_handoff_suffix(p, lens, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t gdn_prefill_decode_workspace_size(const gdn_chunk_args* args) {
+  if (validate_chunk(args, false) != GDN_OK) return 0;
+  return handoff_bytes(problem_of(args, false));
+}
+
+size_t kda_prefill_decode_workspace_size(const gdn_chunk_args* args) {
+  if (validate_chunk(args, true) != GDN_OK) return 0;
+  return handoff_bytes(problem_of(args, true));
+}
+
+gdn_status gdn_prefill_decode_fwd(const gdn_chunk_args* args, const int32_t* prefill_lengths_host, void* workspace,
+                                  size_t workspace_bytes, gdn_stream_t stream) {
+  return prefill_decode(args, prefill_lengths_host, workspace, workspace_bytes, (cudaStream_t)stream, false);
+}
+
+gdn_status kda_prefill_decode_fwd(const gdn_chunk_args* args, const int32_t* prefill_lengths_host, void* workspace,
+                                  size_t workspace_bytes, gdn_stream_t stream) {
+  return prefill_decode(args, prefill_lengths_host, workspace, workspace_bytes, (cudaStream_t)stream, true);
+}
 
 const char* gdn_status_string(gdn_status status) {
   switch (status) {

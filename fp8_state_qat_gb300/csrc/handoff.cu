@@ -1,0 +1,210 @@
+// handoff.cu -- the decode part of a prefill -> decode handoff.
+//
+// Schedule ("Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD
+// workflow", steps 2-3, and its "Ordinary state-QDQ path" flowchart): the first P_n tokens of
+// sequence n run as chunked prefill that leaves a state without internal state QDQ (the chunk
+// kernels, run with per-sequence lengths P_n); when tokens remain, the state is QDQ'd at the
+// handoff and every remaining token is a decode step on the sequence's own tokens (teacher
+// forced): read the state, S' = a S (KDA: row c scaled by a[c]), d = b (v - S'^T k),
+// S = S' + k d^T, o = scale S^T q from the updated state, then QDQ (all dk rows x 64 value
+// columns per tile, scale amax / 448 with a zero guard) before the state is stored for the
+// next token.
+//
+// One CTA per (sequence, head) keeps the state in registers across all of the sequence's
+// decode tokens, so HBM sees the state once in and once out plus each token's q, k, v, g, beta
+// and o. The thread layout is the decode kernel's: warp w owns value columns [16 w, 16 w + 16);
+// lane = 4 rg + cg holds rows rg, rg + 8, ... and the 4 columns 16 w + 4 cg .. + 3; both
+// dk-reductions are 3-level xor shuffles over lane bits 2..4 in a fixed order. The next
+// token's inputs are copied (cp.async) into the other of two shared-memory buffers while the
+// current token is computed; the per-tile maxima alternate between two shared-memory slots.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+// One token's inputs, staged in shared memory by cp.async one token ahead.
+template <int DK, int DV, bool KDA>
+struct __align__(16) TokenBuf {
+  __nv_bfloat16 k[DK], q[DK], v[DV];
+  float g[KDA ? DK : 1];
+  float b;
+};
+
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Issue the copies of token tok's inputs into buf (k, q, v in 16-byte pieces; g, beta in 4-byte
+// pieces, so g needs only 4-byte alignment).
+template <int DK, int DV, bool KDA>
+__device__ __forceinline__ void stage_token(TokenBuf<DK, DV, KDA>& buf, const __nv_bfloat16* __restrict__ q,
+                                            const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                                            const float* __restrict__ g, const float* __restrict__ beta, int64_t tok,
+                                            int Hqk, int Hv, int h, int hq) {
+  constexpr int NK = DK / 8, NV = DV / 8;   // 16-byte pieces of k (and q), of v
+  const int tid = threadIdx.x;
+  if (tid < NK) cp16(&buf.k[8 * tid], k + (tok * Hqk + hq) * DK + 8 * tid);
+  else if (tid < 2 * NK) cp16(&buf.q[8 * (tid - NK)], q + (tok * Hqk + hq) * DK + 8 * (tid - NK));
+  else if (tid < 2 * NK + NV) cp16(&buf.v[8 * (tid - 2 * NK)], v + (tok * Hv + h) * DV + 8 * (tid - 2 * NK));
+  if (KDA) {
+    if (tid < DK) cp4(&buf.g[tid], g + (tok * Hv + h) * DK + tid);
+  } else if (tid == 0) {
+    cp4(&buf.g[0], g + tok * Hv + h);
+  }
+  if (tid == 1) cp4(&buf.b, beta + tok * Hv + h);
+}
+
+// QDQ of the state registers: one tile = all DK rows x 64 columns = 4 consecutive warps.
+template <int DK, int DV>
+__device__ __forceinline__ void qdq_state_regs(float4 (&s)[DK / 8], float amax, float* wmax, int warp, int lane) {
+  constexpr int RPT = DK / 8;
+  amax = warp_max(amax);
+  if (lane == 0) wmax[warp] = amax;
+  __syncthreads();
+  const int t0 = (warp / 4) * 4;
+  const float tmax = fmaxf(fmaxf(wmax[t0], wmax[t0 + 1]), fmaxf(wmax[t0 + 2], wmax[t0 + 3]));
+  const float sc = qdq_scale(tmax), rc = __frcp_rn(sc);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const __nv_fp8x2_e4m3 c01(make_float2(__fmul_rn(s[i].x, rc), __fmul_rn(s[i].y, rc)));
+    const __nv_fp8x2_e4m3 c23(make_float2(__fmul_rn(s[i].z, rc), __fmul_rn(s[i].w, rc)));
+    const float2 f01 = static_cast<float2>(c01), f23 = static_cast<float2>(c23);
+    s[i] = make_float4(__fmul_rn(f01.x, sc), __fmul_rn(f01.y, sc), __fmul_rn(f23.x, sc), __fmul_rn(f23.y, sc));
+  }
+}
+
+template <int DK, int DV, bool KDA>
+__global__ void __launch_bounds__(DV * 2, (DV <= 128 ? 2 : 1))
+handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                      const __nv_bfloat16* __restrict__ v, const float* __restrict__ g,
+                      const float* __restrict__ beta, const int32_t* __restrict__ cu,
+                      const int32_t* __restrict__ plens, float* __restrict__ state, float* __restrict__ o, int T,
+                      int Hqk, int Hv, float scale, int state_qdq) {
+  constexpr int NW = DV / 16;
+  constexpr int RPT = DK / 8;
+  __shared__ float wmax[2][NW];
+  __shared__ __align__(16) TokenBuf<DK, DV, KDA> tb[2];
+  const int64_t unit = blockIdx.x;   // n * Hv + h
+  const int n = (int)(unit / Hv), h = (int)(unit % Hv);
+  const int hq = h / (Hv / Hqk);
+  const int64_t t0 = cu ? (int64_t)cu[n] : (int64_t)n * T;
+  const int64_t len = cu ? (int64_t)cu[n + 1] - t0 : (int64_t)T;
+  const int64_t P = plens[n];
+  if (P >= len) return;   // no decode tokens: the prefill state stays as it is
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = lane >> 2, cg = lane & 3;
+  const int col = warp * 16 + cg * 4;
+
+  float* S = state + unit * (int64_t)(DK * DV);
+  float4 s[RPT];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    s[i] = *reinterpret_cast<const float4*>(S + (rg + 8 * i) * DV + col);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w))));
+  }
+  stage_token<DK, DV, KDA>(tb[0], q, k, v, g, beta, t0 + P, Hqk, Hv, h, hq);
+  int slot = 0;   // the per-tile maxima alternate between two slots, one barrier per QDQ
+  if (state_qdq) {
+    qdq_state_regs<DK, DV>(s, amax, wmax[slot], warp, lane);   // the handoff
+    slot ^= 1;
+  }
+  cp_commit_wait_all();
+  __syncthreads();
+
+  for (int64_t t = P; t < len; ++t) {
+    // the other buffer held token t - 1, which every thread read before the barrier that ended
+    // token t - 1: token t + 1 goes into it now
+    if (t + 1 < len) stage_token<DK, DV, KDA>(tb[(t - P + 1) & 1], q, k, v, g, beta, t0 + t + 1, Hqk, Hv, h, hq);
+    const TokenBuf<DK, DV, KDA>& in = tb[(t - P) & 1];
+    float kr[RPT], qr[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      kr[i] = bf16_to_f32(in.k[rg + 8 * i]);
+      qr[i] = bf16_to_f32(in.q[rg + 8 * i]);
+    }
+    const float a0 = KDA ? 0.f : expf(in.g[0]);
+    const float b = in.b;
+    const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&in.v[col]);
+    const float2 v01 = __bfloat1622float2(vp[0]), v23 = __bfloat1622float2(vp[1]);
+    // S' = a S ; p = S'^T k
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float a = KDA ? expf(in.g[rg + 8 * i]) : a0;
+      s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+      p.x = fmaf(s[i].x, kr[i], p.x); p.y = fmaf(s[i].y, kr[i], p.y);
+      p.z = fmaf(s[i].z, kr[i], p.z); p.w = fmaf(s[i].w, kr[i], p.w);
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      p.x += __shfl_xor_sync(0xffffffffu, p.x, off); p.y += __shfl_xor_sync(0xffffffffu, p.y, off);
+      p.z += __shfl_xor_sync(0xffffffffu, p.z, off); p.w += __shfl_xor_sync(0xffffffffu, p.w, off);
+    }
+    const float4 d = make_float4(b * (v01.x - p.x), b * (v01.y - p.y), b * (v23.x - p.z), b * (v23.y - p.w));
+    // S = S' + k d^T ; o = S^T q
+    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
+    amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      s[i].x = fmaf(kr[i], d.x, s[i].x); s[i].y = fmaf(kr[i], d.y, s[i].y);
+      s[i].z = fmaf(kr[i], d.z, s[i].z); s[i].w = fmaf(kr[i], d.w, s[i].w);
+      ov.x = fmaf(s[i].x, qr[i], ov.x); ov.y = fmaf(s[i].y, qr[i], ov.y);
+      ov.z = fmaf(s[i].z, qr[i], ov.z); ov.w = fmaf(s[i].w, qr[i], ov.w);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w))));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      ov.x += __shfl_xor_sync(0xffffffffu, ov.x, off); ov.y += __shfl_xor_sync(0xffffffffu, ov.y, off);
+      ov.z += __shfl_xor_sync(0xffffffffu, ov.z, off); ov.w += __shfl_xor_sync(0xffffffffu, ov.w, off);
+    }
+    if (rg == 0)
+      *reinterpret_cast<float4*>(o + ((t0 + t) * Hv + h) * DV + col) =
+          make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
+    if (state_qdq) {
+      qdq_state_regs<DK, DV>(s, amax, wmax[slot], warp, lane);
+      slot ^= 1;
+    }
+    cp_commit_wait_all();
+    __syncthreads();   // token t + 1's inputs are staged, token t's are read
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(S + (rg + 8 * i) * DV + col) = s[i];
+}
+
+template <int DK, int DV, bool KDA>
+cudaError_t launch_t(const ChunkProblem& p, const int32_t* plens, cudaStream_t stream) {
+  const int64_t units = (int64_t)p.N * p.Hv;
+  if (units == 0) return cudaSuccess;
+  handoff_suffix_kernel<DK, DV, KDA><<<(unsigned)units, DV * 2, 0, stream>>>(
+      (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, (const __nv_bfloat16*)p.v, p.g, p.beta, p.cu, plens, p.hT,
+      p.o, p.T, p.Hqk, p.Hv, p.scale, p.state_qdq);
+  return cudaGetLastError();
+}
+
+template <bool KDA>
+cudaError_t dispatch(const ChunkProblem& p, const int32_t* plens, cudaStream_t s) {
+#define GDN_HO(DKV, DVV) \
+  if (p.dk == DKV && p.dv == DVV) return launch_t<DKV, DVV, KDA>(p, plens, s);
+  GDN_HO(64, 64) GDN_HO(64, 128) GDN_HO(64, 256) GDN_HO(128, 64) GDN_HO(128, 128) GDN_HO(128, 256)
+#undef GDN_HO
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_handoff_suffix(const ChunkProblem& p, const int32_t* plens, cudaStream_t stream) {
+  if (!p.hT) return cudaErrorInvalidValue;
+  return p.kda ? dispatch<true>(p, plens, stream) : dispatch<false>(p, plens, stream);
+}
+
+}  // namespace gdn

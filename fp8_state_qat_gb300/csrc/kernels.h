@@ -21,6 +21,10 @@ struct ChunkProblem {
   float scale;
   int state_qdq, w_qdq, kda;
   const int32_t* cu_host = nullptr;   // host copy of cu_seqlens (when known): orders the chain CTAs
+  // Tokens of each sequence this pass runs, from the sequence's first token (device [N] and its
+  // host copy), or null for whole sequences: the prefill part of a prefill -> decode handoff.
+  const int32_t* lens = nullptr;
+  const int32_t* lens_host = nullptr;
 };
 
 cudaError_t launch_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int rows, int cols,
@@ -64,7 +68,7 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
 // Chain CTAs of the longest sequences first: with more (sequence, head, slab) chains than SMs the
 // makespan is then close to total work / SMs. Writes the order into ws + off_order (N int32,
 // staged from host memory) and returns its device address, or null for one sequence, dense
-// batches (equal lengths) or no host copy of cu_seqlens.
+// batches of whole sequences (equal lengths) or no host copy of the lengths.
 const int32_t* stage_chain_order(const ChunkProblem& p, unsigned char* ws, size_t off_order, cudaStream_t stream,
                                  cudaError_t* err);
 
@@ -87,5 +91,12 @@ cudaError_t launch_kda_split(const ChunkProblem& p, void* ws, cudaStream_t strea
 // Per-CTA fp32 chunked forward on CUDA cores: one CTA per (sequence, head, 64-column
 // value slab). Used for shapes and variants the tensor-core path does not take.
 cudaError_t launch_chunk_simt(const ChunkProblem& p, cudaStream_t stream);
+
+// The decode part of a prefill -> decode handoff: for every (sequence, head) whose sequence has
+// tokens past its prefill length P_n, read the state from hT, QDQ it (state_qdq), then run the
+// tokens [P_n, L_n) one by one as decode steps (teacher forced: q, k, v, g, beta of those tokens;
+// o of those tokens written), each followed by a state QDQ (state_qdq), and store the state back
+// into hT. plens: device [N]; the state stays in registers across the tokens.
+cudaError_t launch_handoff_suffix(const ChunkProblem& p, const int32_t* plens, cudaStream_t stream);
 
 }  // namespace gdn

@@ -30,6 +30,8 @@ GDN_FLAG_KDA = 4
 # every extern "C" symbol of include/gdnqat.h
 EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
             "kda_chunk_fwd_workspace_size", "kda_chunk_fwd",
+            "gdn_prefill_decode_workspace_size", "gdn_prefill_decode_fwd",
+            "kda_prefill_decode_workspace_size", "kda_prefill_decode_fwd",
             "gdn_decode_step", "fp8_tile_qdq", "gdn_status_string", "gdn_check_device_status")
 
 
@@ -69,12 +71,16 @@ def load(build_if_missing: bool = True):
             _build.build()
         lib = ctypes.CDLL(_build.LIB_PATH)
         P, I32, U32, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float
-        for fn in ("gdn_chunk_fwd_workspace_size", "kda_chunk_fwd_workspace_size"):
+        for fn in ("gdn_chunk_fwd_workspace_size", "kda_chunk_fwd_workspace_size",
+                   "gdn_prefill_decode_workspace_size", "kda_prefill_decode_workspace_size"):
             getattr(lib, fn).restype = ctypes.c_size_t
             getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs)]
         for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
             getattr(lib, fn).restype = ctypes.c_int
             getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, ctypes.c_size_t, P]
+        for fn in ("gdn_prefill_decode_fwd", "kda_prefill_decode_fwd"):
+            getattr(lib, fn).restype = ctypes.c_int
+            getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, P, ctypes.c_size_t, P]
         lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.gdn_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkArgs), P]
         lib.gdn_decode_step.restype = ctypes.c_int
@@ -198,6 +204,57 @@ def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False
     """KDA chunked forward: as gdn_chunk_fwd with g [B,T,Hv,dk] (one log-decay per key channel)."""
     return _chunk("kda_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
                   output_final_state, workspace, stream)
+
+
+def prefill_decode_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False, w_qdq=False, kda=False):
+    """gdn_prefill_decode_workspace_size (kda: kda_prefill_decode_workspace_size) for these shapes."""
+    B, T, Hqk, dk = q_shape
+    Hv, dv = v_shape[2], v_shape[3]
+    cu_host, N = None, B
+    if cu_seqlens is not None:
+        cu_host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+        N = cu_host.numel() - 1
+    fake = [ctypes.c_void_p((1 << 44) + (i << 38)) for i in range(10)]
+    flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_W_QDQ if w_qdq else 0)
+    a = ChunkArgs(fake[0], fake[1], fake[2], fake[3], fake[4], None, fake[6] if cu_host is not None else None,
+                  _ptr(cu_host), fake[8], fake[9], B, T, N, Hqk, Hv, dk, dv, 1.0, flags)
+    fn = "kda_prefill_decode_workspace_size" if kda else "gdn_prefill_decode_workspace_size"
+    return int(getattr(load(), fn)(ctypes.byref(a)))
+
+
+def _prefill_decode(fn_name, q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq, w_qdq, scale, o, hT,
+                    workspace, stream):
+    lib = load()
+    a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, True)
+    pl = torch.as_tensor(prefill_lengths, dtype=torch.int32).to("cpu").contiguous().reshape(-1)
+    if pl.numel() != a.N:
+        raise ValueError(f"prefill_lengths: {pl.numel()} entries for {a.N} sequences")
+    dev = o.device
+    size_fn = "kda_prefill_decode_workspace_size" if fn_name == "kda_prefill_decode_fwd" else \
+        "gdn_prefill_decode_workspace_size"
+    need = int(getattr(lib, size_fn)(ctypes.byref(a)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = getattr(lib, fn_name)(ctypes.byref(a), _ptr(pl), _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(fn_name, st)
+    return o, hT
+
+
+def gdn_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, state_qdq=False,
+                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None):
+    """Prefill -> decode handoff: per sequence the first prefill_lengths[n] tokens chunked with no
+    state QDQ, then (state_qdq) a QDQ at the handoff and one decode step with state QDQ per
+    remaining token. Same tensors as gdn_chunk_fwd; prefill_lengths: N ints (host).
+    Returns (o, hT)."""
+    return _prefill_decode("gdn_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
+                           w_qdq, scale, o, hT, workspace, stream)
+
+
+def kda_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, state_qdq=False,
+                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None):
+    """The handoff schedule for KDA (g [B,T,Hv,dk])."""
+    return _prefill_decode("kda_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
+                           w_qdq, scale, o, hT, workspace, stream)
 
 
 def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale=1.0, o=None, stream=None):

@@ -15,6 +15,9 @@
  *      per-key-channel retention, with causal pairwise decays from prefix differences.
  *  [R] "Add experimental GDN/KDA decode and replay QAT", "What does this PR do?":
  *      per-token FP8 state writes.
+ *  [H] "Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD workflow",
+ *      steps 2-3: chunked prefix without internal state QDQ, QDQ at the handoff, then decode
+ *      tokens that QDQ the state before storing it.
  *
  * Recurrence (the pages name GatedDeltaNet but do not print it), per sequence n and
  * value head h, state S in R^{dk x dv} (row = key channel):
@@ -142,6 +145,30 @@ size_t kda_chunk_fwd_workspace_size(const gdn_chunk_args* args);
  * carry); otherwise on CUDA cores, chunk by chunk (slower, same arithmetic). */
 gdn_status kda_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
                          gdn_stream_t stream);
+
+/* Prefill -> decode handoff ([H]: "Torch GDN/KDA decode QAT with INT8 recurrent state",
+ * "Megatron-Core QAT/QAD workflow", steps 2-3 and the "Ordinary state-QDQ path" flowchart).
+ * Per sequence n of length L_n, the first P_n = prefill_lengths_host[n] tokens run as chunked
+ * prefill from h0 that produces a state WITHOUT internal state QDQ (W QDQ as GDN_FLAG_W_QDQ
+ * asks); when P_n < L_n, the state is QDQ'd at the handoff (GDN_FLAG_STATE_QDQ) and every
+ * remaining token is a decode step on the sequence's own q, k, v, g, beta (teacher forced):
+ * read the state, decay, delta update, o from the updated state, then QDQ
+ * (GDN_FLAG_STATE_QDQ) before the state is stored for the next token. o is written for every
+ * token; hT (required, device fp32 [N, Hv, dk, dv], may alias h0 exactly) receives the final
+ * state: the prefill state itself when P_n == L_n.
+ * prefill_lengths_host: HOST int32 [N], 0 <= P_n <= L_n (else GDN_ERR_INVALID_ARG), read before
+ * the call returns. Other arguments and layouts as gdn_chunk_fwd / kda_chunk_fwd. workspace:
+ * device, 256-byte aligned, at least *_prefill_decode_workspace_size(args) bytes (else
+ * GDN_ERR_WORKSPACE_TOO_SMALL): the prefill's staging plus a device copy of the prefill lengths.
+ * Launches: the prefill kernels, then one CTA per (sequence, head) that keeps the state on chip
+ * across all of the sequence's decode tokens. */
+size_t gdn_prefill_decode_workspace_size(const gdn_chunk_args* args);
+gdn_status gdn_prefill_decode_fwd(const gdn_chunk_args* args, const int32_t* prefill_lengths_host,
+                                  void* workspace, size_t workspace_bytes, gdn_stream_t stream);
+/* The same schedule for KDA (g [B, T, Hv, dk]). */
+size_t kda_prefill_decode_workspace_size(const gdn_chunk_args* args);
+gdn_status kda_prefill_decode_fwd(const gdn_chunk_args* args, const int32_t* prefill_lengths_host,
+                                  void* workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /* One decode token per sequence ([D], [R]). q, k: device bf16 [N, Hqk, dk]; v: device
  * bf16 [N, Hv, dv]; g: device fp32 [N, Hv] (GDN_FLAG_KDA: [N, Hv, dk]); beta: device fp32

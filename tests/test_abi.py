@@ -143,3 +143,45 @@ def test_valid_args_without_device_report_arch(so):
     ptrs = [P(FAKE + (i << 32)) for i in range(7)]
     assert so.gdn_decode_step(*ptrs, 4, 2, 4, 128, 128, 1.0, 1, None) == B.GDN_ERR_UNSUPPORTED_ARCH
     assert so.fp8_tile_qdq(P(FAKE), P(FAKE), None, 2, 8, 64, 64, None) == B.GDN_ERR_UNSUPPORTED_ARCH
+
+
+def call_handoff(so, args, plens, ws=FAKE + (7 << 32), ws_bytes=1 << 30, kda=False):
+    fn = so.kda_prefill_decode_fwd if kda else so.gdn_prefill_decode_fwd
+    arr = None if plens is None else (ctypes.c_int32 * len(plens))(*plens)
+    return fn(ctypes.byref(args), None if arr is None else ctypes.cast(arr, ctypes.c_void_p), ctypes.c_void_p(ws),
+              ws_bytes, None)
+
+
+def test_handoff_workspace_size(so):
+    """The prefill's workspace (the two-kernel staging for dk = 128, the minimum otherwise),
+    rounded up to 256 bytes, plus the device copy of the N prefill lengths."""
+    for kda in (False, True):
+        for over in (dict(), dict(dk=64)):
+            a = good_args(**over)
+            chunk = (so.kda_chunk_fwd_workspace_size if kda else so.gdn_chunk_fwd_workspace_size)(ctypes.byref(a))
+            size = (so.kda_prefill_decode_workspace_size if kda else so.gdn_prefill_decode_workspace_size)
+            assert size(ctypes.byref(a)) == (chunk + 255) // 256 * 256 + 4 * a.N
+    assert so.gdn_prefill_decode_workspace_size(ctypes.byref(good_args(dk=96))) == 0
+    a = good_args()
+    assert B.prefill_decode_workspace_bytes((a.B, a.T, a.Hqk, a.dk), (a.B, a.T, a.Hv, a.dv), state_qdq=True,
+                                            w_qdq=True) == so.gdn_prefill_decode_workspace_size(ctypes.byref(a))
+
+
+def test_handoff_validation(so):
+    """Prefill lengths outside [0, L_n], a missing hT or length array, and a workspace below the
+    size query are refused before any device work (the next check is the device's: none here)."""
+    for kda in (False, True):
+        a = good_args()
+        need = (so.kda_prefill_decode_workspace_size if kda else so.gdn_prefill_decode_workspace_size)(ctypes.byref(a))
+        assert call_handoff(so, a, [129, 0], kda=kda) == B.GDN_ERR_INVALID_ARG
+        assert call_handoff(so, a, [-1, 0], kda=kda) == B.GDN_ERR_INVALID_ARG
+        assert call_handoff(so, a, None, kda=kda) == B.GDN_ERR_INVALID_ARG
+        assert call_handoff(so, good_args(hT=None), [64, 64], kda=kda) == B.GDN_ERR_INVALID_ARG
+        assert call_handoff(so, a, [64, 128], ws_bytes=need - 1, kda=kda) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+        if not torch.cuda.is_available():
+            assert call_handoff(so, a, [64, 128], ws_bytes=need, kda=kda) == B.GDN_ERR_UNSUPPORTED_ARCH
+    cu = (ctypes.c_int32 * 4)(0, 50, 60, 128)
+    a = good_args(B=1, N=3, cu_seqlens=FAKE + (9 << 32), cu_seqlens_host=ctypes.addressof(cu))
+    assert call_handoff(so, a, [50, 11, 0]) == B.GDN_ERR_INVALID_ARG   # 11 > L_1 = 10
+    if not torch.cuda.is_available():
+        assert call_handoff(so, a, [50, 10, 0]) == B.GDN_ERR_UNSUPPORTED_ARCH
