@@ -42,9 +42,13 @@ def algorithmic(x):
     tok = x.tokens()
     C = 64
     by = tok * (s["Hqk"] * 2 * s["dk"] * 2 + s["Hv"] * (2 * s["dv"] + 8 + 4 * s["dv"]))
-    by += 2 * s["N"] * s["Hv"] * s["dk"] * s["dv"] * 4
+    by += (2 if x.h0 is not None else 1) * s["N"] * s["Hv"] * s["dk"] * s["dv"] * 4
     fl_th = 2 * (C * s["dk"] * 2 + C * (s["dk"] + s["dv"]) + 3 * s["dk"] * s["dv"] + C * s["dv"]) + C * C / 3
-    return by, fl_th * tok * s["Hv"]
+    if x.prefill_lengths is None:
+        return by, fl_th * tok * s["Hv"]
+    # prefill -> decode handoff: the decode tokens cost 7 dk dv each (decay, S^T k, k d^T, S^T q)
+    pre = sum(x.prefill_lengths)
+    return by, (fl_th * pre + 7 * s["dk"] * s["dv"] * (tok - pre)) * s["Hv"]
 
 
 def peaks():
@@ -66,6 +70,7 @@ PROFILES = {
                                      ("decode.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
     "qdq_state_n512_h32_d128": ("tile_qdq_qdq_state_n512_h32_d128.md", ("qdq.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
     "gdn_varlen8_hqk16_hv32_d128": ("chunk_fwd_gdn_varlen8_hqk16_hv32_d128.md", PREFILL_SOURCES),
+    "handoff_n256_t128_p64_h16_d128": ("handoff_n256_t128_p64_h16_d128.md", PREFILL_SOURCES + ("handoff.cu",)),
     "kda_b2_h32_t8192_d128": ("chunk_fwd_kda_b2_h32_t8192_d128.md",
                               ("chunk_prep_kda.cu", "chunk_chain_kda.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh",
                                "tc_common.cuh", "tc_epilogue.cuh", "kernels.h")),
@@ -266,20 +271,33 @@ class PrefillCase:
         self.bytes, self.flops = algorithmic(x)
         if x.kda:
             self.bytes += self.tokens * s["Hv"] * 4 * (s["dk"] - 1)
-        self.fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
+        self.handoff = x.prefill_lengths is not None
+        if self.handoff:
+            self.fn = gdn.kda_prefill_decode_fwd if x.kda else gdn.gdn_prefill_decode_fwd
+        else:
+            self.fn = gdn.kda_chunk_fwd if x.kda else gdn.gdn_chunk_fwd
         self.sets = [self.resident(), self.resident()]
         self.cu = x.cu_seqlens
-        # dk = 128 with the full workspace: a parallel prep kernel, then the state chain
-        self.launches = 2 if s["dk"] == 128 else 1
+        # dk = 128 with the full workspace: a parallel prep kernel, then the state chain (and for
+        # the handoff the decode-token kernel)
+        self.launches = (2 if s["dk"] == 128 else 1) + (1 if self.handoff else 0)
 
     def scope(self):
-        if self.launches == 2:
-            pre = "chunk_prep_kda_kernel + chunk_chain_kda_kernel" if self.x.kda else \
-                "chunk_prep_kernel + chunk_chain_kernel"
-            return f"one step = {pre}; achieved is over both"
-        return "one step = one kernel launch"
+        if self.launches == 1:
+            return "one step = one kernel launch"
+        kernels = ["chunk_prep_kda_kernel", "chunk_chain_kda_kernel"] if self.x.kda else \
+            ["chunk_prep_kernel", "chunk_chain_kernel"]
+        if self.s["dk"] != 128:
+            kernels = ["chunk_simt_kernel"]
+        if self.handoff:
+            kernels.append("handoff_suffix_kernel")
+        return f"one step = {' + '.join(kernels)}; achieved is over all of them"
 
     def workspace_bytes(self):
+        if self.handoff:
+            return self.gdn.prefill_decode_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu,
+                                                           state_qdq=self.x.state_qdq, w_qdq=self.x.w_qdq,
+                                                           kda=self.x.kda)
         return self.gdn.chunk_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu, state_qdq=self.x.state_qdq,
                                               w_qdq=self.x.w_qdq, kda=self.x.kda)
 
@@ -292,6 +310,10 @@ class PrefillCase:
 
     def step(self, i, ws, stream):
         b = self.sets[i & 1]
+        if self.handoff:
+            self.fn(b["q"], b["k"], b["v"], b["g"], b["beta"], b["h0"], self.cu, self.x.prefill_lengths,
+                    state_qdq=self.x.state_qdq, w_qdq=self.x.w_qdq, o=b["o"], hT=b["hT"], workspace=ws, stream=stream)
+            return
         self.fn(b["q"], b["k"], b["v"], b["g"], b["beta"], b["h0"], self.cu, state_qdq=self.x.state_qdq,
                 w_qdq=self.x.w_qdq, o=b["o"], hT=b["hT"], workspace=ws, stream=stream)
 
@@ -325,6 +347,9 @@ class PrefillCase:
              "h0": "N(0,0.1)" if x.h0 is not None else "zeros"}
         if self.cu is not None:
             c["seqlens"] = self.cu.diff().tolist()
+        if self.handoff:
+            pl = sorted(set(x.prefill_lengths))
+            c["prefill_lengths"] = pl[0] if len(pl) == 1 else x.prefill_lengths
         return c
 
 
@@ -438,6 +463,8 @@ METRICS = {
     "gdn_decode_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token FP8 state QDQ)",
     "qdq_state_n512_h32_d128": "standalone FP8 tile QDQ elements/s (16384 x [128 x 128] fp32, 64-column tiles)",
     "gdn_b1_h2_t256_d64": "GDN chunked-prefill tokens/s (B1 H2 T256 d64, FP8 state QDQ)",
+    "handoff_n256_t128_p64_h16_d128": "GDN prefill->decode handoff tokens/s (256 seqs x 128 tokens, 64-token "
+                                      "chunked prefix + 64 decode tokens, H16 d128, FP8 state + W QDQ)",
 }
 
 

@@ -12,11 +12,12 @@
 //
 // One CTA per (sequence, head) keeps the state in registers across all of the sequence's
 // decode tokens, so HBM sees the state once in and once out plus each token's q, k, v, g, beta
-// and o. The thread layout is the decode kernel's: warp w owns value columns [16 w, 16 w + 16);
-// lane = 4 rg + cg holds rows rg, rg + 8, ... and the 4 columns 16 w + 4 cg .. + 3; both
-// dk-reductions are 3-level xor shuffles over lane bits 2..4 in a fixed order. The next
-// token's inputs are copied (cp.async) into the other of two shared-memory buffers while the
-// current token is computed; the per-tile maxima alternate between two shared-memory slots.
+// and o. The thread layout and reduction order are the decode kernel's (so a decode token gives
+// the same bits here and there): warp w owns value columns [16 w, 16 w + 16); lane = 4 rg + cg
+// holds rows rg, rg + 8, ... and the 4 columns 16 w + 4 cg .. + 3; both dk-reductions are
+// 3-level xor shuffles over lane bits 2..4 in a fixed order. The inputs of
+// the next kAhead - 1 tokens are in flight (cp.async into a ring of shared-memory buffers)
+// while a token is computed; the per-tile maxima alternate between two shared-memory slots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,9 +40,13 @@ __device__ __forceinline__ void cp4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
                : "memory");
 }
-__device__ __forceinline__ void cp_commit_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Decode tokens whose inputs are in flight ahead of the one being computed: a token's
+// arithmetic is a few hundred cycles, an HBM round trip about a microsecond.
+constexpr int kAhead = 8;
 
 // Issue the copies of token tok's inputs into buf (k, q, v in 16-byte pieces; g, beta in 4-byte
 // pieces, so g needs only 4-byte alignment).
@@ -63,9 +68,13 @@ __device__ __forceinline__ void stage_token(TokenBuf<DK, DV, KDA>& buf, const __
   if (tid == 1) cp4(&buf.b, beta + tok * Hv + h);
 }
 
-// QDQ of the state registers: one tile = all DK rows x 64 columns = 4 consecutive warps.
+// QDQ of the state registers: one tile = all DK rows x 64 columns = 4 consecutive warps. The
+// state registers are column pairs (col, col + 1) and (col + 2, col + 3) so that the
+// elementwise work runs as paired fp32 operations (fma / mul .f32x2, each lane rounded like
+// its scalar form).
 template <int DK, int DV>
-__device__ __forceinline__ void qdq_state_regs(float4 (&s)[DK / 8], float amax, float* wmax, int warp, int lane) {
+__device__ __forceinline__ void qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb)[DK / 8], float amax, float* wmax,
+                                               int warp, int lane) {
   constexpr int RPT = DK / 8;
   amax = warp_max(amax);
   if (lane == 0) wmax[warp] = amax;
@@ -73,12 +82,12 @@ __device__ __forceinline__ void qdq_state_regs(float4 (&s)[DK / 8], float amax, 
   const int t0 = (warp / 4) * 4;
   const float tmax = fmaxf(fmaxf(wmax[t0], wmax[t0 + 1]), fmaxf(wmax[t0 + 2], wmax[t0 + 3]));
   const float sc = qdq_scale(tmax), rc = __frcp_rn(sc);
+  const float2 sc2 = make_float2(sc, sc), rc2 = make_float2(rc, rc);
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const __nv_fp8x2_e4m3 c01(make_float2(__fmul_rn(s[i].x, rc), __fmul_rn(s[i].y, rc)));
-    const __nv_fp8x2_e4m3 c23(make_float2(__fmul_rn(s[i].z, rc), __fmul_rn(s[i].w, rc)));
-    const float2 f01 = static_cast<float2>(c01), f23 = static_cast<float2>(c23);
-    s[i] = make_float4(__fmul_rn(f01.x, sc), __fmul_rn(f01.y, sc), __fmul_rn(f23.x, sc), __fmul_rn(f23.y, sc));
+    const __nv_fp8x2_e4m3 ca(__fmul2_rn(sa[i], rc2)), cb(__fmul2_rn(sb[i], rc2));
+    sa[i] = __fmul2_rn(static_cast<float2>(ca), sc2);
+    sb[i] = __fmul2_rn(static_cast<float2>(cb), sc2);
   }
 }
 
@@ -92,7 +101,7 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   constexpr int NW = DV / 16;
   constexpr int RPT = DK / 8;
   __shared__ float wmax[2][NW];
-  __shared__ __align__(16) TokenBuf<DK, DV, KDA> tb[2];
+  __shared__ __align__(16) TokenBuf<DK, DV, KDA> tb[kAhead];
   const int64_t unit = blockIdx.x;   // n * Hv + h
   const int n = (int)(unit / Hv), h = (int)(unit % Hv);
   const int hq = h / (Hv / Hqk);
@@ -105,27 +114,36 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const int col = warp * 16 + cg * 4;
 
   float* S = state + unit * (int64_t)(DK * DV);
-  float4 s[RPT];
+  float2 sa[RPT], sb[RPT];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    s[i] = *reinterpret_cast<const float4*>(S + (rg + 8 * i) * DV + col);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w))));
+    const float4 f = *reinterpret_cast<const float4*>(S + (rg + 8 * i) * DV + col);
+    sa[i] = make_float2(f.x, f.y);
+    sb[i] = make_float2(f.z, f.w);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
   }
-  stage_token<DK, DV, KDA>(tb[0], q, k, v, g, beta, t0 + P, Hqk, Hv, h, hq);
+  // tokens P .. P + kAhead - 2 in flight, one cp.async group each (empty groups past the end)
+#pragma unroll 1
+  for (int j = 0; j < kAhead - 1; ++j) {
+    if (P + j < len) stage_token<DK, DV, KDA>(tb[j], q, k, v, g, beta, t0 + P + j, Hqk, Hv, h, hq);
+    cp_commit();
+  }
   int slot = 0;   // the per-tile maxima alternate between two slots, one barrier per QDQ
   if (state_qdq) {
-    qdq_state_regs<DK, DV>(s, amax, wmax[slot], warp, lane);   // the handoff
+    qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);   // the handoff
     slot ^= 1;
   }
-  cp_commit_wait_all();
-  __syncthreads();
 
   for (int64_t t = P; t < len; ++t) {
-    // the other buffer held token t - 1, which every thread read before the barrier that ended
-    // token t - 1: token t + 1 goes into it now
-    if (t + 1 < len) stage_token<DK, DV, KDA>(tb[(t - P + 1) & 1], q, k, v, g, beta, t0 + t + 1, Hqk, Hv, h, hq);
-    const TokenBuf<DK, DV, KDA>& in = tb[(t - P) & 1];
+    const int i = (int)(t - P);
+    cp_wait<kAhead - 2>();   // this thread's copies of token t have landed
+    __syncthreads();         // ... and everyone's; every thread is done with token t - 1's buffer
+    // token t + kAhead - 1 goes into the buffer token t - 1 used
+    if (t + kAhead - 1 < len)
+      stage_token<DK, DV, KDA>(tb[(i + kAhead - 1) % kAhead], q, k, v, g, beta, t0 + t + kAhead - 1, Hqk, Hv, h, hq);
+    cp_commit();
+    const TokenBuf<DK, DV, KDA>& in = tb[i % kAhead];
     float kr[RPT], qr[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
@@ -137,48 +155,52 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&in.v[col]);
     const float2 v01 = __bfloat1622float2(vp[0]), v23 = __bfloat1622float2(vp[1]);
     // S' = a S ; p = S'^T k
-    float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const float a = KDA ? expf(in.g[rg + 8 * i]) : a0;
-      s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
-      p.x = fmaf(s[i].x, kr[i], p.x); p.y = fmaf(s[i].y, kr[i], p.y);
-      p.z = fmaf(s[i].z, kr[i], p.z); p.w = fmaf(s[i].w, kr[i], p.w);
+      const float2 a2 = make_float2(a, a), k2 = make_float2(kr[i], kr[i]);
+      sa[i] = __fmul2_rn(sa[i], a2);
+      sb[i] = __fmul2_rn(sb[i], a2);
+      pa = __ffma2_rn(sa[i], k2, pa);
+      pb = __ffma2_rn(sb[i], k2, pb);
     }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
-      p.x += __shfl_xor_sync(0xffffffffu, p.x, off); p.y += __shfl_xor_sync(0xffffffffu, p.y, off);
-      p.z += __shfl_xor_sync(0xffffffffu, p.z, off); p.w += __shfl_xor_sync(0xffffffffu, p.w, off);
+      pa.x += __shfl_xor_sync(0xffffffffu, pa.x, off); pa.y += __shfl_xor_sync(0xffffffffu, pa.y, off);
+      pb.x += __shfl_xor_sync(0xffffffffu, pb.x, off); pb.y += __shfl_xor_sync(0xffffffffu, pb.y, off);
     }
-    const float4 d = make_float4(b * (v01.x - p.x), b * (v01.y - p.y), b * (v23.x - p.z), b * (v23.y - p.w));
+    const float2 da = make_float2(b * (v01.x - pa.x), b * (v01.y - pa.y));
+    const float2 db = make_float2(b * (v23.x - pb.x), b * (v23.y - pb.y));
     // S = S' + k d^T ; o = S^T q
-    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 oa = make_float2(0.f, 0.f), ob = make_float2(0.f, 0.f);
     amax = 0.f;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      s[i].x = fmaf(kr[i], d.x, s[i].x); s[i].y = fmaf(kr[i], d.y, s[i].y);
-      s[i].z = fmaf(kr[i], d.z, s[i].z); s[i].w = fmaf(kr[i], d.w, s[i].w);
-      ov.x = fmaf(s[i].x, qr[i], ov.x); ov.y = fmaf(s[i].y, qr[i], ov.y);
-      ov.z = fmaf(s[i].z, qr[i], ov.z); ov.w = fmaf(s[i].w, qr[i], ov.w);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w))));
+      const float2 k2 = make_float2(kr[i], kr[i]), q2 = make_float2(qr[i], qr[i]);
+      sa[i] = __ffma2_rn(k2, da, sa[i]);
+      sb[i] = __ffma2_rn(k2, db, sb[i]);
+      oa = __ffma2_rn(sa[i], q2, oa);
+      ob = __ffma2_rn(sb[i], q2, ob);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(sa[i].x), fabsf(sa[i].y)), fmaxf(fabsf(sb[i].x), fabsf(sb[i].y))));
     }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
-      ov.x += __shfl_xor_sync(0xffffffffu, ov.x, off); ov.y += __shfl_xor_sync(0xffffffffu, ov.y, off);
-      ov.z += __shfl_xor_sync(0xffffffffu, ov.z, off); ov.w += __shfl_xor_sync(0xffffffffu, ov.w, off);
+      oa.x += __shfl_xor_sync(0xffffffffu, oa.x, off); oa.y += __shfl_xor_sync(0xffffffffu, oa.y, off);
+      ob.x += __shfl_xor_sync(0xffffffffu, ob.x, off); ob.y += __shfl_xor_sync(0xffffffffu, ob.y, off);
     }
     if (rg == 0)
       *reinterpret_cast<float4*>(o + ((t0 + t) * Hv + h) * DV + col) =
-          make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
+          make_float4(scale * oa.x, scale * oa.y, scale * ob.x, scale * ob.y);
     if (state_qdq) {
-      qdq_state_regs<DK, DV>(s, amax, wmax[slot], warp, lane);
+      qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);
       slot ^= 1;
     }
-    cp_commit_wait_all();
-    __syncthreads();   // token t + 1's inputs are staged, token t's are read
   }
+  cp_wait<0>();   // nothing may still be landing in shared memory when the CTA exits
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(S + (rg + 8 * i) * DV + col) = s[i];
+  for (int i = 0; i < RPT; ++i)
+    *reinterpret_cast<float4*>(S + (rg + 8 * i) * DV + col) = make_float4(sa[i].x, sa[i].y, sb[i].x, sb[i].y);
 }
 
 template <int DK, int DV, bool KDA>

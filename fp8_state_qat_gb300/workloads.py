@@ -35,6 +35,9 @@ class PrefillInputs:
     state_qdq: bool = True
     w_qdq: bool = False
     name: str = ""
+    # prefill -> decode handoff: per sequence, the tokens that run as chunked prefill (the rest
+    # run as decode steps); None = plain chunked prefill
+    prefill_lengths: Optional[list] = None
 
     @property
     def shape(self):
@@ -101,6 +104,14 @@ def prefill(B, T, Hqk, Hv, dk, dv, *, seed, kda=False, h0_std=None, seqlens=None
                          state_qdq=state_qdq, w_qdq=w_qdq, name=name)
 
 
+def handoff(B, T, P, Hqk, Hv, dk, dv, *, seed, kda=False, name="") -> PrefillInputs:
+    """Dense batch whose sequences run their first P tokens as chunked prefill and the rest as
+    decode steps; state and W QDQ on, h0 = 0."""
+    x = prefill(B, T, Hqk, Hv, dk, dv, seed=seed, kda=kda, h0_std=None, state_qdq=True, w_qdq=True, name=name)
+    x.prefill_lengths = [P] * B
+    return x
+
+
 def varlen_lengths(n_seqs, max_len, seed):
     """Sequence lengths ~ U[1, max_len] drawn from the workload's own seed."""
     gen = torch.Generator().manual_seed(seed)
@@ -144,6 +155,11 @@ WORKLOADS = {
                                                    name="gdn_decode_n512_h32_d128_s64"),
     # standalone tile QDQ over a decode-sized state tensor: 16384 x [128 x 128], 64-column tiles
     "qdq_state_n512_h32_d128": lambda: qdq(512 * 32, 128, 128, 64, seed=5, name="qdq_state_n512_h32_d128"),
+    # prefill -> decode handoff, the QAT/QAD workflow's example shape (128-token sequences, the
+    # first 64 tokens as chunked prefill, the last 64 as decode steps) over 256 sequences x 16
+    # heads; state + W QDQ, h0 = 0 (a training sequence starts from an empty state)
+    "handoff_n256_t128_p64_h16_d128": lambda: handoff(256, 128, 64, 16, 16, 128, 128, seed=6,
+                                                      name="handoff_n256_t128_p64_h16_d128"),
     # KDA: per-key-channel decay, state + W QDQ, h0 = 0
     "kda_b2_h32_t8192_d128": lambda: prefill(2, 8192, 32, 32, 128, 128, seed=4, kda=True, state_qdq=True,
                                              w_qdq=True, name="kda_b2_h32_t8192_d128"),
