@@ -10,7 +10,8 @@ g++ and marshals numpy arrays through ctypes. Sources for every step are cited i
 file: "GDN state/W QAT foundation" (state and W QDQ contract), "Torch GDN/KDA decode QAT
 with INT8 recurrent state" (decode order), "Add KDA prefill numerical emulation for QAT"
 (per-key-channel retention), "Add experimental GDN/KDA decode and replay QAT" (per-token
-state writes).
+state writes). Every prefill / decode function takes ``codec``: the state QDQ format, "e4m3"
+(tiles of all dk rows x 64 value columns) or "int8" (blocks of one key row x 32 value columns).
 
 Pins: every function here is checked in tests/test_oracle_*.py against closed forms,
 invariants, hand-worked examples and brute force.
@@ -65,6 +66,10 @@ def _load():
             lib.oracle_gdn_chunked.argtypes = [P] * 7 + [I] * 11 + [D, P, I, P, P]
             lib.oracle_gdn_decode.restype = I
             lib.oracle_gdn_decode.argtypes = [P] * 5 + [I] * 8 + [D, P, I, P, P]
+            lib.oracle_int8_block_qdq_f32.restype = I
+            lib.oracle_int8_block_qdq_f32.argtypes = [P, P, P, ctypes.c_int64, I, I]
+            lib.oracle_int8_block_qdq_f64.restype = I
+            lib.oracle_int8_block_qdq_f64.argtypes = [P, P, ctypes.c_int64, I, I]
             lib.oracle_gdn_prefill_decode.restype = I
             lib.oracle_gdn_prefill_decode.argtypes = [P] * 8 + [I] * 10 + [D, P, I, P, P]
             _lib = lib
@@ -131,6 +136,43 @@ def tile_qdq_f64(x, tile_cols: int):
     return y, sc
 
 
+def _codec(state_qdq, codec):
+    """The oracle's state-QDQ selector: 0 off, 1 E4M3 tiles, 2 INT8 blocks of 32 value columns."""
+    if not state_qdq:
+        return 0
+    if codec not in ("e4m3", "int8"):
+        raise ValueError(f"unknown state codec {codec!r}")
+    return 2 if codec == "int8" else 1
+
+
+def int8_block_qdq_f32(x, block_cols: int = 32):
+    """INT8 block QDQ of x [rows, cols] (any leading shape is flattened into rows) in fp32.
+    Returns (y fp32, scales fp32 [rows, ceil(cols / block_cols)])."""
+    xa = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    cols = xa.shape[-1] if xa.ndim else 1
+    rows = xa.size // cols if cols else 0
+    y = np.empty_like(xa)
+    nb = (cols + block_cols - 1) // block_cols if cols else 0
+    sc = np.empty((rows, nb), np.float32)
+    rc = _load().oracle_int8_block_qdq_f32(_ptr(xa), _ptr(y), _ptr(sc), rows, cols, block_cols)
+    if rc:
+        raise ValueError("oracle_int8_block_qdq_f32: bad arguments")
+    return y, sc
+
+
+def int8_block_qdq_f64(x, block_cols: int = 32):
+    """The INT8 block codec in fp64. Returns (y fp64, scales fp64)."""
+    y = np.array(x, dtype=np.float64, copy=True, order="C")
+    cols = y.shape[-1] if y.ndim else 1
+    rows = y.size // cols if cols else 0
+    nb = (cols + block_cols - 1) // block_cols if cols else 0
+    sc = np.empty((rows, nb), np.float64)
+    rc = _load().oracle_int8_block_qdq_f64(_ptr(y), _ptr(sc), rows, cols, block_cols)
+    if rc:
+        raise ValueError("oracle_int8_block_qdq_f64: bad arguments")
+    return y, sc
+
+
 def _prefill_args(q, k, v, g, beta, h0, cu_seqlens, kda):
     q, k, v, g, beta = (_f32(t) for t in (q, k, v, g, beta))
     h0 = _f64(h0)
@@ -157,14 +199,14 @@ def _mask(unit_mask, N, Hv):
 
 
 def gdn_recurrent(q, k, v, g, beta, h0=None, cu_seqlens=None, *, kda=False, state_qdq=False,
-                  qdq_period=64, scale=1.0, unit_mask=None, threads=None):
+                  qdq_period=64, scale=1.0, unit_mask=None, threads=None, codec="e4m3"):
     """O1: token-by-token fp64 recurrence. Returns (o [B,T,Hv,dv], hT [N,Hv,dk,dv]) fp64."""
     q, k, v, g, beta, h0, cu, B, T, N, Hqk, Hv, dk, dv = _prefill_args(q, k, v, g, beta, h0, cu_seqlens, kda)
     o = np.zeros((B, T, Hv, dv), np.float64)
     hT = np.zeros((N, Hv, dk, dv), np.float64)
     m = _mask(unit_mask, N, Hv)
     rc = _load().oracle_gdn_recurrent(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu),
-                                      B, T, N, Hqk, Hv, dk, dv, int(kda), int(state_qdq), int(qdq_period),
+                                      B, T, N, Hqk, Hv, dk, dv, int(kda), _codec(state_qdq, codec), int(qdq_period),
                                       float(scale), _ptr(m), _threads(threads), _ptr(o), _ptr(hT))
     if rc:
         raise ValueError("oracle_gdn_recurrent: bad arguments")
@@ -172,14 +214,14 @@ def gdn_recurrent(q, k, v, g, beta, h0=None, cu_seqlens=None, *, kda=False, stat
 
 
 def gdn_chunked(q, k, v, g, beta, h0=None, cu_seqlens=None, *, kda=False, chunk=64, state_qdq=False,
-                w_qdq=False, scale=1.0, unit_mask=None, threads=None):
+                w_qdq=False, scale=1.0, unit_mask=None, threads=None, codec="e4m3"):
     """O2: chunked / WY fp64 form (needed for W QDQ). Returns (o, hT) fp64."""
     q, k, v, g, beta, h0, cu, B, T, N, Hqk, Hv, dk, dv = _prefill_args(q, k, v, g, beta, h0, cu_seqlens, kda)
     o = np.zeros((B, T, Hv, dv), np.float64)
     hT = np.zeros((N, Hv, dk, dv), np.float64)
     m = _mask(unit_mask, N, Hv)
     rc = _load().oracle_gdn_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu),
-                                    B, T, N, Hqk, Hv, dk, dv, int(kda), int(chunk), int(state_qdq), int(w_qdq),
+                                    B, T, N, Hqk, Hv, dk, dv, int(kda), int(chunk), _codec(state_qdq, codec), int(w_qdq),
                                     float(scale), _ptr(m), _threads(threads), _ptr(o), _ptr(hT))
     if rc:
         raise ValueError("oracle_gdn_chunked: bad arguments")
@@ -187,7 +229,7 @@ def gdn_chunked(q, k, v, g, beta, h0=None, cu_seqlens=None, *, kda=False, chunk=
 
 
 def gdn_decode(q, k, v, g, beta, state, *, kda=False, state_qdq=True, scale=1.0, unit_mask=None,
-               threads=None):
+               threads=None, codec="e4m3"):
     """Decode steps. q,k [steps,N,Hqk,dk]; v [steps,N,Hv,dv]; g [steps,N,Hv] (KDA [..,dk]);
     beta [steps,N,Hv]; state [N,Hv,dk,dv] (copied to fp64). Returns (o fp64, final state fp64)."""
     q, k, v, g, beta = (_f32(t) for t in (q, k, v, g, beta))
@@ -197,7 +239,7 @@ def gdn_decode(q, k, v, g, beta, state, *, kda=False, state_qdq=True, scale=1.0,
     o = np.zeros((steps, N, Hv, dv), np.float64)
     m = _mask(unit_mask, N, Hv)
     rc = _load().oracle_gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), steps, N, Hqk, Hv, dk, dv,
-                                   int(kda), int(state_qdq), float(scale), _ptr(m), _threads(threads),
+                                   int(kda), _codec(state_qdq, codec), float(scale), _ptr(m), _threads(threads),
                                    _ptr(st), _ptr(o))
     if rc:
         raise ValueError("oracle_gdn_decode: bad arguments")
@@ -205,7 +247,7 @@ def gdn_decode(q, k, v, g, beta, state, *, kda=False, state_qdq=True, scale=1.0,
 
 
 def gdn_prefill_decode(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, kda=False,
-                       state_qdq=False, w_qdq=False, scale=1.0, unit_mask=None, threads=None):
+                       state_qdq=False, w_qdq=False, scale=1.0, unit_mask=None, threads=None, codec="e4m3"):
     """Prefill -> decode handoff: per sequence the first prefill_lengths[n] tokens chunked with no
     state QDQ, QDQ at the handoff when tokens remain, then one decode step (with state QDQ) per
     remaining token. Returns (o, hT) fp64."""
@@ -215,7 +257,7 @@ def gdn_prefill_decode(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengt
     hT = np.zeros((N, Hv, dk, dv), np.float64)
     m = _mask(unit_mask, N, Hv)
     rc = _load().oracle_gdn_prefill_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu),
-                                           _ptr(pl), B, T, N, Hqk, Hv, dk, dv, int(kda), int(state_qdq), int(w_qdq),
+                                           _ptr(pl), B, T, N, Hqk, Hv, dk, dv, int(kda), _codec(state_qdq, codec), int(w_qdq),
                                            float(scale), _ptr(m), _threads(threads), _ptr(o), _ptr(hT))
     if rc:
         raise ValueError("oracle_gdn_prefill_decode: bad arguments")

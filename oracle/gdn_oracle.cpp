@@ -20,6 +20,14 @@
 //        exponentials come from prefix differences of the log decay.
 //   [R]  "Add experimental GDN/KDA decode and replay QAT" (#2509), section "What does
 //        this PR do?": per-token FP8 state writes in decode.
+//   [I]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519): the summary's "dynamic
+//        INT8 state recipes, including block-32", the shipped recipe
+//        linear_attention_state_int8_block32_dynamic ("Megatron-Core QAT/QAD workflow" step 1
+//        and "Usage"), "signed INT8 state"; and "Add experimental GDN/KDA decode and replay QAT",
+//        which tests "state/value tails at codec blocks 32/128". Read as: a block is 32
+//        consecutive value columns of one key row of the state (the last block of a row may be
+//        narrower); scale = amax / 127 with the same zero guard as the E4M3 tiles; code = the
+//        signed integer nearest x / scale (ties to even), kept within [-127, 127].
 //   [H]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519), section
 //        "Megatron-Core QAT/QAD workflow", steps 2-3 and the "Ordinary state-QDQ path"
 //        flowchart: a sequence's first prefill_lengths tokens run as chunked prefill that
@@ -40,6 +48,10 @@
 //   oracle_gdn_decode        single-token decode steps with per-token state QDQ
 //   oracle_gdn_prefill_decode  [H]: chunked prefix (no state QDQ), QDQ at the handoff,
 //                            recurrent suffix with per-token state QDQ
+//   oracle_int8_block_qdq_f32 / _f64  [I]: the INT8 block codec (fp32: bit-for-bit definition
+//                            of the standalone op)
+// The state_qdq argument of the prefill / decode functions selects the state codec: 0 off,
+// 1 E4M3 tiles [F], 2 INT8 blocks of 32 value columns [I].
 // Every function is pinned by tests/test_oracle_*.py against closed forms, invariants,
 // hand-worked examples and brute force.
 
@@ -94,10 +106,40 @@ R qdq_tile(R* x, int64_t ld, int rows, int cols) {
   return s;
 }
 
-// State QDQ of one (sequence, head) state S[dk][dv]: one tile per 64 value columns,
-// spanning all dk key rows [F].
+// INT8 [I]: round to the nearest integer (ties to even), kept within [-127, 127].
+double int8_rne_sat(double y) {
+  if (std::isnan(y)) return y;
+  const double c = std::nearbyint(y);   // default mode: nearest, ties to even
+  return std::min(127.0, std::max(-127.0, c));
+}
+
+// One INT8 block: n consecutive elements; scale = amax / 127 (zero guard: 0 -> 1),
+// x <- INT8(x / scale) * scale.
+template <typename R>
+R qdq_int8_block(R* x, int n) {
+  R amax = 0;
+  for (int j = 0; j < n; ++j) amax = std::max(amax, (R)std::fabs(x[j]));
+  R s = amax / (R)127;
+  if (s == (R)0) s = (R)1;
+  for (int j = 0; j < n; ++j) {
+    R y = x[j] / s;
+    R c = (R)int8_rne_sat((double)y);   // exact: an integer of magnitude <= 127
+    x[j] = c * s;
+  }
+  return s;
+}
+
+// State QDQ of one (sequence, head) state S[dk][dv]. Codec 1 [F]: one E4M3 tile per 64 value
+// columns spanning all dk key rows. Codec 2 [I]: one INT8 block per key row and 32 value columns.
 const int kStateTileCols = 64;
-void qdq_state(double* S, int dk, int dv) {
+const int kInt8BlockCols = 32;
+void qdq_state(double* S, int dk, int dv, int codec) {
+  if (codec == 2) {
+    for (int c = 0; c < dk; ++c)
+      for (int j0 = 0; j0 < dv; j0 += kInt8BlockCols)
+        qdq_int8_block<double>(S + (size_t)c * dv + j0, std::min(kInt8BlockCols, dv - j0));
+    return;
+  }
   for (int j0 = 0; j0 < dv; j0 += kStateTileCols)
     qdq_tile<double>(S + j0, dv, dk, std::min(kStateTileCols, dv - j0));
 }
@@ -185,7 +227,7 @@ void recurrent_unit(const Problem& p, int n, int h, int state_qdq, int qdq_perio
   for (int64_t t = 0; t < u.len; ++t) {
     recurrent_step(p, u.t0 + t, h, S.data(), o);
     // 6. state QDQ at the boundary
-    if (state_qdq && ((t + 1) % qdq_period) == 0) qdq_state(S.data(), dk, dv);
+    if (state_qdq && ((t + 1) % qdq_period) == 0) qdq_state(S.data(), dk, dv, state_qdq);
   }
   if (hT) std::copy(S.begin(), S.end(), hT + ((int64_t)n * p.Hv + h) * (int64_t)dk * dv);
 }
@@ -300,7 +342,7 @@ void chunked_range(const Problem& p, UnitRange u, int h, int C, int state_qdq, i
       }
     }
     S.swap(S1);
-    if (state_qdq && ((c0 + L) % 64) == 0) qdq_state(S.data(), dk, dv);
+    if (state_qdq && ((c0 + L) % 64) == 0) qdq_state(S.data(), dk, dv, state_qdq);
   }
 }
 
@@ -322,10 +364,10 @@ void prefill_decode_unit(const Problem& p, int n, int h, int64_t P, int state_qd
   load_h0(p, n, h, S.data());
   chunked_range(p, UnitRange{u.t0, P}, h, 64, 0, w_qdq, o, S);
   if (P < u.len) {
-    if (state_qdq) qdq_state(S.data(), p.dk, p.dv);
+    if (state_qdq) qdq_state(S.data(), p.dk, p.dv, state_qdq);
     for (int64_t t = P; t < u.len; ++t) {
       recurrent_step(p, u.t0 + t, h, S.data(), o);
-      if (state_qdq) qdq_state(S.data(), p.dk, p.dv);
+      if (state_qdq) qdq_state(S.data(), p.dk, p.dv, state_qdq);
     }
   }
   if (hT) std::copy(S.begin(), S.end(), hT + ((int64_t)n * p.Hv + h) * (int64_t)p.dk * p.dv);
@@ -402,13 +444,42 @@ int oracle_tile_qdq_f64(double* x, double* scales, int64_t lead, int rows, int c
 
 // O1. Outputs o [B, T, Hv, dv] and hT [N, Hv, dk, dv] in fp64 (either may be null);
 // unit_mask [N * Hv] (nullable) selects the (n, h) units to compute.
+// INT8 block codec [I], every step in fp32 with IEEE round-to-nearest: per block of
+// block_cols consecutive columns of a row (the last block of a row may be narrower),
+// amax = max |x|, s = amax / 127 (s == 0 -> 1), c = nearest integer to x / s (ties to even)
+// within [-127, 127], y = c * s. x, y: [rows, cols] fp32 (y may equal x); scales (nullable):
+// [rows, ceil(cols / block_cols)].
+int oracle_int8_block_qdq_f32(const float* x, float* y, float* scales, int64_t rows, int cols, int block_cols) {
+  if (!x || !y || rows < 0 || cols < 0 || block_cols <= 0) return 1;
+  const int nb = (cols + block_cols - 1) / block_cols;
+  if (y != x) std::memcpy(y, x, sizeof(float) * (size_t)(rows * cols));
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b) {
+      const float s = qdq_int8_block<float>(y + r * cols + b * block_cols, std::min(block_cols, cols - b * block_cols));
+      if (scales) scales[r * nb + b] = s;
+    }
+  return 0;
+}
+
+// The same codec in fp64 (the arithmetic used inside the fp64 oracles).
+int oracle_int8_block_qdq_f64(double* x, double* scales, int64_t rows, int cols, int block_cols) {
+  if (!x || rows < 0 || cols < 0 || block_cols <= 0) return 1;
+  const int nb = (cols + block_cols - 1) / block_cols;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b) {
+      const double s = qdq_int8_block<double>(x + r * cols + b * block_cols, std::min(block_cols, cols - b * block_cols));
+      if (scales) scales[r * nb + b] = s;
+    }
+  return 0;
+}
+
 int oracle_gdn_recurrent(const float* q, const float* k, const float* v, const float* g,
                          const float* beta, const double* h0, const int32_t* cu_seqlens,
                          int B, int T, int N, int Hqk, int Hv, int dk, int dv, int kda,
                          int state_qdq, int qdq_period, double scale,
                          const uint8_t* unit_mask, int threads, double* o, double* hT) {
   Problem p{q, k, v, g, beta, h0, cu_seqlens, B, T, N, Hqk, Hv, dk, dv, kda, scale};
-  if (check_problem(p) || qdq_period <= 0) return 1;
+  if (check_problem(p) || qdq_period <= 0 || state_qdq < 0 || state_qdq > 2) return 1;
   for_units(N, Hv, unit_mask, threads, [&](int n, int h) {
     recurrent_unit(p, n, h, state_qdq, qdq_period, o, hT);
   });
@@ -422,7 +493,7 @@ int oracle_gdn_chunked(const float* q, const float* k, const float* v, const flo
                        int chunk, int state_qdq, int w_qdq, double scale,
                        const uint8_t* unit_mask, int threads, double* o, double* hT) {
   Problem p{q, k, v, g, beta, h0, cu_seqlens, B, T, N, Hqk, Hv, dk, dv, kda, scale};
-  if (check_problem(p) || chunk <= 0) return 1;
+  if (check_problem(p) || chunk <= 0 || state_qdq < 0 || state_qdq > 2) return 1;
   for_units(N, Hv, unit_mask, threads, [&](int n, int h) {
     chunked_unit(p, n, h, chunk, state_qdq, w_qdq, o, hT);
   });
@@ -436,7 +507,7 @@ int oracle_gdn_prefill_decode(const float* q, const float* k, const float* v, co
                               int dk, int dv, int kda, int state_qdq, int w_qdq, double scale,
                               const uint8_t* unit_mask, int threads, double* o, double* hT) {
   Problem p{q, k, v, g, beta, h0, cu_seqlens, B, T, N, Hqk, Hv, dk, dv, kda, scale};
-  if (check_problem(p) || !prefill_lengths) return 1;
+  if (check_problem(p) || !prefill_lengths || state_qdq < 0 || state_qdq > 2) return 1;
   for (int n = 0; n < N; ++n)
     if (prefill_lengths[n] < 0 || prefill_lengths[n] > unit_range(p, n).len) return 1;
   for_units(N, Hv, unit_mask, threads, [&](int n, int h) {
@@ -454,7 +525,7 @@ int oracle_gdn_decode(const float* q, const float* k, const float* v, const floa
                       const float* beta, int steps, int N, int Hqk, int Hv, int dk, int dv,
                       int kda, int state_qdq, double scale, const uint8_t* unit_mask,
                       int threads, double* state, double* o) {
-  if (!q || !k || !v || !g || !beta || !state || steps < 0 || N < 0) return 1;
+  if (!q || !k || !v || !g || !beta || !state || steps < 0 || N < 0 || state_qdq < 0 || state_qdq > 2) return 1;
   if (Hqk <= 0 || Hv <= 0 || Hv % Hqk != 0 || dk <= 0 || dv <= 0) return 1;
   const int G = Hv / Hqk;
   for_units(N, Hv, unit_mask, threads, [&](int n, int h) {
@@ -485,7 +556,7 @@ int oracle_gdn_decode(const float* q, const float* k, const float* v, const floa
           o[(row * Hv + h) * dv + j] = scale * acc;
         }
       }
-      if (state_qdq) qdq_state(S, dk, dv);
+      if (state_qdq) qdq_state(S, dk, dv, state_qdq);
     }
   });
   return 0;
