@@ -6,6 +6,7 @@ this package is its ctypes binding plus the seeded synthetic-input generators.
 from .gdnqat import (  # noqa: F401
     EXPORTED,
     GDN_FLAG_KDA,
+    GDN_FLAG_STATE_INT8,
     GDN_FLAG_STATE_QDQ,
     GDN_FLAG_W_QDQ,
     ChunkArgs,
@@ -16,6 +17,7 @@ from .gdnqat import (  # noqa: F401
     gdn_chunk_fwd,
     gdn_decode_step,
     gdn_prefill_decode_fwd,
+    int8_block_qdq,
     kda_chunk_fwd,
     kda_prefill_decode_fwd,
     lib_path,

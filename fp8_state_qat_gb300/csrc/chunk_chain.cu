@@ -4,7 +4,8 @@
 //
 // One CTA (256 threads) per (sequence n, v-head h, 64-column value slab); the slab is one
 // state-QDQ tile (all 128 key rows x 64 value columns), so its amax is CTA-local ("GDN state/W QAT
-// foundation", "What does this PR do?"). Two warpgroups split each 64-token chunk:
+// foundation", "What does this PR do?"); with the INT8 codec each thread's key row holds its two
+// 32-column blocks, and the QDQ'd state is carried as bf16 hi + lo. Two warpgroups split each 64-token chunk:
 //   chain  (warps 4-7)  X = W S0 -> Delta = U - X, Dt = exp(gam_63 - gam) Delta -> C = K^T Dt ->
 //                       S1 = Gam_63 S0 + C, QDQ(S1) at a 64-token boundary -> the next chunk.
 //                       Only this loop is serial from chunk to chunk. It also refills the W^T
@@ -477,7 +478,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
           for (int j = 0; j < 64; ++j) s1[j] = fmaf(el, s1[j], cv[j]);
         }
-        if (p.state_qdq && L == 64) {
+        if (p.state_qdq == 1 && L == 64) {
           float m8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) m8[u] = fabsf(s1[u]);
@@ -500,6 +501,17 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           s_exact = true;
           s_scale = sS;
         } else {
+          if (p.state_qdq == 2 && L == 64) {   // INT8: this row's two 32-column blocks, in registers
+#pragma unroll
+            for (int b0 = 0; b0 < 64; b0 += kInt8BlockCols) {
+              float m = 0.f;
+#pragma unroll
+              for (int j = 0; j < kInt8BlockCols; ++j) m = fmaxf(m, fabsf(s1[b0 + j]));
+              const float sc = int8_scale(m), rc = __frcp_rn(sc);
+#pragma unroll
+              for (int j = 0; j < kInt8BlockCols; ++j) s1[b0 + j] = int8_qdq_rcp(s1[b0 + j], rc, sc);
+            }
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             uint4 h16, l16;

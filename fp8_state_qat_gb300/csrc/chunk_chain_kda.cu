@@ -452,7 +452,7 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
       tc::tmem_ld_wait();
       const uint32_t nb = (par ^ 1u) * 32 * KB;
       if (c > 0) wait(par ? B_Y0 : B_Y1, (uint32_t)(((c - 1) >> 1) & 1));
-      if (p.state_qdq && L == 64) {
+      if (p.state_qdq == 1 && L == 64) {
         float m8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) m8[u] = fabsf(s1[u]);
@@ -475,6 +475,17 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
         s_exact = true;
         s_scale = sS;
       } else {
+        if (p.state_qdq == 2 && L == 64) {   // INT8: this row's two 32-column blocks, in registers
+#pragma unroll
+          for (int b0 = 0; b0 < 64; b0 += kInt8BlockCols) {
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < kInt8BlockCols; ++j) m = fmaxf(m, fabsf(s1[b0 + j]));
+            const float sc = int8_scale(m), rc = __frcp_rn(sc);
+#pragma unroll
+            for (int j = 0; j < kInt8BlockCols; ++j) s1[b0 + j] = int8_qdq_rcp(s1[b0 + j], rc, sc);
+          }
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           uint4 h16, l16;

@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
 #pragma unroll
           for (int b = 0; b < 4; ++b) sacc[a][b] = fmaf(ka[a], db[b], sacc[a][b]);
       }
-      if (p.state_qdq && L == C) {   // the chunk ended on a 64-token boundary
+      if (p.state_qdq == 1 && L == C) {   // the chunk ended on a 64-token boundary
         float m = 0.f;
 #pragma unroll
         for (int a = 0; a < TM; ++a)
@@ -363,6 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
         for (int a = 0; a < TM; ++a)
 #pragma unroll
           for (int b = 0; b < 4; ++b) sacc[a][b] = qdq1(sacc[a][b], s);
+      } else if (p.state_qdq == 2 && L == C) {
+        // INT8 blocks of one key row x 32 value columns: row ty + 16 a, columns tx + 16 b, so
+        // block 0 holds b = 0, 1 and block 1 b = 2, 3; the 16 threads of a row are the 16
+        // consecutive lanes tx = 0..15 of one half-warp
+#pragma unroll
+        for (int a = 0; a < TM; ++a)
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            float m = fmaxf(fabsf(sacc[a][2 * blk]), fabsf(sacc[a][2 * blk + 1]));
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float sc = int8_scale(m), rc = __frcp_rn(sc);
+            sacc[a][2 * blk] = int8_qdq_rcp(sacc[a][2 * blk], rc, sc);
+            sacc[a][2 * blk + 1] = int8_qdq_rcp(sacc[a][2 * blk + 1], rc, sc);
+          }
       }
 #pragma unroll
       for (int a = 0; a < TM; ++a)

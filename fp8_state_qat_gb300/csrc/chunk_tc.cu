@@ -583,7 +583,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
       const float el = vegam[63];
 #pragma unroll
       for (int j = 0; j < 32; ++j) s0[j] = fmaf(el, s0[j], cv[j]);
-      const bool q = p.state_qdq && L == 64;
+      const bool q = p.state_qdq == 1 && L == 64;
       if (q) {
         float m = 0.f;
 #pragma unroll
@@ -607,6 +607,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         s_exact = true;
         s_scale = sS;
       } else {
+        if (p.state_qdq == 2 && L == 64) {   // INT8: this thread's 32 columns are one block of its row
+          float m = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(s0[j]));
+          const float sc = int8_scale(m), rc = __frcp_rn(sc);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s0[j] = int8_qdq_rcp(s0[j], rc, sc);
+        }
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           uint4 hi, lo;

@@ -35,6 +35,20 @@ __device__ __forceinline__ float qdq1(float a, float s) {
   return qdq2(a, 0.0f, s).x;
 }
 
+// ---- INT8 block codec of the state ("Torch GDN/KDA decode QAT with INT8 recurrent state":
+// dynamic INT8 state recipes with block-32, signed INT8 state): a block is 32 consecutive value
+// columns of one key row; scale = amax / 127 (IEEE divide) with the zero guard; code = nearest
+// integer to x / scale, ties to even, within [-127, 127]; value = code * scale.
+constexpr int kInt8BlockCols = 32;
+constexpr float kInt8Max = 127.0f;
+__device__ __forceinline__ float int8_scale(float amax) {
+  const float s = __fdiv_rn(amax, kInt8Max);
+  return s == 0.0f ? 1.0f : s;
+}
+// Fused form: x times the round-to-nearest reciprocal r of the scale. |x| <= amax keeps |x r|
+// below 127 (1 + 2^-21), whose nearest integer lies within +-127, so no clamp is needed.
+__device__ __forceinline__ float int8_qdq_rcp(float x, float r, float s) { return __fmul_rn(rintf(__fmul_rn(x, r)), s); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

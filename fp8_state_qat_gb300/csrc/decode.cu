@@ -1,10 +1,12 @@
-// decode.cu -- single-token decode step with per-token E4M3 state QDQ.
+// decode.cu -- single-token decode step with per-token state QDQ (E4M3 tiles or INT8 blocks).
 //
 // Order per (sequence, head), as stated on "Torch GDN/KDA decode QAT with INT8 recurrent
 // state" ("Megatron-Core QAT/QAD workflow", step 3) and "Add experimental GDN/KDA decode and
 // replay QAT" (per-token FP8 state writes): read the stored state, S' = a S (KDA: row c scaled
 // by a[c]), d = b (v - S'^T k), S = S' + k d^T, o = scale S^T q from the updated state, then
-// per-tile QDQ (all dk rows x 64 value columns, scale amax / 448, zero guard) and store.
+// per-tile QDQ (all dk rows x 64 value columns, scale amax / 448, zero guard) and store; with
+// the INT8 codec ("Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 block-32
+// state recipes) one scale per key row and 32 value columns, amax / 127.
 //
 // HBM-bound: per (sequence, head) the state is read once and written once (2 * 4 dk dv
 // bytes) plus the token's q, k, v, g, beta and o. The QDQ multiplies by the reciprocal of the
@@ -96,7 +98,25 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     *reinterpret_cast<float4*>(o + unit * DV + col) =
         make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
 
-  if (state_qdq) {
+  if (state_qdq == 2) {
+    // INT8 blocks: one key row x 32 value columns = one row of warps 2 b and 2 b + 1
+    __shared__ float rmax[NW][DK];
+    float m[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      m[i] = fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w)));
+      m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 1));
+      m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 2));
+      if (cg == 0) rmax[warp][rg + 8 * i] = m[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const float sc = int8_scale(fmaxf(m[i], rmax[warp ^ 1][rg + 8 * i])), rc = __frcp_rn(sc);
+      s[i] = make_float4(int8_qdq_rcp(s[i].x, rc, sc), int8_qdq_rcp(s[i].y, rc, sc), int8_qdq_rcp(s[i].z, rc, sc),
+                         int8_qdq_rcp(s[i].w, rc, sc));
+    }
+  } else if (state_qdq) {
     // one tile = all DK rows x 64 columns = 4 consecutive warps
     __shared__ float wmax[NW];
     amax = warp_max(amax);

@@ -47,6 +47,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 bool dk_ok(int dk) { return dk == 64 || dk == 128; }
+
+// the kernels' state-QDQ selector: 0 off, 1 E4M3 tiles, 2 INT8 blocks
+int state_codec(uint32_t flags) {
+  if (!(flags & GDN_FLAG_STATE_QDQ)) return 0;
+  return (flags & GDN_FLAG_STATE_INT8) ? 2 : 1;
+}
 bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
 
 constexpr size_t kWorkspaceBytes = gdn::kStatusBytes;   // device status word (+ padding to one line)
@@ -57,7 +63,7 @@ gdn_status validate_chunk(const gdn_chunk_args* a, bool kda) {
   if (a->B < 0 || a->T < 0 || a->N < 0 || a->Hqk <= 0 || a->Hv <= 0 || a->dk <= 0 || a->dv <= 0)
     return GDN_ERR_INVALID_ARG;
   if (a->Hv % a->Hqk != 0) return GDN_ERR_INVALID_ARG;
-  if (a->flags & ~(GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ)) return GDN_ERR_INVALID_ARG;
+  if (a->flags & ~(GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ | GDN_FLAG_STATE_INT8)) return GDN_ERR_INVALID_ARG;
   if (!dk_ok(a->dk) || !dv_ok(a->dv)) return GDN_ERR_UNSUPPORTED_SHAPE;
   const int64_t tokens = (int64_t)a->B * a->T;
   if (a->cu_seqlens) {
@@ -100,7 +106,7 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
   if ((int64_t)a->N * a->Hv == 0) return GDN_OK;
   ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
-                 (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
+                 state_codec(a->flags), (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
   p.cu_host = a->cu_seqlens ? a->cu_seqlens_host : nullptr;
   // dk = 128: the two-kernel path (parallel prep, then the state chain) when the workspace
   // holds its staging, else (GDN) the single fused kernel; other shapes and KDA with a small
@@ -131,7 +137,7 @@ size_t handoff_bytes(const ChunkProblem& p) { return handoff_lens_offset(p) + (s
 ChunkProblem problem_of(const gdn_chunk_args* a, bool kda) {
   ChunkProblem p{a->q, a->k, a->v, a->g, a->beta, a->h0, a->cu_seqlens, a->o, a->hT,
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
-                 (a->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
+                 state_codec(a->flags), (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
   p.cu_host = a->cu_seqlens ? a->cu_seqlens_host : nullptr;
   return p;
 }
@@ -218,7 +224,7 @@ size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args) {
   if (gdn_ok) {
     const gdn::ChunkProblem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                               args->B, args->T, args->N, args->Hqk, args->Hv, args->dk, args->dv, args->scale,
-                              (args->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 0};
+                              state_codec(args->flags), (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 0};
     if (gdn::chunk_split_supported(p)) return gdn::chunk_split_layout(p).total;
   }
   return kWorkspaceBytes;
@@ -228,7 +234,7 @@ size_t kda_chunk_fwd_workspace_size(const gdn_chunk_args* args) {
   if (validate_chunk(args, true) != GDN_OK) return 0;
   const gdn::ChunkProblem p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                             args->B, args->T, args->N, args->Hqk, args->Hv, args->dk, args->dv, args->scale,
-                            (args->flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 1};
+                            state_codec(args->flags), (args->flags & GDN_FLAG_W_QDQ) ? 1 : 0, 1};
   if (gdn::kda_split_supported(p)) return gdn::kda_split_layout(p).total;
   return kWorkspaceBytes;
 }
@@ -247,7 +253,7 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            float* state, float* o, int32_t N, int32_t Hqk, int32_t Hv, int32_t dk, int32_t dv,
                            float scale, uint32_t flags, gdn_stream_t stream) {
   if (N < 0 || Hqk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hqk != 0) return GDN_ERR_INVALID_ARG;
-  if (flags & ~(GDN_FLAG_STATE_QDQ | GDN_FLAG_KDA)) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(GDN_FLAG_STATE_QDQ | GDN_FLAG_KDA | GDN_FLAG_STATE_INT8)) return GDN_ERR_INVALID_ARG;
   if (!dk_ok(dk) || !dv_ok(dv)) return GDN_ERR_UNSUPPORTED_SHAPE;
   if (N > 0) {
     if (!q || !k || !v || !g || !beta || !state || !o) return GDN_ERR_INVALID_ARG;
@@ -262,7 +268,7 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
   gdn_status s = check_device();
   if (s != GDN_OK) return s;
   return gdn::launch_decode(q, k, v, g, beta, state, o, N, Hqk, Hv, dk, dv, scale,
-                            (flags & GDN_FLAG_STATE_QDQ) ? 1 : 0, (flags & GDN_FLAG_KDA) ? 1 : 0,
+                            state_codec(flags), (flags & GDN_FLAG_KDA) ? 1 : 0,
                             (cudaStream_t)stream) == cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
@@ -278,6 +284,20 @@ gdn_status fp8_tile_qdq(const float* x, float* y, float* scales, int64_t lead, i
   gdn_status s = check_device();
   if (s != GDN_OK) return s;
   return gdn::launch_tile_qdq(x, y, scales, lead, rows, cols, tile_cols, (cudaStream_t)stream) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+gdn_status int8_block_qdq(const float* x, float* y, float* scales, int64_t rows, int32_t cols, int32_t block_cols,
+                          gdn_stream_t stream) {
+  if (rows < 0 || cols < 0 || block_cols <= 0) return GDN_ERR_INVALID_ARG;
+  const size_t n = (size_t)rows * cols * 4;
+  if (n > 0 && (!x || !y || !aligned(x, 4) || !aligned(y, 4))) return GDN_ERR_INVALID_ARG;
+  if (x != y && overlaps(x, n, y, n)) return GDN_ERR_INVALID_ARG;
+  if (scales && !aligned(scales, 4)) return GDN_ERR_INVALID_ARG;
+  gdn_status s = check_device();
+  if (s != GDN_OK) return s;
+  return gdn::launch_int8_block_qdq(x, y, scales, rows, cols, block_cols, (cudaStream_t)stream) == cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
 }

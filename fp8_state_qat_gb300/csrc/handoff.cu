@@ -6,9 +6,9 @@
 // kernels, run with per-sequence lengths P_n); when tokens remain, the state is QDQ'd at the
 // handoff and every remaining token is a decode step on the sequence's own tokens (teacher
 // forced): read the state, S' = a S (KDA: row c scaled by a[c]), d = b (v - S'^T k),
-// S = S' + k d^T, o = scale S^T q from the updated state, then QDQ (all dk rows x 64 value
-// columns per tile, scale amax / 448 with a zero guard) before the state is stored for the
-// next token.
+// S = S' + k d^T, o = scale S^T q from the updated state, then QDQ (E4M3: all dk rows x 64 value
+// columns per tile, scale amax / 448 with a zero guard; INT8: one key row x 32 value columns per
+// block, amax / 127) before the state is stored for the next token.
 //
 // One CTA per (sequence, head) keeps the state in registers across all of the sequence's
 // decode tokens, so HBM sees the state once in and once out plus each token's q, k, v, g, beta
@@ -91,6 +91,30 @@ __device__ __forceinline__ void qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb
   }
 }
 
+// INT8 block QDQ of the state registers (state_qdq == 2): one block = one key row x 32 value
+// columns = that row's 8 lanes (cg 0..3) in warps 2 b and 2 b + 1. rmax: shared [NW][DK]. The
+// caller keeps a barrier between one call's reads of rmax and the next call's writes.
+template <int DK, int DV>
+__device__ __forceinline__ void int8_state_regs(float2 (&sa)[DK / 8], float2 (&sb)[DK / 8], float (*rmax)[DK],
+                                                int warp, int rg, int cg) {
+  constexpr int RPT = DK / 8;
+  float m[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    m[i] = fmaxf(fmaxf(fabsf(sa[i].x), fabsf(sa[i].y)), fmaxf(fabsf(sb[i].x), fabsf(sb[i].y)));
+    m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 1));
+    m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 2));
+    if (cg == 0) rmax[warp][rg + 8 * i] = m[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float sc = int8_scale(fmaxf(m[i], rmax[warp ^ 1][rg + 8 * i])), rc = __frcp_rn(sc);
+    sa[i] = make_float2(int8_qdq_rcp(sa[i].x, rc, sc), int8_qdq_rcp(sa[i].y, rc, sc));
+    sb[i] = make_float2(int8_qdq_rcp(sb[i].x, rc, sc), int8_qdq_rcp(sb[i].y, rc, sc));
+  }
+}
+
 template <int DK, int DV, bool KDA>
 __global__ void __launch_bounds__(DV * 2, (DV <= 128 ? 2 : 1))
 handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -101,6 +125,7 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   constexpr int NW = DV / 16;
   constexpr int RPT = DK / 8;
   __shared__ float wmax[2][NW];
+  __shared__ float rmax[NW][DK];   // INT8 codec: per-row maxima of each warp's 16 columns
   __shared__ __align__(16) TokenBuf<DK, DV, KDA> tb[kAhead];
   const int64_t unit = blockIdx.x;   // n * Hv + h
   const int n = (int)(unit / Hv), h = (int)(unit % Hv);
@@ -130,7 +155,9 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     cp_commit();
   }
   int slot = 0;   // the per-tile maxima alternate between two slots, one barrier per QDQ
-  if (state_qdq) {
+  if (state_qdq == 2) {
+    int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg);   // the handoff
+  } else if (state_qdq) {
     qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);   // the handoff
     slot ^= 1;
   }
@@ -192,7 +219,9 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     if (rg == 0)
       *reinterpret_cast<float4*>(o + ((t0 + t) * Hv + h) * DV + col) =
           make_float4(scale * oa.x, scale * oa.y, scale * ob.x, scale * ob.y);
-    if (state_qdq) {
+    if (state_qdq == 2) {
+      int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg);
+    } else if (state_qdq) {
       qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);
       slot ^= 1;
     }

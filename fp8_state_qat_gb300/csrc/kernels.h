@@ -29,6 +29,9 @@ struct ChunkProblem {
 
 cudaError_t launch_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int rows, int cols,
                             int tile_cols, cudaStream_t stream);
+// INT8 block QDQ: x, y [rows, cols] fp32, one block = block_cols consecutive columns of a row.
+cudaError_t launch_int8_block_qdq(const float* x, float* y, float* scales, int64_t rows, int cols, int block_cols,
+                                  cudaStream_t stream);
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
                           float* state, float* o, int N, int Hqk, int Hv, int dk, int dv, float scale,

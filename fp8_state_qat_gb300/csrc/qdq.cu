@@ -10,6 +10,7 @@
 // that rereads the tile from L2.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_epilogue.cuh"
 
 namespace gdn {
 namespace {
@@ -173,7 +174,57 @@ tile_qdq_kernel(const float* x, float* y, float* __restrict__ scales, int rows, 
   }
 }
 
+// INT8 block codec ("Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 block-32
+// state recipes): one warp per block of one row (block_cols consecutive columns, the last block
+// of a row narrower), amax = max |x| (redux), s = amax / 127 (IEEE divide, zero guard), c =
+// nearest integer to x / s (ties to even) within [-127, 127], y = c * s. x / s is the correctly
+// rounded quotient (the corrected reciprocal above for normal s, else an IEEE divide; a
+// subnormal quotient rounds to 0 either way), so the result is bit-for-bit the fp32 definition.
+// HBM-bound: 4 bytes read + 4 written per element; with 32-column blocks a warp moves 128
+// contiguous bytes each way.
+constexpr int kInt8Warps = 8;
+__global__ void __launch_bounds__(kInt8Warps * 32)
+int8_block_qdq_kernel(const float* x, float* y, float* __restrict__ scales, int64_t rows, int cols, int block_cols,
+                      int nb) {
+  const int lane = threadIdx.x & 31;
+  const int64_t total = rows * nb;
+  for (int64_t blk = (int64_t)blockIdx.x * kInt8Warps + (threadIdx.x >> 5); blk < total;
+       blk += (int64_t)gridDim.x * kInt8Warps) {
+    const int64_t r = blk / nb;
+    const int b = (int)(blk - r * nb);
+    const int j0 = b * block_cols, n = min(block_cols, cols - j0);
+    const float* xb = x + r * cols + j0;
+    float* yb = y + r * cols + j0;
+    // blocks of up to 32 columns: one element per lane, held in a register between the passes
+    const float v0 = lane < n ? __ldcs(xb + lane) : 0.0f;
+    float amax = fabsf(v0);
+    for (int j = lane + 32; j < n; j += 32) amax = fmaxf(amax, fabsf(xb[j]));
+    amax = warp_absmax(amax);
+    const float s = int8_scale(amax);
+    if (scales && lane == 0) scales[blk] = s;
+    const bool fast = s >= 1.17549435e-38f;
+    const float rs = fast ? __frcp_rn(s) : 0.0f;
+    for (int j = lane; j < n; j += 32) {
+      const float v = j == lane ? v0 : xb[j];
+      const float q = fast ? quotient(v, s, rs) : __fdiv_rn(v, s);
+      const float c = fminf(fmaxf(rintf(q), -kInt8Max), kInt8Max);
+      __stcs(yb + j, __fmul_rn(c, s));
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_int8_block_qdq(const float* x, float* y, float* scales, int64_t rows, int cols, int block_cols,
+                                  cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int nb = (cols + block_cols - 1) / block_cols;
+  const int64_t warps = rows * nb;
+  int64_t grid = (warps + kInt8Warps - 1) / kInt8Warps;
+  if (grid > 152 * 64) grid = 152 * 64;   // grid-stride beyond 64 resident-sized waves of CTAs
+  int8_block_qdq_kernel<<<(unsigned)grid, kInt8Warps * 32, 0, stream>>>(x, y, scales, rows, cols, block_cols, nb);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int rows,
                             int cols, int tile_cols, cudaStream_t stream) {

@@ -26,13 +26,14 @@ GDN_ERR_DEVICE_TIMEOUT = 6
 GDN_FLAG_STATE_QDQ = 1
 GDN_FLAG_W_QDQ = 2
 GDN_FLAG_KDA = 4
+GDN_FLAG_STATE_INT8 = 8
 
 # every extern "C" symbol of include/gdnqat.h
 EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
             "kda_chunk_fwd_workspace_size", "kda_chunk_fwd",
             "gdn_prefill_decode_workspace_size", "gdn_prefill_decode_fwd",
             "kda_prefill_decode_workspace_size", "kda_prefill_decode_fwd",
-            "gdn_decode_step", "fp8_tile_qdq", "gdn_status_string", "gdn_check_device_status")
+            "gdn_decode_step", "fp8_tile_qdq", "int8_block_qdq", "gdn_status_string", "gdn_check_device_status")
 
 
 class GdnError(RuntimeError):
@@ -87,6 +88,8 @@ def load(build_if_missing: bool = True):
         lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, F, U32, P]
         lib.fp8_tile_qdq.restype = ctypes.c_int
         lib.fp8_tile_qdq.argtypes = [P, P, P, ctypes.c_int64, I32, I32, I32, P]
+        lib.int8_block_qdq.restype = ctypes.c_int
+        lib.int8_block_qdq.argtypes = [P, P, P, ctypes.c_int64, I32, I32, P]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_status_string.argtypes = [ctypes.c_int]
         lib.gdn_check_device_status.restype = ctypes.c_int
@@ -112,6 +115,15 @@ def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _state_flags(state_qdq, codec):
+    """GDN_FLAG_STATE_QDQ (and GDN_FLAG_STATE_INT8 for codec "int8")."""
+    if codec not in ("e4m3", "int8"):
+        raise ValueError(f"unknown state codec {codec!r}")
+    if not state_qdq:
+        return 0
+    return GDN_FLAG_STATE_QDQ | (GDN_FLAG_STATE_INT8 if codec == "int8" else 0)
 
 
 def _dev(t, dtype, name):
@@ -148,7 +160,7 @@ def chunk_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False,
     return workspace_bytes(a, kda)
 
 
-def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state):
+def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state, codec="e4m3"):
     q = _dev(q, torch.bfloat16, "q")
     k = _dev(k, torch.bfloat16, "k")
     v = _dev(v, torch.bfloat16, "v")
@@ -169,7 +181,7 @@ def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT
         o = torch.empty((B, T, Hv, dv), dtype=torch.float32, device=dev)
     if hT is None and output_final_state:
         hT = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
-    flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_W_QDQ if w_qdq else 0)
+    flags = _state_flags(state_qdq, codec) | (GDN_FLAG_W_QDQ if w_qdq else 0)
     # the host copy of cu_seqlens must outlive the call: it is returned with the args
     a = ChunkArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_dev), _ptr(cu_host),
                   _ptr(o), _ptr(hT), B, T, N, Hqk, Hv, dk, dv, float(scale), flags)
@@ -177,10 +189,10 @@ def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT
 
 
 def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state,
-           workspace, stream):
+           workspace, stream, codec="e4m3"):
     lib = load()
     a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
-                                    output_final_state)
+                                    output_final_state, codec)
     dev = o.device
     need = workspace_bytes(a, fn_name == "kda_chunk_fwd")
     if workspace is None:
@@ -191,19 +203,20 @@ def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False, w_qdq=False, scale=1.0,
-                  o=None, hT=None, output_final_state=True, workspace=None, stream=None):
+                  o=None, hT=None, output_final_state=True, workspace=None, stream=None, codec="e4m3"):
     """Chunked GDN forward. q, k [B,T,Hqk,dk] bf16; v [B,T,Hv,dv] bf16; g, beta [B,T,Hv] fp32;
-    h0 [N,Hv,dk,dv] fp32 or None; cu_seqlens int32 [N+1] (CPU or CUDA) or None.
+    h0 [N,Hv,dk,dv] fp32 or None; cu_seqlens int32 [N+1] (CPU or CUDA) or None; codec: the state
+    QDQ format, "e4m3" (tiles) or "int8" (blocks of 32 value columns per key row).
     Returns (o [B,T,Hv,dv] fp32, hT [N,Hv,dk,dv] fp32 or None)."""
     return _chunk("gdn_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
-                  output_final_state, workspace, stream)
+                  output_final_state, workspace, stream, codec)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False, w_qdq=False, scale=1.0,
-                  o=None, hT=None, output_final_state=True, workspace=None, stream=None):
+                  o=None, hT=None, output_final_state=True, workspace=None, stream=None, codec="e4m3"):
     """KDA chunked forward: as gdn_chunk_fwd with g [B,T,Hv,dk] (one log-decay per key channel)."""
     return _chunk("kda_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
-                  output_final_state, workspace, stream)
+                  output_final_state, workspace, stream, codec)
 
 
 def prefill_decode_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False, w_qdq=False, kda=False):
@@ -223,9 +236,9 @@ def prefill_decode_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_q
 
 
 def _prefill_decode(fn_name, q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq, w_qdq, scale, o, hT,
-                    workspace, stream):
+                    workspace, stream, codec="e4m3"):
     lib = load()
-    a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, True)
+    a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, True, codec)
     pl = torch.as_tensor(prefill_lengths, dtype=torch.int32).to("cpu").contiguous().reshape(-1)
     if pl.numel() != a.N:
         raise ValueError(f"prefill_lengths: {pl.numel()} entries for {a.N} sequences")
@@ -241,23 +254,24 @@ def _prefill_decode(fn_name, q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, 
 
 
 def gdn_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, state_qdq=False,
-                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None):
+                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None, codec="e4m3"):
     """Prefill -> decode handoff: per sequence the first prefill_lengths[n] tokens chunked with no
     state QDQ, then (state_qdq) a QDQ at the handoff and one decode step with state QDQ per
     remaining token. Same tensors as gdn_chunk_fwd; prefill_lengths: N ints (host).
     Returns (o, hT)."""
     return _prefill_decode("gdn_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
-                           w_qdq, scale, o, hT, workspace, stream)
+                           w_qdq, scale, o, hT, workspace, stream, codec)
 
 
 def kda_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, state_qdq=False,
-                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None):
+                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None, codec="e4m3"):
     """The handoff schedule for KDA (g [B,T,Hv,dk])."""
     return _prefill_decode("kda_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
-                           w_qdq, scale, o, hT, workspace, stream)
+                           w_qdq, scale, o, hT, workspace, stream, codec)
 
 
-def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale=1.0, o=None, stream=None):
+def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale=1.0, o=None, stream=None,
+                    codec="e4m3"):
     """One decode token per sequence; `state` [N,Hv,dk,dv] fp32 is updated in place.
     q, k [N,Hqk,dk] bf16; v [N,Hv,dv] bf16; g [N,Hv] (kda: [N,Hv,dk]) fp32; beta [N,Hv] fp32.
     Returns o [N,Hv,dv] fp32."""
@@ -272,7 +286,7 @@ def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale
     Hv, dv = v.shape[1], v.shape[2]
     if o is None:
         o = torch.empty((N, Hv, dv), dtype=torch.float32, device=q.device)
-    flags = (GDN_FLAG_STATE_QDQ if state_qdq else 0) | (GDN_FLAG_KDA if kda else 0)
+    flags = _state_flags(state_qdq, codec) | (GDN_FLAG_KDA if kda else 0)
     st = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o), N, Hqk, Hv,
                              dk, dv, float(scale), flags, _stream(stream, q.device))
     _check("gdn_decode_step", st)
@@ -294,6 +308,24 @@ def fp8_tile_qdq(x, tile_cols, *, y=None, scales=True, stream=None):
         sc = torch.empty((lead, (cols + tile_cols - 1) // tile_cols), dtype=torch.float32, device=x.device)
     st = lib.fp8_tile_qdq(_ptr(x), _ptr(y), _ptr(sc), lead, rows, cols, int(tile_cols), _stream(stream, x.device))
     _check("fp8_tile_qdq", st)
+    return y, sc
+
+
+def int8_block_qdq(x, block_cols=32, *, y=None, scales=True, stream=None):
+    """INT8 block QDQ of x (fp32, last dimension = columns; leading dimensions are rows): one
+    scale per block_cols consecutive columns of a row. Returns (y, scales [rows, ceil(cols /
+    block_cols)] or None). y may be x."""
+    lib = load()
+    x = _dev(x, torch.float32, "x")
+    cols = x.shape[-1] if x.dim() else 1
+    rows = x.numel() // cols if cols else 0
+    if y is None:
+        y = torch.empty_like(x)
+    sc = None
+    if scales:
+        sc = torch.empty((rows, (cols + block_cols - 1) // block_cols), dtype=torch.float32, device=x.device)
+    st = lib.int8_block_qdq(_ptr(x), _ptr(y), _ptr(sc), rows, cols, int(block_cols), _stream(stream, x.device))
+    _check("int8_block_qdq", st)
     return y, sc
 
 

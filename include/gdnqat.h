@@ -15,6 +15,9 @@
  *      per-key-channel retention, with causal pairwise decays from prefix differences.
  *  [R] "Add experimental GDN/KDA decode and replay QAT", "What does this PR do?":
  *      per-token FP8 state writes.
+ *  [I] "Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 state recipes with
+ *      block-32 and signed INT8 state; "Add experimental GDN/KDA decode and replay QAT": codec
+ *      blocks along the value columns of the state.
  *  [H] "Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD workflow",
  *      steps 2-3: chunked prefix without internal state QDQ, QDQ at the handoff, then decode
  *      tokens that QDQ the state before storing it.
@@ -68,6 +71,10 @@ typedef enum {
 #define GDN_FLAG_STATE_QDQ 1u  /* E4M3 QDQ of S after every 64th token of a sequence ([F]) */
 #define GDN_FLAG_W_QDQ 2u      /* E4M3 QDQ of W, one scale per (sequence, head, chunk) ([F]) */
 #define GDN_FLAG_KDA 4u        /* decode only: g holds one log-decay per key channel ([K]) */
+#define GDN_FLAG_STATE_INT8 8u /* with GDN_FLAG_STATE_QDQ: the state QDQ uses the INT8 block codec
+                                  ([I]) instead of E4M3 tiles -- one scale per key row and 32 value
+                                  columns, amax / 127 with the zero guard, signed codes within
+                                  +-127 (nearest, ties to even). Chunk, handoff and decode calls. */
 
 typedef struct {
   const void* q;               /* device bf16 [B, T, Hqk, dk] */
@@ -82,7 +89,7 @@ typedef struct {
   float* hT;                   /* device fp32 [N, Hv, dk, dv] or NULL; may alias h0 exactly */
   int32_t B, T, N, Hqk, Hv, dk, dv;
   float scale;                 /* multiplies o (1.0 = plain S^T q) */
-  uint32_t flags;              /* GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ */
+  uint32_t flags;              /* GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ | GDN_FLAG_STATE_INT8 */
 } gdn_chunk_args;
 
 /* Smallest workspace gdn_chunk_fwd / kda_chunk_fwd accept: the device status word of the
@@ -174,7 +181,8 @@ gdn_status kda_prefill_decode_fwd(const gdn_chunk_args* args, const int32_t* pre
  * bf16 [N, Hv, dv]; g: device fp32 [N, Hv] (GDN_FLAG_KDA: [N, Hv, dk]); beta: device fp32
  * [N, Hv]; state: device fp32 [N, Hv, dk, dv], read and overwritten in place; o: device
  * fp32 [N, Hv, dv]. Order per (sequence, head): read S, decay, delta update, o from the
- * updated state, then (GDN_FLAG_STATE_QDQ) per-tile E4M3 QDQ, then store S. */
+ * updated state, then (GDN_FLAG_STATE_QDQ) per-tile E4M3 QDQ (GDN_FLAG_STATE_INT8: INT8 blocks),
+ * then store S. */
 gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
                            const float* beta, float* state, float* o, int32_t N, int32_t Hqk,
                            int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
@@ -188,6 +196,15 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
  * y = c * s. State tiles: rows = dk, tile_cols = 64. W tiles: rows = 64, tile_cols = dk. */
 gdn_status fp8_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int32_t rows,
                         int32_t cols, int32_t tile_cols, gdn_stream_t stream);
+
+/* Standalone INT8 block QDQ ([I]). x, y: device fp32 [rows, cols] (y may equal x); a block is
+ * block_cols consecutive columns of one row (the last block of a row may be narrower). scales:
+ * device fp32 [rows, ceil(cols / block_cols)] or NULL. Per block, in fp32 with IEEE
+ * round-to-nearest: amax = max |x|, s = amax / 127 (s == 0 -> 1), c = the integer nearest x / s
+ * (ties to even) within [-127, 127], y = c * s. The state codec: rows = N Hv dk (one per key row
+ * of every state), cols = dv, block_cols = 32. */
+gdn_status int8_block_qdq(const float* x, float* y, float* scales, int64_t rows, int32_t cols,
+                          int32_t block_cols, gdn_stream_t stream);
 
 /* Static description of a status code. */
 const char* gdn_status_string(gdn_status status);

@@ -62,7 +62,7 @@ def call_chunk(so, args, ws=FAKE + (7 << 32), ws_bytes=1 << 20):
     (dict(N=3), B.GDN_ERR_INVALID_ARG),           # dense needs N == B
     (dict(q=None), B.GDN_ERR_INVALID_ARG),
     (dict(q=FAKE + 2), B.GDN_ERR_INVALID_ARG),    # misaligned
-    (dict(flags=8), B.GDN_ERR_INVALID_ARG),       # unknown flag
+    (dict(flags=16), B.GDN_ERR_INVALID_ARG),      # unknown flag
     (dict(o=FAKE + (2 << 32) + 64), B.GDN_ERR_INVALID_ARG),   # o overlaps v
     (dict(h0=FAKE + (8 << 32), hT=FAKE + (8 << 32) + 256), B.GDN_ERR_INVALID_ARG),  # partial alias
 ])
@@ -185,3 +185,19 @@ def test_handoff_validation(so):
     assert call_handoff(so, a, [50, 11, 0]) == B.GDN_ERR_INVALID_ARG   # 11 > L_1 = 10
     if not torch.cuda.is_available():
         assert call_handoff(so, a, [50, 10, 0]) == B.GDN_ERR_UNSUPPORTED_ARCH
+
+
+def test_int8_codec_flags_and_standalone_validation(so):
+    """GDN_FLAG_STATE_INT8 is accepted by the chunk, handoff and decode calls (the next check is
+    the device's); the standalone INT8 op validates like the E4M3 one."""
+    P = ctypes.c_void_p
+    flags = B.GDN_FLAG_STATE_QDQ | B.GDN_FLAG_W_QDQ | B.GDN_FLAG_STATE_INT8
+    want = B.GDN_ERR_UNSUPPORTED_ARCH if not torch.cuda.is_available() else None
+    if want is not None:
+        assert call_chunk(so, good_args(flags=flags)) == want
+        ptrs = [P(FAKE + (i << 32)) for i in range(7)]
+        assert so.gdn_decode_step(*ptrs, 4, 2, 4, 128, 128, 1.0, B.GDN_FLAG_STATE_QDQ | B.GDN_FLAG_STATE_INT8,
+                                  None) == want
+    assert so.int8_block_qdq(P(FAKE), P(FAKE), None, 2, 64, 0, None) == B.GDN_ERR_INVALID_ARG
+    assert so.int8_block_qdq(P(FAKE), P(FAKE + 4), None, 2, 64, 32, None) == B.GDN_ERR_INVALID_ARG   # overlap
+    assert so.int8_block_qdq(P(FAKE), P(FAKE), None, -1, 64, 32, None) == B.GDN_ERR_INVALID_ARG
