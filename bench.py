@@ -380,7 +380,7 @@ class DecodeCase:
     def step(self, i, ws, stream):
         t = self.tok[i % self.steps_avail]
         self.gdn.gdn_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], self.state, state_qdq=self.d.state_qdq,
-                                 kda=self.d.kda, o=self.o, stream=stream)
+                                 kda=self.d.kda, o=self.o, stream=stream, codec=self.d.codec)
 
     def host(self):
         self.h_in = {k: getattr(self.d, k)[0].pin_memory() for k in ("q", "k", "v", "g", "beta")}
@@ -395,7 +395,7 @@ class DecodeCase:
     def run(self, slot, ws, stream):
         t = self.tok[slot]
         self.gdn.gdn_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], self.state, state_qdq=self.d.state_qdq,
-                                 kda=self.d.kda, o=self.o_slots[slot], stream=stream)
+                                 kda=self.d.kda, o=self.o_slots[slot], stream=stream, codec=self.d.codec)
 
     def d2h(self, slot):
         self.h_out[slot].copy_(self.o_slots[slot], non_blocking=True)
@@ -403,7 +403,8 @@ class DecodeCase:
     def config(self):
         d = self.d
         return {"workload": d.name, "N": d.q.shape[1], "H": d.v.shape[2], "dk": d.q.shape[3], "dv": d.v.shape[3],
-                "state_qdq": d.state_qdq, "kda": d.kda, "state": "N(0,0.05), updated in place across steps"}
+                "state_qdq": d.state_qdq, "codec": d.codec, "kda": d.kda,
+                "state": "N(0,0.05), updated in place across steps"}
 
 
 class QdqCase:
@@ -415,7 +416,8 @@ class QdqCase:
         lead, rows, cols = d.x.shape
         ntiles = (cols + d.tile_cols - 1) // d.tile_cols
         self.tokens = lead * rows * cols                      # elements
-        self.bytes = 8 * self.tokens + 4 * lead * ntiles
+        # E4M3: one scale per tile of a leading index; INT8: one per block of a row
+        self.bytes = 8 * self.tokens + 4 * ntiles * (lead * rows if d.codec == "int8" else lead)
         self.flops = 0
         self.unit = "elements/s"
         self.xs = [d.x.to(dev), d.x.to(dev).neg_()]
@@ -428,11 +430,14 @@ class QdqCase:
     def scope(self):
         return "one step = one kernel launch"
 
-    def _call(self, x, stream):
-        self.gdn.fp8_tile_qdq(x, self.d.tile_cols, y=self.y, stream=stream)
+    def _call(self, x, y, stream):
+        if self.d.codec == "int8":
+            self.gdn.int8_block_qdq(x, self.d.tile_cols, y=y, stream=stream)
+        else:
+            self.gdn.fp8_tile_qdq(x, self.d.tile_cols, y=y, stream=stream)
 
     def step(self, i, ws, stream):
-        self._call(self.xs[i & 1], stream)
+        self._call(self.xs[i & 1], self.y, stream)
 
     def host(self):
         self.h_in = self.d.x.pin_memory()
@@ -444,7 +449,7 @@ class QdqCase:
         self.xs[slot].copy_(self.h_in, non_blocking=True)
 
     def run(self, slot, ws, stream):
-        self.gdn.fp8_tile_qdq(self.xs[slot], self.d.tile_cols, y=self.y_slots[slot], stream=stream)
+        self._call(self.xs[slot], self.y_slots[slot], stream)
 
     def d2h(self, slot):
         self.h_out[slot].copy_(self.y_slots[slot], non_blocking=True)
@@ -452,8 +457,10 @@ class QdqCase:
     def config(self):
         d = self.d
         lead, rows, cols = d.x.shape
-        return {"workload": d.name, "lead": lead, "rows": rows, "cols": cols, "tile_cols": d.tile_cols,
-                "x": "N(0,0.05) fp32, out of place"}
+        c = {"workload": d.name, "lead": lead, "rows": rows, "cols": cols, "codec": d.codec,
+             "x": "N(0,0.05) fp32, out of place"}
+        c["block_cols" if d.codec == "int8" else "tile_cols"] = d.tile_cols
+        return c
 
 
 METRICS = {
@@ -462,6 +469,8 @@ METRICS = {
     "kda_b2_h32_t8192_d128": "KDA chunked-prefill tokens/s (B2 H32 T8192 d128, FP8 state + W QDQ)",
     "gdn_decode_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token FP8 state QDQ)",
     "qdq_state_n512_h32_d128": "standalone FP8 tile QDQ elements/s (16384 x [128 x 128] fp32, 64-column tiles)",
+    "int8_state_n512_h32_d128": "standalone INT8 block QDQ elements/s (16384 x [128 x 128] fp32, 32-column blocks)",
+    "gdn_decode_int8_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token INT8 block-32 state QDQ)",
     "gdn_b1_h2_t256_d64": "GDN chunked-prefill tokens/s (B1 H2 T256 d64, FP8 state QDQ)",
     "handoff_n256_t128_p64_h16_d128": "GDN prefill->decode handoff tokens/s (256 seqs x 128 tokens, 64-token "
                                       "chunked prefix + 64 decode tokens, H16 d128, FP8 state + W QDQ)",

@@ -41,8 +41,18 @@ __device__ __forceinline__ float qdq1(float a, float s) {
 // integer to x / scale, ties to even, within [-127, 127]; value = code * scale.
 constexpr int kInt8BlockCols = 32;
 constexpr float kInt8Max = 127.0f;
+// fl32(amax / 127) by Markstein's correction: with r = RN(1 / 127), q0 = RN(amax r) and the
+// exact residual e = amax - q0 127 (one FMA), RN(q0 + e r) is the correctly rounded quotient
+// whenever it is a normal number; smaller amax take the IEEE divide.
 __device__ __forceinline__ float int8_scale(float amax) {
-  const float s = __fdiv_rn(amax, kInt8Max);
+  constexpr float r = 1.0f / 127.0f;
+  float s;
+  if (amax >= 1.0e-30f) {
+    const float q0 = __fmul_rn(amax, r);
+    s = __fmaf_rn(__fmaf_rn(-q0, kInt8Max, amax), r, q0);
+  } else {
+    s = __fdiv_rn(amax, kInt8Max);
+  }
   return s == 0.0f ? 1.0f : s;
 }
 // Fused form: x times the round-to-nearest reciprocal r of the scale. |x| <= amax keeps |x r|

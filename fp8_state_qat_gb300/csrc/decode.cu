@@ -110,9 +110,22 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
       if (cg == 0) rmax[warp][rg + 8 * i] = m[i];
     }
     __syncthreads();
+    // the 4 lanes of a row group share its rows: lane cg computes the scales of rows i = cg mod 4
+    // and hands them to the other three
+    float scl[RPT / 4], rcl[RPT / 4];
+#pragma unroll
+    for (int j = 0; j < RPT / 4; ++j) {
+      const int i = 4 * j + cg;
+      float bm = m[4 * j];
+#pragma unroll
+      for (int c = 1; c < 4; ++c) bm = c == cg ? m[4 * j + c] : bm;   // m[i] without dynamic indexing
+      scl[j] = int8_scale(fmaxf(bm, rmax[warp ^ 1][rg + 8 * i]));
+      rcl[j] = __frcp_rn(scl[j]);
+    }
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const float sc = int8_scale(fmaxf(m[i], rmax[warp ^ 1][rg + 8 * i])), rc = __frcp_rn(sc);
+      const int src = (lane & ~3) | (i & 3);
+      const float sc = __shfl_sync(0xffffffffu, scl[i >> 2], src), rc = __shfl_sync(0xffffffffu, rcl[i >> 2], src);
       s[i] = make_float4(int8_qdq_rcp(s[i].x, rc, sc), int8_qdq_rcp(s[i].y, rc, sc), int8_qdq_rcp(s[i].z, rc, sc),
                          int8_qdq_rcp(s[i].w, rc, sc));
     }

@@ -107,9 +107,22 @@ __device__ __forceinline__ void int8_state_regs(float2 (&sa)[DK / 8], float2 (&s
     if (cg == 0) rmax[warp][rg + 8 * i] = m[i];
   }
   __syncthreads();
+  // the 4 lanes of a row group share its rows: lane cg computes the scales of rows i = cg mod 4
+  // and hands them to the other three
+  float scl[RPT / 4], rcl[RPT / 4];
+#pragma unroll
+  for (int j = 0; j < RPT / 4; ++j) {
+    float bm = m[4 * j];
+#pragma unroll
+    for (int c = 1; c < 4; ++c) bm = c == cg ? m[4 * j + c] : bm;   // m[4 j + cg] without dynamic indexing
+    scl[j] = int8_scale(fmaxf(bm, rmax[warp ^ 1][rg + 8 * (4 * j + cg)]));
+    rcl[j] = __frcp_rn(scl[j]);
+  }
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const float sc = int8_scale(fmaxf(m[i], rmax[warp ^ 1][rg + 8 * i])), rc = __frcp_rn(sc);
+    const int src = (lane & ~3) | (i & 3);
+    const float sc = __shfl_sync(0xffffffffu, scl[i >> 2], src), rc = __shfl_sync(0xffffffffu, rcl[i >> 2], src);
     sa[i] = make_float2(int8_qdq_rcp(sa[i].x, rc, sc), int8_qdq_rcp(sa[i].y, rc, sc));
     sb[i] = make_float2(int8_qdq_rcp(sb[i].x, rc, sc), int8_qdq_rcp(sb[i].y, rc, sc));
   }

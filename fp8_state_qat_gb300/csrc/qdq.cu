@@ -213,12 +213,59 @@ int8_block_qdq_kernel(const float* x, float* y, float* __restrict__ scales, int6
   }
 }
 
+// The same codec for 32-column blocks of 16-byte aligned rows (the state codec's shape): a lane
+// holds one float4, 8 lanes one block, and each warp keeps kInt8Unroll x 512 bytes in flight, so
+// the copy runs at HBM speed instead of one 128-byte block per warp at a time.
+constexpr int kInt8Unroll = 4;
+__global__ void __launch_bounds__(kInt8Warps * 32)
+int8_block32_qdq_kernel(const float4* x, float4* y, float* __restrict__ scales, int64_t nblk) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * kInt8Warps;
+  // a warp step covers kInt8Unroll x 4 consecutive blocks (block = 8 float4)
+  for (int64_t base = ((int64_t)blockIdx.x * kInt8Warps + (threadIdx.x >> 5)) * (4 * kInt8Unroll); base < nblk;
+       base += warps * 4 * kInt8Unroll) {
+    float4 v[kInt8Unroll];
+#pragma unroll
+    for (int u = 0; u < kInt8Unroll; ++u) {
+      const int64_t blk = base + 4 * u + (lane >> 3);
+      v[u] = blk < nblk ? __ldcs(x + blk * 8 + (lane & 7)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kInt8Unroll; ++u) {
+      const int64_t blk = base + 4 * u + (lane >> 3);
+      float m = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      if (blk >= nblk) continue;
+      const float s = int8_scale(m);
+      if (scales && (lane & 7) == 0) scales[blk] = s;
+      const bool fast = s >= 1.17549435e-38f;
+      const float rs = fast ? __frcp_rn(s) : 0.0f;
+      auto q = [&](float e) {
+        const float t = fast ? quotient(e, s, rs) : __fdiv_rn(e, s);
+        return __fmul_rn(fminf(fmaxf(rintf(t), -kInt8Max), kInt8Max), s);
+      };
+      __stcs(y + blk * 8 + (lane & 7), make_float4(q(v[u].x), q(v[u].y), q(v[u].z), q(v[u].w)));
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_int8_block_qdq(const float* x, float* y, float* scales, int64_t rows, int cols, int block_cols,
                                   cudaStream_t stream) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const int nb = (cols + block_cols - 1) / block_cols;
+  if (block_cols == 32 && cols % 32 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+    const int64_t nblk = rows * nb, per_warp = 4 * kInt8Unroll;
+    int64_t grid = (nblk + per_warp * kInt8Warps - 1) / (per_warp * kInt8Warps);
+    if (grid > 152 * 16) grid = 152 * 16;   // grid-stride: 16 CTAs of 8 warps per SM at most
+    int8_block32_qdq_kernel<<<(unsigned)grid, kInt8Warps * 32, 0, stream>>>(
+        reinterpret_cast<const float4*>(x), reinterpret_cast<float4*>(y), scales, nblk);
+    return cudaGetLastError();
+  }
   const int64_t warps = rows * nb;
   int64_t grid = (warps + kInt8Warps - 1) / kInt8Warps;
   if (grid > 152 * 64) grid = 152 * 64;   // grid-stride beyond 64 resident-sized waves of CTAs

@@ -52,8 +52,9 @@ class PrefillInputs:
 @dataclass
 class QdqInputs:
     x: torch.Tensor      # [lead, rows, cols] fp32
-    tile_cols: int
+    tile_cols: int       # E4M3: a tile is all rows x tile_cols columns; INT8: a block is tile_cols columns of a row
     name: str = ""
+    codec: str = "e4m3"
 
 
 @dataclass
@@ -67,6 +68,7 @@ class DecodeInputs:
     kda: bool = False
     state_qdq: bool = True
     name: str = ""
+    codec: str = "e4m3"  # state QDQ format: "e4m3" tiles or "int8" blocks
 
 
 def _normal(gen, shape, mean=0.0, std=1.0):
@@ -118,7 +120,8 @@ def varlen_lengths(n_seqs, max_len, seed):
     return torch.randint(1, max_len + 1, (n_seqs,), generator=gen).tolist()
 
 
-def decode(steps, N, H, dk, dv, *, seed, kda=False, state_std=0.05, state_qdq=True, name="") -> DecodeInputs:
+def decode(steps, N, H, dk, dv, *, seed, kda=False, state_std=0.05, state_qdq=True, name="",
+           codec="e4m3") -> DecodeInputs:
     gen = torch.Generator().manual_seed(seed)
     state = _normal(gen, (N, H, dk, dv), std=state_std)
     q = _unit_bf16(gen, (steps, N, H, dk))
@@ -128,13 +131,13 @@ def decode(steps, N, H, dk, dv, *, seed, kda=False, state_std=0.05, state_qdq=Tr
     gshape = (steps, N, H, dk) if kda else (steps, N, H)
     g = torch.log(torch.sigmoid(_normal(gen, gshape, mean=3.0)))
     return DecodeInputs(q, k, v, g.contiguous(), beta.contiguous(), state, kda=kda,
-                        state_qdq=state_qdq, name=name)
+                        state_qdq=state_qdq, name=name, codec=codec)
 
 
-def qdq(lead, rows, cols, tile_cols, *, seed, std=0.05, name="") -> QdqInputs:
-    """Standalone tile QDQ input: a state-shaped fp32 tensor."""
+def qdq(lead, rows, cols, tile_cols, *, seed, std=0.05, name="", codec="e4m3") -> QdqInputs:
+    """Standalone QDQ input: a state-shaped fp32 tensor."""
     gen = torch.Generator().manual_seed(seed)
-    return QdqInputs(_normal(gen, (lead, rows, cols), std=std), tile_cols, name=name)
+    return QdqInputs(_normal(gen, (lead, rows, cols), std=std), tile_cols, name=name, codec=codec)
 
 
 # --- the named workloads --------------------------------------------------------------
@@ -153,6 +156,12 @@ WORKLOADS = {
     # decode: 512 sequences x 32 heads, 64 single-token steps, QDQ on every write
     "gdn_decode_n512_h32_d128_s64": lambda: decode(64, 512, 32, 128, 128, seed=3, state_std=0.05,
                                                    name="gdn_decode_n512_h32_d128_s64"),
+    # the decode workload with the INT8 block-32 state codec
+    "gdn_decode_int8_n512_h32_d128_s64": lambda: decode(64, 512, 32, 128, 128, seed=3, state_std=0.05,
+                                                        name="gdn_decode_int8_n512_h32_d128_s64", codec="int8"),
+    # standalone INT8 block QDQ over the same decode-sized state tensor, 32-column blocks per key row
+    "int8_state_n512_h32_d128": lambda: qdq(512 * 32, 128, 128, 32, seed=5, name="int8_state_n512_h32_d128",
+                                            codec="int8"),
     # standalone tile QDQ over a decode-sized state tensor: 16384 x [128 x 128], 64-column tiles
     "qdq_state_n512_h32_d128": lambda: qdq(512 * 32, 128, 128, 64, seed=5, name="qdq_state_n512_h32_d128"),
     # prefill -> decode handoff, the QAT/QAD workflow's example shape (128-token sequences, the
