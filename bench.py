@@ -68,9 +68,15 @@ PROFILES = {
     "gdn_b4_h16_t4096_d128": ("chunk_fwd_gdn_b4_h16_t4096_d128.md", PREFILL_SOURCES),
     "gdn_decode_n512_h32_d128_s64": ("decode_gdn_decode_n512_h32_d128_s64.md",
                                      ("decode.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
-    "qdq_state_n512_h32_d128": ("tile_qdq_qdq_state_n512_h32_d128.md", ("qdq.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
+    "qdq_state_n512_h32_d128": ("tile_qdq_qdq_state_n512_h32_d128.md",
+                                ("qdq.cu", "gdnqat_api.cu", "common.cuh", "tc_epilogue.cuh", "tc_common.cuh", "kernels.h")),
     "gdn_varlen8_hqk16_hv32_d128": ("chunk_fwd_gdn_varlen8_hqk16_hv32_d128.md", PREFILL_SOURCES),
     "handoff_n256_t128_p64_h16_d128": ("handoff_n256_t128_p64_h16_d128.md", PREFILL_SOURCES + ("handoff.cu",)),
+    "gdn_decode_int8_n512_h32_d128_s64": ("decode_gdn_decode_int8_n512_h32_d128_s64.md",
+                                          ("decode.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
+    "int8_state_n512_h32_d128": ("int8_block_qdq_int8_state_n512_h32_d128.md",
+                                 ("qdq.cu", "gdnqat_api.cu", "common.cuh", "tc_epilogue.cuh", "tc_common.cuh",
+                                  "kernels.h")),
     "kda_b2_h32_t8192_d128": ("chunk_fwd_kda_b2_h32_t8192_d128.md",
                               ("chunk_prep_kda.cu", "chunk_chain_kda.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh",
                                "tc_common.cuh", "tc_epilogue.cuh", "kernels.h")),
