@@ -166,6 +166,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The slowest replica's figure: every rank's x reduced with MAX (a collective when world > 1;
+    it runs on the ranks' NCCL group on GPUs, on gloo in the CPU tests)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput of `world` replicas (weak scaling): every rank's units over the
+    slowest rank's milliseconds."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -537,12 +555,8 @@ def run_gpu(args):
     time.sleep(0.2)
     clocks.stop()
     gdn.gdn_check_device_status(ws)
-    ms = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
 
     # end to end through the public API: every step copies its inputs from pinned host memory,
     # calls the library and copies its result back to pinned host memory. Copies in, calls and
@@ -585,11 +599,7 @@ def run_gpu(args):
     s_out.wait_event(ev_run[(e2e_steps - 1) & 1])
     e1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     if rank == 0:
         hbm, bf16, src = peaks()
@@ -598,7 +608,7 @@ def run_gpu(args):
         cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
         cfg["l2"] = "inputs larger than L2 (129 MB); prefill alternates two resident input sets"
         unit = getattr(case, "unit", UNIT)
-        line = {"metric": METRICS.get(args.workload, args.workload), "value": world * case.tokens * args.steps / (ms * 1e-3),
+        line = {"metric": METRICS.get(args.workload, args.workload), "value": job_rate(case.tokens * args.steps, world, ms),
                 "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic", "config": cfg,
@@ -608,7 +618,7 @@ def run_gpu(args):
                              "peak_source": src, "scope": case.scope(), "bytes_per_launch": case.bytes,
                              "flops_per_launch": case.flops,
                              "tensor_frac": case.flops / (launch_ms * 1e-3) / (bf16 * 1e12), "kernel_ms": launch_ms},
-                "e2e": {"value": world * case.tokens * e2e_steps / (e2e_ms * 1e-3), "unit": unit,
+                "e2e": {"value": job_rate(case.tokens * e2e_steps, world, e2e_ms), "unit": unit,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": args.steps * case.launches,
                 "clocks": clocks.summary()}

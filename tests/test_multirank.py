@@ -1,0 +1,51 @@
+"""The N > 1 path of bench.py on CPU: two ranks over gloo (no GPU). The path shards into
+independent replicas (every (sequence, head) chain is independent; there is no exchange step), so
+the only multi-rank logic is the timing aggregation: the job's time is the slowest rank's, and the
+job's throughput counts every rank's units."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, times, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, local = bench.dist_env()
+        assert (w, r, local) == (world, rank, rank)
+        ms = bench.max_over_ranks(times[rank], w, torch.device("cpu"))
+        out[rank] = (ms, bench.job_rate(1000, w, ms))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_max_over_ranks_and_job_rate(world):
+    times = [4.0 + 3.0 * r for r in range(world)]   # the last rank is the slowest
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.start_processes(_rank, args=(world, _free_port(), times, out), nprocs=world, start_method="spawn")
+    slowest = max(times)
+    for r in range(world):
+        ms, rate = out[r]
+        assert ms == slowest
+        assert rate == pytest.approx(world * 1000 / (slowest * 1e-3))
+
+
+def test_single_rank_is_local():
+    assert bench.max_over_ranks(5.0, 1, torch.device("cpu")) == 5.0
+    assert bench.job_rate(500, 1, 2.0) == pytest.approx(250000.0)
