@@ -152,3 +152,27 @@ def test_teacher_forced_decode_tokens(gdn, oracle_mod, kda, dv):
         same = np.isclose(S_next, so, rtol=1e-5, atol=0).mean()
         assert same >= 0.999, (t, same)
         S = S_next
+
+
+def test_handoff_full_size_sampled(gdn, oracle_mod):
+    """The benchmarked handoff workload (256 sequences x 128 tokens, 64-token prefix, H16 d128,
+    state + W QDQ) in the launch configuration bench.py times; the oracle recomputes 32 sampled
+    (sequence, head) units: o within the QDQ bound over the sampled units together, the final
+    states free of gross errors (their decode tokens carry independent quantization noise, see
+    check()), and every decode token's step checked teacher forced in
+    test_teacher_forced_decode_tokens."""
+    from helpers import UNIT_SANITY, mask_for, sample_units
+    x = workloads.workload("handoff_n256_t128_p64_h16_d128")
+    c = to_cuda(x)
+    o, hT = gdn.gdn_prefill_decode_fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], None, x.prefill_lengths,
+                                       state_qdq=True, w_qdq=True)
+    torch.cuda.synchronize()
+    units = sample_units(256, 16, 32, seed=7)
+    oref, href = oracle_mod.gdn_prefill_decode(x.q, x.k, x.v, x.g, x.beta, x.h0, None, x.prefill_lengths,
+                                               state_qdq=True, w_qdq=True, unit_mask=mask_for(units, 256, 16))
+    o, hT = o.cpu().double().numpy(), hT.cpu().double().numpy()
+    ns, hs = (list(t) for t in zip(*units))
+    assert rel(o[ns, :, hs], oref[ns, :, hs]) <= TOL_QDQ
+    for n, h in units:
+        assert rel(hT[n, h], href[n, h]) <= UNIT_SANITY
+        assert rel(o[n, :64, h], oref[n, :64, h]) <= TOL_QDQ   # the prefix: W QDQ, no state QDQ

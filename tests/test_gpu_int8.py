@@ -127,3 +127,37 @@ def test_handoff_int8_teacher_forced(gdn, oracle_mod, kda):
         same = np.isclose(S_next, so, rtol=1e-5, atol=0).mean()
         assert same >= 0.999, (t, same)
         S = S_next
+
+
+def test_standalone_full_workload_bit_exact(gdn, oracle_mod):
+    """The benchmarked INT8 block QDQ workload (16384 x [128 x 128] fp32, 32-column blocks), in
+    the launch configuration bench.py times, bit for bit against the oracle's fp32 definition."""
+    d = workloads.workload("int8_state_n512_h32_d128")
+    x = d.x.reshape(-1, 128)
+    y_ref, s_ref = oracle_mod.int8_block_qdq_f32(x.numpy(), 32)
+    y, s = gdn.int8_block_qdq(x.cuda(), 32)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(y), bits(y_ref)) and np.array_equal(bits(s), bits(s_ref))
+
+
+def test_decode_int8_full_size_sampled(gdn, oracle_mod):
+    """The benchmarked INT8 decode workload (512 sequences x 32 heads, 64 steps, INT8 block QDQ
+    on every write); the oracle recomputes 48 sampled (sequence, head) units over all 64 steps."""
+    from helpers import UNIT_SANITY, mask_for, sample_units
+    d = workloads.workload("gdn_decode_int8_n512_h32_d128_s64")
+    st = d.state.cuda()
+    outs = []
+    for s in range(64):
+        outs.append(gdn.gdn_decode_step(d.q[s].cuda(), d.k[s].cuda(), d.v[s].cuda(), d.g[s].cuda(), d.beta[s].cuda(),
+                                        st, codec="int8"))
+    torch.cuda.synchronize()
+    o = torch.stack(outs).cpu().double().numpy()
+    st = st.cpu().double().numpy()
+    units = sample_units(512, 32, 48, seed=3)
+    oo, so = oracle_mod.gdn_decode(d.q, d.k, d.v, d.g, d.beta, d.state, state_qdq=True, codec="int8",
+                                   unit_mask=mask_for(units, 512, 32))
+    ns, hs = (list(t) for t in zip(*units))
+    assert rel(o[:, ns, hs], oo[:, ns, hs]) <= TOL_QDQ
+    assert rel(st[ns, hs], so[ns, hs]) <= TOL_QDQ
+    for n, h in units:
+        assert rel(st[n, h], so[n, h]) <= UNIT_SANITY
