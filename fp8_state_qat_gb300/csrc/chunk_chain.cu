@@ -86,6 +86,7 @@ struct ChainParams {
   int T, Hqk, Hv, dv;
   float scale;
   int state_qdq, w_qdq;
+  float* sscale;   // final-state QDQ scales or null (layout: ChunkProblem::state_scales)
 };
 
 __device__ __forceinline__ void wg_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
@@ -377,6 +378,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     if (ctid == 0) tc::mbar_arrive(bar(B_SRDY));
     bool s_exact = false;   // S0 operand holds exact codes with scale s_scale
     float s_scale = 1.f;
+    float i8s[2] = {0.f, 0.f};   // INT8: this row's two block scales of the last QDQ'd state
     for (int64_t c = 0; c < nchunks; ++c) {
       const int s = (int)(c & 1);
       const int L = chunk_len(c);
@@ -510,6 +512,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
               const float sc = int8_scale(m), rc = __frcp_rn(sc);
 #pragma unroll
               for (int j = 0; j < kInt8BlockCols; ++j) s1[b0 + j] = int8_qdq_rcp(s1[b0 + j], rc, sc);
+              i8s[b0 / kInt8BlockCols] = sc;
             }
           }
 #pragma unroll
@@ -542,6 +545,17 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       float4* out = reinterpret_cast<float4*>(p.hT + sb + (int64_t)lane128 * p.dv);
 #pragma unroll
       for (int j = 0; j < 64; j += 4) out[j >> 2] = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+    if (live() && p.sscale) {   // the final state was QDQ'd iff its last token was a 64th token
+      const bool q = len > 0 && len % 64 == 0;
+      const int64_t unit = (int64_t)n * p.Hv + h;
+      if (p.state_qdq == 2) {
+        float* dst = p.sscale + (unit * 128 + lane128) * (p.dv / kInt8BlockCols) + slab * 2;
+        dst[0] = q ? i8s[0] : 0.f;
+        dst[1] = q ? i8s[1] : 0.f;
+      } else if (ctid == 0) {
+        p.sscale[unit * nslab + slab] = q ? s_scale : 0.f;
+      }
     }
   }
 
@@ -619,6 +633,7 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   if (e != cudaSuccess) return e;
   ChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.lens, p.o, p.hT, reinterpret_cast<int*>(ws),
                  p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
+  cp.sscale = p.state_scales;
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, twt, ttt, cp);

@@ -74,6 +74,7 @@ struct KdaChainParams {
   int T, Hqk, Hv, dv;
   float scale;
   int state_qdq, w_qdq;
+  float* sscale;   // final-state QDQ scales or null (layout: ChunkProblem::state_scales)
 };
 
 __device__ __forceinline__ void wg_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
@@ -372,6 +373,7 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
     if (ctid == 0) tc::mbar_arrive(bar(B_SRDY0));
     bool s_exact = false;
     float s_scale = 1.f;
+    float i8s[2] = {0.f, 0.f};   // INT8: this row's two block scales of the last QDQ'd state
     for (int64_t c = 0; c < nchunks; ++c) {
       const int L = chunk_len(c);
       const uint32_t par = (uint32_t)(c & 1);
@@ -484,6 +486,7 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
             const float sc = int8_scale(m), rc = __frcp_rn(sc);
 #pragma unroll
             for (int j = 0; j < kInt8BlockCols; ++j) s1[b0 + j] = int8_qdq_rcp(s1[b0 + j], rc, sc);
+            i8s[b0 / kInt8BlockCols] = sc;
           }
         }
 #pragma unroll
@@ -519,6 +522,17 @@ chunk_chain_kda_kernel(const __grid_constant__ CUtensorMap tv, const __grid_cons
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
       if (ctid == 0) tc::mbar_arrive(bar(par ? B_SRDY0 : B_SRDY1));   // S0 of chunk c + 1 is stored
+    }
+    if (live() && p.sscale) {   // the final state was QDQ'd iff its last token was a 64th token
+      const bool q = len > 0 && len % 64 == 0;
+      const int64_t unit = (int64_t)n * p.Hv + h;
+      if (p.state_qdq == 2) {
+        float* dst = p.sscale + (unit * 128 + lane128) * (p.dv / kInt8BlockCols) + slab * 2;
+        dst[0] = q ? i8s[0] : 0.f;
+        dst[1] = q ? i8s[1] : 0.f;
+      } else if (ctid == 0) {
+        p.sscale[unit * nslab + slab] = q ? s_scale : 0.f;
+      }
     }
   }
 
@@ -584,6 +598,7 @@ cudaError_t launch_kda_split(const ChunkProblem& p, void* ws, cudaStream_t strea
   if (e != cudaSuccess) return e;
   KdaChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.lens, p.o, p.hT,
                     reinterpret_cast<int*>(ws), p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
+  cp.sscale = p.state_scales;
   e = cudaFuncSetAttribute(chunk_chain_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   chunk_chain_kda_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tv, twt, ttt, tpp, tqd, tkd, cp);

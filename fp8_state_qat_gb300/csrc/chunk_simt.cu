@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
     sm.S[c][j] = p.h0 ? p.h0[sbase + (int64_t)c * p.dv + j] : 0.f;
   }
 
+  constexpr int kTM = DK / 16;
+  float last_s = 0.f, last_i8[kTM][2];   // scales of the last QDQ'd state (E4M3 tile; INT8 blocks)
+#pragma unroll
+  for (int a = 0; a < kTM; ++a) last_i8[a][0] = last_i8[a][1] = 0.f;
   for (int64_t c0 = 0; c0 < len; c0 += C) {
     const int L = (len - c0) < C ? (int)(len - c0) : C;
     __syncthreads();
@@ -359,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
 #pragma unroll
           for (int b = 0; b < 4; ++b) m = fmaxf(m, fabsf(sacc[a][b]));
         const float s = qdq_scale(block_max(m, sm.red));
+        last_s = s;
 #pragma unroll
         for (int a = 0; a < TM; ++a)
 #pragma unroll
@@ -375,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             const float sc = int8_scale(m), rc = __frcp_rn(sc);
+            last_i8[a][blk] = sc;
             sacc[a][2 * blk] = int8_qdq_rcp(sacc[a][2 * blk], rc, sc);
             sacc[a][2 * blk + 1] = int8_qdq_rcp(sacc[a][2 * blk + 1], rc, sc);
           }
@@ -390,6 +396,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkProblem p)
     for (int e = tid; e < DK * SL; e += kThreads) {
       const int c = e / SL, j = e % SL;
       p.hT[sbase + (int64_t)c * p.dv + j] = sm.S[c][j];
+    }
+  }
+  if (p.state_scales) {   // the final state was QDQ'd iff its last token was a 64th token
+    const bool q = len > 0 && len % C == 0;
+    const int64_t unit = (int64_t)n * p.Hv + h;
+    if (p.state_qdq == 2) {
+      if (tx == 0) {
+#pragma unroll
+        for (int a = 0; a < kTM; ++a) {
+          float* dst = p.state_scales + (unit * DK + ty + 16 * a) * (p.dv / kInt8BlockCols) + slab * 2;
+          dst[0] = q ? last_i8[a][0] : 0.f;
+          dst[1] = q ? last_i8[a][1] : 0.f;
+        }
+      }
+    } else if (tid == 0) {
+      p.state_scales[unit * nslab + slab] = q ? last_s : 0.f;
     }
   }
 }

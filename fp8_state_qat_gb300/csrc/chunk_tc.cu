@@ -77,6 +77,7 @@ struct TcParams {
   int T, Hqk, Hv, dv;
   float scale;
   int state_qdq, w_qdq;
+  float* sscale = nullptr;   // final-state QDQ scales or null (layout: ChunkProblem::state_scales)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -170,6 +171,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
   }
   bool s_exact = false;   // S operand holds exact codes (one bf16 pass) with scale s_scale
   float s_scale = 1.f;
+  float i8s = 0.f;        // INT8: the scale of this thread's block (row, 32 columns) in the last QDQ'd state
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -614,6 +616,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
           const float sc = int8_scale(m), rc = __frcp_rn(sc);
 #pragma unroll
           for (int j = 0; j < 32; ++j) s0[j] = int8_qdq_rcp(s0[j], rc, sc);
+          i8s = sc;
         }
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
@@ -665,6 +668,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
     for (int j = 0; j < 32; j += 4) out[j >> 2] = make_float4(s0[j], s0[j + 1], s0[j + 2], s0[j + 3]);
   }
+  if (!aborted && p.sscale) {   // the final state was QDQ'd iff its last token was a 64th token
+    const bool q = len > 0 && len % 64 == 0;
+    const int64_t unit = (int64_t)n * p.Hv + h;
+    if (p.state_qdq == 2)
+      p.sscale[(unit * 128 + lane128) * (p.dv / kInt8BlockCols) + slab * 2 + half] = q ? i8s : 0.f;
+    else if (tid == 0)
+      p.sscale[unit * nslab + slab] = q ? s_scale : 0.f;
+  }
   if (aborted) {
     if (tid == 0) atomicExch(p.status, 1);
     // the TMA of the last issued chunk may still be in flight: wait for it (bounded)
@@ -691,6 +702,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, int* status, cudaStream_t str
       !make_bf16_map(&tv, p.v, p.dv, p.Hv, tmap))
     return cudaErrorInvalidValue;
   TcParams tp{p.g, p.beta, p.h0, p.cu, p.o, p.hT, status, p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
+  tp.sscale = p.state_scales;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   chunk_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tp);

@@ -92,6 +92,15 @@ gdn_status validate_chunk(const gdn_chunk_args* a, bool kda) {
       overlaps(a->o, no, a->hT, st))
     return GDN_ERR_INVALID_ARG;
   if (a->hT && a->h0 && a->hT != a->h0 && overlaps(a->hT, st, a->h0, st)) return GDN_ERR_INVALID_ARG;
+  if (a->state_scales) {   // final-state QDQ scales: only with the state quantizer on
+    if (!(a->flags & GDN_FLAG_STATE_QDQ) || !aligned(a->state_scales, 4)) return GDN_ERR_INVALID_ARG;
+    const size_t ns = (a->flags & GDN_FLAG_STATE_INT8)
+                          ? (size_t)a->N * a->Hv * a->dk * ((a->dv + 31) / 32) * 4
+                          : (size_t)a->N * a->Hv * ((a->dv + 63) / 64) * 4;
+    if (overlaps(a->state_scales, ns, a->o, no) || overlaps(a->state_scales, ns, a->hT, st) ||
+        overlaps(a->state_scales, ns, a->h0, st))
+      return GDN_ERR_INVALID_ARG;
+  }
   return GDN_OK;
 }
 
@@ -108,6 +117,7 @@ gdn_status chunk_fwd(const gdn_chunk_args* a, void* ws, size_t ws_bytes, cudaStr
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
                  state_codec(a->flags), (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
   p.cu_host = a->cu_seqlens ? a->cu_seqlens_host : nullptr;
+  p.state_scales = a->state_scales;
   // dk = 128: the two-kernel path (parallel prep, then the state chain) when the workspace
   // holds its staging, else (GDN) the single fused kernel; other shapes and KDA with a small
   // workspace: CUDA cores
@@ -139,6 +149,7 @@ ChunkProblem problem_of(const gdn_chunk_args* a, bool kda) {
                  a->B, a->T, a->N, a->Hqk, a->Hv, a->dk, a->dv, a->scale,
                  state_codec(a->flags), (a->flags & GDN_FLAG_W_QDQ) ? 1 : 0, kda ? 1 : 0};
   p.cu_host = a->cu_seqlens ? a->cu_seqlens_host : nullptr;
+  p.state_scales = a->state_scales;
   return p;
 }
 
@@ -165,7 +176,9 @@ gdn_status prefill_decode(const gdn_chunk_args* a, const int32_t* plens, void* w
     return GDN_ERR_CUDA;
   // the prefix: chunked, W QDQ as asked, no state QDQ
   const int state_qdq = p.state_qdq;
+  float* const state_scales = p.state_scales;
   p.state_qdq = 0;
+  p.state_scales = nullptr;   // the prefix leaves its state unquantized; the decode part writes the scales
   p.lens = lens;
   p.lens_host = plens;
   cudaError_t e;
@@ -178,6 +191,7 @@ gdn_status prefill_decode(const gdn_chunk_args* a, const int32_t* plens, void* w
   if (e != cudaSuccess) return GDN_ERR_CUDA;
   // the handoff and the decode tokens
   p.state_qdq = state_qdq;
+  p.state_scales = state_scales;
   return gdn::launch_handoff_suffix(p, lens, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

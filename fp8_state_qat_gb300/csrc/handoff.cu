@@ -73,8 +73,8 @@ __device__ __forceinline__ void stage_token(TokenBuf<DK, DV, KDA>& buf, const __
 // elementwise work runs as paired fp32 operations (fma / mul .f32x2, each lane rounded like
 // its scalar form).
 template <int DK, int DV>
-__device__ __forceinline__ void qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb)[DK / 8], float amax, float* wmax,
-                                               int warp, int lane) {
+__device__ __forceinline__ float qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb)[DK / 8], float amax, float* wmax,
+                                                int warp, int lane) {
   constexpr int RPT = DK / 8;
   amax = warp_max(amax);
   if (lane == 0) wmax[warp] = amax;
@@ -89,6 +89,7 @@ __device__ __forceinline__ void qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb
     sa[i] = __fmul2_rn(static_cast<float2>(ca), sc2);
     sb[i] = __fmul2_rn(static_cast<float2>(cb), sc2);
   }
+  return sc;
 }
 
 // INT8 block QDQ of the state registers (state_qdq == 2): one block = one key row x 32 value
@@ -96,7 +97,7 @@ __device__ __forceinline__ void qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb
 // caller keeps a barrier between one call's reads of rmax and the next call's writes.
 template <int DK, int DV>
 __device__ __forceinline__ void int8_state_regs(float2 (&sa)[DK / 8], float2 (&sb)[DK / 8], float (*rmax)[DK],
-                                                int warp, int rg, int cg) {
+                                                int warp, int rg, int cg, float* srow) {
   constexpr int RPT = DK / 8;
   float m[RPT];
 #pragma unroll
@@ -123,6 +124,7 @@ __device__ __forceinline__ void int8_state_regs(float2 (&sa)[DK / 8], float2 (&s
   for (int i = 0; i < RPT; ++i) {
     const int src = (lane & ~3) | (i & 3);
     const float sc = __shfl_sync(0xffffffffu, scl[i >> 2], src), rc = __shfl_sync(0xffffffffu, rcl[i >> 2], src);
+    if (srow) srow[(rg + 8 * i) * (DV / kInt8BlockCols)] = sc;   // the final state's scales
     sa[i] = make_float2(int8_qdq_rcp(sa[i].x, rc, sc), int8_qdq_rcp(sa[i].y, rc, sc));
     sb[i] = make_float2(int8_qdq_rcp(sb[i].x, rc, sc), int8_qdq_rcp(sb[i].y, rc, sc));
   }
@@ -134,7 +136,7 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
                       const __nv_bfloat16* __restrict__ v, const float* __restrict__ g,
                       const float* __restrict__ beta, const int32_t* __restrict__ cu,
                       const int32_t* __restrict__ plens, float* __restrict__ state, float* __restrict__ o, int T,
-                      int Hqk, int Hv, float scale, int state_qdq) {
+                      int Hqk, int Hv, float scale, int state_qdq, float* __restrict__ sscale) {
   constexpr int NW = DV / 16;
   constexpr int RPT = DK / 8;
   __shared__ float wmax[2][NW];
@@ -146,10 +148,24 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const int64_t t0 = cu ? (int64_t)cu[n] : (int64_t)n * T;
   const int64_t len = cu ? (int64_t)cu[n + 1] - t0 : (int64_t)T;
   const int64_t P = plens[n];
-  if (P >= len) return;   // no decode tokens: the prefill state stays as it is
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = lane >> 2, cg = lane & 3;
   const int col = warp * 16 + cg * 4;
+  // final-state scales (layout: ChunkProblem::state_scales): E4M3 by lane 0 of each tile's first
+  // warp; INT8 by the cg = 0 lanes of each block's first warp (rows rg + 8 i), inside the last QDQ
+  float* const i8dst = (sscale && state_qdq == 2 && cg == 0 && (warp & 1) == 0)
+                           ? sscale + unit * DK * (DV / kInt8BlockCols) + warp / 2
+                           : nullptr;
+  float last_tile = 0.f;
+  if (P >= len) {   // no decode tokens: the prefill state stays as it is, not QDQ'd
+    if (i8dst) {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) i8dst[(rg + 8 * i) * (DV / kInt8BlockCols)] = 0.f;
+    } else if (sscale && state_qdq != 2 && lane == 0 && (warp & 3) == 0) {
+      sscale[unit * (DV / 64) + warp / 4] = 0.f;
+    }
+    return;
+  }
 
   float* S = state + unit * (int64_t)(DK * DV);
   float2 sa[RPT], sb[RPT];
@@ -169,9 +185,9 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   }
   int slot = 0;   // the per-tile maxima alternate between two slots, one barrier per QDQ
   if (state_qdq == 2) {
-    int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg);   // the handoff
+    int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg, nullptr);   // the handoff (decode tokens follow)
   } else if (state_qdq) {
-    qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);   // the handoff
+    last_tile = qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);   // the handoff
     slot ^= 1;
   }
 
@@ -233,13 +249,14 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
       *reinterpret_cast<float4*>(o + ((t0 + t) * Hv + h) * DV + col) =
           make_float4(scale * oa.x, scale * oa.y, scale * ob.x, scale * ob.y);
     if (state_qdq == 2) {
-      int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg);
+      int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg, t + 1 == len ? i8dst : nullptr);
     } else if (state_qdq) {
-      qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);
+      last_tile = qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);
       slot ^= 1;
     }
   }
   cp_wait<0>();   // nothing may still be landing in shared memory when the CTA exits
+  if (sscale && state_qdq != 2 && lane == 0 && (warp & 3) == 0) sscale[unit * (DV / 64) + warp / 4] = last_tile;
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
     *reinterpret_cast<float4*>(S + (rg + 8 * i) * DV + col) = make_float4(sa[i].x, sa[i].y, sb[i].x, sb[i].y);
@@ -251,7 +268,7 @@ cudaError_t launch_t(const ChunkProblem& p, const int32_t* plens, cudaStream_t s
   if (units == 0) return cudaSuccess;
   handoff_suffix_kernel<DK, DV, KDA><<<(unsigned)units, DV * 2, 0, stream>>>(
       (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, (const __nv_bfloat16*)p.v, p.g, p.beta, p.cu, plens, p.hT,
-      p.o, p.T, p.Hqk, p.Hv, p.scale, p.state_qdq);
+      p.o, p.T, p.Hqk, p.Hv, p.scale, p.state_qdq, p.state_scales);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,9 @@ struct ChunkProblem {
   // host copy), or null for whole sequences: the prefill part of a prefill -> decode handoff.
   const int32_t* lens = nullptr;
   const int32_t* lens_host = nullptr;
+  // Scales of the final state's QDQ, or null: E4M3 (state_qdq 1) fp32 [N, Hv, dv / 64] per tile,
+  // INT8 (state_qdq 2) fp32 [N, Hv, dk, dv / 32] per block; 0 where the final state was not QDQ'd.
+  float* state_scales = nullptr;
 };
 
 cudaError_t launch_tile_qdq(const float* x, float* y, float* scales, int64_t lead, int rows, int cols,

@@ -49,7 +49,7 @@ class ChunkArgs(ctypes.Structure):
                 ("o", ctypes.c_void_p), ("hT", ctypes.c_void_p),
                 ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("N", ctypes.c_int32), ("Hqk", ctypes.c_int32),
                 ("Hv", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
+                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32), ("state_scales", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -160,7 +160,8 @@ def chunk_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False,
     return workspace_bytes(a, kda)
 
 
-def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state, codec="e4m3"):
+def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state, codec="e4m3",
+                state_scales=None):
     q = _dev(q, torch.bfloat16, "q")
     k = _dev(k, torch.bfloat16, "k")
     v = _dev(v, torch.bfloat16, "v")
@@ -183,16 +184,17 @@ def _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT
         hT = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
     flags = _state_flags(state_qdq, codec) | (GDN_FLAG_W_QDQ if w_qdq else 0)
     # the host copy of cu_seqlens must outlive the call: it is returned with the args
+    state_scales = _dev(state_scales, torch.float32, "state_scales")
     a = ChunkArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_dev), _ptr(cu_host),
-                  _ptr(o), _ptr(hT), B, T, N, Hqk, Hv, dk, dv, float(scale), flags)
+                  _ptr(o), _ptr(hT), B, T, N, Hqk, Hv, dk, dv, float(scale), flags, _ptr(state_scales))
     return a, (o, hT), (cu_host, cu_dev)
 
 
 def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, output_final_state,
-           workspace, stream, codec="e4m3"):
+           workspace, stream, codec="e4m3", state_scales=None):
     lib = load()
     a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
-                                    output_final_state, codec)
+                                    output_final_state, codec, state_scales)
     dev = o.device
     need = workspace_bytes(a, fn_name == "kda_chunk_fwd")
     if workspace is None:
@@ -203,20 +205,24 @@ def _chunk(fn_name, q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False, w_qdq=False, scale=1.0,
-                  o=None, hT=None, output_final_state=True, workspace=None, stream=None, codec="e4m3"):
+                  o=None, hT=None, output_final_state=True, workspace=None, stream=None, codec="e4m3",
+                  state_scales=None):
     """Chunked GDN forward. q, k [B,T,Hqk,dk] bf16; v [B,T,Hv,dv] bf16; g, beta [B,T,Hv] fp32;
     h0 [N,Hv,dk,dv] fp32 or None; cu_seqlens int32 [N+1] (CPU or CUDA) or None; codec: the state
-    QDQ format, "e4m3" (tiles) or "int8" (blocks of 32 value columns per key row).
+    QDQ format, "e4m3" (tiles) or "int8" (blocks of 32 value columns per key row); state_scales:
+    an fp32 CUDA tensor that receives the final state's QDQ scales ([N,Hv,dv/64], INT8
+    [N,Hv,dk,dv/32]; 0 where not QDQ'd) or None.
     Returns (o [B,T,Hv,dv] fp32, hT [N,Hv,dk,dv] fp32 or None)."""
     return _chunk("gdn_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
-                  output_final_state, workspace, stream, codec)
+                  output_final_state, workspace, stream, codec, state_scales)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, state_qdq=False, w_qdq=False, scale=1.0,
-                  o=None, hT=None, output_final_state=True, workspace=None, stream=None, codec="e4m3"):
+                  o=None, hT=None, output_final_state=True, workspace=None, stream=None, codec="e4m3",
+                  state_scales=None):
     """KDA chunked forward: as gdn_chunk_fwd with g [B,T,Hv,dk] (one log-decay per key channel)."""
     return _chunk("kda_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT,
-                  output_final_state, workspace, stream, codec)
+                  output_final_state, workspace, stream, codec, state_scales)
 
 
 def prefill_decode_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_qdq=False, w_qdq=False, kda=False):
@@ -236,9 +242,10 @@ def prefill_decode_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, state_q
 
 
 def _prefill_decode(fn_name, q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq, w_qdq, scale, o, hT,
-                    workspace, stream, codec="e4m3"):
+                    workspace, stream, codec="e4m3", state_scales=None):
     lib = load()
-    a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, True, codec)
+    a, (o, hT), _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, w_qdq, scale, o, hT, True, codec,
+                                    state_scales)
     pl = torch.as_tensor(prefill_lengths, dtype=torch.int32).to("cpu").contiguous().reshape(-1)
     if pl.numel() != a.N:
         raise ValueError(f"prefill_lengths: {pl.numel()} entries for {a.N} sequences")
@@ -254,20 +261,22 @@ def _prefill_decode(fn_name, q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, 
 
 
 def gdn_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, state_qdq=False,
-                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None, codec="e4m3"):
+                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None, codec="e4m3",
+                           state_scales=None):
     """Prefill -> decode handoff: per sequence the first prefill_lengths[n] tokens chunked with no
     state QDQ, then (state_qdq) a QDQ at the handoff and one decode step with state QDQ per
     remaining token. Same tensors as gdn_chunk_fwd; prefill_lengths: N ints (host).
     Returns (o, hT)."""
     return _prefill_decode("gdn_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
-                           w_qdq, scale, o, hT, workspace, stream, codec)
+                           w_qdq, scale, o, hT, workspace, stream, codec, state_scales)
 
 
 def kda_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_lengths=None, *, state_qdq=False,
-                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None, codec="e4m3"):
+                           w_qdq=False, scale=1.0, o=None, hT=None, workspace=None, stream=None, codec="e4m3",
+                           state_scales=None):
     """The handoff schedule for KDA (g [B,T,Hv,dk])."""
     return _prefill_decode("kda_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
-                           w_qdq, scale, o, hT, workspace, stream, codec)
+                           w_qdq, scale, o, hT, workspace, stream, codec, state_scales)
 
 
 def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale=1.0, o=None, stream=None,

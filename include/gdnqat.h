@@ -90,6 +90,11 @@ typedef struct {
   int32_t B, T, N, Hqk, Hv, dk, dv;
   float scale;                 /* multiplies o (1.0 = plain S^T q) */
   uint32_t flags;              /* GDN_FLAG_STATE_QDQ | GDN_FLAG_W_QDQ | GDN_FLAG_STATE_INT8 */
+  float* state_scales;         /* device fp32 or NULL (requires GDN_FLAG_STATE_QDQ): the scales of the
+                                  final state's QDQ -- E4M3 [N, Hv, dv / 64] per tile, INT8 [N, Hv, dk,
+                                  dv / 32] per block; 0 where the final state was not QDQ'd (its last
+                                  token was not a 64th token; a handoff without decode tokens). hT
+                                  then equals code x scale, so a consumer can store hT as codes. */
 } gdn_chunk_args;
 
 /* Smallest workspace gdn_chunk_fwd / kda_chunk_fwd accept: the device status word of the

@@ -201,3 +201,13 @@ def test_int8_codec_flags_and_standalone_validation(so):
     assert so.int8_block_qdq(P(FAKE), P(FAKE), None, 2, 64, 0, None) == B.GDN_ERR_INVALID_ARG
     assert so.int8_block_qdq(P(FAKE), P(FAKE + 4), None, 2, 64, 32, None) == B.GDN_ERR_INVALID_ARG   # overlap
     assert so.int8_block_qdq(P(FAKE), P(FAKE), None, -1, 64, 32, None) == B.GDN_ERR_INVALID_ARG
+
+
+def test_state_scales_validation(so):
+    """The optional final-state scales need the state quantizer, 4-byte alignment and no overlap
+    with o, h0 or hT."""
+    assert call_chunk(so, good_args(flags=B.GDN_FLAG_W_QDQ, state_scales=FAKE + (10 << 32))) == B.GDN_ERR_INVALID_ARG
+    assert call_chunk(so, good_args(state_scales=FAKE + (10 << 32) + 2)) == B.GDN_ERR_INVALID_ARG
+    assert call_chunk(so, good_args(state_scales=FAKE + (5 << 32) + 64)) == B.GDN_ERR_INVALID_ARG   # inside o
+    if not torch.cuda.is_available():
+        assert call_chunk(so, good_args(state_scales=FAKE + (10 << 32))) == B.GDN_ERR_UNSUPPORTED_ARCH
