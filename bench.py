@@ -184,6 +184,26 @@ def job_rate(units_per_rank, world, ms):
     return world * units_per_rank / (ms * 1e-3)
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name, else implementer / part), and the ISA."""
+    import platform
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "CPU part"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    name = line.split(":", 1)[1].strip()
+                    break
+            if name:
+                name = f"{key} {name}" if key == "CPU part" else name
+                break
+    except OSError:
+        pass
+    return f"{platform.machine()} {name}".strip()
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -235,7 +255,8 @@ def cpu_baseline(x, target_s=15.0):
     dt, toks = oracle_sample(x, oracle_inputs(x, s["T"]), units, cores)
     return {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{units} of {total_units} (sequence, head) units x all {s['T']} tokens, chunked fp64 "
-                      f"oracle with state+W QDQ, {cores} threads, {dt:.2f} s wall"}
+                      f"oracle with state+W QDQ, {cores} threads, {dt:.2f} s wall",
+            "single_core_value": (512 / s["Hv"]) / dt1, "cpu": cpu_model()}
 
 
 def run_reference(args):
