@@ -11,13 +11,16 @@ from .gdnqat import (  # noqa: F401
     GDN_FLAG_W_QDQ,
     ChunkArgs,
     GdnError,
+    chunk_bwd_workspace_bytes,
     chunk_workspace_bytes,
     fp8_tile_qdq,
     gdn_check_device_status,
+    gdn_chunk_bwd,
     gdn_chunk_fwd,
     gdn_decode_step,
     gdn_prefill_decode_fwd,
     int8_block_qdq,
+    kda_chunk_bwd,
     kda_chunk_fwd,
     kda_prefill_decode_fwd,
     lib_path,

@@ -58,7 +58,7 @@ bool dv_ok(int dv) { return dv == 64 || dv == 128 || dv == 256; }
 constexpr size_t kWorkspaceBytes = gdn::kStatusBytes;   // device status word (+ padding to one line)
 static_assert(kWorkspaceBytes == GDN_CHUNK_MIN_WORKSPACE_BYTES, "the header's minimum must match");
 
-gdn_status validate_chunk(const gdn_chunk_args* a, bool kda) {
+gdn_status validate_chunk(const gdn_chunk_args* a, bool kda, bool need_o = true) {
   if (!a) return GDN_ERR_INVALID_ARG;
   if (a->B < 0 || a->T < 0 || a->N < 0 || a->Hqk <= 0 || a->Hv <= 0 || a->dk <= 0 || a->dv <= 0)
     return GDN_ERR_INVALID_ARG;
@@ -76,7 +76,7 @@ gdn_status validate_chunk(const gdn_chunk_args* a, bool kda) {
     return GDN_ERR_INVALID_ARG;
   }
   if (tokens > 0) {
-    if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->o) return GDN_ERR_INVALID_ARG;
+    if (!a->q || !a->k || !a->v || !a->g || !a->beta || (need_o && !a->o)) return GDN_ERR_INVALID_ARG;
     if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
         !aligned(a->g, 4) || !aligned(a->beta, 4))
       return GDN_ERR_INVALID_ARG;
@@ -195,9 +195,56 @@ gdn_status prefill_decode(const gdn_chunk_args* a, const int32_t* plens, void* w
   return gdn::launch_handoff_suffix(p, lens, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// ---- backward ----
+bool bwd_shape_ok(const gdn_chunk_args* a) { return !(a->flags & GDN_FLAG_W_QDQ); }
+
+gdn_status chunk_bwd(const gdn_chunk_args* a, const gdn_chunk_grads* gr, void* ws, size_t ws_bytes,
+                     cudaStream_t stream, bool kda) {
+  gdn_status s = validate_chunk(a, kda, false);
+  if (s != GDN_OK) return s;
+  // the straight-through gradient of W QDQ lives in the chunked form, which this backward does not take
+  if (!bwd_shape_ok(a) || a->state_scales) return GDN_ERR_INVALID_ARG;
+  if (!gr) return GDN_ERR_INVALID_ARG;
+  const int64_t tokens = (int64_t)a->B * a->T;
+  if (tokens > 0) {
+    if (!gr->dout || !gr->dq || !gr->dk || !gr->dv || !gr->dg || !gr->dbeta) return GDN_ERR_INVALID_ARG;
+    if (!aligned(gr->dout, 16) || !aligned(gr->dv, 16) || !aligned(gr->dq, 4) || !aligned(gr->dk, 4) ||
+        !aligned(gr->dg, 4) || !aligned(gr->dbeta, 4))
+      return GDN_ERR_INVALID_ARG;
+  }
+  if ((gr->dhT && !aligned(gr->dhT, 16)) || (gr->dh0 && !aligned(gr->dh0, 16))) return GDN_ERR_INVALID_ARG;
+  ChunkProblem p = problem_of(a, kda);
+  p.state_scales = nullptr;
+  if (!ws || ws_bytes < gdn::chunk_bwd_layout(p).total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return GDN_ERR_INVALID_ARG;
+  s = check_device();
+  if (s != GDN_OK) return s;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return GDN_ERR_CUDA;
+  const gdn::BwdGrads g{gr->dout, gr->dhT, gr->dq, gr->dk, gr->dv, gr->dg, gr->dbeta, gr->dh0};
+  return gdn::launch_chunk_bwd(p, g, ws, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+size_t bwd_workspace(const gdn_chunk_args* a, bool kda) {
+  if (validate_chunk(a, kda, false) != GDN_OK || !bwd_shape_ok(a)) return 0;
+  return gdn::chunk_bwd_layout(problem_of(a, kda)).total;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t gdn_chunk_bwd_workspace_size(const gdn_chunk_args* args) { return bwd_workspace(args, false); }
+size_t kda_chunk_bwd_workspace_size(const gdn_chunk_args* args) { return bwd_workspace(args, true); }
+
+gdn_status gdn_chunk_bwd(const gdn_chunk_args* args, const gdn_chunk_grads* grads, void* workspace,
+                         size_t workspace_bytes, gdn_stream_t stream) {
+  return chunk_bwd(args, grads, workspace, workspace_bytes, (cudaStream_t)stream, false);
+}
+
+gdn_status kda_chunk_bwd(const gdn_chunk_args* args, const gdn_chunk_grads* grads, void* workspace,
+                         size_t workspace_bytes, gdn_stream_t stream) {
+  return chunk_bwd(args, grads, workspace, workspace_bytes, (cudaStream_t)stream, true);
+}
 
 size_t gdn_prefill_decode_workspace_size(const gdn_chunk_args* args) {
   if (validate_chunk(args, false) != GDN_OK) return 0;

@@ -105,4 +105,23 @@ cudaError_t launch_chunk_simt(const ChunkProblem& p, cudaStream_t stream);
 // into hT. plens: device [N]; the state stays in registers across the tokens.
 cudaError_t launch_handoff_suffix(const ChunkProblem& p, const int32_t* plens, cudaStream_t stream);
 
+// ---- backward with straight-through state QDQ (CUDA cores, recurrent form) ----
+struct BwdGrads {
+  const float* dout;   // [tokens, Hv, dv]
+  const float* dhT;    // [N, Hv, dk, dv] or null (zero)
+  float* dq;           // [tokens, Hqk, dk]
+  float* dk;           // [tokens, Hqk, dk]
+  float* dv;           // [tokens, Hv, dv]
+  float* dg;           // [tokens, Hv] (KDA [tokens, Hv, dk])
+  float* dbeta;        // [tokens, Hv]
+  float* dh0;          // [N, Hv, dk, dv] or null
+};
+// workspace: status word, the state entering every chunk (per chunk slot and v-head), one
+// 64-state scratch per CTA, and with GQA the per-v-head dq / dk before the head sums
+struct BwdLayout {
+  size_t off_ckpt, off_scratch, off_part, total;
+};
+BwdLayout chunk_bwd_layout(const ChunkProblem& p);
+cudaError_t launch_chunk_bwd(const ChunkProblem& p, const BwdGrads& gr, void* ws, cudaStream_t stream);
+
 }  // namespace gdn

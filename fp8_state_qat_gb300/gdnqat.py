@@ -32,6 +32,7 @@ GDN_FLAG_STATE_INT8 = 8
 EXPORTED = ("gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
             "kda_chunk_fwd_workspace_size", "kda_chunk_fwd",
             "gdn_prefill_decode_workspace_size", "gdn_prefill_decode_fwd",
+            "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd",
             "kda_prefill_decode_workspace_size", "kda_prefill_decode_fwd",
             "gdn_decode_step", "fp8_tile_qdq", "int8_block_qdq", "gdn_status_string", "gdn_check_device_status")
 
@@ -50,6 +51,11 @@ class ChunkArgs(ctypes.Structure):
                 ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("N", ctypes.c_int32), ("Hqk", ctypes.c_int32),
                 ("Hv", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("flags", ctypes.c_uint32), ("state_scales", ctypes.c_void_p)]
+
+
+class ChunkGrads(ctypes.Structure):
+    _fields_ = [("dout", ctypes.c_void_p), ("dhT", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+                ("dv", ctypes.c_void_p), ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p), ("dh0", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -79,6 +85,12 @@ def load(build_if_missing: bool = True):
         for fn in ("gdn_chunk_fwd", "kda_chunk_fwd"):
             getattr(lib, fn).restype = ctypes.c_int
             getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, ctypes.c_size_t, P]
+        for fn in ("gdn_chunk_bwd_workspace_size", "kda_chunk_bwd_workspace_size"):
+            getattr(lib, fn).restype = ctypes.c_size_t
+            getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs)]
+        for fn in ("gdn_chunk_bwd", "kda_chunk_bwd"):
+            getattr(lib, fn).restype = ctypes.c_int
+            getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), ctypes.POINTER(ChunkGrads), P, ctypes.c_size_t, P]
         for fn in ("gdn_prefill_decode_fwd", "kda_prefill_decode_fwd"):
             getattr(lib, fn).restype = ctypes.c_int
             getattr(lib, fn).argtypes = [ctypes.POINTER(ChunkArgs), P, P, ctypes.c_size_t, P]
@@ -277,6 +289,63 @@ def kda_prefill_decode_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, prefill_l
     """The handoff schedule for KDA (g [B,T,Hv,dk])."""
     return _prefill_decode("kda_prefill_decode_fwd", q, k, v, g, beta, h0, cu_seqlens, prefill_lengths, state_qdq,
                            w_qdq, scale, o, hT, workspace, stream, codec, state_scales)
+
+
+def _chunk_bwd(fn_name, q, k, v, g, beta, h0, cu_seqlens, dout, dhT, state_qdq, scale, codec, want_dh0, workspace,
+               stream):
+    lib = load()
+    dev = q.device
+    # the forward's arguments (o and hT are not read by the backward)
+    a, _, _keep = _chunk_args(q, k, v, g, beta, h0, cu_seqlens, state_qdq, False, scale,
+                              torch.empty(0, device=dev), None, False, codec)
+    a.o = None
+    dout = _dev(dout, torch.float32, "dout")
+    dhT = _dev(dhT, torch.float32, "dhT")
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    dg = torch.empty(g.shape, dtype=torch.float32, device=dev)
+    dbeta = torch.empty(beta.shape, dtype=torch.float32, device=dev)
+    dh0 = torch.empty((a.N, a.Hv, a.dk, a.dv), dtype=torch.float32, device=dev) if want_dh0 else None
+    gr = ChunkGrads(_ptr(dout), _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0))
+    size_fn = fn_name + "_workspace_size"
+    need = int(getattr(lib, size_fn)(ctypes.byref(a)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = getattr(lib, fn_name)(ctypes.byref(a), ctypes.byref(gr), _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(fn_name, st)
+    return dq, dk, dv, dg, dbeta, dh0
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, h0=None, cu_seqlens=None, dout=None, dhT=None, *, state_qdq=False, scale=1.0,
+                  codec="e4m3", want_dh0=True, workspace=None, stream=None):
+    """Gradients of <o, dout> + <hT, dhT> for the forward with straight-through state QDQ (no W QDQ).
+    Inputs as gdn_chunk_fwd; dout [B,T,Hv,dv] fp32; dhT [N,Hv,dk,dv] fp32 or None.
+    Returns (dq, dk, dv, dg, dbeta, dh0) fp32 (dh0 None unless want_dh0)."""
+    return _chunk_bwd("gdn_chunk_bwd", q, k, v, g, beta, h0, cu_seqlens, dout, dhT, state_qdq, scale, codec, want_dh0,
+                      workspace, stream)
+
+
+def kda_chunk_bwd(q, k, v, g, beta, h0=None, cu_seqlens=None, dout=None, dhT=None, *, state_qdq=False, scale=1.0,
+                  codec="e4m3", want_dh0=True, workspace=None, stream=None):
+    """The KDA backward (g and dg [B,T,Hv,dk])."""
+    return _chunk_bwd("kda_chunk_bwd", q, k, v, g, beta, h0, cu_seqlens, dout, dhT, state_qdq, scale, codec, want_dh0,
+                      workspace, stream)
+
+
+def chunk_bwd_workspace_bytes(q_shape, v_shape, cu_seqlens=None, *, kda=False):
+    """gdn_chunk_bwd_workspace_size (kda: kda_chunk_bwd_workspace_size) for these shapes."""
+    B, T, Hqk, dk = q_shape
+    Hv, dv = v_shape[2], v_shape[3]
+    cu_host, N = None, B
+    if cu_seqlens is not None:
+        cu_host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+        N = cu_host.numel() - 1
+    fake = [ctypes.c_void_p((1 << 44) + (i << 38)) for i in range(10)]
+    a = ChunkArgs(fake[0], fake[1], fake[2], fake[3], fake[4], None, fake[6] if cu_host is not None else None,
+                  _ptr(cu_host), None, None, B, T, N, Hqk, Hv, dk, dv, 1.0, GDN_FLAG_STATE_QDQ)
+    fn = "kda_chunk_bwd_workspace_size" if kda else "gdn_chunk_bwd_workspace_size"
+    return int(getattr(load(), fn)(ctypes.byref(a)))
 
 
 def gdn_decode_step(q, k, v, g, beta, state, *, state_qdq=True, kda=False, scale=1.0, o=None, stream=None,

@@ -158,6 +158,42 @@ size_t kda_chunk_fwd_workspace_size(const gdn_chunk_args* args);
 gdn_status kda_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t workspace_bytes,
                          gdn_stream_t stream);
 
+/* Gradients of the forward with straight-through state QDQ ("Torch GDN/KDA decode QAT with INT8
+ * recurrent state", "Megatron-Core QAT/QAD workflow" step 4: recurrent surrogate gradients,
+ * identity straight-through estimator through QDQ; [F]: identity straight-through gradients).
+ * For L = <o, dout> + <hT, dhT>, the derivatives of the token recurrence whose forward values
+ * carry the state QDQ of GDN_FLAG_STATE_QDQ (either codec) and whose backward treats that QDQ as
+ * the identity. All device fp32: dout [B, T, Hv, dv] (16-byte aligned); dhT [N, Hv, dk, dv] or NULL
+ * (zero); outputs dq, dk [B, T, Hqk, dk] (summed over the value heads that share a q/k head),
+ * dv [B, T, Hv, dv] (16-byte aligned), dg [B, T, Hv] (kda_chunk_bwd: [B, T, Hv, dk]),
+ * dbeta [B, T, Hv], dh0 [N, Hv, dk, dv] or NULL. */
+typedef struct {
+  const float* dout;
+  const float* dhT;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dg;
+  float* dbeta;
+  float* dh0;
+} gdn_chunk_grads;
+
+/* Workspace of gdn_chunk_bwd (0 for invalid arguments): the status word, the state entering every
+ * 64-token chunk (per chunk slot and v-head), a 64-state scratch per CTA (at most 152 CTAs), and
+ * with GQA the per-value-head dq / dk before their sums. */
+size_t gdn_chunk_bwd_workspace_size(const gdn_chunk_args* args);
+/* The backward on CUDA cores: per (sequence, head) a forward pass that stores the chunk-entry
+ * states, then the chunks in reverse, each recomputed and walked token by token with the state
+ * gradient in registers. args: the forward's inputs and flags (o, hT unused and may be NULL);
+ * GDN_FLAG_W_QDQ and state_scales are refused (GDN_ERR_INVALID_ARG): the straight-through gradient
+ * of the W QDQ belongs to the chunked form, which this backward does not take. */
+gdn_status gdn_chunk_bwd(const gdn_chunk_args* args, const gdn_chunk_grads* grads, void* workspace,
+                         size_t workspace_bytes, gdn_stream_t stream);
+/* KDA (g [B, T, Hv, dk], dg [B, T, Hv, dk]). */
+size_t kda_chunk_bwd_workspace_size(const gdn_chunk_args* args);
+gdn_status kda_chunk_bwd(const gdn_chunk_args* args, const gdn_chunk_grads* grads, void* workspace,
+                         size_t workspace_bytes, gdn_stream_t stream);
+
 /* Prefill -> decode handoff ([H]: "Torch GDN/KDA decode QAT with INT8 recurrent state",
  * "Megatron-Core QAT/QAD workflow", steps 2-3 and the "Ordinary state-QDQ path" flowchart).
  * Per sequence n of length L_n, the first P_n = prefill_lengths_host[n] tokens run as chunked

@@ -211,3 +211,25 @@ def test_state_scales_validation(so):
     assert call_chunk(so, good_args(state_scales=FAKE + (5 << 32) + 64)) == B.GDN_ERR_INVALID_ARG   # inside o
     if not torch.cuda.is_available():
         assert call_chunk(so, good_args(state_scales=FAKE + (10 << 32))) == B.GDN_ERR_UNSUPPORTED_ARCH
+
+
+def test_backward_validation(so):
+    """The backward refuses W QDQ (its straight-through gradient belongs to the chunked form) and
+    missing gradient buffers; its workspace covers the chunk-entry states and the per-CTA scratch."""
+    P = ctypes.c_void_p
+    a = good_args(flags=B.GDN_FLAG_STATE_QDQ, o=None)
+    need = so.gdn_chunk_bwd_workspace_size(ctypes.byref(a))
+    slots = (a.B * a.T) // 64 + a.N
+    state = a.dk * a.dv * 4
+    assert need >= 256 + slots * a.Hv * state + min(a.N * a.Hv, 152) * 64 * state
+    assert so.gdn_chunk_bwd_workspace_size(ctypes.byref(good_args(flags=3))) == 0        # W QDQ
+    assert so.kda_chunk_bwd_workspace_size(ctypes.byref(a)) == need
+    g = B.ChunkGrads(*[P(FAKE + ((11 + i) << 32)) for i in range(8)])
+    fn = so.gdn_chunk_bwd
+    assert fn(ctypes.byref(good_args(flags=3, o=None)), ctypes.byref(g), P(FAKE + (7 << 32)), need,
+              None) == B.GDN_ERR_INVALID_ARG
+    g_missing = B.ChunkGrads(*[P(FAKE + ((11 + i) << 32)) for i in range(2)], None)
+    assert fn(ctypes.byref(a), ctypes.byref(g_missing), P(FAKE + (7 << 32)), need, None) == B.GDN_ERR_INVALID_ARG
+    assert fn(ctypes.byref(a), ctypes.byref(g), P(FAKE + (7 << 32)), need - 1, None) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+    if not torch.cuda.is_available():
+        assert fn(ctypes.byref(a), ctypes.byref(g), P(FAKE + (7 << 32)), need, None) == B.GDN_ERR_UNSUPPORTED_ARCH

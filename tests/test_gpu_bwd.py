@@ -1,0 +1,67 @@
+"""gdn_chunk_bwd / kda_chunk_bwd on the GPU against the fp64 gradient oracle.
+
+The backward of the token recurrence with the state QDQ in the forward values and the identity in
+the backward ("Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD
+workflow" step 4; "GDN state/W QAT foundation": identity straight-through gradients). Bounds
+(relative L2 per gradient tensor): 1e-3 with the state quantizer off; 2e-2 with it on (an fp32 and
+an fp64 forward state can round to neighbouring codes at a boundary).
+"""
+import numpy as np
+import pytest
+import torch
+
+from fp8_state_qat_gb300 import workloads
+from helpers import TOL_OFF, TOL_QDQ, rel, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+def run(gdn, oracle_mod, x, state_qdq, codec="e4m3", with_dhT=True, seed=0):
+    from oracle.grad import gdn_recurrent_grads
+    gen = torch.Generator().manual_seed(seed)
+    B, T = x.q.shape[:2]
+    N, Hv, dk, dv = x.shape["N"], x.shape["Hv"], x.shape["dk"], x.shape["dv"]
+    dout = torch.randn((B, T, Hv, dv), generator=gen)
+    dhT = torch.randn((N, Hv, dk, dv), generator=gen) if with_dhT else None
+    c = to_cuda(x)
+    fn = gdn.kda_chunk_bwd if x.kda else gdn.gdn_chunk_bwd
+    got = fn(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], x.cu_seqlens, dout.cuda(),
+             None if dhT is None else dhT.cuda(), state_qdq=state_qdq, codec=codec)
+    torch.cuda.synchronize()
+    ref = gdn_recurrent_grads(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, dout.double(),
+                              None if dhT is None else dhT.double(), kda=x.kda, state_qdq=state_qdq, codec=codec)[:6]
+    tol = TOL_QDQ if state_qdq else TOL_OFF
+    for name, a, b in zip(NAMES, got, ref):
+        if b.size == 0 or not np.any(b):
+            continue
+        e = rel(a.cpu().double().numpy(), b)
+        assert e <= tol, (name, e)
+
+
+@pytest.mark.parametrize("kda", [False, True])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (128, 64), (64, 256)])
+def test_bwd_shapes_no_qdq(gdn, oracle_mod, kda, dk, dv):
+    x = workloads.prefill(1, 0, 2, 4, dk, dv, seed=80 + dk + dv + kda, kda=kda, h0_std=0.1, seqlens=[0, 1, 63, 64, 130])
+    run(gdn, oracle_mod, x, False, seed=1)
+
+
+@pytest.mark.parametrize("kda", [False, True])
+@pytest.mark.parametrize("codec", ["e4m3", "int8"])
+def test_bwd_state_qdq(gdn, oracle_mod, kda, codec):
+    x = workloads.prefill(1, 0, 1, 2, 128, 128, seed=90 + kda, kda=kda, h0_std=0.1, seqlens=[64, 150, 20])
+    run(gdn, oracle_mod, x, True, codec=codec, seed=2)
+
+
+def test_bwd_dense_no_final_grad(gdn, oracle_mod):
+    x = workloads.prefill(2, 96, 2, 2, 128, 128, seed=95, h0_std=0.1)
+    run(gdn, oracle_mod, x, True, with_dhT=False, seed=3)
+
+
+def test_bwd_refuses_w_qdq(gdn):
+    x = workloads.prefill(1, 64, 1, 1, 64, 64, seed=96)
+    c = to_cuda(x)
+    a, _, _ = gdn.gdnqat._chunk_args(c["q"], c["k"], c["v"], c["g"], c["beta"], None, None, True, True, 1.0,
+                                     torch.empty(0, device="cuda"), None, False)
+    assert gdn.load().gdn_chunk_bwd_workspace_size(__import__("ctypes").byref(a)) == 0
