@@ -398,6 +398,67 @@ class PrefillCase:
         return c
 
 
+class BwdCase(PrefillCase):
+    """One step = one gdn_chunk_bwd over the workload (the gradients of <o, dout> for the forward
+    with straight-through state QDQ); inputs and dout resident, two alternating sets."""
+
+    def __init__(self, x, dev, torch, gdn):
+        super().__init__(x, dev, torch, gdn)
+        s = self.s
+        gen = torch.Generator().manual_seed(11)
+        self.dout_h = torch.randn((s["B"], s["T"], s["Hv"], s["dv"]), generator=gen)
+        for b in self.sets:
+            b["dout"] = self.dout_h.to(dev)
+        self.fn = gdn.kda_chunk_bwd if x.kda else gdn.gdn_chunk_bwd
+        tok, Hv, Hqk, dk, dv = self.tokens, s["Hv"], s["Hqk"], s["dk"], s["dv"]
+        gk = dk if x.kda else 1
+        # in: q, k (per q/k head), v, g, beta, dout, h0; out: dq, dk (per q/k head), dv, dg, dbeta, dh0
+        self.bytes = tok * (Hqk * 2 * dk * 2 + Hv * (2 * dv + 4 * gk + 4 + 4 * dv)) + \
+            tok * (Hqk * 2 * dk * 4 + Hv * (4 * dv + 4 * gk + 4)) + \
+            (2 if x.h0 is not None else 1) * s["N"] * Hv * dk * dv * 4
+        # two forward passes (the checkpointing pass and the per-chunk recompute) and the backward
+        self.flops = tok * Hv * (2 * 7 + 12) * dk * dv
+        self.launches = 1 + (2 if Hv != Hqk else 0)
+
+    def scope(self):
+        return "one step = chunk_bwd_kernel" + (" + 2 sum_heads_kernel" if self.launches > 1 else "")
+
+    def workspace_bytes(self):
+        return self.gdn.chunk_bwd_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu, kda=self.x.kda)
+
+    def step(self, i, ws, stream):
+        b = self.sets[i & 1]
+        b["grads"] = self.fn(b["q"], b["k"], b["v"], b["g"], b["beta"], b["h0"], self.cu, b["dout"],
+                             state_qdq=self.x.state_qdq, workspace=ws, stream=stream)
+
+    def host(self):
+        x = self.x
+        inp = dict(q=x.q, k=x.k, v=x.v, g=x.g, beta=x.beta, dout=self.dout_h)
+        if x.h0 is not None:
+            inp["h0"] = x.h0
+        self.h_in = {k: t.pin_memory() for k, t in inp.items()}
+        s = self.s
+        shapes = dict(dq=x.q.shape, dk=x.k.shape, dv=x.v.shape, dg=x.g.shape, dbeta=x.beta.shape,
+                      dh0=(s["N"], s["Hv"], s["dk"], s["dv"]))
+        self.h_out = [{k: self.torch.empty(sh, dtype=self.torch.float32).pin_memory() for k, sh in shapes.items()}
+                      for _ in range(2)]
+        return (sum(t.numel() * t.element_size() for t in self.h_in.values()),
+                sum(t.numel() * 4 for t in self.h_out[0].values()))
+
+    def run(self, slot, ws, stream):
+        self.step(slot, ws, stream)
+
+    def d2h(self, slot):
+        got = dict(zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), self.sets[slot]["grads"]))
+        for k, t in self.h_out[slot].items():
+            t.copy_(got[k], non_blocking=True)
+
+    def config(self):
+        c = super().config()
+        c["pass"] = "backward, straight-through state QDQ"
+        return c
+
+
 class DecodeCase:
     """One step = one decode token for every (sequence, head); the state stays resident and is
     updated in place; the 64 token sets of the workload are cycled."""
@@ -515,6 +576,7 @@ METRICS = {
     "gdn_decode_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token FP8 state QDQ)",
     "qdq_state_n512_h32_d128": "standalone FP8 tile QDQ elements/s (16384 x [128 x 128] fp32, 64-column tiles)",
     "int8_state_n512_h32_d128": "standalone INT8 block QDQ elements/s (16384 x [128 x 128] fp32, 32-column blocks)",
+    "gdn_bwd_b4_h16_t4096_d128": "GDN backward tokens/s (B4 H16 T4096 d128, straight-through FP8 state QDQ)",
     "gdn_decode_int8_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token INT8 block-32 state QDQ)",
     "gdn_b1_h2_t256_d64": "GDN chunked-prefill tokens/s (B1 H2 T256 d64, FP8 state QDQ)",
     "handoff_n256_t128_p64_h16_d128": "GDN prefill->decode handoff tokens/s (256 seqs x 128 tokens, 64-token "
@@ -544,6 +606,8 @@ def run_gpu(args):
         case = DecodeCase(x, dev, torch, gdn)
     elif isinstance(x, workloads.QdqInputs):
         case = QdqCase(x, dev, torch, gdn)
+    elif x.backward:
+        case = BwdCase(x, dev, torch, gdn)
     else:
         case = PrefillCase(x, dev, torch, gdn)
     ws = torch.empty(max(case.workspace_bytes(), 1 << 16), dtype=torch.uint8, device=dev)

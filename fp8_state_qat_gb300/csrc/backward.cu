@@ -13,14 +13,18 @@
 //   dP' = dS - k du^T,  dg = (dL/da) a = <dP', P> a = <dP', P'> (KDA: per key row),  dS_{t-1} = a o dP'.
 // After the first token, dS is dh0.
 //
-// One CTA per (sequence, head) unit at a time (a persistent grid walks the units), with the
-// decode kernel's thread layout (warp w owns value columns [16 w, 16 w + 16); lane 4 rg + cg
-// holds rows rg + 8 i and 4 columns): the first pass runs the forward recurrence, QDQ included,
-// and stores the state entering every 64-token chunk; the second pass takes the chunks in reverse,
-// recomputes the chunk's 64 token states into the CTA's scratch, then walks its tokens backward
-// with dS in registers. Column sums (over key rows) are warp shuffles; row sums (over value
-// columns) go through shared memory, one barrier per token. With GQA the per-v-head dq / dk go to
-// the workspace and a second kernel sums each q/k head's value heads in a fixed order.
+// Apart from the state QDQ (a tile or block spans columns) and the quantities summed over the value
+// columns (dq, dk, db, dg), the recurrence and its backward are column-local, so the work splits
+// into one CTA per (sequence, head, 64-column value slab) -- the E4M3 tile width, so the forward
+// QDQ stays CTA-local -- and a persistent grid walks those units, two CTAs per SM. Each CTA uses the
+// decode kernel's thread layout (warp w owns slab columns [16 w, 16 w + 16); lane 4 rg + cg holds
+// rows rg + 8 i and 4 columns): the first pass runs the forward recurrence, QDQ included, and
+// stores the state entering every 64-token chunk; the second pass takes the chunks in reverse,
+// recomputes the chunk's token states into the CTA's scratch, then walks its tokens backward with
+// dS in registers. Column sums (over key rows) are warp shuffles; row sums (over the slab's
+// columns) go through shared memory. The slab partials of dq, dk, db and dg land in the workspace
+// and a second kernel sums them -- over slabs, and with GQA over the value heads that share a q/k
+// head -- in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -37,30 +41,33 @@ struct BwdParams {
   const int32_t* cu;
   const float* dout;    // [tokens, Hv, dv]
   const float* dhT;     // [N, Hv, dk, dv] or null
-  float* dq;            // [tokens, Hqk or Hv, dk]: the output, or the per-v-head partial (GQA)
-  float* dk;            // same
-  float* dv;            // [tokens, Hv, dv]
-  float* dg;            // [tokens, Hv] (KDA [tokens, Hv, dk])
-  float* dbeta;         // [tokens, Hv]
+  float* part_q;        // [slabs][tokens, Hv, dk]: per-slab, per-v-head dq
+  float* part_k;        // same for dk
+  float* part_b;        // [slabs][tokens, Hv]: db
+  float* part_g;        // [slabs][tokens, Hv] (KDA [slabs][tokens, Hv, dk]): dg
+  float* grad_v;        // [tokens, Hv, dv]
   float* dh0;           // [N, Hv, dk, dv] or null
   float* ckpt;          // per (chunk slot, v-head): the state entering the chunk
-  float* scratch;       // per CTA: the 64 states before the tokens of the current chunk
-  int T, N, Hqk, Hv;
+  float* scratch;       // per CTA: the 64 slab states before the tokens of the current chunk
+  int64_t tokens;
+  int T, N, Hqk, Hv, dv;
   float scale;
   int state_qdq;
-  int qk_heads_out;     // Hqk (direct output) or Hv (per-v-head partials)
 };
 
-template <int DK, int DV>
+constexpr int SL = 64;        // value columns per CTA (one E4M3 tile)
+constexpr int NW = SL / 16;   // warps per CTA
+
+template <int DK>
 struct BwdSmem {
-  float rs[DV / 16][DK][4];   // per warp, per key row: partial row sums
-  float tot[DV / 16][2];      // per warp partial full sums
-  float wmax[DV / 16];
-  float rmax[DV / 16][DK];
+  float rs[NW][DK][4];   // per warp, per key row: partial row sums
+  float tot[NW][2];      // per warp partial full sums
+  float wmax[NW];
+  float rmax[NW][DK];
 };
 
 // ---- the forward step on the register state (decode layout) ----
-template <int DK, int DV, bool KDA>
+template <int DK, bool KDA>
 __device__ __forceinline__ void load_token(const BwdParams& p, int64_t tok, int h, int hq, int rg, int col,
                                            float* kr, float* qr, float* ar, float& b, float4& vv, float4& dov) {
   constexpr int RPT = DK / 8;
@@ -80,10 +87,10 @@ __device__ __forceinline__ void load_token(const BwdParams& p, int64_t tok, int 
     for (int i = 0; i < RPT; ++i) ar[i] = a;
   }
   b = p.beta[tok * p.Hv + h];
-  const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(p.v + (tok * p.Hv + h) * DV + col);
+  const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(p.v + (tok * p.Hv + h) * p.dv + col);
   const float2 v01 = __bfloat1622float2(vp[0]), v23 = __bfloat1622float2(vp[1]);
   vv = make_float4(v01.x, v01.y, v23.x, v23.y);
-  dov = *reinterpret_cast<const float4*>(p.dout + (tok * p.Hv + h) * DV + col);
+  dov = *reinterpret_cast<const float4*>(p.dout + (tok * p.Hv + h) * p.dv + col);
 }
 
 // column sums over the key rows of this warp's 4 columns per lane: partial over RPT rows, then the
@@ -119,8 +126,8 @@ __device__ __forceinline__ void fwd_step(float4 (&s)[DK / 8], const float* kr, c
 
 // the forward's state QDQ on the register state (E4M3 tiles of 64 columns = 4 warps; INT8 blocks
 // of one row x 32 columns = two warps); one barrier
-template <int DK, int DV>
-__device__ __forceinline__ void state_qdq(float4 (&s)[DK / 8], int codec, BwdSmem<DK, DV>& sm, int warp, int lane,
+template <int DK>
+__device__ __forceinline__ void state_qdq(float4 (&s)[DK / 8], int codec, BwdSmem<DK>& sm, int warp, int lane,
                                           int rg, int cg) {
   constexpr int RPT = DK / 8;
   if (codec == 2) {
@@ -147,8 +154,7 @@ __device__ __forceinline__ void state_qdq(float4 (&s)[DK / 8], int codec, BwdSme
     amax = warp_max(amax);
     if (lane == 0) sm.wmax[warp] = amax;
     __syncthreads();
-    const int w0 = (warp / 4) * 4;
-    const float tmax = fmaxf(fmaxf(sm.wmax[w0], sm.wmax[w0 + 1]), fmaxf(sm.wmax[w0 + 2], sm.wmax[w0 + 3]));
+    const float tmax = fmaxf(fmaxf(sm.wmax[0], sm.wmax[1]), fmaxf(sm.wmax[2], sm.wmax[3]));   // the slab
     const float sc = qdq_scale(tmax), rc = __frcp_rn(sc);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
@@ -161,26 +167,30 @@ __device__ __forceinline__ void state_qdq(float4 (&s)[DK / 8], int codec, BwdSme
   __syncthreads();   // the next QDQ's shared-memory writes come after every thread's reads
 }
 
-template <int DK, int DV, bool KDA>
-__global__ void __launch_bounds__(DV * 2, 1) chunk_bwd_kernel(const BwdParams p) {
-  constexpr int NW = DV / 16;
+template <int DK, bool KDA>
+__global__ void __launch_bounds__(SL * 2, 2) chunk_bwd_kernel(const BwdParams p) {
   constexpr int RPT = DK / 8;
-  __shared__ BwdSmem<DK, DV> sm;
+  __shared__ BwdSmem<DK> sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = lane >> 2, cg = lane & 3;
-  const int col = warp * 16 + cg * 4;
-  const int64_t units = (int64_t)p.N * p.Hv;
-  float* const scr = p.scratch + (int64_t)blockIdx.x * 64 * DK * DV;
-  auto at = [&](float* base, int i) { return reinterpret_cast<float4*>(base + (rg + 8 * i) * DV + col); };
+  const int nslab = p.dv / SL;
+  const int64_t units = (int64_t)p.N * p.Hv * nslab;
+  float* const scr = p.scratch + (int64_t)blockIdx.x * 64 * DK * SL;
+  auto sat = [&](int r, int i) { return reinterpret_cast<float4*>(scr + ((int64_t)r * DK + rg + 8 * i) * SL + warp * 16 + cg * 4); };
 
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    const int n = (int)(unit / p.Hv), h = (int)(unit % p.Hv);
+    const int slab = (int)(unit % nslab);
+    const int64_t nh = unit / nslab;   // n * Hv + h
+    const int n = (int)(nh / p.Hv), h = (int)(nh % p.Hv);
     const int hq = h / (p.Hv / p.Hqk);
+    const int col = slab * SL + warp * 16 + cg * 4;   // this lane's first value column
     const int64_t t0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * p.T;
     const int64_t len = p.cu ? (int64_t)p.cu[n + 1] - t0 : (int64_t)p.T;
     const int64_t nch = (len + 63) / 64;
     const int64_t slot0 = t0 / 64 + n;
-    auto ck = [&](int64_t c) { return p.ckpt + ((slot0 + c) * p.Hv + h) * (int64_t)(DK * DV); };
+    const int64_t st = (int64_t)DK * p.dv;   // one state
+    auto srow = [&](const float* base, int i) { return base + (int64_t)(rg + 8 * i) * p.dv + col; };
+    auto ck = [&](int64_t c) { return p.ckpt + ((slot0 + c) * p.Hv + h) * st; };
     float kr[RPT], qr[RPT], ar[RPT], b;
     float4 vv, dov;
 
@@ -188,44 +198,42 @@ __global__ void __launch_bounds__(DV * 2, 1) chunk_bwd_kernel(const BwdParams p)
     float4 s[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i)
-      s[i] = p.h0 ? *reinterpret_cast<const float4*>(p.h0 + unit * (DK * DV) + (rg + 8 * i) * DV + col)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      s[i] = p.h0 ? *reinterpret_cast<const float4*>(srow(p.h0 + nh * st, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t t = 0; t < len; ++t) {
       if (t % 64 == 0) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) *at(ck(t / 64), i) = s[i];
+        for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(const_cast<float*>(srow(ck(t / 64), i))) = s[i];
       }
-      load_token<DK, DV, KDA>(p, t0 + t, h, hq, rg, col, kr, qr, ar, b, vv, dov);
+      load_token<DK, KDA>(p, t0 + t, h, hq, rg, col, kr, qr, ar, b, vv, dov);
       fwd_step<DK>(s, kr, ar, b, vv);
-      if (p.state_qdq && (t + 1) % 64 == 0) state_qdq<DK, DV>(s, p.state_qdq, sm, warp, lane, rg, cg);
+      if (p.state_qdq && (t + 1) % 64 == 0) state_qdq<DK>(s, p.state_qdq, sm, warp, lane, rg, cg);
     }
 
     // ---- pass 2: chunks in reverse; dS in registers ----
     float4 ds[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i)
-      ds[i] = p.dhT ? *reinterpret_cast<const float4*>(p.dhT + unit * (DK * DV) + (rg + 8 * i) * DV + col)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      ds[i] = p.dhT ? *reinterpret_cast<const float4*>(srow(p.dhT + nh * st, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t c = nch - 1; c >= 0; --c) {
       const int L = (int)((len - c * 64) < 64 ? (len - c * 64) : 64);
       // the chunk's token states (before each token) into the scratch
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) s[i] = *at(ck(c), i);
+      for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float4*>(srow(ck(c), i));
       for (int r = 0; r < L; ++r) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) *at(scr + (int64_t)r * DK * DV, i) = s[i];
+        for (int i = 0; i < RPT; ++i) *sat(r, i) = s[i];
         if (r + 1 < L) {
-          load_token<DK, DV, KDA>(p, t0 + c * 64 + r, h, hq, rg, col, kr, qr, ar, b, vv, dov);
+          load_token<DK, KDA>(p, t0 + c * 64 + r, h, hq, rg, col, kr, qr, ar, b, vv, dov);
           fwd_step<DK>(s, kr, ar, b, vv);
         }
       }
       for (int r = L - 1; r >= 0; --r) {
         const int64_t tok = t0 + c * 64 + r;
-        load_token<DK, DV, KDA>(p, tok, h, hq, rg, col, kr, qr, ar, b, vv, dov);
+        load_token<DK, KDA>(p, tok, h, hq, rg, col, kr, qr, ar, b, vv, dov);
         float4 pp[RPT];   // P' = a o P
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
-          const float4 P = *at(scr + (int64_t)r * DK * DV, i);
+          const float4 P = *sat(r, i);
           pp[i] = make_float4(ar[i] * P.x, ar[i] * P.y, ar[i] * P.z, ar[i] * P.w);
         }
         // u = v - P'^T k
@@ -249,9 +257,9 @@ __global__ void __launch_bounds__(DV * 2, 1) chunk_bwd_kernel(const BwdParams p)
         }
         du = col_sum(du);
         du = make_float4(b * du.x, b * du.y, b * du.z, b * du.w);
-        if (rg == 0) *reinterpret_cast<float4*>(p.dv + (tok * p.Hv + h) * DV + col) = du;
+        if (rg == 0) *reinterpret_cast<float4*>(p.grad_v + (tok * p.Hv + h) * p.dv + col) = du;
         // row sums over this lane's 4 columns: r0 = S do (S = P' + b k u^T), r1 = dS u, r2 = P' du,
-        // r3 = dP' . P with dP' = dS - k du^T
+        // r3 = dP' . P' with dP' = dS - k du^T
         float r0[RPT], r1[RPT], r2[RPT], r3[RPT];
         const float4 bu = make_float4(b * u.x, b * u.y, b * u.z, b * u.w);
 #pragma unroll
@@ -284,8 +292,9 @@ __global__ void __launch_bounds__(DV * 2, 1) chunk_bwd_kernel(const BwdParams p)
           }
         }
         __syncthreads();
-        // per key row c (threads c < DK): the sums over all warps, in warp order
-        float kb_c = 0.f, da_c = 0.f;
+        // per key row cr (threads cr < DK): the slab's sums over its warps, in warp order
+        const int64_t ph = (int64_t)slab * p.tokens * p.Hv + tok * p.Hv + h;   // slab partial index of (tok, h)
+        float kb_c = 0.f, dg_c = 0.f;
         if (threadIdx.x < DK) {
           const int cr = threadIdx.x;
           float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -294,15 +303,15 @@ __global__ void __launch_bounds__(DV * 2, 1) chunk_bwd_kernel(const BwdParams p)
             a0 += sm.rs[w][cr][0]; a1 += sm.rs[w][cr][1]; a2 += sm.rs[w][cr][2]; a3 += sm.rs[w][cr][3];
           }
           const float kc = bf16_to_f32(p.k[(tok * p.Hqk + hq) * DK + cr]);
-          p.dq[(tok * p.qk_heads_out + (p.qk_heads_out == p.Hv ? h : hq)) * DK + cr] = p.scale * a0;
-          p.dk[(tok * p.qk_heads_out + (p.qk_heads_out == p.Hv ? h : hq)) * DK + cr] = b * a1 - a2;
+          p.part_q[ph * DK + cr] = p.scale * a0;
+          p.part_k[ph * DK + cr] = b * a1 - a2;
           kb_c = kc * a1;   // contribution to db
-          da_c = a3;        // contribution to dg (GDN: summed over the rows)
-          if (KDA) p.dg[(tok * p.Hv + h) * DK + cr] = a3;
+          dg_c = a3;        // contribution to dg (GDN: summed over the rows)
+          if (KDA) p.part_g[ph * DK + cr] = a3;
         }
-        // db and (GDN) da: sums over the key rows (warps 0 .. DK/32 - 1 hold them)
+        // db and (GDN) dg: sums over the key rows (warps 0 .. DK/32 - 1 hold them)
         if (warp < DK / 32) {
-          float x0 = kb_c, x1 = da_c;
+          float x0 = kb_c, x1 = dg_c;
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) {
             x0 += __shfl_xor_sync(0xffffffffu, x0, off);
@@ -315,50 +324,57 @@ __global__ void __launch_bounds__(DV * 2, 1) chunk_bwd_kernel(const BwdParams p)
         }
         __syncthreads();
         if (threadIdx.x == 0) {
-          float db = 0.f, da = 0.f;
+          float db = 0.f, dg = 0.f;
 #pragma unroll
           for (int w = 0; w < DK / 32; ++w) {
             db += sm.tot[w][0];
-            da += sm.tot[w][1];
+            dg += sm.tot[w][1];
           }
-          p.dbeta[tok * p.Hv + h] = db;
-          if (!KDA) p.dg[tok * p.Hv + h] = da;
+          p.part_b[ph] = db;
+          if (!KDA) p.part_g[ph] = dg;
         }
         __syncthreads();   // sm.rs / sm.tot are rewritten by the next token
       }
     }
     if (p.dh0) {
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(p.dh0 + unit * (DK * DV) + (rg + 8 * i) * DV + col) = ds[i];
+      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(p.dh0 + nh * st + (int64_t)(rg + 8 * i) * p.dv + col) = ds[i];
     }
   }
 }
 
-// dq / dk of each q/k head: the sum of its G value heads' partials, in head order
-__global__ void sum_heads_kernel(const float* __restrict__ part, float* __restrict__ out, int64_t tokens, int Hqk,
-                                 int G, int dk) {
-  const int64_t total = tokens * Hqk * dk;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(e % dk);
-    const int64_t th = e / dk;   // tok * Hqk + hq
-    const int hq = (int)(th % Hqk);
-    const int64_t tok = th / Hqk;
+// out[e] = sum over slabs s < nslab and value heads j < G of part[s * slab_stride + src(e, j)],
+// src(e, j) = ((e / inner) G + j) inner + e mod inner (dq / dk: inner = dk, G value heads per q/k
+// head; db, dg: G = 1), in that fixed order
+__global__ void sum_parts_kernel(const float* __restrict__ part, float* __restrict__ out, int64_t n_out, int nslab,
+                                 int64_t slab_stride, int G, int inner) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_out; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t base = (e / inner) * G * inner + e % inner;
     float acc = 0.f;
-    for (int j = 0; j < G; ++j) acc += part[((tok * Hqk + hq) * G + j) * dk + c];
+    for (int s = 0; s < nslab; ++s)
+      for (int j = 0; j < G; ++j) acc += part[s * slab_stride + base + (int64_t)j * inner];
     out[e] = acc;
   }
 }
 
-constexpr int kBwdCtas = 152;   // at most one CTA per GB300 SM; each owns a 64-state scratch
+constexpr int kBwdCtas = 2 * 152;   // two CTAs per GB300 SM at most; each owns a 64-state scratch
 
-template <int DK, int DV, bool KDA>
+template <int DK, bool KDA>
 cudaError_t launch_t(const BwdParams& bp, int64_t units, cudaStream_t stream) {
-  int dev = 0, sms = kBwdCtas;
+  int dev = 0, sms = kBwdCtas / 2;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaGetLastError();
-  int64_t grid = units < sms ? units : sms;
+  int64_t grid = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;
   if (grid > kBwdCtas) grid = kBwdCtas;
-  chunk_bwd_kernel<DK, DV, KDA><<<(unsigned)grid, DV * 2, 0, stream>>>(bp);
+  chunk_bwd_kernel<DK, KDA><<<(unsigned)grid, SL * 2, 0, stream>>>(bp);
+  return cudaGetLastError();
+}
+
+cudaError_t sum_parts(const float* part, float* out, int64_t n_out, int nslab, int64_t slab_stride, int G, int inner,
+                      cudaStream_t stream) {
+  if (n_out == 0) return cudaSuccess;
+  const int64_t blocks = (n_out + 255) / 256 < 152 * 32 ? (n_out + 255) / 256 : 152 * 32;
+  sum_parts_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, out, n_out, nslab, slab_stride, G, inner);
   return cudaGetLastError();
 }
 
@@ -369,45 +385,46 @@ BwdLayout chunk_bwd_layout(const ChunkProblem& p) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const int64_t tokens = (int64_t)p.B * p.T;
   const int64_t slots = tokens / 64 + p.N;
-  const int64_t units = (int64_t)p.N * p.Hv;
-  const size_t state = (size_t)p.dk * p.dv * 4;
+  const int nslab = p.dv / SL;
+  const int64_t units = (int64_t)p.N * p.Hv * nslab;
   const int64_t ctas = units < kBwdCtas ? units : kBwdCtas;
+  const size_t part = (size_t)nslab * tokens * p.Hv * 4;
   l.off_ckpt = up(kStatusBytes);
-  l.off_scratch = up(l.off_ckpt + (size_t)slots * p.Hv * state);
-  l.off_part = up(l.off_scratch + (size_t)ctas * 64 * state);
-  const bool gqa = p.Hv != p.Hqk;
-  const size_t part = gqa ? (size_t)tokens * p.Hv * p.dk * 4 : 0;
-  l.total = up(l.off_part + 2 * part);
+  l.off_scratch = up(l.off_ckpt + (size_t)slots * p.Hv * p.dk * p.dv * 4);
+  l.off_part_q = up(l.off_scratch + (size_t)ctas * 64 * p.dk * SL * 4);
+  l.off_part_k = up(l.off_part_q + part * p.dk);
+  l.off_part_b = up(l.off_part_k + part * p.dk);
+  l.off_part_g = up(l.off_part_b + part);
+  l.total = up(l.off_part_g + part * (p.kda ? p.dk : 1));
   return l;
 }
 
 cudaError_t launch_chunk_bwd(const ChunkProblem& p, const BwdGrads& gr, void* ws, cudaStream_t stream) {
   const BwdLayout lay = chunk_bwd_layout(p);
-  const int64_t units = (int64_t)p.N * p.Hv;
+  const int nslab = p.dv / SL;
+  const int64_t units = (int64_t)p.N * p.Hv * nslab;
   if (units == 0) return cudaSuccess;
   unsigned char* w = static_cast<unsigned char*>(ws);
   const int64_t tokens = (int64_t)p.B * p.T;
-  const bool gqa = p.Hv != p.Hqk;
-  float* pq = gqa ? reinterpret_cast<float*>(w + lay.off_part) : gr.dq;
-  float* pk = gqa ? pq + (size_t)tokens * p.Hv * p.dk : gr.dk;
+  float* pq = reinterpret_cast<float*>(w + lay.off_part_q);
+  float* pk = reinterpret_cast<float*>(w + lay.off_part_k);
+  float* pb = reinterpret_cast<float*>(w + lay.off_part_b);
+  float* pg = reinterpret_cast<float*>(w + lay.off_part_g);
   BwdParams bp{(const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, (const __nv_bfloat16*)p.v, p.g, p.beta, p.h0,
-               p.cu, gr.dout, gr.dhT, pq, pk, gr.dv, gr.dg, gr.dbeta, gr.dh0,
-               reinterpret_cast<float*>(w + lay.off_ckpt), reinterpret_cast<float*>(w + lay.off_scratch),
-               p.T, p.N, p.Hqk, p.Hv, p.scale, p.state_qdq, gqa ? p.Hv : p.Hqk};
+               p.cu, gr.dout, gr.dhT, pq, pk, pb, pg, gr.dv, gr.dh0,
+               reinterpret_cast<float*>(w + lay.off_ckpt), reinterpret_cast<float*>(w + lay.off_scratch), tokens,
+               p.T, p.N, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq};
   cudaError_t e = cudaErrorInvalidValue;
-#define GDN_BWD(DKV, DVV)                                                                    \
-  if (p.dk == DKV && p.dv == DVV)                                                            \
-    e = p.kda ? launch_t<DKV, DVV, true>(bp, units, stream) : launch_t<DKV, DVV, false>(bp, units, stream);
-  GDN_BWD(64, 64) GDN_BWD(64, 128) GDN_BWD(64, 256) GDN_BWD(128, 64) GDN_BWD(128, 128) GDN_BWD(128, 256)
-#undef GDN_BWD
-  if (e != cudaSuccess || !gqa || tokens == 0) return e;
-  const int64_t total = tokens * p.Hqk * p.dk;
-  const int64_t blocks = (total + 255) / 256 < 152 * 32 ? (total + 255) / 256 : 152 * 32;
-  sum_heads_kernel<<<(unsigned)blocks, 256, 0, stream>>>(pq, gr.dq, tokens, p.Hqk, p.Hv / p.Hqk, p.dk);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  sum_heads_kernel<<<(unsigned)blocks, 256, 0, stream>>>(pk, gr.dk, tokens, p.Hqk, p.Hv / p.Hqk, p.dk);
-  return cudaGetLastError();
+  if (p.dk == 64) e = p.kda ? launch_t<64, true>(bp, units, stream) : launch_t<64, false>(bp, units, stream);
+  if (p.dk == 128) e = p.kda ? launch_t<128, true>(bp, units, stream) : launch_t<128, false>(bp, units, stream);
+  if (e != cudaSuccess || tokens == 0) return e;
+  const int G = p.Hv / p.Hqk;
+  const int64_t sh = tokens * p.Hv;   // per-slab stride in (token, v-head) units
+  if ((e = sum_parts(pq, gr.dq, tokens * p.Hqk * p.dk, nslab, sh * p.dk, G, p.dk, stream)) != cudaSuccess) return e;
+  if ((e = sum_parts(pk, gr.dk, tokens * p.Hqk * p.dk, nslab, sh * p.dk, G, p.dk, stream)) != cudaSuccess) return e;
+  if ((e = sum_parts(pb, gr.dbeta, sh, nslab, sh, 1, 1, stream)) != cudaSuccess) return e;
+  const int gk = p.kda ? p.dk : 1;
+  return sum_parts(pg, gr.dg, sh * gk, nslab, sh * gk, 1, 1, stream);
 }
 
 }  // namespace gdn

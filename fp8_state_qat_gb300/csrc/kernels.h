@@ -117,9 +117,9 @@ struct BwdGrads {
   float* dh0;          // [N, Hv, dk, dv] or null
 };
 // workspace: status word, the state entering every chunk (per chunk slot and v-head), one
-// 64-state scratch per CTA, and with GQA the per-v-head dq / dk before the head sums
+// 64-state slab scratch per CTA, and the per-slab, per-v-head dq, dk, db, dg before their sums
 struct BwdLayout {
-  size_t off_ckpt, off_scratch, off_part, total;
+  size_t off_ckpt, off_scratch, off_part_q, off_part_k, off_part_b, off_part_g, total;
 };
 BwdLayout chunk_bwd_layout(const ChunkProblem& p);
 cudaError_t launch_chunk_bwd(const ChunkProblem& p, const BwdGrads& gr, void* ws, cudaStream_t stream);

@@ -38,6 +38,7 @@ class PrefillInputs:
     # prefill -> decode handoff: per sequence, the tokens that run as chunked prefill (the rest
     # run as decode steps); None = plain chunked prefill
     prefill_lengths: Optional[list] = None
+    backward: bool = False   # the workload times the backward pass
 
     @property
     def shape(self):
@@ -106,6 +107,11 @@ def prefill(B, T, Hqk, Hv, dk, dv, *, seed, kda=False, h0_std=None, seqlens=None
                          state_qdq=state_qdq, w_qdq=w_qdq, name=name)
 
 
+def _backward(x: PrefillInputs) -> PrefillInputs:
+    x.backward = True
+    return x
+
+
 def handoff(B, T, P, Hqk, Hv, dk, dv, *, seed, kda=False, name="") -> PrefillInputs:
     """Dense batch whose sequences run their first P tokens as chunked prefill and the rest as
     decode steps; state and W QDQ on, h0 = 0."""
@@ -156,6 +162,11 @@ WORKLOADS = {
     # decode: 512 sequences x 32 heads, 64 single-token steps, QDQ on every write
     "gdn_decode_n512_h32_d128_s64": lambda: decode(64, 512, 32, 128, 128, seed=3, state_std=0.05,
                                                    name="gdn_decode_n512_h32_d128_s64"),
+    # the backward of the prefill benchmark's shape (state QDQ straight through; no W QDQ, whose
+    # straight-through gradient needs the chunked form)
+    "gdn_bwd_b4_h16_t4096_d128": lambda: _backward(prefill(4, 4096, 16, 16, 128, 128, seed=1, h0_std=0.1,
+                                                           state_qdq=True, w_qdq=False,
+                                                           name="gdn_bwd_b4_h16_t4096_d128")),
     # the decode workload with the INT8 block-32 state codec
     "gdn_decode_int8_n512_h32_d128_s64": lambda: decode(64, 512, 32, 128, 128, seed=3, state_std=0.05,
                                                         name="gdn_decode_int8_n512_h32_d128_s64", codec="int8"),

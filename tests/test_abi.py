@@ -215,13 +215,15 @@ def test_state_scales_validation(so):
 
 def test_backward_validation(so):
     """The backward refuses W QDQ (its straight-through gradient belongs to the chunked form) and
-    missing gradient buffers; its workspace covers the chunk-entry states and the per-CTA scratch."""
+    missing gradient buffers; its workspace covers the chunk-entry states and the per-CTA
+    64-column scratch (at most two CTAs per SM)."""
     P = ctypes.c_void_p
     a = good_args(flags=B.GDN_FLAG_STATE_QDQ, o=None)
     need = so.gdn_chunk_bwd_workspace_size(ctypes.byref(a))
     slots = (a.B * a.T) // 64 + a.N
     state = a.dk * a.dv * 4
-    assert need >= 256 + slots * a.Hv * state + min(a.N * a.Hv, 152) * 64 * state
+    slabs = a.dv // 64
+    assert need >= 256 + slots * a.Hv * state + min(a.N * a.Hv * slabs, 304) * 64 * a.dk * 64 * 4
     assert so.gdn_chunk_bwd_workspace_size(ctypes.byref(good_args(flags=3))) == 0        # W QDQ
     assert so.kda_chunk_bwd_workspace_size(ctypes.byref(a)) == need
     g = B.ChunkGrads(*[P(FAKE + ((11 + i) << 32)) for i in range(8)])
