@@ -49,11 +49,13 @@ def _t(x):
 
 
 def gdn_recurrent_grads(q, k, v, g, beta, h0=None, cu_seqlens=None, do=None, dhT=None, *, kda=False,
-                        state_qdq=False, scale=1.0, codec="e4m3", qdq_period=64):
+                        state_qdq=False, scale=1.0, codec="e4m3", qdq_period=64, units=None):
     """Gradients of sum(o * do) + sum(hT * dhT) with respect to q, k, v, g, beta and h0, for the
     recurrence above (layouts of the forward oracle: q, k [B, T, Hqk, dk]; v [B, T, Hv, dv];
     g [B, T, Hv] (KDA [B, T, Hv, dk]); beta [B, T, Hv]; h0, hT [N, Hv, dk, dv]; do like o
-    [B, T, Hv, dv]). Returns fp64 numpy arrays (dq, dk, dv, dg, dbeta, dh0, o, hT)."""
+    [B, T, Hv, dv]). units: a list of (sequence, v-head) pairs to include (the loss then covers only
+    their outputs and final states), or None for all. Returns fp64 numpy arrays
+    (dq, dk, dv, dg, dbeta, dh0, o, hT)."""
     q, k, v, g, beta = (_t(x).requires_grad_(True) for x in (q, k, v, g, beta))
     B, T, Hqk, dk = q.shape
     Hv, dv = v.shape[2], v.shape[3]
@@ -71,8 +73,12 @@ def gdn_recurrent_grads(q, k, v, g, beta, h0=None, cu_seqlens=None, do=None, dhT
     dhT = None if dhT is None else _t(dhT)
     head_of = torch.arange(Hv) // G   # v-head h reads q / k head h / G
     o_rows, hTs, loss = {}, [], torch.zeros((), dtype=torch.float64)
+    keep = None if units is None else set((int(n), int(h)) for n, h in units)
     for n, (b, t0, L) in enumerate(spans):
         for h in range(Hv):
+            if keep is not None and (n, h) not in keep:
+                hTs.append(torch.zeros((dk, dv), dtype=torch.float64))
+                continue
             hq = int(head_of[h])
             S = h0[n, h]
             for t in range(L):

@@ -65,3 +65,26 @@ def test_bwd_refuses_w_qdq(gdn):
     a, _, _ = gdn.gdnqat._chunk_args(c["q"], c["k"], c["v"], c["g"], c["beta"], None, None, True, True, 1.0,
                                      torch.empty(0, device="cuda"), None, False)
     assert gdn.load().gdn_chunk_bwd_workspace_size(__import__("ctypes").byref(a)) == 0
+
+
+def test_bwd_full_size_sampled(gdn, oracle_mod):
+    """The benchmarked backward workload (B4 H16 T4096 d128, state QDQ straight through) in the
+    launch configuration bench.py times; the oracle recomputes two sampled (sequence, head) units
+    over all 4096 tokens (no GQA: each unit's dq and dk are its own)."""
+    from oracle.grad import gdn_recurrent_grads
+    x = workloads.workload("gdn_bwd_b4_h16_t4096_d128")
+    gen = torch.Generator().manual_seed(12)
+    dout = torch.randn((4, 4096, 16, 128), generator=gen)
+    c = to_cuda(x)
+    got = gdn.gdn_chunk_bwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], None, dout.cuda(), state_qdq=True)
+    torch.cuda.synchronize()
+    units = [(1, 5), (3, 12)]
+    ref = gdn_recurrent_grads(x.q, x.k, x.v, x.g, x.beta, x.h0, None, dout.double(), None, state_qdq=True,
+                              units=units)[:6]
+    got = [t.cpu().double().numpy() for t in got]
+    for n, h in units:
+        sel = {"dq": (n, slice(None), h), "dk": (n, slice(None), h), "dv": (n, slice(None), h),
+               "dg": (n, slice(None), h), "dbeta": (n, slice(None), h), "dh0": (n, h)}
+        for name, a, b in zip(NAMES, got, ref):
+            e = rel(a[sel[name]], b[sel[name]])
+            assert e <= TOL_QDQ, (name, n, h, e)
