@@ -69,8 +69,8 @@ def test_bwd_refuses_w_qdq(gdn):
 
 def test_bwd_full_size_sampled(gdn, oracle_mod):
     """The benchmarked backward workload (B4 H16 T4096 d128, state QDQ straight through) in the
-    launch configuration bench.py times; the oracle recomputes two sampled (sequence, head) units
-    over all 4096 tokens (no GQA: each unit's dq and dk are its own)."""
+    launch configuration bench.py times; the oracle recomputes one sampled (sequence, head) unit
+    over all 4096 tokens (fp64 autograd, ~2 minutes; no GQA: the unit's dq and dk are its own)."""
     from oracle.grad import gdn_recurrent_grads
     x = workloads.workload("gdn_bwd_b4_h16_t4096_d128")
     gen = torch.Generator().manual_seed(12)
@@ -78,7 +78,7 @@ def test_bwd_full_size_sampled(gdn, oracle_mod):
     c = to_cuda(x)
     got = gdn.gdn_chunk_bwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], None, dout.cuda(), state_qdq=True)
     torch.cuda.synchronize()
-    units = [(1, 5), (3, 12)]
+    units = [(3, 12)]
     ref = gdn_recurrent_grads(x.q, x.k, x.v, x.g, x.beta, x.h0, None, dout.double(), None, state_qdq=True,
                               units=units)[:6]
     got = [t.cpu().double().numpy() for t in got]
