@@ -77,6 +77,8 @@ PROFILES = {
     "int8_state_n512_h32_d128": ("int8_block_qdq_int8_state_n512_h32_d128.md",
                                  ("qdq.cu", "gdnqat_api.cu", "common.cuh", "tc_epilogue.cuh", "tc_common.cuh",
                                   "kernels.h")),
+    "gdn_bwd_b4_h16_t4096_d128": ("chunk_bwd_gdn_bwd_b4_h16_t4096_d128.md",
+                                  ("backward.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
     "kda_b2_h32_t8192_d128": ("chunk_fwd_kda_b2_h32_t8192_d128.md",
                               ("chunk_prep_kda.cu", "chunk_chain_kda.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh",
                                "tc_common.cuh", "tc_epilogue.cuh", "kernels.h")),
@@ -418,10 +420,10 @@ class BwdCase(PrefillCase):
             (2 if x.h0 is not None else 1) * s["N"] * Hv * dk * dv * 4
         # two forward passes (the checkpointing pass and the per-chunk recompute) and the backward
         self.flops = tok * Hv * (2 * 7 + 12) * dk * dv
-        self.launches = 1 + (2 if Hv != Hqk else 0)
+        self.launches = 5   # the backward kernel and the sums of the dq, dk, dbeta, dg partials
 
     def scope(self):
-        return "one step = chunk_bwd_kernel" + (" + 2 sum_heads_kernel" if self.launches > 1 else "")
+        return "one step = chunk_bwd_kernel + 4 sum_parts_kernel; achieved is over all of them"
 
     def workspace_bytes(self):
         return self.gdn.chunk_bwd_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu, kda=self.x.kda)

@@ -16,15 +16,20 @@
 // Apart from the state QDQ (a tile or block spans columns) and the quantities summed over the value
 // columns (dq, dk, db, dg), the recurrence and its backward are column-local, so the work splits
 // into one CTA per (sequence, head, 64-column value slab) -- the E4M3 tile width, so the forward
-// QDQ stays CTA-local -- and a persistent grid walks those units, two CTAs per SM. Each CTA uses the
-// decode kernel's thread layout (warp w owns slab columns [16 w, 16 w + 16); lane 4 rg + cg holds
-// rows rg + 8 i and 4 columns): the first pass runs the forward recurrence, QDQ included, and
-// stores the state entering every 64-token chunk; the second pass takes the chunks in reverse,
-// recomputes the chunk's token states into the CTA's scratch, then walks its tokens backward with
-// dS in registers. Column sums (over key rows) are warp shuffles; row sums (over the slab's
-// columns) go through shared memory. The slab partials of dq, dk, db and dg land in the workspace
-// and a second kernel sums them -- over slabs, and with GQA over the value heads that share a q/k
-// head -- in a fixed order.
+// QDQ stays CTA-local -- and a persistent grid (one CTA per SM) walks those units. 256 threads:
+// warp w owns slab columns [8 w, 8 w + 8); lane 4 rg + cg holds key rows rg + 8 i and the two
+// columns 8 w + 2 cg, + 1, so a column sum over the key rows is a 3-level xor shuffle.
+//
+// Pass 1 runs the forward recurrence, QDQ included, and stores the state entering every 64-token
+// chunk. Pass 2 takes the chunks in reverse: the chunk's token inputs are staged in shared memory
+// (cp.async), a forward sweep stores the state entering every 4-token sub-chunk in a per-CTA
+// scratch small enough to stay in L2, and then each sub-chunk, last first, is recomputed from its
+// checkpoint -- three states into per-thread shared-memory slots, the fourth left in registers --
+// and walked backward with dS in registers. Per token one barrier: the row sums (over the slab's
+// columns) are reduced within a lane quad by a reduce-scatter, then over the warps through a
+// double-buffered shared array. The slab (and per-warp) partials of dq, dk, db and dg land in the
+// workspace and a second kernel sums them -- over slabs, and with GQA over the value heads that
+// share a q/k head -- in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -43,302 +48,405 @@ struct BwdParams {
   const float* dhT;     // [N, Hv, dk, dv] or null
   float* part_q;        // [slabs][tokens, Hv, dk]: per-slab, per-v-head dq
   float* part_k;        // same for dk
-  float* part_b;        // [slabs][tokens, Hv]: db
-  float* part_g;        // [slabs][tokens, Hv] (KDA [slabs][tokens, Hv, dk]): dg
+  float* part_b;        // [slabs * dk / 32][tokens, Hv]: db per slab and reducing warp
+  float* part_g;        // GDN: as part_b; KDA [slabs][tokens, Hv, dk]: dg
   float* grad_v;        // [tokens, Hv, dv]
   float* dh0;           // [N, Hv, dk, dv] or null
   float* ckpt;          // per (chunk slot, v-head): the state entering the chunk
-  float* scratch;       // per CTA: the 64 slab states before the tokens of the current chunk
+  float* scratch;       // per CTA: the 16 sub-chunk checkpoints of the current chunk (thread-major)
   int64_t tokens;
   int T, N, Hqk, Hv, dv;
   float scale;
   int state_qdq;
 };
 
-constexpr int SL = 64;        // value columns per CTA (one E4M3 tile)
-constexpr int NW = SL / 16;   // warps per CTA
+constexpr int SL = 64;          // value columns per CTA (one E4M3 tile)
+constexpr int NT = 256;         // threads per CTA
+constexpr int NW = NT / 32;     // warps; warp w owns slab columns [8 w, 8 w + 8)
+constexpr int SUB = 4;          // tokens per sub-chunk
+constexpr int NSUB = kChunk / SUB;
 
-template <int DK>
+// One token's inputs in shared memory (byte offsets): k, q (dk bf16 each), the slab's v (bf16) and
+// dout (fp32) columns, the gate(s) (fp32, turned into a = exp(g) after staging), beta.
+template <int DK, bool KDA>
+struct Rec {
+  static constexpr int K = 0, Q = 2 * DK, V = 4 * DK, DO = 4 * DK + 2 * SL, G = 4 * DK + 6 * SL;
+  static constexpr int NG = KDA ? DK : 1;
+  static constexpr int B = G + 4 * NG;
+  static constexpr int BYTES = (B + 4 + 15) / 16 * 16;
+  static constexpr int N16 = DK / 4 + SL / 8 + SL / 4 + (KDA ? DK / 4 : 0);   // 16-byte pieces
+  static constexpr int NP = N16 + (KDA ? 1 : 2);                               // + 4-byte g (GDN), beta
+};
+
+template <int DK, bool KDA>
 struct BwdSmem {
-  float rs[NW][DK][4];   // per warp, per key row: partial row sums
-  float tot[NW][2];      // per warp partial full sums
+  alignas(16) unsigned char stage[kChunk * Rec<DK, KDA>::BYTES];
+  float2 slot[SUB - 1][DK / 8][NT];   // per-thread copies of the sub-chunk's first token states
+  float4 rs[2][NW][DK];               // per token (double-buffered), warp, key row: 4 row sums
   float wmax[NW];
   float rmax[NW][DK];
 };
 
-// ---- the forward step on the register state (decode layout) ----
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Stage tokens tok0 .. tok0 + count - 1 (count <= 64) of head (h, hq), value slab `slab`, into
+// consecutive records at dst; every thread issues its share of the pieces (no commit here).
 template <int DK, bool KDA>
-__device__ __forceinline__ void load_token(const BwdParams& p, int64_t tok, int h, int hq, int rg, int col,
-                                           float* kr, float* qr, float* ar, float& b, float4& vv, float4& dov) {
-  constexpr int RPT = DK / 8;
-  const __nv_bfloat16* kp = p.k + (tok * p.Hqk + hq) * DK;
-  const __nv_bfloat16* qp = p.q + (tok * p.Hqk + hq) * DK;
-#pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    kr[i] = bf16_to_f32(kp[rg + 8 * i]);
-    qr[i] = bf16_to_f32(qp[rg + 8 * i]);
+__device__ __forceinline__ void stage_tokens(const BwdParams& p, unsigned char* dst, int64_t tok0, int count, int h,
+                                             int hq, int slab) {
+  using R = Rec<DK, KDA>;
+  for (int e = threadIdx.x; e < count * R::NP; e += NT) {
+    const int r = e / R::NP;
+    int j = e - r * R::NP;
+    const int64_t tok = tok0 + r, th = tok * p.Hv + h;
+    unsigned char* d = dst + r * R::BYTES;
+    if (j < DK / 8) { cp16(d + R::K + 16 * j, p.k + (tok * p.Hqk + hq) * DK + 8 * j); continue; }
+    j -= DK / 8;
+    if (j < DK / 8) { cp16(d + R::Q + 16 * j, p.q + (tok * p.Hqk + hq) * DK + 8 * j); continue; }
+    j -= DK / 8;
+    if (j < SL / 8) { cp16(d + R::V + 16 * j, p.v + th * p.dv + slab * SL + 8 * j); continue; }
+    j -= SL / 8;
+    if (j < SL / 4) { cp16(d + R::DO + 16 * j, p.dout + th * p.dv + slab * SL + 4 * j); continue; }
+    j -= SL / 4;
+    if (KDA) {
+      if (j < DK / 4) { cp16(d + R::G + 16 * j, p.g + th * DK + 4 * j); continue; }
+      j -= DK / 4;
+    } else {
+      if (j == 0) { cp4(d + R::G, p.g + th); continue; }
+      j -= 1;
+    }
+    cp4(d + R::B, p.beta + th);
   }
-  if (KDA) {
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) ar[i] = expf(p.g[(tok * p.Hv + h) * DK + rg + 8 * i]);
-  } else {
-    const float a = expf(p.g[tok * p.Hv + h]);
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) ar[i] = a;
-  }
-  b = p.beta[tok * p.Hv + h];
-  const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(p.v + (tok * p.Hv + h) * p.dv + col);
-  const float2 v01 = __bfloat1622float2(vp[0]), v23 = __bfloat1622float2(vp[1]);
-  vv = make_float4(v01.x, v01.y, v23.x, v23.y);
-  dov = *reinterpret_cast<const float4*>(p.dout + (tok * p.Hv + h) * p.dv + col);
 }
 
-// column sums over the key rows of this warp's 4 columns per lane: partial over RPT rows, then the
-// 8 row groups (lane bits 2..4)
-__device__ __forceinline__ float4 col_sum(float4 x) {
+// g -> a = exp(g) in `count` staged records (after the copies are visible to every thread)
+template <int DK, bool KDA>
+__device__ __forceinline__ void exp_gates(unsigned char* rec0, int count) {
+  using R = Rec<DK, KDA>;
+  for (int e = threadIdx.x; e < count * R::NG; e += NT) {
+    const int r = e / R::NG;
+    float* gp = reinterpret_cast<float*>(rec0 + r * R::BYTES + R::G) + (e - r * R::NG);
+    *gp = expf(*gp);
+  }
+}
+
+// This thread's view of one staged token: k, q and a on its key rows; beta; v and dout on its columns.
+template <int DK>
+struct TokView {
+  float kr[DK / 8], qr[DK / 8], ar[DK / 8];
+  float b;
+  float2 vv, dov;
+};
+
+template <int DK, bool KDA>
+__device__ __forceinline__ void read_token(const unsigned char* rec, int rg, int c0, bool need_q, TokView<DK>& t) {
+  using R = Rec<DK, KDA>;
+  constexpr int RPT = DK / 8;
+  const __nv_bfloat16* kk = reinterpret_cast<const __nv_bfloat16*>(rec + R::K);
+  const __nv_bfloat16* qq = reinterpret_cast<const __nv_bfloat16*>(rec + R::Q);
+  const float* ga = reinterpret_cast<const float*>(rec + R::G);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    t.kr[i] = bf16_to_f32(kk[rg + 8 * i]);
+    if (need_q) t.qr[i] = bf16_to_f32(qq[rg + 8 * i]);
+    t.ar[i] = KDA ? ga[rg + 8 * i] : ga[0];
+  }
+  t.b = *reinterpret_cast<const float*>(rec + R::B);
+  t.vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(rec + R::V + 2 * c0));
+  t.dov = *reinterpret_cast<const float2*>(rec + R::DO + 4 * c0);
+}
+
+// column sums over the key rows: partial over this lane's rows, then the 8 row groups (lane bits 2..4)
+__device__ __forceinline__ float2 col_sum(float2 x) {
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
-    x.x += __shfl_xor_sync(0xffffffffu, x.x, off); x.y += __shfl_xor_sync(0xffffffffu, x.y, off);
-    x.z += __shfl_xor_sync(0xffffffffu, x.z, off); x.w += __shfl_xor_sync(0xffffffffu, x.w, off);
+    x.x += __shfl_xor_sync(0xffffffffu, x.x, off);
+    x.y += __shfl_xor_sync(0xffffffffu, x.y, off);
   }
   return x;
 }
 
-// S <- a S + b k (v - (a S)^T k)^T for one token (P' and u as in the header); returns u
+// S <- a S + b k (v - (a S)^T k)^T for one token
 template <int DK>
-__device__ __forceinline__ void fwd_step(float4 (&s)[DK / 8], const float* kr, const float* ar, float b, float4 vv) {
+__device__ __forceinline__ void fwd_step(float2 (&s)[DK / 8], const TokView<DK>& t) {
   constexpr int RPT = DK / 8;
-  float4 pk = make_float4(0.f, 0.f, 0.f, 0.f);
+  float2 pk = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    s[i].x *= ar[i]; s[i].y *= ar[i]; s[i].z *= ar[i]; s[i].w *= ar[i];
-    pk.x = fmaf(s[i].x, kr[i], pk.x); pk.y = fmaf(s[i].y, kr[i], pk.y);
-    pk.z = fmaf(s[i].z, kr[i], pk.z); pk.w = fmaf(s[i].w, kr[i], pk.w);
+    s[i].x *= t.ar[i]; s[i].y *= t.ar[i];
+    pk.x = fmaf(s[i].x, t.kr[i], pk.x); pk.y = fmaf(s[i].y, t.kr[i], pk.y);
   }
   pk = col_sum(pk);
-  const float4 d = make_float4(b * (vv.x - pk.x), b * (vv.y - pk.y), b * (vv.z - pk.z), b * (vv.w - pk.w));
+  const float2 d = make_float2(t.b * (t.vv.x - pk.x), t.b * (t.vv.y - pk.y));
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    s[i].x = fmaf(kr[i], d.x, s[i].x); s[i].y = fmaf(kr[i], d.y, s[i].y);
-    s[i].z = fmaf(kr[i], d.z, s[i].z); s[i].w = fmaf(kr[i], d.w, s[i].w);
+    s[i].x = fmaf(t.kr[i], d.x, s[i].x); s[i].y = fmaf(t.kr[i], d.y, s[i].y);
   }
 }
 
-// the forward's state QDQ on the register state (E4M3 tiles of 64 columns = 4 warps; INT8 blocks
-// of one row x 32 columns = two warps); one barrier
-template <int DK>
-__device__ __forceinline__ void state_qdq(float4 (&s)[DK / 8], int codec, BwdSmem<DK>& sm, int warp, int lane,
+// the forward's state QDQ on the register state (E4M3: the slab is one tile, all 8 warps; INT8: a
+// block is one key row of 32 columns = warps 4 b .. 4 b + 3); barriers on both sides of the exchange
+template <int DK, bool KDA>
+__device__ __forceinline__ void state_qdq(float2 (&s)[DK / 8], int codec, BwdSmem<DK, KDA>& sm, int warp, int lane,
                                           int rg, int cg) {
   constexpr int RPT = DK / 8;
   if (codec == 2) {
     float m[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      m[i] = fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w)));
+      m[i] = fmaxf(fabsf(s[i].x), fabsf(s[i].y));
       m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 1));
       m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 2));
       if (cg == 0) sm.rmax[warp][rg + 8 * i] = m[i];
     }
     __syncthreads();
+    const int w0 = warp & ~3;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const float sc = int8_scale(fmaxf(m[i], sm.rmax[warp ^ 1][rg + 8 * i])), rc = __frcp_rn(sc);
-      s[i] = make_float4(int8_qdq_rcp(s[i].x, rc, sc), int8_qdq_rcp(s[i].y, rc, sc), int8_qdq_rcp(s[i].z, rc, sc),
-                         int8_qdq_rcp(s[i].w, rc, sc));
+      const int row = rg + 8 * i;
+      const float bm = fmaxf(fmaxf(sm.rmax[w0][row], sm.rmax[w0 + 1][row]), fmaxf(sm.rmax[w0 + 2][row], sm.rmax[w0 + 3][row]));
+      const float sc = int8_scale(bm), rc = __frcp_rn(sc);
+      s[i] = make_float2(int8_qdq_rcp(s[i].x, rc, sc), int8_qdq_rcp(s[i].y, rc, sc));
     }
   } else {
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(s[i].x), fabsf(s[i].y)), fmaxf(fabsf(s[i].z), fabsf(s[i].w))));
+    for (int i = 0; i < RPT; ++i) amax = fmaxf(amax, fmaxf(fabsf(s[i].x), fabsf(s[i].y)));
     amax = warp_max(amax);
     if (lane == 0) sm.wmax[warp] = amax;
     __syncthreads();
-    const float tmax = fmaxf(fmaxf(sm.wmax[0], sm.wmax[1]), fmaxf(sm.wmax[2], sm.wmax[3]));   // the slab
+    float tmax = sm.wmax[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) tmax = fmaxf(tmax, sm.wmax[w]);
     const float sc = qdq_scale(tmax), rc = __frcp_rn(sc);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
-      const __nv_fp8x2_e4m3 c01(make_float2(__fmul_rn(s[i].x, rc), __fmul_rn(s[i].y, rc)));
-      const __nv_fp8x2_e4m3 c23(make_float2(__fmul_rn(s[i].z, rc), __fmul_rn(s[i].w, rc)));
-      const float2 f01 = static_cast<float2>(c01), f23 = static_cast<float2>(c23);
-      s[i] = make_float4(__fmul_rn(f01.x, sc), __fmul_rn(f01.y, sc), __fmul_rn(f23.x, sc), __fmul_rn(f23.y, sc));
+      const __nv_fp8x2_e4m3 c(make_float2(__fmul_rn(s[i].x, rc), __fmul_rn(s[i].y, rc)));
+      const float2 f = static_cast<float2>(c);
+      s[i] = make_float2(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
     }
   }
   __syncthreads();   // the next QDQ's shared-memory writes come after every thread's reads
 }
 
+// One token backward (header formulas) from P, the state before the token, with dS in ds (updated
+// to dS_{t-1}). Writes dv; leaves the token's four row sums of every key row in sm.rs[buf] and,
+// after the barrier, the reducing threads (the first dk) write the slab partials.
 template <int DK, bool KDA>
-__global__ void __launch_bounds__(SL * 2, 2) chunk_bwd_kernel(const BwdParams p) {
+__device__ __forceinline__ void bwd_token(const BwdParams& p, BwdSmem<DK, KDA>& sm, const float2 (&P)[DK / 8],
+                                          float2 (&ds)[DK / 8], const TokView<DK>& t, const unsigned char* rec,
+                                          int64_t tok, int h, int slab, int buf, int warp, int lane, int rg, int cg,
+                                          int c0) {
   constexpr int RPT = DK / 8;
-  __shared__ BwdSmem<DK> sm;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float2 pp[RPT];   // P' = a o P
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) pp[i] = make_float2(t.ar[i] * P[i].x, t.ar[i] * P[i].y);
+  // u = v - P'^T k
+  float2 u = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    u.x = fmaf(pp[i].x, t.kr[i], u.x); u.y = fmaf(pp[i].y, t.kr[i], u.y);
+  }
+  u = col_sum(u);
+  u = make_float2(t.vv.x - u.x, t.vv.y - u.y);
+  // dS += scale q do^T; du = b dS^T k
+  const float2 sdo = make_float2(p.scale * t.dov.x, p.scale * t.dov.y);
+  float2 du = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    ds[i].x = fmaf(t.qr[i], sdo.x, ds[i].x); ds[i].y = fmaf(t.qr[i], sdo.y, ds[i].y);
+    du.x = fmaf(ds[i].x, t.kr[i], du.x); du.y = fmaf(ds[i].y, t.kr[i], du.y);
+  }
+  du = col_sum(du);
+  du = make_float2(t.b * du.x, t.b * du.y);
+  if (rg == 0) *reinterpret_cast<float2*>(p.grad_v + (tok * p.Hv + h) * p.dv + slab * SL + c0) = du;
+  // per key row, over this lane's 2 columns: x0 = S do (S = P' + b k u^T), x1 = dS u, x2 = P' du,
+  // x3 = dP' . P' with dP' = dS - k du^T; then a reduce-scatter over the lane quad leaves the quad's
+  // sum of x_cg in lane cg
+  const float2 bu = make_float2(t.b * u.x, t.b * u.y);
+  const bool hi = (cg & 2) != 0, lo = (cg & 1) != 0;
+  float* rsb = reinterpret_cast<float*>(&sm.rs[buf][warp][0]);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float2 S = make_float2(fmaf(t.kr[i], bu.x, pp[i].x), fmaf(t.kr[i], bu.y, pp[i].y));
+    const float x0 = S.x * t.dov.x + S.y * t.dov.y;
+    const float x1 = ds[i].x * u.x + ds[i].y * u.y;
+    const float x2 = pp[i].x * du.x + pp[i].y * du.y;
+    const float2 dpp = make_float2(fmaf(-t.kr[i], du.x, ds[i].x), fmaf(-t.kr[i], du.y, ds[i].y));
+    // dg = (dL/da) a = <dP', P> a = <dP', P'> (per key row for KDA)
+    const float x3 = dpp.x * pp[i].x + dpp.y * pp[i].y;
+    ds[i] = make_float2(t.ar[i] * dpp.x, t.ar[i] * dpp.y);   // dS_{t-1}
+    float a0 = hi ? x2 : x0, a1 = hi ? x3 : x1;
+    a0 += __shfl_xor_sync(0xffffffffu, hi ? x0 : x2, 2);
+    a1 += __shfl_xor_sync(0xffffffffu, hi ? x1 : x3, 2);
+    float r = lo ? a1 : a0;
+    r += __shfl_xor_sync(0xffffffffu, lo ? a0 : a1, 1);
+    rsb[(rg + 8 * i) * 4 + cg] = r;
+  }
+  __syncthreads();
+  // per key row cr (threads cr < DK): the slab's sums over its warps, in warp order
+  if (threadIdx.x < DK) {
+    const int cr = threadIdx.x;
+    float4 a = sm.rs[buf][0][cr];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+      const float4 x = sm.rs[buf][w][cr];
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+    }
+    const int64_t ph = (int64_t)slab * p.tokens * p.Hv + tok * p.Hv + h;   // slab partial index of (tok, h)
+    p.part_q[ph * DK + cr] = p.scale * a.x;
+    p.part_k[ph * DK + cr] = t.b * a.y - a.z;
+    if (KDA) p.part_g[ph * DK + cr] = a.w;
+    const float kc = bf16_to_f32(reinterpret_cast<const __nv_bfloat16*>(rec + Rec<DK, KDA>::K)[cr]);
+    // db = sum over key rows of k (dS u); GDN dg = sum over key rows of dP' . P'
+    const float db = warp_sum(kc * a.y);
+    const float dg = KDA ? 0.f : warp_sum(a.w);
+    if (lane == 0) {
+      const int64_t pw = ((int64_t)slab * (DK / 32) + warp) * p.tokens * p.Hv + tok * p.Hv + h;
+      p.part_b[pw] = db;
+      if (!KDA) p.part_g[pw] = dg;
+    }
+  }
+}
+
+template <int DK, bool KDA>
+__global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(const BwdParams p) {
+  constexpr int RPT = DK / 8;
+  using R = Rec<DK, KDA>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BwdSmem<DK, KDA>& sm = *reinterpret_cast<BwdSmem<DK, KDA>*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = lane >> 2, cg = lane & 3;
+  const int c0 = warp * 8 + cg * 2;   // this lane's first column within the slab
   const int nslab = p.dv / SL;
   const int64_t units = (int64_t)p.N * p.Hv * nslab;
-  float* const scr = p.scratch + (int64_t)blockIdx.x * 64 * DK * SL;
-  auto sat = [&](int r, int i) { return reinterpret_cast<float4*>(scr + ((int64_t)r * DK + rg + 8 * i) * SL + warp * 16 + cg * 4); };
+  float2* const scr = reinterpret_cast<float2*>(p.scratch) + (int64_t)blockIdx.x * NSUB * RPT * NT;
+  auto sub_at = [&](int j, int i) { return scr + ((int64_t)j * RPT + i) * NT + tid; };
+  int tc = 0;   // backward tokens so far (selects the row-sum buffer)
 
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
     const int slab = (int)(unit % nslab);
     const int64_t nh = unit / nslab;   // n * Hv + h
     const int n = (int)(nh / p.Hv), h = (int)(nh % p.Hv);
     const int hq = h / (p.Hv / p.Hqk);
-    const int col = slab * SL + warp * 16 + cg * 4;   // this lane's first value column
+    const int col = slab * SL + c0;    // this lane's first value column
     const int64_t t0 = p.cu ? (int64_t)p.cu[n] : (int64_t)n * p.T;
     const int64_t len = p.cu ? (int64_t)p.cu[n + 1] - t0 : (int64_t)p.T;
-    const int64_t nch = (len + 63) / 64;
-    const int64_t slot0 = t0 / 64 + n;
+    const int64_t nch = (len + kChunk - 1) / kChunk;
+    const int64_t slot0 = t0 / kChunk + n;
     const int64_t st = (int64_t)DK * p.dv;   // one state
     auto srow = [&](const float* base, int i) { return base + (int64_t)(rg + 8 * i) * p.dv + col; };
     auto ck = [&](int64_t c) { return p.ckpt + ((slot0 + c) * p.Hv + h) * st; };
-    float kr[RPT], qr[RPT], ar[RPT], b;
-    float4 vv, dov;
+    TokView<DK> tv;
 
-    // ---- pass 1: the forward recurrence, storing the state entering every chunk ----
-    float4 s[RPT];
+    // ---- pass 1: the forward recurrence, storing the state entering every chunk; the tokens
+    // stream through the two halves of the staging area, 32 at a time ----
+    float2 s[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i)
-      s[i] = p.h0 ? *reinterpret_cast<const float4*>(srow(p.h0 + nh * st, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t t = 0; t < len; ++t) {
-      if (t % 64 == 0) {
+      s[i] = p.h0 ? *reinterpret_cast<const float2*>(srow(p.h0 + nh * st, i)) : make_float2(0.f, 0.f);
+    const int64_t nblk = (len + 31) / 32;
+    __syncthreads();   // the previous unit's last reads of the staging area are done
+    for (int64_t b = 0; b < 2 && b < nblk; ++b) {
+      stage_tokens<DK, KDA>(p, sm.stage + b * 32 * R::BYTES, t0 + 32 * b, (int)min((int64_t)32, len - 32 * b), h,
+                            hq, slab);
+      cp_commit();
+    }
+    for (int64_t b = 0; b < nblk; ++b) {
+      if (b + 1 < nblk) cp_wait<1>(); else cp_wait<0>();
+      __syncthreads();
+      unsigned char* half = sm.stage + (b & 1) * 32 * R::BYTES;
+      const int nb = (int)min((int64_t)32, len - 32 * b);
+      exp_gates<DK, KDA>(half, nb);
+      __syncthreads();
+      for (int r = 0; r < nb; ++r) {
+        const int64_t t = 32 * b + r;
+        if (t % kChunk == 0) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(const_cast<float*>(srow(ck(t / 64), i))) = s[i];
+          for (int i = 0; i < RPT; ++i) *reinterpret_cast<float2*>(const_cast<float*>(srow(ck(t / kChunk), i))) = s[i];
+        }
+        read_token<DK, KDA>(half + r * R::BYTES, rg, c0, false, tv);
+        fwd_step<DK>(s, tv);
+        if (p.state_qdq && (t + 1) % kChunk == 0) state_qdq<DK, KDA>(s, p.state_qdq, sm, warp, lane, rg, cg);
       }
-      load_token<DK, KDA>(p, t0 + t, h, hq, rg, col, kr, qr, ar, b, vv, dov);
-      fwd_step<DK>(s, kr, ar, b, vv);
-      if (p.state_qdq && (t + 1) % 64 == 0) state_qdq<DK>(s, p.state_qdq, sm, warp, lane, rg, cg);
+      __syncthreads();   // every thread is done with this half
+      if (b + 2 < nblk) {
+        stage_tokens<DK, KDA>(p, half, t0 + 32 * (b + 2), (int)min((int64_t)32, len - 32 * (b + 2)), h, hq, slab);
+        cp_commit();
+      }
     }
 
     // ---- pass 2: chunks in reverse; dS in registers ----
-    float4 ds[RPT];
+    float2 ds[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i)
-      ds[i] = p.dhT ? *reinterpret_cast<const float4*>(srow(p.dhT + nh * st, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ds[i] = p.dhT ? *reinterpret_cast<const float2*>(srow(p.dhT + nh * st, i)) : make_float2(0.f, 0.f);
     for (int64_t c = nch - 1; c >= 0; --c) {
-      const int L = (int)((len - c * 64) < 64 ? (len - c * 64) : 64);
-      // the chunk's token states (before each token) into the scratch
+      const int L = (int)min((int64_t)kChunk, len - c * kChunk);
+      const int64_t tc0 = t0 + c * kChunk;
+      __syncthreads();   // the staging area is free
+      stage_tokens<DK, KDA>(p, sm.stage, tc0, L, h, hq, slab);
+      cp_commit();
+      cp_wait<0>();
+      __syncthreads();
+      exp_gates<DK, KDA>(sm.stage, L);
+      __syncthreads();
+      // the sub-chunk checkpoints: the state before tokens 0, 4, .., 4 (jmax - 1) to the scratch; the
+      // state before token 4 jmax stays in registers
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float4*>(srow(ck(c), i));
-      for (int r = 0; r < L; ++r) {
+      for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float2*>(srow(ck(c), i));
+      const int jmax = (L - 1) / SUB;
+      for (int r = 0; r < SUB * jmax; ++r) {
+        if (r % SUB == 0) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) *sat(r, i) = s[i];
-        if (r + 1 < L) {
-          load_token<DK, KDA>(p, t0 + c * 64 + r, h, hq, rg, col, kr, qr, ar, b, vv, dov);
-          fwd_step<DK>(s, kr, ar, b, vv);
+          for (int i = 0; i < RPT; ++i) *sub_at(r / SUB, i) = s[i];
         }
+        read_token<DK, KDA>(sm.stage + r * R::BYTES, rg, c0, false, tv);
+        fwd_step<DK>(s, tv);
       }
-      for (int r = L - 1; r >= 0; --r) {
-        const int64_t tok = t0 + c * 64 + r;
-        load_token<DK, KDA>(p, tok, h, hq, rg, col, kr, qr, ar, b, vv, dov);
-        float4 pp[RPT];   // P' = a o P
+      for (int j = jmax; j >= 0; --j) {
+        if (j < jmax) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-          const float4 P = *sat(r, i);
-          pp[i] = make_float4(ar[i] * P.x, ar[i] * P.y, ar[i] * P.z, ar[i] * P.w);
+          for (int i = 0; i < RPT; ++i) s[i] = *sub_at(j, i);
         }
-        // u = v - P'^T k
-        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int r0 = SUB * j, cnt = min(SUB, L - r0);
+        // the states before tokens r0 .. r0 + cnt - 2 into this thread's slots; s ends as the state
+        // before the sub-chunk's last token
+        for (int m = 0; m + 1 < cnt; ++m) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-          u.x = fmaf(pp[i].x, kr[i], u.x); u.y = fmaf(pp[i].y, kr[i], u.y);
-          u.z = fmaf(pp[i].z, kr[i], u.z); u.w = fmaf(pp[i].w, kr[i], u.w);
+          for (int i = 0; i < RPT; ++i) sm.slot[m][i][tid] = s[i];
+          read_token<DK, KDA>(sm.stage + (r0 + m) * R::BYTES, rg, c0, false, tv);
+          fwd_step<DK>(s, tv);
         }
-        u = col_sum(u);
-        u = make_float4(vv.x - u.x, vv.y - u.y, vv.z - u.z, vv.w - u.w);
-        // dS += scale q do^T; du = b dS^T k
-        const float4 sdo = make_float4(p.scale * dov.x, p.scale * dov.y, p.scale * dov.z, p.scale * dov.w);
-        float4 du = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = cnt - 1; m >= 0; --m) {
+          float2 P[RPT];
+          if (m == cnt - 1) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-          ds[i].x = fmaf(qr[i], sdo.x, ds[i].x); ds[i].y = fmaf(qr[i], sdo.y, ds[i].y);
-          ds[i].z = fmaf(qr[i], sdo.z, ds[i].z); ds[i].w = fmaf(qr[i], sdo.w, ds[i].w);
-          du.x = fmaf(ds[i].x, kr[i], du.x); du.y = fmaf(ds[i].y, kr[i], du.y);
-          du.z = fmaf(ds[i].z, kr[i], du.z); du.w = fmaf(ds[i].w, kr[i], du.w);
-        }
-        du = col_sum(du);
-        du = make_float4(b * du.x, b * du.y, b * du.z, b * du.w);
-        if (rg == 0) *reinterpret_cast<float4*>(p.grad_v + (tok * p.Hv + h) * p.dv + col) = du;
-        // row sums over this lane's 4 columns: r0 = S do (S = P' + b k u^T), r1 = dS u, r2 = P' du,
-        // r3 = dP' . P' with dP' = dS - k du^T
-        float r0[RPT], r1[RPT], r2[RPT], r3[RPT];
-        const float4 bu = make_float4(b * u.x, b * u.y, b * u.z, b * u.w);
+            for (int i = 0; i < RPT; ++i) P[i] = s[i];
+          } else {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-          const float4 S = make_float4(fmaf(kr[i], bu.x, pp[i].x), fmaf(kr[i], bu.y, pp[i].y), fmaf(kr[i], bu.z, pp[i].z),
-                                       fmaf(kr[i], bu.w, pp[i].w));
-          r0[i] = S.x * dov.x + S.y * dov.y + S.z * dov.z + S.w * dov.w;
-          r1[i] = ds[i].x * u.x + ds[i].y * u.y + ds[i].z * u.z + ds[i].w * u.w;
-          r2[i] = pp[i].x * du.x + pp[i].y * du.y + pp[i].z * du.z + pp[i].w * du.w;
-          const float4 dpp = make_float4(fmaf(-kr[i], du.x, ds[i].x), fmaf(-kr[i], du.y, ds[i].y),
-                                         fmaf(-kr[i], du.z, ds[i].z), fmaf(-kr[i], du.w, ds[i].w));
-          // dg = (dL/da) a = <dP', P> a = <dP', P'> (per key row for KDA)
-          r3[i] = dpp.x * pp[i].x + dpp.y * pp[i].y + dpp.z * pp[i].z + dpp.w * pp[i].w;
-          ds[i] = make_float4(ar[i] * dpp.x, ar[i] * dpp.y, ar[i] * dpp.z, ar[i] * dpp.w);   // dS_{t-1}
-        }
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-#pragma unroll
-          for (int off = 1; off < 4; off <<= 1) {
-            r0[i] += __shfl_xor_sync(0xffffffffu, r0[i], off);
-            r1[i] += __shfl_xor_sync(0xffffffffu, r1[i], off);
-            r2[i] += __shfl_xor_sync(0xffffffffu, r2[i], off);
-            r3[i] += __shfl_xor_sync(0xffffffffu, r3[i], off);
+            for (int i = 0; i < RPT; ++i) P[i] = sm.slot[m][i][tid];
           }
-          if (cg == 0) {
-            sm.rs[warp][rg + 8 * i][0] = r0[i];
-            sm.rs[warp][rg + 8 * i][1] = r1[i];
-            sm.rs[warp][rg + 8 * i][2] = r2[i];
-            sm.rs[warp][rg + 8 * i][3] = r3[i];
-          }
+          const unsigned char* rec = sm.stage + (r0 + m) * R::BYTES;
+          read_token<DK, KDA>(rec, rg, c0, true, tv);
+          bwd_token<DK, KDA>(p, sm, P, ds, tv, rec, tc0 + r0 + m, h, slab, tc & 1, warp, lane, rg, cg, c0);
+          ++tc;
         }
-        __syncthreads();
-        // per key row cr (threads cr < DK): the slab's sums over its warps, in warp order
-        const int64_t ph = (int64_t)slab * p.tokens * p.Hv + tok * p.Hv + h;   // slab partial index of (tok, h)
-        float kb_c = 0.f, dg_c = 0.f;
-        if (threadIdx.x < DK) {
-          const int cr = threadIdx.x;
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            a0 += sm.rs[w][cr][0]; a1 += sm.rs[w][cr][1]; a2 += sm.rs[w][cr][2]; a3 += sm.rs[w][cr][3];
-          }
-          const float kc = bf16_to_f32(p.k[(tok * p.Hqk + hq) * DK + cr]);
-          p.part_q[ph * DK + cr] = p.scale * a0;
-          p.part_k[ph * DK + cr] = b * a1 - a2;
-          kb_c = kc * a1;   // contribution to db
-          dg_c = a3;        // contribution to dg (GDN: summed over the rows)
-          if (KDA) p.part_g[ph * DK + cr] = a3;
-        }
-        // db and (GDN) dg: sums over the key rows (warps 0 .. DK/32 - 1 hold them)
-        if (warp < DK / 32) {
-          float x0 = kb_c, x1 = dg_c;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            x0 += __shfl_xor_sync(0xffffffffu, x0, off);
-            x1 += __shfl_xor_sync(0xffffffffu, x1, off);
-          }
-          if (lane == 0) {
-            sm.tot[warp][0] = x0;
-            sm.tot[warp][1] = x1;
-          }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          float db = 0.f, dg = 0.f;
-#pragma unroll
-          for (int w = 0; w < DK / 32; ++w) {
-            db += sm.tot[w][0];
-            dg += sm.tot[w][1];
-          }
-          p.part_b[ph] = db;
-          if (!KDA) p.part_g[ph] = dg;
-        }
-        __syncthreads();   // sm.rs / sm.tot are rewritten by the next token
       }
     }
     if (p.dh0) {
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4*>(p.dh0 + nh * st + (int64_t)(rg + 8 * i) * p.dv + col) = ds[i];
+      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float2*>(p.dh0 + nh * st + (int64_t)(rg + 8 * i) * p.dv + col) = ds[i];
     }
   }
 }
@@ -357,16 +465,19 @@ __global__ void sum_parts_kernel(const float* __restrict__ part, float* __restri
   }
 }
 
-constexpr int kBwdCtas = 2 * 152;   // two CTAs per GB300 SM at most; each owns a 64-state scratch
+constexpr int kBwdCtas = 152;   // one CTA per GB300 SM at most; each owns a sub-chunk scratch
 
 template <int DK, bool KDA>
 cudaError_t launch_t(const BwdParams& bp, int64_t units, cudaStream_t stream) {
-  int dev = 0, sms = kBwdCtas / 2;
+  int dev = 0, sms = kBwdCtas;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaGetLastError();
-  int64_t grid = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;
+  int64_t grid = units < (int64_t)sms ? units : (int64_t)sms;
   if (grid > kBwdCtas) grid = kBwdCtas;
-  chunk_bwd_kernel<DK, KDA><<<(unsigned)grid, SL * 2, 0, stream>>>(bp);
+  const size_t smem = sizeof(BwdSmem<DK, KDA>);
+  cudaError_t e = cudaFuncSetAttribute(chunk_bwd_kernel<DK, KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  chunk_bwd_kernel<DK, KDA><<<(unsigned)grid, NT, smem, stream>>>(bp);
   return cudaGetLastError();
 }
 
@@ -390,12 +501,13 @@ BwdLayout chunk_bwd_layout(const ChunkProblem& p) {
   const int64_t ctas = units < kBwdCtas ? units : kBwdCtas;
   const size_t part = (size_t)nslab * tokens * p.Hv * 4;
   l.off_ckpt = up(kStatusBytes);
+  const int nwr = p.dk / 32;   // reducing warps: db (and GDN dg) partials per slab
   l.off_scratch = up(l.off_ckpt + (size_t)slots * p.Hv * p.dk * p.dv * 4);
-  l.off_part_q = up(l.off_scratch + (size_t)ctas * 64 * p.dk * SL * 4);
+  l.off_part_q = up(l.off_scratch + (size_t)ctas * NSUB * p.dk * SL * 4);
   l.off_part_k = up(l.off_part_q + part * p.dk);
   l.off_part_b = up(l.off_part_k + part * p.dk);
-  l.off_part_g = up(l.off_part_b + part);
-  l.total = up(l.off_part_g + part * (p.kda ? p.dk : 1));
+  l.off_part_g = up(l.off_part_b + part * nwr);
+  l.total = up(l.off_part_g + part * (p.kda ? p.dk : nwr));
   return l;
 }
 
@@ -422,9 +534,10 @@ cudaError_t launch_chunk_bwd(const ChunkProblem& p, const BwdGrads& gr, void* ws
   const int64_t sh = tokens * p.Hv;   // per-slab stride in (token, v-head) units
   if ((e = sum_parts(pq, gr.dq, tokens * p.Hqk * p.dk, nslab, sh * p.dk, G, p.dk, stream)) != cudaSuccess) return e;
   if ((e = sum_parts(pk, gr.dk, tokens * p.Hqk * p.dk, nslab, sh * p.dk, G, p.dk, stream)) != cudaSuccess) return e;
-  if ((e = sum_parts(pb, gr.dbeta, sh, nslab, sh, 1, 1, stream)) != cudaSuccess) return e;
-  const int gk = p.kda ? p.dk : 1;
-  return sum_parts(pg, gr.dg, sh * gk, nslab, sh * gk, 1, 1, stream);
+  const int nwr = p.dk / 32;
+  if ((e = sum_parts(pb, gr.dbeta, sh, nslab * nwr, sh, 1, 1, stream)) != cudaSuccess) return e;
+  if (p.kda) return sum_parts(pg, gr.dg, sh * p.dk, nslab, sh * p.dk, 1, 1, stream);
+  return sum_parts(pg, gr.dg, sh, nslab * nwr, sh, 1, 1, stream);
 }
 
 }  // namespace gdn

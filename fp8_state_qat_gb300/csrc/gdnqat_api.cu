@@ -211,6 +211,7 @@ gdn_status chunk_bwd(const gdn_chunk_args* a, const gdn_chunk_grads* gr, void* w
     if (!aligned(gr->dout, 16) || !aligned(gr->dv, 16) || !aligned(gr->dq, 4) || !aligned(gr->dk, 4) ||
         !aligned(gr->dg, 4) || !aligned(gr->dbeta, 4))
       return GDN_ERR_INVALID_ARG;
+    if (kda && !aligned(a->g, 16)) return GDN_ERR_INVALID_ARG;   // staged in 16-byte copies
   }
   if ((gr->dhT && !aligned(gr->dhT, 16)) || (gr->dh0 && !aligned(gr->dh0, 16))) return GDN_ERR_INVALID_ARG;
   ChunkProblem p = problem_of(a, kda);

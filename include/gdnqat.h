@@ -179,13 +179,15 @@ typedef struct {
 } gdn_chunk_grads;
 
 /* Workspace of gdn_chunk_bwd (0 for invalid arguments): the status word, the state entering every
- * 64-token chunk (per chunk slot and v-head), a 64-token scratch of 64-column state slabs per CTA
- * (at most 304 CTAs), and the per-slab, per-value-head dq, dk, dbeta, dg before their sums. */
+ * 64-token chunk (per chunk slot and v-head), per CTA (at most 152) the 16 sub-chunk checkpoints
+ * of one 64-column state slab, and the per-slab, per-value-head dq, dk, dbeta, dg before their
+ * sums (dbeta and the GDN dg also per dk / 32 key-row groups). */
 size_t gdn_chunk_bwd_workspace_size(const gdn_chunk_args* args);
 /* The backward on CUDA cores: per (sequence, head, 64-column value slab) a forward pass that
- * stores the chunk-entry states, then the chunks in reverse, each recomputed and walked token by
- * token with the state gradient in registers; a second kernel sums the slab (and, with GQA,
- * value-head) partials of dq, dk, dbeta and dg in a fixed order. args: the forward's inputs and flags (o, hT unused and may be NULL);
+ * stores the chunk-entry states, then the chunks in reverse, each recomputed in 4-token sub-chunks
+ * and walked token by token with the state gradient in registers; a second kernel sums the slab
+ * (and, with GQA, value-head) partials of dq, dk, dbeta and dg in a fixed order. With
+ * kda_chunk_bwd, g must be 16-byte aligned (else GDN_ERR_INVALID_ARG). args: the forward's inputs and flags (o, hT unused and may be NULL);
  * GDN_FLAG_W_QDQ and state_scales are refused (GDN_ERR_INVALID_ARG): the straight-through gradient
  * of the W QDQ belongs to the chunked form, which this backward does not take. */
 gdn_status gdn_chunk_bwd(const gdn_chunk_args* args, const gdn_chunk_grads* grads, void* workspace,

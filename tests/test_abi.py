@@ -1,7 +1,8 @@
 """The C ABI library (CPU-only checks): it builds, loads, exports every function that
 include/gdnqat.h declares, and its host-side validation returns the documented status
 before touching a device ("GDN state/W QAT foundation": errors are raised before any
-kernel launches). No compute call is made here."""
+kernel launches). No compute call is made here: the pointers are fake, so a call that passes
+validation is made only where no GPU is present (it then stops at the device check)."""
 import ctypes
 import os
 import re
@@ -90,8 +91,10 @@ def test_workspace_checks(so):
     a = good_args()
     assert call_chunk(so, a, ws_bytes=MIN_WS - 1) == B.GDN_ERR_WORKSPACE_TOO_SMALL
     assert call_chunk(so, a, ws=0) == B.GDN_ERR_WORKSPACE_TOO_SMALL
-    # with enough workspace the next check is the device's (none here)
-    assert call_chunk(so, a, ws_bytes=MIN_WS) == B.GDN_ERR_UNSUPPORTED_ARCH
+    # with enough workspace the next check is the device's (where there is none); with a GPU the
+    # call would go on to use the fake addresses, so it is made only without one
+    if not torch.cuda.is_available():
+        assert call_chunk(so, a, ws_bytes=MIN_WS) == B.GDN_ERR_UNSUPPORTED_ARCH
     assert so.gdn_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=96))) == 0
 
 
@@ -216,17 +219,17 @@ def test_state_scales_validation(so):
 def test_backward_validation(so):
     """The backward refuses W QDQ (its straight-through gradient belongs to the chunked form) and
     missing gradient buffers; its workspace covers the chunk-entry states and the per-CTA
-    64-column scratch (at most two CTAs per SM)."""
+    sub-chunk checkpoints of a 64-column slab (at most one CTA per SM)."""
     P = ctypes.c_void_p
     a = good_args(flags=B.GDN_FLAG_STATE_QDQ, o=None)
     need = so.gdn_chunk_bwd_workspace_size(ctypes.byref(a))
     slots = (a.B * a.T) // 64 + a.N
     state = a.dk * a.dv * 4
     slabs = a.dv // 64
-    assert need >= 256 + slots * a.Hv * state + min(a.N * a.Hv * slabs, 304) * 64 * a.dk * 64 * 4
+    assert need >= 256 + slots * a.Hv * state + min(a.N * a.Hv * slabs, 152) * 16 * a.dk * 64 * 4
     assert so.gdn_chunk_bwd_workspace_size(ctypes.byref(good_args(flags=3))) == 0        # W QDQ
     # KDA adds a per-key-channel dg partial for every slab and (token, v-head)
-    assert so.kda_chunk_bwd_workspace_size(ctypes.byref(a)) >= need + (a.dv // 64) * a.B * a.T * a.Hv * (a.dk - 1) * 4
+    assert so.kda_chunk_bwd_workspace_size(ctypes.byref(a)) >= need + slabs * a.B * a.T * a.Hv * (a.dk - a.dk // 32) * 4
     g = B.ChunkGrads(*[P(FAKE + ((11 + i) << 32)) for i in range(8)])
     fn = so.gdn_chunk_bwd
     assert fn(ctypes.byref(good_args(flags=3, o=None)), ctypes.byref(g), P(FAKE + (7 << 32)), need,
@@ -234,5 +237,10 @@ def test_backward_validation(so):
     g_missing = B.ChunkGrads(*[P(FAKE + ((11 + i) << 32)) for i in range(2)], None)
     assert fn(ctypes.byref(a), ctypes.byref(g_missing), P(FAKE + (7 << 32)), need, None) == B.GDN_ERR_INVALID_ARG
     assert fn(ctypes.byref(a), ctypes.byref(g), P(FAKE + (7 << 32)), need - 1, None) == B.GDN_ERR_WORKSPACE_TOO_SMALL
+    # KDA stages g in 16-byte copies: a 4-byte aligned g is refused
+    a_g4 = good_args(flags=B.GDN_FLAG_STATE_QDQ, o=None, g=FAKE + (3 << 32) + 4)
+    kneed = so.kda_chunk_bwd_workspace_size(ctypes.byref(good_args(flags=B.GDN_FLAG_STATE_QDQ, o=None)))
+    assert so.kda_chunk_bwd(ctypes.byref(a_g4), ctypes.byref(g), P(FAKE + (7 << 32)), kneed,
+                            None) == B.GDN_ERR_INVALID_ARG
     if not torch.cuda.is_available():
         assert fn(ctypes.byref(a), ctypes.byref(g), P(FAKE + (7 << 32)), need, None) == B.GDN_ERR_UNSUPPORTED_ARCH
