@@ -603,7 +603,8 @@ def run_gpu(args):
     if args.batch:   # profiling case of the same kernel: the first `batch` sequences
         x = workloads.PrefillInputs(x.q[:args.batch], x.k[:args.batch], x.v[:args.batch], x.g[:args.batch],
                                     x.beta[:args.batch], None if x.h0 is None else x.h0[:args.batch], None,
-                                    kda=x.kda, state_qdq=x.state_qdq, w_qdq=x.w_qdq, name=x.name)
+                                    kda=x.kda, state_qdq=x.state_qdq, w_qdq=x.w_qdq, name=x.name,
+                                    backward=x.backward)
     if isinstance(x, workloads.DecodeInputs):
         case = DecodeCase(x, dev, torch, gdn)
     elif isinstance(x, workloads.QdqInputs):

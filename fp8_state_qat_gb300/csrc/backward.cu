@@ -17,8 +17,11 @@
 // columns (dq, dk, db, dg), the recurrence and its backward are column-local, so the work splits
 // into one CTA per (sequence, head, 64-column value slab) -- the E4M3 tile width, so the forward
 // QDQ stays CTA-local -- and a persistent grid (one CTA per SM) walks those units. 256 threads:
-// warp w owns slab columns [8 w, 8 w + 8); lane 4 rg + cg holds key rows rg + 8 i and the two
-// columns 8 w + 2 cg, + 1, so a column sum over the key rows is a 3-level xor shuffle.
+// warp w owns slab columns [8 w, 8 w + 8); lane 4 rg + cg holds the dk / 8 consecutive key rows
+// from (dk / 8) rg and the two columns 8 w + 2 cg, + 1, so a column sum over the key rows is a
+// 3-level xor shuffle. The registers pair two adjacent key rows of one column, so k, q and a
+// arrive as natural pairs for the paired fp32 instructions (fma / mul .f32x2) and only the
+// per-column scalars of a token are broadcast.
 //
 // Pass 1 runs the forward recurrence, QDQ included, and stores the state entering every 64-token
 // chunk. Pass 2 takes the chunks in reverse: the chunk's token inputs are staged in shared memory
@@ -82,6 +85,7 @@ template <int DK, bool KDA>
 struct BwdSmem {
   alignas(16) unsigned char stage[kChunk * Rec<DK, KDA>::BYTES];
   float2 slot[SUB - 1][DK / 8][NT];   // per-thread copies of the sub-chunk's first token states
+                                      // (the row sums below are indexed by rs_slot of the key row)
   float4 rs[2][NW][DK];               // per token (double-buffered), warp, key row: 4 row sums
   float wmax[NW];
   float rmax[NW][DK];
@@ -140,10 +144,11 @@ __device__ __forceinline__ void exp_gates(unsigned char* rec0, int count) {
   }
 }
 
-// This thread's view of one staged token: k, q and a on its key rows; beta; v and dout on its columns.
+// This thread's view of one staged token: k, q and a on its key rows as (row 2 j, row 2 j + 1)
+// pairs; beta; v and dout on its two columns.
 template <int DK>
 struct TokView {
-  float kr[DK / 8], qr[DK / 8], ar[DK / 8];
+  float2 k2[DK / 16], q2[DK / 16], a2[DK / 16];
   float b;
   float2 vv, dov;
 };
@@ -151,23 +156,43 @@ struct TokView {
 template <int DK, bool KDA>
 __device__ __forceinline__ void read_token(const unsigned char* rec, int rg, int c0, bool need_q, TokView<DK>& t) {
   using R = Rec<DK, KDA>;
-  constexpr int RPT = DK / 8;
-  const __nv_bfloat16* kk = reinterpret_cast<const __nv_bfloat16*>(rec + R::K);
-  const __nv_bfloat16* qq = reinterpret_cast<const __nv_bfloat16*>(rec + R::Q);
-  const float* ga = reinterpret_cast<const float*>(rec + R::G);
+  constexpr int RPT = DK / 8, NPR = RPT / 2;
+  const uint4* kk = reinterpret_cast<const uint4*>(rec + R::K + 2 * RPT * rg);
+  const uint4* qq = reinterpret_cast<const uint4*>(rec + R::Q + 2 * RPT * rg);
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    t.kr[i] = bf16_to_f32(kk[rg + 8 * i]);
-    if (need_q) t.qr[i] = bf16_to_f32(qq[rg + 8 * i]);
-    t.ar[i] = KDA ? ga[rg + 8 * i] : ga[0];
+  for (int j = 0; j < RPT / 8; ++j) {
+    const uint4 x = kk[j];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) t.k2[4 * j + e] = __bfloat1622float2(h[e]);
+    if (need_q) {
+      const uint4 y = qq[j];
+      const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t.q2[4 * j + e] = __bfloat1622float2(hq[e]);
+    }
+  }
+  if (KDA) {
+    const float4* ga = reinterpret_cast<const float4*>(rec + R::G + 4 * RPT * rg);
+#pragma unroll
+    for (int j = 0; j < RPT / 4; ++j) {
+      const float4 x = ga[j];
+      t.a2[2 * j] = make_float2(x.x, x.y);
+      t.a2[2 * j + 1] = make_float2(x.z, x.w);
+    }
+  } else {
+    const float a = *reinterpret_cast<const float*>(rec + R::G);
+#pragma unroll
+    for (int j = 0; j < NPR; ++j) t.a2[j] = make_float2(a, a);
   }
   t.b = *reinterpret_cast<const float*>(rec + R::B);
   t.vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(rec + R::V + 2 * c0));
   t.dov = *reinterpret_cast<const float2*>(rec + R::DO + 4 * c0);
 }
 
-// column sums over the key rows: partial over this lane's rows, then the 8 row groups (lane bits 2..4)
-__device__ __forceinline__ float2 col_sum(float2 x) {
+// column sums over the key rows: the two row halves of each pair, then the 8 row groups (lane bits 2..4)
+__device__ __forceinline__ float2 col_sum(float2 acc0, float2 acc1) {
+  float2 x = make_float2(acc0.x + acc0.y, acc1.x + acc1.y);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     x.x += __shfl_xor_sync(0xffffffffu, x.x, off);
@@ -176,52 +201,87 @@ __device__ __forceinline__ float2 col_sum(float2 x) {
   return x;
 }
 
+__device__ __forceinline__ float2 bcast(float x) { return make_float2(x, x); }
+
+// a [dk, dv] state in global memory <-> this thread's pairs (s[c][j] = rows 2 j, 2 j + 1 of column c)
+template <int DK>
+__device__ __forceinline__ void load_state(float2 (&s)[2][DK / 16], const float* base, int64_t dv, int r0, int col) {
+#pragma unroll
+  for (int j = 0; j < DK / 16; ++j) {
+    const float2 x = *reinterpret_cast<const float2*>(base + (int64_t)(r0 + 2 * j) * dv + col);
+    const float2 y = *reinterpret_cast<const float2*>(base + (int64_t)(r0 + 2 * j + 1) * dv + col);
+    s[0][j] = make_float2(x.x, y.x);
+    s[1][j] = make_float2(x.y, y.y);
+  }
+}
+template <int DK>
+__device__ __forceinline__ void store_state(const float2 (&s)[2][DK / 16], float* base, int64_t dv, int r0, int col) {
+#pragma unroll
+  for (int j = 0; j < DK / 16; ++j) {
+    *reinterpret_cast<float2*>(base + (int64_t)(r0 + 2 * j) * dv + col) = make_float2(s[0][j].x, s[1][j].x);
+    *reinterpret_cast<float2*>(base + (int64_t)(r0 + 2 * j + 1) * dv + col) = make_float2(s[0][j].y, s[1][j].y);
+  }
+}
+
 // S <- a S + b k (v - (a S)^T k)^T for one token
 template <int DK>
-__device__ __forceinline__ void fwd_step(float2 (&s)[DK / 8], const TokView<DK>& t) {
-  constexpr int RPT = DK / 8;
-  float2 pk = make_float2(0.f, 0.f);
+__device__ __forceinline__ void fwd_step(float2 (&s)[2][DK / 16], const TokView<DK>& t) {
+  constexpr int NPR = DK / 16;
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    s[i].x *= t.ar[i]; s[i].y *= t.ar[i];
-    pk.x = fmaf(s[i].x, t.kr[i], pk.x); pk.y = fmaf(s[i].y, t.kr[i], pk.y);
+  for (int j = 0; j < NPR; ++j) {
+    s[0][j] = __fmul2_rn(s[0][j], t.a2[j]);
+    s[1][j] = __fmul2_rn(s[1][j], t.a2[j]);
+    acc0 = __ffma2_rn(s[0][j], t.k2[j], acc0);
+    acc1 = __ffma2_rn(s[1][j], t.k2[j], acc1);
   }
-  pk = col_sum(pk);
-  const float2 d = make_float2(t.b * (t.vv.x - pk.x), t.b * (t.vv.y - pk.y));
+  const float2 pk = col_sum(acc0, acc1);
+  const float2 d0 = bcast(t.b * (t.vv.x - pk.x)), d1 = bcast(t.b * (t.vv.y - pk.y));
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    s[i].x = fmaf(t.kr[i], d.x, s[i].x); s[i].y = fmaf(t.kr[i], d.y, s[i].y);
+  for (int j = 0; j < NPR; ++j) {
+    s[0][j] = __ffma2_rn(t.k2[j], d0, s[0][j]);
+    s[1][j] = __ffma2_rn(t.k2[j], d1, s[1][j]);
   }
 }
 
 // the forward's state QDQ on the register state (E4M3: the slab is one tile, all 8 warps; INT8: a
 // block is one key row of 32 columns = warps 4 b .. 4 b + 3); barriers on both sides of the exchange
 template <int DK, bool KDA>
-__device__ __forceinline__ void state_qdq(float2 (&s)[DK / 8], int codec, BwdSmem<DK, KDA>& sm, int warp, int lane,
-                                          int rg, int cg) {
-  constexpr int RPT = DK / 8;
+__device__ __forceinline__ void state_qdq(float2 (&s)[2][DK / 16], int codec, BwdSmem<DK, KDA>& sm, int warp,
+                                          int lane, int rg, int cg) {
+  constexpr int RPT = DK / 8, NPR = RPT / 2;
+  const int r0 = RPT * rg;
   if (codec == 2) {
-    float m[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      m[i] = fmaxf(fabsf(s[i].x), fabsf(s[i].y));
-      m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 1));
-      m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 2));
-      if (cg == 0) sm.rmax[warp][rg + 8 * i] = m[i];
+    for (int j = 0; j < NPR; ++j) {
+      float m0 = fmaxf(fabsf(s[0][j].x), fabsf(s[1][j].x)), m1 = fmaxf(fabsf(s[0][j].y), fabsf(s[1][j].y));
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+      if (cg == 0) {
+        sm.rmax[warp][r0 + 2 * j] = m0;
+        sm.rmax[warp][r0 + 2 * j + 1] = m1;
+      }
     }
     __syncthreads();
     const int w0 = warp & ~3;
+    auto rowmax = [&](int row) {
+      return fmaxf(fmaxf(sm.rmax[w0][row], sm.rmax[w0 + 1][row]), fmaxf(sm.rmax[w0 + 2][row], sm.rmax[w0 + 3][row]));
+    };
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int row = rg + 8 * i;
-      const float bm = fmaxf(fmaxf(sm.rmax[w0][row], sm.rmax[w0 + 1][row]), fmaxf(sm.rmax[w0 + 2][row], sm.rmax[w0 + 3][row]));
-      const float sc = int8_scale(bm), rc = __frcp_rn(sc);
-      s[i] = make_float2(int8_qdq_rcp(s[i].x, rc, sc), int8_qdq_rcp(s[i].y, rc, sc));
+    for (int j = 0; j < NPR; ++j) {
+      const float sa = int8_scale(rowmax(r0 + 2 * j)), sb = int8_scale(rowmax(r0 + 2 * j + 1));
+      const float ra = __frcp_rn(sa), rb = __frcp_rn(sb);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        s[c][j] = make_float2(int8_qdq_rcp(s[c][j].x, ra, sa), int8_qdq_rcp(s[c][j].y, rb, sb));
     }
   } else {
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) amax = fmaxf(amax, fmaxf(fabsf(s[i].x), fabsf(s[i].y)));
+    for (int j = 0; j < NPR; ++j)
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(s[0][j].x), fabsf(s[0][j].y)), fmaxf(fabsf(s[1][j].x), fabsf(s[1][j].y))));
     amax = warp_max(amax);
     if (lane == 0) sm.wmax[warp] = amax;
     __syncthreads();
@@ -229,78 +289,102 @@ __device__ __forceinline__ void state_qdq(float2 (&s)[DK / 8], int codec, BwdSme
 #pragma unroll
     for (int w = 1; w < NW; ++w) tmax = fmaxf(tmax, sm.wmax[w]);
     const float sc = qdq_scale(tmax), rc = __frcp_rn(sc);
+    const float2 sc2 = bcast(sc), rc2 = bcast(rc);
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const __nv_fp8x2_e4m3 c(make_float2(__fmul_rn(s[i].x, rc), __fmul_rn(s[i].y, rc)));
-      const float2 f = static_cast<float2>(c);
-      s[i] = make_float2(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
-    }
+    for (int j = 0; j < NPR; ++j)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const __nv_fp8x2_e4m3 q(__fmul2_rn(s[c][j], rc2));
+        s[c][j] = __fmul2_rn(static_cast<float2>(q), sc2);
+      }
   }
   __syncthreads();   // the next QDQ's shared-memory writes come after every thread's reads
+}
+
+// Slot of key row `row` in a warp's row-sum array: rows r0 .. r0 + dk / 8 - 1 of row group rg are
+// permuted by xor with rg, so the stores of the 8 row groups (one row each) and the loads of 8
+// consecutive rows both fall in distinct banks.
+template <int DK>
+__device__ __forceinline__ int rs_slot(int row) {
+  constexpr int RPT = DK / 8;
+  const int g = row / RPT;
+  return RPT * g + ((row - RPT * g) ^ g);
 }
 
 // One token backward (header formulas) from P, the state before the token, with dS in ds (updated
 // to dS_{t-1}). Writes dv; leaves the token's four row sums of every key row in sm.rs[buf] and,
 // after the barrier, the reducing threads (the first dk) write the slab partials.
 template <int DK, bool KDA>
-__device__ __forceinline__ void bwd_token(const BwdParams& p, BwdSmem<DK, KDA>& sm, const float2 (&P)[DK / 8],
-                                          float2 (&ds)[DK / 8], const TokView<DK>& t, const unsigned char* rec,
+__device__ __forceinline__ void bwd_token(const BwdParams& p, BwdSmem<DK, KDA>& sm, const float2 (&P)[2][DK / 16],
+                                          float2 (&ds)[2][DK / 16], const TokView<DK>& t, const unsigned char* rec,
                                           int64_t tok, int h, int slab, int buf, int warp, int lane, int rg, int cg,
                                           int c0) {
-  constexpr int RPT = DK / 8;
-  float2 pp[RPT];   // P' = a o P
+  constexpr int RPT = DK / 8, NPR = RPT / 2;
+  float2 pp[2][NPR];   // P' = a o P
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) pp[i] = make_float2(t.ar[i] * P[i].x, t.ar[i] * P[i].y);
-  // u = v - P'^T k
-  float2 u = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    u.x = fmaf(pp[i].x, t.kr[i], u.x); u.y = fmaf(pp[i].y, t.kr[i], u.y);
+  for (int j = 0; j < NPR; ++j) {
+    pp[0][j] = __fmul2_rn(P[0][j], t.a2[j]);
+    pp[1][j] = __fmul2_rn(P[1][j], t.a2[j]);
+    acc0 = __ffma2_rn(pp[0][j], t.k2[j], acc0);
+    acc1 = __ffma2_rn(pp[1][j], t.k2[j], acc1);
   }
-  u = col_sum(u);
+  // u = v - P'^T k
+  float2 u = col_sum(acc0, acc1);
   u = make_float2(t.vv.x - u.x, t.vv.y - u.y);
   // dS += scale q do^T; du = b dS^T k
-  const float2 sdo = make_float2(p.scale * t.dov.x, p.scale * t.dov.y);
-  float2 du = make_float2(0.f, 0.f);
+  const float2 sdo0 = bcast(p.scale * t.dov.x), sdo1 = bcast(p.scale * t.dov.y);
+  acc0 = make_float2(0.f, 0.f);
+  acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    ds[i].x = fmaf(t.qr[i], sdo.x, ds[i].x); ds[i].y = fmaf(t.qr[i], sdo.y, ds[i].y);
-    du.x = fmaf(ds[i].x, t.kr[i], du.x); du.y = fmaf(ds[i].y, t.kr[i], du.y);
+  for (int j = 0; j < NPR; ++j) {
+    ds[0][j] = __ffma2_rn(t.q2[j], sdo0, ds[0][j]);
+    ds[1][j] = __ffma2_rn(t.q2[j], sdo1, ds[1][j]);
+    acc0 = __ffma2_rn(ds[0][j], t.k2[j], acc0);
+    acc1 = __ffma2_rn(ds[1][j], t.k2[j], acc1);
   }
-  du = col_sum(du);
+  float2 du = col_sum(acc0, acc1);
   du = make_float2(t.b * du.x, t.b * du.y);
   if (rg == 0) *reinterpret_cast<float2*>(p.grad_v + (tok * p.Hv + h) * p.dv + slab * SL + c0) = du;
-  // per key row, over this lane's 2 columns: x0 = S do (S = P' + b k u^T), x1 = dS u, x2 = P' du,
-  // x3 = dP' . P' with dP' = dS - k du^T; then a reduce-scatter over the lane quad leaves the quad's
-  // sum of x_cg in lane cg
-  const float2 bu = make_float2(t.b * u.x, t.b * u.y);
+  // per key-row pair, over this lane's 2 columns: X0 = S do (S = P' + b k u^T), X1 = dS u, X2 = P' du,
+  // X3 = dP' . P' with dP' = dS - k du^T; then a reduce-scatter over the lane quad leaves the quad's
+  // sum of X_cg in lane cg
+  const float2 bu0 = bcast(t.b * u.x), bu1 = bcast(t.b * u.y);
+  const float2 do0 = bcast(t.dov.x), do1 = bcast(t.dov.y);
+  const float2 u0 = bcast(u.x), u1 = bcast(u.y);
+  const float2 du0 = bcast(du.x), du1 = bcast(du.y), ndu0 = bcast(-du.x), ndu1 = bcast(-du.y);
   const bool hi = (cg & 2) != 0, lo = (cg & 1) != 0;
   float* rsb = reinterpret_cast<float*>(&sm.rs[buf][warp][0]);
+  const int r0 = RPT * rg;
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const float2 S = make_float2(fmaf(t.kr[i], bu.x, pp[i].x), fmaf(t.kr[i], bu.y, pp[i].y));
-    const float x0 = S.x * t.dov.x + S.y * t.dov.y;
-    const float x1 = ds[i].x * u.x + ds[i].y * u.y;
-    const float x2 = pp[i].x * du.x + pp[i].y * du.y;
-    const float2 dpp = make_float2(fmaf(-t.kr[i], du.x, ds[i].x), fmaf(-t.kr[i], du.y, ds[i].y));
+  for (int j = 0; j < NPR; ++j) {
+    const float2 S0 = __ffma2_rn(t.k2[j], bu0, pp[0][j]), S1 = __ffma2_rn(t.k2[j], bu1, pp[1][j]);
+    const float2 X0 = __ffma2_rn(S1, do1, __fmul2_rn(S0, do0));
+    const float2 X1 = __ffma2_rn(ds[1][j], u1, __fmul2_rn(ds[0][j], u0));
+    const float2 X2 = __ffma2_rn(pp[1][j], du1, __fmul2_rn(pp[0][j], du0));
+    const float2 dp0 = __ffma2_rn(t.k2[j], ndu0, ds[0][j]), dp1 = __ffma2_rn(t.k2[j], ndu1, ds[1][j]);
     // dg = (dL/da) a = <dP', P> a = <dP', P'> (per key row for KDA)
-    const float x3 = dpp.x * pp[i].x + dpp.y * pp[i].y;
-    ds[i] = make_float2(t.ar[i] * dpp.x, t.ar[i] * dpp.y);   // dS_{t-1}
-    float a0 = hi ? x2 : x0, a1 = hi ? x3 : x1;
-    a0 += __shfl_xor_sync(0xffffffffu, hi ? x0 : x2, 2);
-    a1 += __shfl_xor_sync(0xffffffffu, hi ? x1 : x3, 2);
-    float r = lo ? a1 : a0;
-    r += __shfl_xor_sync(0xffffffffu, lo ? a0 : a1, 1);
-    rsb[(rg + 8 * i) * 4 + cg] = r;
+    const float2 X3 = __ffma2_rn(dp1, pp[1][j], __fmul2_rn(dp0, pp[0][j]));
+    ds[0][j] = __fmul2_rn(t.a2[j], dp0);   // dS_{t-1}
+    ds[1][j] = __fmul2_rn(t.a2[j], dp1);
+    const float2 s0 = hi ? X0 : X2, s1 = hi ? X1 : X3;
+    float2 k0 = hi ? X2 : X0, k1 = hi ? X3 : X1;
+    k0 = __fadd2_rn(k0, make_float2(__shfl_xor_sync(0xffffffffu, s0.x, 2), __shfl_xor_sync(0xffffffffu, s0.y, 2)));
+    k1 = __fadd2_rn(k1, make_float2(__shfl_xor_sync(0xffffffffu, s1.x, 2), __shfl_xor_sync(0xffffffffu, s1.y, 2)));
+    const float2 sn = lo ? k0 : k1;
+    float2 r = lo ? k1 : k0;
+    r = __fadd2_rn(r, make_float2(__shfl_xor_sync(0xffffffffu, sn.x, 1), __shfl_xor_sync(0xffffffffu, sn.y, 1)));
+    rsb[rs_slot<DK>(r0 + 2 * j) * 4 + cg] = r.x;
+    rsb[rs_slot<DK>(r0 + 2 * j + 1) * 4 + cg] = r.y;
   }
   __syncthreads();
   // per key row cr (threads cr < DK): the slab's sums over its warps, in warp order
   if (threadIdx.x < DK) {
-    const int cr = threadIdx.x;
-    float4 a = sm.rs[buf][0][cr];
+    const int cr = threadIdx.x, slot = rs_slot<DK>(cr);
+    float4 a = sm.rs[buf][0][slot];
 #pragma unroll
     for (int w = 1; w < NW; ++w) {
-      const float4 x = sm.rs[buf][w][cr];
+      const float4 x = sm.rs[buf][w][slot];
       a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
     }
     const int64_t ph = (int64_t)slab * p.tokens * p.Hv + tok * p.Hv + h;   // slab partial index of (tok, h)
@@ -321,17 +405,20 @@ __device__ __forceinline__ void bwd_token(const BwdParams& p, BwdSmem<DK, KDA>& 
 
 template <int DK, bool KDA>
 __global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(const BwdParams p) {
-  constexpr int RPT = DK / 8;
+  constexpr int RPT = DK / 8, NPR = RPT / 2;
   using R = Rec<DK, KDA>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem<DK, KDA>& sm = *reinterpret_cast<BwdSmem<DK, KDA>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = lane >> 2, cg = lane & 3;
   const int c0 = warp * 8 + cg * 2;   // this lane's first column within the slab
+  const int r0 = RPT * rg;            // this lane's first key row
   const int nslab = p.dv / SL;
   const int64_t units = (int64_t)p.N * p.Hv * nslab;
   float2* const scr = reinterpret_cast<float2*>(p.scratch) + (int64_t)blockIdx.x * NSUB * RPT * NT;
-  auto sub_at = [&](int j, int i) { return scr + ((int64_t)j * RPT + i) * NT + tid; };
+  // thread-major copies of a register state: element (c, j) of sub-chunk checkpoint q / slot m
+  auto sub_at = [&](int q, int c, int j) { return scr + ((int64_t)q * RPT + c * NPR + j) * NT + tid; };
+  auto slot_at = [&](int m, int c, int j) { return &sm.slot[m][c * NPR + j][tid]; };
   int tc = 0;   // backward tokens so far (selects the row-sum buffer)
 
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
@@ -345,16 +432,18 @@ __global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(const BwdParams p) {
     const int64_t nch = (len + kChunk - 1) / kChunk;
     const int64_t slot0 = t0 / kChunk + n;
     const int64_t st = (int64_t)DK * p.dv;   // one state
-    auto srow = [&](const float* base, int i) { return base + (int64_t)(rg + 8 * i) * p.dv + col; };
     auto ck = [&](int64_t c) { return p.ckpt + ((slot0 + c) * p.Hv + h) * st; };
     TokView<DK> tv;
 
     // ---- pass 1: the forward recurrence, storing the state entering every chunk; the tokens
     // stream through the two halves of the staging area, 32 at a time ----
-    float2 s[RPT];
+    float2 s[2][NPR];
+    if (p.h0) {
+      load_state<DK>(s, p.h0 + nh * st, p.dv, r0, col);
+    } else {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
-      s[i] = p.h0 ? *reinterpret_cast<const float2*>(srow(p.h0 + nh * st, i)) : make_float2(0.f, 0.f);
+      for (int j = 0; j < NPR; ++j) s[0][j] = s[1][j] = make_float2(0.f, 0.f);
+    }
     const int64_t nblk = (len + 31) / 32;
     __syncthreads();   // the previous unit's last reads of the staging area are done
     for (int64_t b = 0; b < 2 && b < nblk; ++b) {
@@ -371,10 +460,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(const BwdParams p) {
       __syncthreads();
       for (int r = 0; r < nb; ++r) {
         const int64_t t = 32 * b + r;
-        if (t % kChunk == 0) {
-#pragma unroll
-          for (int i = 0; i < RPT; ++i) *reinterpret_cast<float2*>(const_cast<float*>(srow(ck(t / kChunk), i))) = s[i];
-        }
+        if (t % kChunk == 0) store_state<DK>(s, ck(t / kChunk), p.dv, r0, col);
         read_token<DK, KDA>(half + r * R::BYTES, rg, c0, false, tv);
         fwd_step<DK>(s, tv);
         if (p.state_qdq && (t + 1) % kChunk == 0) state_qdq<DK, KDA>(s, p.state_qdq, sm, warp, lane, rg, cg);
@@ -387,10 +473,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(const BwdParams p) {
     }
 
     // ---- pass 2: chunks in reverse; dS in registers ----
-    float2 ds[RPT];
+    float2 ds[2][NPR];
+    if (p.dhT) {
+      load_state<DK>(ds, p.dhT + nh * st, p.dv, r0, col);
+    } else {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
-      ds[i] = p.dhT ? *reinterpret_cast<const float2*>(srow(p.dhT + nh * st, i)) : make_float2(0.f, 0.f);
+      for (int j = 0; j < NPR; ++j) ds[0][j] = ds[1][j] = make_float2(0.f, 0.f);
+    }
     for (int64_t c = nch - 1; c >= 0; --c) {
       const int L = (int)min((int64_t)kChunk, len - c * kChunk);
       const int64_t tc0 = t0 + c * kChunk;
@@ -403,51 +492,62 @@ __global__ void __launch_bounds__(NT, 1) chunk_bwd_kernel(const BwdParams p) {
       __syncthreads();
       // the sub-chunk checkpoints: the state before tokens 0, 4, .., 4 (jmax - 1) to the scratch; the
       // state before token 4 jmax stays in registers
-#pragma unroll
-      for (int i = 0; i < RPT; ++i) s[i] = *reinterpret_cast<const float2*>(srow(ck(c), i));
+      load_state<DK>(s, ck(c), p.dv, r0, col);
       const int jmax = (L - 1) / SUB;
       for (int r = 0; r < SUB * jmax; ++r) {
         if (r % SUB == 0) {
 #pragma unroll
-          for (int i = 0; i < RPT; ++i) *sub_at(r / SUB, i) = s[i];
+          for (int j = 0; j < NPR; ++j) {
+            *sub_at(r / SUB, 0, j) = s[0][j];
+            *sub_at(r / SUB, 1, j) = s[1][j];
+          }
         }
         read_token<DK, KDA>(sm.stage + r * R::BYTES, rg, c0, false, tv);
         fwd_step<DK>(s, tv);
       }
-      for (int j = jmax; j >= 0; --j) {
-        if (j < jmax) {
+      for (int q = jmax; q >= 0; --q) {
+        if (q < jmax) {
 #pragma unroll
-          for (int i = 0; i < RPT; ++i) s[i] = *sub_at(j, i);
+          for (int j = 0; j < NPR; ++j) {
+            s[0][j] = *sub_at(q, 0, j);
+            s[1][j] = *sub_at(q, 1, j);
+          }
         }
-        const int r0 = SUB * j, cnt = min(SUB, L - r0);
-        // the states before tokens r0 .. r0 + cnt - 2 into this thread's slots; s ends as the state
+        const int rq = SUB * q, cnt = min(SUB, L - rq);
+        // the states before tokens rq .. rq + cnt - 2 into this thread's slots; s ends as the state
         // before the sub-chunk's last token
         for (int m = 0; m + 1 < cnt; ++m) {
 #pragma unroll
-          for (int i = 0; i < RPT; ++i) sm.slot[m][i][tid] = s[i];
-          read_token<DK, KDA>(sm.stage + (r0 + m) * R::BYTES, rg, c0, false, tv);
+          for (int j = 0; j < NPR; ++j) {
+            *slot_at(m, 0, j) = s[0][j];
+            *slot_at(m, 1, j) = s[1][j];
+          }
+          read_token<DK, KDA>(sm.stage + (rq + m) * R::BYTES, rg, c0, false, tv);
           fwd_step<DK>(s, tv);
         }
         for (int m = cnt - 1; m >= 0; --m) {
-          float2 P[RPT];
+          float2 P[2][NPR];
           if (m == cnt - 1) {
 #pragma unroll
-            for (int i = 0; i < RPT; ++i) P[i] = s[i];
+            for (int j = 0; j < NPR; ++j) {
+              P[0][j] = s[0][j];
+              P[1][j] = s[1][j];
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < RPT; ++i) P[i] = sm.slot[m][i][tid];
+            for (int j = 0; j < NPR; ++j) {
+              P[0][j] = *slot_at(m, 0, j);
+              P[1][j] = *slot_at(m, 1, j);
+            }
           }
-          const unsigned char* rec = sm.stage + (r0 + m) * R::BYTES;
+          const unsigned char* rec = sm.stage + (rq + m) * R::BYTES;
           read_token<DK, KDA>(rec, rg, c0, true, tv);
-          bwd_token<DK, KDA>(p, sm, P, ds, tv, rec, tc0 + r0 + m, h, slab, tc & 1, warp, lane, rg, cg, c0);
+          bwd_token<DK, KDA>(p, sm, P, ds, tv, rec, tc0 + rq + m, h, slab, tc & 1, warp, lane, rg, cg, c0);
           ++tc;
         }
       }
     }
-    if (p.dh0) {
-#pragma unroll
-      for (int i = 0; i < RPT; ++i) *reinterpret_cast<float2*>(p.dh0 + nh * st + (int64_t)(rg + 8 * i) * p.dv + col) = ds[i];
-    }
+    if (p.dh0) store_state<DK>(ds, p.dh0 + nh * st, p.dv, r0, col);
   }
 }
 
