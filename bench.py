@@ -423,7 +423,7 @@ class BwdCase(PrefillCase):
         self.launches = 5   # the backward kernel and the sums of the dq, dk, dbeta, dg partials
 
     def scope(self):
-        return "one step = chunk_bwd_kernel + 4 sum_parts_kernel; achieved is over all of them"
+        return "one step = chunk_bwd_kernel + 4 partial-sum launches (sum_parts4_kernel); achieved is over all of them"
 
     def workspace_bytes(self):
         return self.gdn.chunk_bwd_workspace_bytes(self.x.q.shape, self.x.v.shape, self.cu, kda=self.x.kda)

@@ -565,6 +565,23 @@ __global__ void sum_parts_kernel(const float* __restrict__ part, float* __restri
   }
 }
 
+// The same sums, four consecutive outputs per thread as float4 (when inner is a multiple of 4, or
+// inner = G = 1, the four sources of every term are consecutive; sizes, strides and the output
+// are 16-byte aligned), each output summed in the same order as above.
+__global__ void sum_parts4_kernel(const float4* __restrict__ part, float4* __restrict__ out, int64_t n_out4, int nslab,
+                                  int64_t slab_stride4, int G, int inner4) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_out4; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t base = (e / inner4) * G * inner4 + e % inner4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nslab; ++s)
+      for (int j = 0; j < G; ++j) {
+        const float4 x = part[s * slab_stride4 + base + (int64_t)j * inner4];
+        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+      }
+    out[e] = acc;
+  }
+}
+
 constexpr int kBwdCtas = 152;   // one CTA per GB300 SM at most; each owns a sub-chunk scratch
 
 template <int DK, bool KDA>
@@ -584,8 +601,17 @@ cudaError_t launch_t(const BwdParams& bp, int64_t units, cudaStream_t stream) {
 cudaError_t sum_parts(const float* part, float* out, int64_t n_out, int nslab, int64_t slab_stride, int G, int inner,
                       cudaStream_t stream) {
   if (n_out == 0) return cudaSuccess;
-  const int64_t blocks = (n_out + 255) / 256 < 152 * 32 ? (n_out + 255) / 256 : 152 * 32;
-  sum_parts_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, out, n_out, nslab, slab_stride, G, inner);
+  const bool vec = n_out % 4 == 0 && slab_stride % 4 == 0 && (inner % 4 == 0 || (inner == 1 && G == 1)) &&
+                   (reinterpret_cast<uintptr_t>(part) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+  if (vec) {
+    const int64_t n4 = n_out / 4, blocks = (n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16;
+    sum_parts4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(part),
+                                                            reinterpret_cast<float4*>(out), n4, nslab, slab_stride / 4,
+                                                            G, inner == 1 ? 1 : inner / 4);
+  } else {
+    const int64_t blocks = (n_out + 255) / 256 < 152 * 32 ? (n_out + 255) / 256 : 152 * 32;
+    sum_parts_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, out, n_out, nslab, slab_stride, G, inner);
+  }
   return cudaGetLastError();
 }
 

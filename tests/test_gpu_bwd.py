@@ -54,6 +54,15 @@ def test_bwd_state_qdq(gdn, oracle_mod, kda, codec):
     run(gdn, oracle_mod, x, True, codec=codec, seed=2)
 
 
+@pytest.mark.parametrize("kda", [False, True])
+def test_bwd_more_units_than_ctas(gdn, oracle_mod, kda):
+    """160 (sequence, head, slab) units on a grid of at most one CTA per SM: some CTAs walk a
+    second unit (persistent loop), with ragged lengths and state QDQ on."""
+    lens = torch.randint(1, 90, (40,), generator=torch.Generator().manual_seed(97)).tolist()
+    x = workloads.prefill(1, 0, 2, 4, 64, 64, seed=98 + kda, kda=kda, h0_std=0.1, seqlens=lens)
+    run(gdn, oracle_mod, x, True, seed=4)
+
+
 def test_bwd_dense_no_final_grad(gdn, oracle_mod):
     x = workloads.prefill(2, 96, 2, 2, 128, 128, seed=95, h0_std=0.1)
     run(gdn, oracle_mod, x, True, with_dhT=False, seed=3)
