@@ -51,6 +51,14 @@ def algorithmic(x):
     return by, (fl_th * pre + 7 * s["dk"] * s["dv"] * (tok - pre)) * s["Hv"]
 
 
+def alu_peak(dev, torch, sm_max_mhz):
+    """fp32 CUDA-core peak in TFLOP/s from unit counts and clocks: SMs x 128 fp32 lanes x 2 flop
+    (an FMA) x the maximum SM clock (the sampled clocks.max.sm, else 2070 MHz)."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = sm_max_mhz or 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 fp32 lanes x 2 flop x {mhz:.0f} MHz"
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -78,6 +86,8 @@ PROFILES = {
                                  ("qdq.cu", "gdnqat_api.cu", "common.cuh", "tc_epilogue.cuh", "tc_common.cuh",
                                   "kernels.h")),
     "gdn_bwd_b4_h16_t4096_d128": ("chunk_bwd_gdn_bwd_b4_h16_t4096_d128.md",
+                                  ("backward.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
+    "kda_bwd_b2_h32_t8192_d128": ("chunk_bwd_kda_bwd_b2_h32_t8192_d128.md",
                                   ("backward.cu", "gdnqat_api.cu", "common.cuh", "kernels.h")),
     "kda_b2_h32_t8192_d128": ("chunk_fwd_kda_b2_h32_t8192_d128.md",
                               ("chunk_prep_kda.cu", "chunk_chain_kda.cu", "tma_maps.cu", "gdnqat_api.cu", "common.cuh",
@@ -418,9 +428,12 @@ class BwdCase(PrefillCase):
         self.bytes = tok * (Hqk * 2 * dk * 2 + Hv * (2 * dv + 4 * gk + 4 + 4 * dv)) + \
             tok * (Hqk * 2 * dk * 4 + Hv * (4 * dv + 4 * gk + 4)) + \
             (2 if x.h0 is not None else 1) * s["N"] * Hv * dk * dv * 4
-        # two forward passes (the checkpointing pass and the per-chunk recompute) and the backward
-        self.flops = tok * Hv * (2 * 7 + 12) * dk * dv
+        # per token and state element: the forward step that rebuilds the state (decay 1, S^T k 2,
+        # k d^T 2) and the backward step (P' 1, u 2, dS += q do^T 2, du 2, S 2, the four row sums
+        # 8, dP' 2, dS_{t-1} 1); the kernel's extra recomputes are not counted
+        self.flops = tok * Hv * (5 + 20) * dk * dv
         self.launches = 5   # the backward kernel and the sums of the dq, dk, dbeta, dg partials
+        self.bound = "alu"  # fp32 arithmetic on the CUDA cores (issue-bound, not DRAM-bound)
 
     def scope(self):
         return "one step = chunk_bwd_kernel + 4 partial-sum launches (sum_parts4_kernel); achieved is over all of them"
@@ -579,6 +592,7 @@ METRICS = {
     "qdq_state_n512_h32_d128": "standalone FP8 tile QDQ elements/s (16384 x [128 x 128] fp32, 64-column tiles)",
     "int8_state_n512_h32_d128": "standalone INT8 block QDQ elements/s (16384 x [128 x 128] fp32, 32-column blocks)",
     "gdn_bwd_b4_h16_t4096_d128": "GDN backward tokens/s (B4 H16 T4096 d128, straight-through FP8 state QDQ)",
+    "kda_bwd_b2_h32_t8192_d128": "KDA backward tokens/s (B2 H32 T8192 d128, straight-through FP8 state QDQ)",
     "gdn_decode_int8_n512_h32_d128_s64": "GDN decode tokens/s (N512 H32 d128, per-token INT8 block-32 state QDQ)",
     "gdn_b1_h2_t256_d64": "GDN chunked-prefill tokens/s (B1 H2 T256 d64, FP8 state QDQ)",
     "handoff_n256_t128_p64_h16_d128": "GDN prefill->decode handoff tokens/s (256 seqs x 128 tokens, 64-token "
@@ -710,6 +724,13 @@ def run_gpu(args):
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": args.steps * case.launches,
                 "clocks": clocks.summary()}
+        if getattr(case, "bound", "hbm") == "alu":
+            clk = line["clocks"].get("sm_max_mhz") if isinstance(line["clocks"], dict) else None
+            peak, psrc = alu_peak(dev, torch, clk)
+            r = line["roofline"]
+            tflops = case.flops / (launch_ms * 1e-3) / 1e12
+            r.update({"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                      "peak_source": psrc, "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm})
         if world == 1 and not args.no_cpu_baseline and isinstance(case, PrefillCase) and args.workload == WORKLOAD:
             line["cpu_baseline"] = cpu_baseline(x)
         print(json.dumps(line), flush=True)

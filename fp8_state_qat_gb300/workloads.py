@@ -167,6 +167,10 @@ WORKLOADS = {
     "gdn_bwd_b4_h16_t4096_d128": lambda: _backward(prefill(4, 4096, 16, 16, 128, 128, seed=1, h0_std=0.1,
                                                            state_qdq=True, w_qdq=False,
                                                            name="gdn_bwd_b4_h16_t4096_d128")),
+    # the backward of the KDA benchmark's shape (state QDQ straight through, no W QDQ)
+    "kda_bwd_b2_h32_t8192_d128": lambda: _backward(prefill(2, 8192, 32, 32, 128, 128, seed=4, kda=True, h0_std=0.1,
+                                                           state_qdq=True, w_qdq=False,
+                                                           name="kda_bwd_b2_h32_t8192_d128")),
     # the decode workload with the INT8 block-32 state codec
     "gdn_decode_int8_n512_h32_d128_s64": lambda: decode(64, 512, 32, 128, 128, seed=3, state_std=0.05,
                                                         name="gdn_decode_int8_n512_h32_d128_s64", codec="int8"),
