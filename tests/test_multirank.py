@@ -49,3 +49,14 @@ def test_max_over_ranks_and_job_rate(world):
 def test_single_rank_is_local():
     assert bench.max_over_ranks(5.0, 1, torch.device("cpu")) == 5.0
     assert bench.job_rate(500, 1, 2.0) == pytest.approx(250000.0)
+
+
+def test_alu_peak_from_unit_counts():
+    """The fp32 CUDA-core peak of an ALU-bound line: SMs x 128 lanes x 2 flop x the maximum SM clock
+    (the sampled one, else 2070 MHz)."""
+    import types
+    props = types.SimpleNamespace(multi_processor_count=152)
+    fake = types.SimpleNamespace(cuda=types.SimpleNamespace(get_device_properties=lambda dev: props))
+    peak, src = bench.alu_peak(None, fake, 2070.0)
+    assert abs(peak - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9 and "152 SMs" in src
+    assert bench.alu_peak(None, fake, None)[0] == peak
