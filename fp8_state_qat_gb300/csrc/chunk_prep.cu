@@ -17,7 +17,7 @@
 // uses all 128 TMEM lanes (one key channel per thread).
 //
 // None of this depends on the state, so a chunk never waits for the one before it: the grid is
-// (slots x v-heads) CTAs of 128 threads, three resident per SM. Every mbarrier wait is bounded;
+// (slots x v-heads) CTAs of 128 threads, four resident per SM. Every mbarrier wait is bounded;
 // a CTA whose wait gives up records it in the status word, stores nothing, waits (bounded) for its
 // TMA load in flight, frees its TMEM and exits.
 #include "common.cuh"
@@ -36,10 +36,12 @@ constexpr uint32_t OFF_K = 0;                          // K tile: key columns 0-
 constexpr uint32_t OFF_A = 16 * KB;                    // A fp32 [64][68]; after the solve: T'' hi | lo
 constexpr uint32_t OFF_T = 34 * KB;                    // T fp32 [64][68]
 constexpr uint32_t OFF_SCR = OFF_T + 64 * A_LD * 4;    // solve scratch, 3 x 16 x 16 fp32
-constexpr uint32_t OFF_W = 54 * KB;                    // T' hi | lo; after the W MMA: W^T codes (or hi)
-constexpr uint32_t OFF_VEC = 70 * KB;                  // gam, Gam, decay-to-end, beta [64]; 4 partial maxima
-constexpr uint32_t kSmemBytes = OFF_VEC + 4 * 256 + 64 + 1024;   // + slack to align the base
-static_assert(OFF_SCR + 3 * 1024 <= OFF_W, "solve scratch overlaps the W region");
+constexpr uint32_t OFF_W = OFF_T;                      // T' hi | lo over T once T is read; after the W MMA: W^T codes (or hi)
+constexpr uint32_t OFF_VEC = OFF_SCR + 3 * KB;         // gam, Gam, beta [64]; 4 partial maxima
+constexpr uint32_t kSmemBytes = OFF_VEC + 3 * 256 + 64 + 1024;   // + slack to align the base
+static_assert(OFF_W + 16 * KB <= OFF_SCR, "T' overlaps the solve scratch");
+// four CTAs per SM: shared memory (with the 1 KB each CTA reserves) and TMEM columns fit exactly
+static_assert(4 * (kSmemBytes + 1024) <= 228 * KB, "four CTAs per SM no longer fit");
 
 constexpr uint32_t TM_G = 0, TM_WT = 64;
 constexpr uint32_t kTmemCols = 128;
@@ -61,7 +63,7 @@ __device__ __forceinline__ int64_t seq_start(const PrepParams& p, int n) {
   return p.cu ? (int64_t)p.cu[n] : (int64_t)n * p.T;
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap twt,
                   const __grid_constant__ CUtensorMap ttt, const PrepParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -96,8 +98,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   float* const scr = reinterpret_cast<float*>(sm + OFF_SCR);
   float* const vgam = reinterpret_cast<float*>(sm + OFF_VEC);
   float* const vegam = vgam + 64;
-  float* const vbeta = vgam + 192;
-  float* const red = vgam + 256;
+  float* const vbeta = vgam + 128;
+  float* const red = vgam + 192;
   const uint32_t bar_k = tc::smem_u32(&bars[0]), bar_g = tc::smem_u32(&bars[1]), bar_w = tc::smem_u32(&bars[2]);
 
   if (tid == 0) {
@@ -261,12 +263,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       __syncthreads();
     }
 
-    // ---- T'' = T diag(beta) -> the A region, T' = T'' diag(Gam) -> the W region (bf16 hi | lo, [r][i]) ----
-#pragma unroll 1
+    // ---- T'' = T diag(beta) -> the A region, T' = T'' diag(Gam) -> the W region (bf16 hi | lo, [r][i]),
+    // which lies over T: every thread reads its T entries before any writes ----
+    float4 tr[8];
+#pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int task = tid + t * kThreads, r = task >> 3, i0 = (task & 7) * 8;
-      const float4 ta = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
-      const float4 tb = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
+      tr[2 * t] = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0);
+      tr[2 * t + 1] = *reinterpret_cast<const float4*>(Tm + r * A_LD + i0 + 4);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int task = tid + t * kThreads, r = task >> 3, i0 = (task & 7) * 8;
+      const float4 ta = tr[2 * t], tb = tr[2 * t + 1];
       const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
       float t2[8], t1[8];
 #pragma unroll
