@@ -97,3 +97,37 @@ def test_bwd_full_size_sampled(gdn, oracle_mod):
         for name, a, b in zip(NAMES, got, ref):
             e = rel(a[sel[name]], b[sel[name]])
             assert e <= TOL_QDQ, (name, n, h, e)
+
+
+def test_kda_bwd_full_size_consistency(gdn, oracle_mod):
+    """The KDA backward workload (B2 H32 T8192 d128, state QDQ straight through) in the launch
+    configuration bench.py times. A unit's gradients depend only on its own sequence and head
+    (no GQA here) and the kernels sum in a fixed order, so sequence 1's gradients must equal, bit
+    for bit, those of the same call on sequence 1 alone. Its first 512 tokens, run alone, are
+    checked against the oracle for one (sequence, head) unit."""
+    from oracle.grad import gdn_recurrent_grads
+    x = workloads.workload("kda_bwd_b2_h32_t8192_d128")
+    gen = torch.Generator().manual_seed(13)
+    dout = torch.randn((2, 8192, 32, 128), generator=gen)
+    c = to_cuda(x)
+    full = gdn.kda_chunk_bwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], None, dout.cuda(), state_qdq=True)
+    one = lambda t: t[1:2].contiguous()
+    alone = gdn.kda_chunk_bwd(one(c["q"]), one(c["k"]), one(c["v"]), one(c["g"]), one(c["beta"]), one(c["h0"]), None,
+                              dout[1:2].contiguous().cuda(), state_qdq=True)
+    torch.cuda.synchronize()
+    for name, a, b in zip(NAMES, full, alone):
+        assert torch.equal(a[1:2], b), name
+    T = 512
+    pre = lambda t: t[1:2, :T].contiguous()
+    got = gdn.kda_chunk_bwd(pre(c["q"]), pre(c["k"]), pre(c["v"]), pre(c["g"]), pre(c["beta"]), one(c["h0"]), None,
+                            dout[1:2, :T].contiguous().cuda(), state_qdq=True)
+    torch.cuda.synchronize()
+    h = 21
+    ref = gdn_recurrent_grads(x.q[1:2, :T], x.k[1:2, :T], x.v[1:2, :T], x.g[1:2, :T], x.beta[1:2, :T], x.h0[1:2],
+                              None, dout[1:2, :T].double(), None, kda=True, state_qdq=True, units=[(0, h)])[:6]
+    got = [t.cpu().double().numpy() for t in got]
+    sel = {"dq": (0, slice(None), h), "dk": (0, slice(None), h), "dv": (0, slice(None), h),
+           "dg": (0, slice(None), h), "dbeta": (0, slice(None), h), "dh0": (0, h)}
+    for name, a, b in zip(NAMES, got, ref):
+        e = rel(a[sel[name]], b[sel[name]])
+        assert e <= TOL_QDQ, (name, e)
