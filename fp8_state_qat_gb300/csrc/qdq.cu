@@ -30,11 +30,19 @@ __device__ __forceinline__ float quotient(float x, float s, float r) {
   const float e = __fmaf_rn(-q0, s, x);
   return copysignf(__fmaf_rn(e, r, q0), x);
 }
+// The same for two elements with the paired fp32 instructions (each component rounded as the
+// scalar form rounds it): ns2 = (-s, -s), r2 = (r, r).
+__device__ __forceinline__ float2 quotient2(float2 x, float2 ns2, float2 r2) {
+  const float2 q0 = __fmul2_rn(x, r2);
+  const float2 e = __ffma2_rn(q0, ns2, x);
+  const float2 q1 = __ffma2_rn(e, r2, q0);
+  return make_float2(copysignf(q1.x, x.x), copysignf(q1.y, x.y));
+}
 __device__ __forceinline__ float2 qdq_exact2(float a, float b, float s, float r, bool fast) {
-  const float2 y = fast ? make_float2(quotient(a, s, r), quotient(b, s, r)) : make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+  const float2 y = fast ? quotient2(make_float2(a, b), make_float2(-s, -s), make_float2(r, r))
+                        : make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
   const __nv_fp8x2_e4m3 c(y);          // cvt.rn.satfinite.e4m3x2.f32
-  const float2 cf = static_cast<float2>(c);
-  return make_float2(__fmul_rn(cf.x, s), __fmul_rn(cf.y, s));
+  return __fmul2_rn(static_cast<float2>(c), make_float2(s, s));
 }
 
 __device__ __forceinline__ float block_max(float v, float* red) {
@@ -242,11 +250,15 @@ int8_block32_qdq_kernel(const float4* x, float4* y, float* __restrict__ scales, 
       if (scales && (lane & 7) == 0) scales[blk] = s;
       const bool fast = s >= 1.17549435e-38f;
       const float rs = fast ? __frcp_rn(s) : 0.0f;
-      auto q = [&](float e) {
-        const float t = fast ? quotient(e, s, rs) : __fdiv_rn(e, s);
-        return __fmul_rn(fminf(fmaxf(rintf(t), -kInt8Max), kInt8Max), s);
+      auto q2 = [&](float a, float b) {   // codes: nearest integer of the quotient within +-127
+        const float2 t = fast ? quotient2(make_float2(a, b), make_float2(-s, -s), make_float2(rs, rs))
+                              : make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+        const float2 c = make_float2(fminf(fmaxf(rintf(t.x), -kInt8Max), kInt8Max),
+                                     fminf(fmaxf(rintf(t.y), -kInt8Max), kInt8Max));
+        return __fmul2_rn(c, make_float2(s, s));
       };
-      __stcs(y + blk * 8 + (lane & 7), make_float4(q(v[u].x), q(v[u].y), q(v[u].z), q(v[u].w)));
+      const float2 lo = q2(v[u].x, v[u].y), hi = q2(v[u].z, v[u].w);
+      __stcs(y + blk * 8 + (lane & 7), make_float4(lo.x, lo.y, hi.x, hi.y));
     }
   }
 }
