@@ -95,12 +95,21 @@ PROFILES = {
 }
 
 
+def code_only(text):
+    """C / CUDA source without its comments and trailing blanks: what the compiler sees (the
+    sources have no string literal holding a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(sources=PREFILL_SOURCES):
+    """Hash of the code (comments excluded) of the sources that build a step's kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_state_qat_gb300", "csrc")
     for name in sorted(sources):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

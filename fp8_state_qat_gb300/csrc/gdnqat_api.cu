@@ -1,9 +1,9 @@
 // gdnqat_api.cu -- the extern "C" surface declared in include/gdnqat.h.
 //
 // Every entry point validates its arguments on the host, then probes the current device,
-// and only then enqueues work; a non-OK status means nothing was launched ("GDN state/W QAT
-// foundation": requirements are enforced by explicit errors raised before any kernel
-// launches). The library allocates nothing.
+// and only then enqueues work; a non-OK status means nothing was launched (per "GDN state/W QAT
+// foundation", unmet hardware or version requirements fail with an error before any kernel
+// runs). The library allocates nothing.
 #include <atomic>
 #include <cstring>
 

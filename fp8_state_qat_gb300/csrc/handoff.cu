@@ -7,7 +7,7 @@
 // handoff and every remaining token is a decode step on the sequence's own tokens (teacher
 // forced): read the state, S' = a S (KDA: row c scaled by a[c]), d = b (v - S'^T k),
 // S = S' + k d^T, o = scale S^T q from the updated state, then QDQ (E4M3: all dk rows x 64 value
-// columns per tile, scale amax / 448 with a zero guard; INT8: one key row x 32 value columns per
+// columns per tile, scale amax / 448, 1 for an all-zero tile; INT8: one key row x 32 value columns per
 // block, amax / 127) before the state is stored for the next token.
 //
 // One CTA per (sequence, head) keeps the state in registers across all of the sequence's

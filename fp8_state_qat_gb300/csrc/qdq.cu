@@ -1,7 +1,7 @@
 // qdq.cu -- standalone dynamic per-tile FP8 E4M3 fake quantize-dequantize.
 //
-// "GDN state/W QAT foundation", "What does this PR do?": each tile has its own scalar
-// scale amax / 448 with a zero guard, and a QDQ helper applies a supplied scale. One CTA
+// "GDN state/W QAT foundation", "What does this PR do?": one scale per tile, amax / 448 (1 for
+// an all-zero tile); the page's helper applies a scale it is given. One CTA
 // per tile: max|x| over the tile (max is exact, so the order does not matter), then
 // E4M3(x / s) * s with x / s correctly rounded. HBM-bound: 4 bytes read + 4 bytes written per
 // element. Three launch forms, by shape: whole rows of a leading index per CTA (state and W

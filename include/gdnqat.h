@@ -4,13 +4,13 @@
  * Sources (pages of the NVIDIA/Model-Optimizer pull requests on the method):
  *  [F] "GDN state/W QAT foundation", "What does this PR do?": the fused path uses chunk
  *      size 64; state QDQ at each 64-token boundary with amax recomputed over each
- *      full-key x 64-value-column tile, per sequence and head, scale = amax / 448 with a
- *      zero guard; a separate dynamic FP8 QDQ of the WY-transformed W; quantizers start
+ *      full-key x 64-value-column tile, per sequence and head, scale = amax / 448 (1 for an
+ *      all-zero tile); a separate dynamic FP8 QDQ of the WY-transformed W; quantizers start
  *      disabled; a supplied-scale QDQ helper; errors are raised before any launch.
  *  [D] "Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD
- *      workflow", step 3: a decode token reads the stored state, computes its output from
- *      the updated working state, then applies QDQ before storing; state stays in
- *      floating-point storage.
+ *      workflow", step 3: per decode token the stored state is loaded and updated, the
+ *      output is taken from that updated (not yet quantized) state, and the state is QDQ'd
+ *      before it is written back; the stored state keeps a floating-point type.
  *  [K] "Add KDA prefill numerical emulation for QAT", "What does this PR do?": KDA uses
  *      per-key-channel retention, with causal pairwise decays from prefix differences.
  *  [R] "Add experimental GDN/KDA decode and replay QAT", "What does this PR do?":
@@ -200,7 +200,7 @@ gdn_status kda_chunk_bwd(const gdn_chunk_args* args, const gdn_chunk_grads* grad
 /* Prefill -> decode handoff ([H]: "Torch GDN/KDA decode QAT with INT8 recurrent state",
  * "Megatron-Core QAT/QAD workflow", steps 2-3 and the "Ordinary state-QDQ path" flowchart).
  * Per sequence n of length L_n, the first P_n = prefill_lengths_host[n] tokens run as chunked
- * prefill from h0 that produces a state WITHOUT internal state QDQ (W QDQ as GDN_FLAG_W_QDQ
+ * prefill from h0 whose state is NOT quantized inside the prefix (W QDQ as GDN_FLAG_W_QDQ
  * asks); when P_n < L_n, the state is QDQ'd at the handoff (GDN_FLAG_STATE_QDQ) and every
  * remaining token is a decode step on the sequence's own q, k, v, g, beta (teacher forced):
  * read the state, decay, delta update, o from the updated state, then QDQ
@@ -232,7 +232,7 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            int32_t Hv, int32_t dk, int32_t dv, float scale, uint32_t flags,
                            gdn_stream_t stream);
 
-/* Standalone dynamic tile QDQ ([F]: amax / 448 with a zero guard, E4M3). x, y: device fp32
+/* Standalone dynamic tile QDQ ([F]: E4M3, scale amax / 448, 1 for an all-zero tile). x, y: device fp32
  * [lead, rows, cols] (y may equal x); a tile is all `rows` rows x `tile_cols` columns of one
  * leading index (the last tile may be narrower). scales: device fp32 [lead, ceil(cols /
  * tile_cols)] or NULL. Per tile, in fp32 with IEEE round-to-nearest: amax = max |x|,

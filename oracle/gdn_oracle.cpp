@@ -9,31 +9,31 @@
 // Sources (web pages of the NVIDIA/Model-Optimizer pull requests on the method):
 //   [F]  "GDN state/W QAT foundation" (#2497), section "What does this PR do?":
 //        state QDQ at 64-token boundaries, one scale per full-key x 64-value-column
-//        tile per sequence and head, scale = amax / 448 with a zero guard, E4M3
+//        tile per sequence and head, scale = amax / 448 (1 for an all-zero tile), E4M3
 //        (num_bits (4,3)); independent dynamic FP8 QDQ of the WY-transformed W.
 //   [D]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519), section
-//        "Megatron-Core QAT/QAD workflow", step 3: each decode token reads the stored
-//        state, computes its output from the updated working state, then applies QDQ
-//        before storing the state for the next token.
+//        "Megatron-Core QAT/QAD workflow", step 3: per decode token the stored state is
+//        loaded and updated, the output comes from that updated state before any
+//        quantization, and the state is QDQ'd before it is written back for the next token.
 //   [K]  "Add KDA prefill numerical emulation for QAT" (#2506), section "What does
 //        this PR do?": KDA has per-key-channel retention; causal pairwise
 //        exponentials come from prefix differences of the log decay.
 //   [R]  "Add experimental GDN/KDA decode and replay QAT" (#2509), section "What does
 //        this PR do?": per-token FP8 state writes in decode.
-//   [I]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519): the summary's "dynamic
-//        INT8 state recipes, including block-32", the shipped recipe
+//   [I]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519): its summary lists
+//        dynamic INT8 state recipes with a block-32 variant; the shipped recipe
 //        linear_attention_state_int8_block32_dynamic ("Megatron-Core QAT/QAD workflow" step 1
-//        and "Usage"), "signed INT8 state"; and "Add experimental GDN/KDA decode and replay QAT",
-//        which tests "state/value tails at codec blocks 32/128". Read as: a block is 32
+//        and "Usage"); the INT8 state is signed; and "Add experimental GDN/KDA decode and replay
+//        QAT" tests state and value tails at codec block sizes 32 and 128. Read as: a block is 32
 //        consecutive value columns of one key row of the state (the last block of a row may be
 //        narrower); scale = amax / 127 with the same zero guard as the E4M3 tiles; code = the
 //        signed integer nearest x / scale (ties to even), kept within [-127, 127].
 //   [H]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519), section
 //        "Megatron-Core QAT/QAD workflow", steps 2-3 and the "Ordinary state-QDQ path"
-//        flowchart: a sequence's first prefill_lengths tokens run as chunked prefill that
-//        produces a state without internal state QDQ; for a nonempty suffix QDQ is applied
-//        at the handoff, then each suffix token (teacher forced, the sequence's own tokens)
-//        is a decode step that QDQs the state before storing it.
+//        flowchart: a sequence's first prefill_lengths tokens run as chunked prefill whose
+//        state is never quantized inside the prefix; if any tokens are left, the state is
+//        QDQ'd once when the prefix hands over, and each remaining token (teacher forced, the
+//        sequence's own tokens) is a decode step that QDQs the state before storing it.
 // The pages name GatedDeltaNet but never print its recurrence. The oracle uses the
 // standard gated delta rule for a state S in R^{dk x dv}:
 //     S_t = a_t S_{t-1} + b_t k_t (v_t - a_t S_{t-1}^T k_t)^T,   o_t = S_t^T q_t,
@@ -519,8 +519,8 @@ int oracle_gdn_prefill_decode(const float* q, const float* k, const float* v, co
 // Decode: `steps` single-token steps for N sequences. Inputs per step s:
 // q, k [steps, N, Hqk, dk]; v [steps, N, Hv, dv]; g [steps, N, Hv] (KDA [.., dk]);
 // beta [steps, N, Hv]. state [N, Hv, dk, dv] fp64 in/out; o [steps, N, Hv, dv] fp64.
-// Per token, in the order of [D]: read the stored state, update it, emit o from the
-// updated working state, then QDQ (when state_qdq) before storing it.
+// Per token, in the order of [D]: load the stored state, update it, take o from the updated
+// state, then QDQ it (when state_qdq) and store it.
 int oracle_gdn_decode(const float* q, const float* k, const float* v, const float* g,
                       const float* beta, int steps, int N, int Hqk, int Hv, int dk, int dv,
                       int kda, int state_qdq, double scale, const uint8_t* unit_mask,

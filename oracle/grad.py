@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE ONLY (as the rest of ``oracle/``): the slow, plain reference
 backward is checked against. Only tests/ and bench.py's CPU leg may import it.
 
 What it differentiates ("Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core
-QAT/QAD workflow" step 4: Torch provides recurrent surrogate gradients and QDQ uses an identity
-straight-through estimator; "GDN state/W QAT foundation": identity straight-through gradients for
+QAT/QAD workflow" step 4: the recurrent surrogate gradients come from Torch, and the QDQ passes
+gradients through unchanged (a straight-through estimator); "GDN state/W QAT foundation": identity straight-through gradients for
 QAT): the token recurrence of the forward oracle,
     S_t = a_t S_{t-1} + b_t k_t (v_t - a_t S_{t-1}^T k_t)^T,   o_t = scale S_t^T q_t,
 with a_t = exp(g_t) (KDA: row c of S scaled by exp(g_t[c])), and the state QDQ after every 64th

@@ -2,8 +2,8 @@
 
 The schedule is the one of "Torch GDN/KDA decode QAT with INT8 recurrent state", section
 "Megatron-Core QAT/QAD workflow", steps 2-3 (and its "Ordinary state-QDQ path" flowchart): a
-sequence's first prefill_lengths[n] tokens run as chunked prefill that produces a state without
-internal state QDQ; when tokens remain, QDQ is applied at the handoff, then every remaining
+sequence's first prefill_lengths[n] tokens run as chunked prefill whose state is not quantized
+inside the prefix; if tokens remain, the state is QDQ'd once at the hand-over, and every remaining
 token (teacher forced: the sequence's own tokens) is a decode step that stores a QDQ'd state.
 
 Each check reaches the answer by another route: the plain recurrence without any QDQ (the

@@ -1,7 +1,7 @@
 """Pins for the oracle's E4M3 rounding and tile QDQ (CPU only).
 
 The QDQ contract ("GDN state/W QAT foundation", "What does this PR do?"): dynamic FP8
-E4M3 (num_bits (4,3)), one scalar scale per tile, scale = amax / 448 with a zero guard,
+E4M3 (num_bits (4,3)), one scalar scale per tile, scale = amax / 448 (1 for an all-zero tile),
 x -> E4M3(x / scale) * scale. Every check here reaches the oracle's answer by another
 route: decoding the 256 bit patterns, brute-force nearest search, torch's own float8 cast,
 hand-worked values, and invariants (amax element -> +-448, zero tile, idempotence).
