@@ -60,3 +60,13 @@ def test_alu_peak_from_unit_counts():
     peak, src = bench.alu_peak(None, fake, 2070.0)
     assert abs(peak - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9 and "152 SMs" in src
     assert bench.alu_peak(None, fake, None)[0] == peak
+
+
+def test_profile_hash_ignores_comments_only():
+    """The source hash that ties an ncu summary to the kernels' code sees code, not comments."""
+    a = "// header\nint f(int x) {  /* multi\n line */ return x + 1;  // inc\n}\n"
+    b = "// other words\nint f(int x) {  /* changed */ return x + 1;\n}\n"
+    c = "// header\nint f(int x) {  /* multi\n line */ return x + 2;  // inc\n}\n"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert "return x + 1;" in bench.code_only(a) and "header" not in bench.code_only(a)
