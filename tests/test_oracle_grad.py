@@ -104,3 +104,57 @@ def test_straight_through_pure_decay(oracle_mod, kda, codec):
     assert rel(dh0[0, 0], dh0_ref) < 1e-12
     assert not dv.any()
     assert rel(hT[0, 0], S) < 1e-12
+
+
+@pytest.mark.parametrize("kda", [False, True])
+@pytest.mark.parametrize("state_qdq,w_qdq", [(False, False), (True, False), (False, True), (True, True)])
+def test_chunked_forward_equals_the_cpp_chunked_oracle(oracle_mod, kda, state_qdq, w_qdq):
+    """The chunked-form gradient oracle differentiates the pinned C++ chunked / WY forward (O2),
+    W QDQ included: o and hT agree for varlen sequences of 5, 64 and 70 tokens."""
+    from oracle.grad import gdn_chunked_grads
+    x = workloads.prefill(1, 0, 1, 2, 8, 64, seed=13, kda=kda, h0_std=0.3, seqlens=[5, 64, 70])
+    *_, o, hT = gdn_chunked_grads(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, kda=kda, state_qdq=state_qdq,
+                                  w_qdq=w_qdq)
+    o1, h1 = oracle_mod.gdn_chunked(x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, kda=kda, state_qdq=state_qdq,
+                                    w_qdq=w_qdq)
+    assert rel(o, o1) < 1e-11 and rel(hT, h1) < 1e-11
+
+
+@pytest.mark.parametrize("kda", [False, True])
+@pytest.mark.parametrize("state_qdq,codec", [(False, "e4m3"), (True, "e4m3"), (True, "int8")])
+def test_chunked_gradients_equal_the_recurrent_ones(oracle_mod, kda, state_qdq, codec):
+    """Without W QDQ the chunked form is the token recurrence rewritten, and the straight-through
+    state quantizer sits at the same 64-token boundaries in both: every gradient agrees (GQA,
+    varlen with an empty sequence and one that crosses a boundary)."""
+    from oracle.grad import gdn_chunked_grads, gdn_recurrent_grads
+    x, do, dhT = tiny(kda, seed=14 + kda, seqlens=[2, 0, 70])
+    args = (x.q, x.k, x.v, x.g, x.beta, x.h0, x.cu_seqlens, do, dhT)
+    a = gdn_recurrent_grads(*args, kda=kda, state_qdq=state_qdq, codec=codec)
+    b = gdn_chunked_grads(*args, kda=kda, state_qdq=state_qdq, codec=codec)
+    for name, ga, gb in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0", "o", "hT"), a, b):
+        assert rel(gb, ga) < 1e-10, (name, rel(gb, ga))
+
+
+def test_w_qdq_on_an_exact_tile_changes_no_gradient(oracle_mod):
+    """One-token sequences with beta = 1 and g = 0 make W = k; keys of small integers with
+    max |k| = 2 give the tile scale 2 / 448, whose codes (k x 224) are all exact E4M3 values, so
+    QDQ(W) = W. The straight-through W quantizer then leaves every gradient as it was, which
+    pins that it acts on W and nowhere else; random keys show it is active."""
+    from oracle.grad import gdn_chunked_grads
+    x = workloads.prefill(1, 0, 1, 2, 8, 16, seed=15, h0_std=0.3, seqlens=[1, 1, 1])
+    gen = torch.Generator().manual_seed(16)
+    keys = torch.randint(-2, 3, x.k.shape, generator=gen).float()
+    keys[..., 0] = 2.0                      # every row reaches the tile maximum
+    x.beta.fill_(1.0)
+    x.g.zero_()
+    do = torch.randn((1, 3, 2, 16), generator=gen, dtype=torch.float64)
+    dhT = torch.randn((3, 2, 8, 16), generator=gen, dtype=torch.float64)
+
+    def grads(k, w_qdq):
+        return gdn_chunked_grads(x.q, k.to(x.k.dtype), x.v, x.g, x.beta, x.h0, x.cu_seqlens, do, dhT, w_qdq=w_qdq)
+
+    exact_on, exact_off = grads(keys, True), grads(keys, False)
+    for ga, gb in zip(exact_on, exact_off):
+        np.testing.assert_array_equal(ga, gb)
+    rand_on, rand_off = grads(x.k.float() * 0.7, True), grads(x.k.float() * 0.7, False)
+    assert max(rel(ga, gb) for ga, gb in zip(rand_on[:6], rand_off[:6])) > 1e-4
