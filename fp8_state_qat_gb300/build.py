@@ -32,24 +32,31 @@ def _sources(csrc=CSRC):
     return sorted(glob.glob(os.path.join(csrc, "*.cu")))
 
 
-def _deps():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [
+def headers():
+    return glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [
         os.path.join(ROOT, "include", "gdnqat.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _deps():
+    return _sources() + headers()
+
+
+def newer_than(out: str, deps) -> bool:
+    """`out` exists and no file in `deps` was modified after it."""
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    t = os.path.getmtime(out)
+    return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, csrc: str = CSRC, out: str = LIB_PATH) -> str:
-    """Compile `csrc`/*.cu into the shared library `out` (defaults: this package's sources and
-    library)."""
-    if not force and csrc == CSRC and out == LIB_PATH and up_to_date():
-        return LIB_PATH
-    obj_dir = os.path.join(os.path.dirname(out), "_obj_" + os.path.basename(out)) if out != LIB_PATH else OBJ_DIR
+def up_to_date() -> bool:
+    return newer_than(LIB_PATH, _deps())
+
+
+def compile_library(sources, out: str, obj_dir: str, verbose: bool = False) -> str:
+    """nvcc each of `sources` (objects in `obj_dir`, in parallel) and link them into the shared
+    library `out` with the CUDA runtime linked statically. A source is a path, or a pair
+    (path, extra -D macros for that file)."""
     os.makedirs(obj_dir, exist_ok=True)
     os.makedirs(os.path.dirname(out), exist_ok=True)
     cc = nvcc()
@@ -58,15 +65,17 @@ def build(force: bool = False, verbose: bool = False, csrc: str = CSRC, out: str
     if verbose:
         flags += ["-Xptxas", "-v"]
 
-    def compile_one(src):
+    def compile_one(item):
+        src, defines = (item, ()) if isinstance(item, str) else item
         obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
-        r = subprocess.run([cc, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
+        cmd = [cc, *flags, *[f"-D{d}" for d in defines], "-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
-        results = list(ex.map(compile_one, _sources(csrc)))
+        results = list(ex.map(compile_one, sources))
     if verbose:
         for _, log in results:
             print(log)
@@ -76,6 +85,13 @@ def build(force: bool = False, verbose: bool = False, csrc: str = CSRC, out: str
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, out)
     return out
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu into libgdnqat.so (skipped when it is up to date)."""
+    if not force and up_to_date():
+        return LIB_PATH
+    return compile_library(_sources(), LIB_PATH, OBJ_DIR, verbose=verbose)
 
 
 if __name__ == "__main__":

@@ -10,43 +10,42 @@
 //
 // The array is a file-scope __device__ object: every GPU that loads the library holds these
 // kNoAllocScratchBytes until the process exits, and all calls on a device share it. The host
-// symbol is only a stand-in; its device address is looked up once per device with
-// cudaGetSymbolAddress (on the first call made while that device is current).
-#include <mutex>
-
+// symbol is only a stand-in: each call looks up the array's device address on the current
+// device with cudaGetSymbolAddress (cheap once the library's device code is loaded there; a
+// looked-up address is never reused across calls, so a context that was reset and re-created
+// cannot leave a stale one behind).
 #include "../../include/gdnqat.h"
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 256;   // the chunk forward's minimum workspace
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices];   // device address of g_noalloc_scratch, per device
-
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device.
 gdn_status scratch_for_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
     cudaGetLastError();
-    return GDN_ERR_UNSUPPORTED_ARCH;
+    return GDN_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return GDN_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return GDN_OK;
 }
 
 }  // namespace
+
+namespace gdn {
+gdn_status noalloc_status_word(int* word) {
+  gdn_status s = check_device();
+  if (s != GDN_OK) return s;
+  void* scratch = nullptr;
+  s = scratch_for_current_device(&scratch);
+  if (s != GDN_OK) return s;
+  return cudaMemcpy(word, scratch, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+}  // namespace gdn
 
 extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream) {
   if (gdn_chunk_fwd_workspace_size(args) == 0) {
@@ -55,8 +54,11 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stre
   }
   // the smallest workspace gdn_chunk_fwd accepts (it then takes its single-kernel path)
   if (GDN_CHUNK_MIN_WORKSPACE_BYTES > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  // the device check comes first: on another GPU the array has no device image to look up
+  gdn_status s = gdn::check_device();
+  if (s != GDN_OK) return s;
   void* scratch = nullptr;
-  const gdn_status s = scratch_for_current_device(&scratch);
+  s = scratch_for_current_device(&scratch);
   if (s != GDN_OK) return s;
   // gdn_chunk_fwd clears the status word on `stream` before its kernel runs
   return gdn_chunk_fwd(args, scratch, kNoAllocScratchBytes, stream);

@@ -35,8 +35,32 @@ __device__ __forceinline__ float qdq1(float a, float s) {
   return qdq2(a, 0.0f, s).x;
 }
 
-// ---- INT8 block codec of the state ("Torch GDN/KDA decode QAT with INT8 recurrent state":
-// dynamic INT8 state recipes with block-32, signed INT8 state): a block is 32 consecutive value
+// fl32(x / s) for the standalone QDQ ops from the round-to-nearest reciprocal r of s and two
+// FMA corrections. q0 = fl32(x r) is within two ulps of x / s, so q1 = fl32(q0 + fl32(x - q0 s) r)
+// misses x / s by far less than an ulp and is faithful (one of the two floats around x / s);
+// its residual x - q1 s is exact in one FMA, and by Markstein's theorem (a faithful quotient, r
+// correctly rounded) q2 = fl32(q1 + (x - q1 s) r) is the correctly rounded quotient, barring a
+// subnormal quotient. A single correction is not enough in general: q0 need not be faithful.
+// Callers use it only for normal s (then 1 / s is finite and normal); a subnormal quotient is
+// below 2^-126, far under half the smallest E4M3 subnormal, so its code is 0 either way -- the
+// E4M3 code of every element is the one the IEEE division gives (checked exhaustively over
+// significands on the GPU against the IEEE divide by the test suite).
+// The corrections turn -0 into +0; x / s with s > 0 always has the sign of x, so it is copied back.
+__device__ __forceinline__ float quotient(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x), r, q0);
+  return copysignf(__fmaf_rn(__fmaf_rn(-q1, s, x), r, q1), x);
+}
+// The same for two elements with the paired fp32 instructions (each component rounded as the
+// scalar form rounds it): ns2 = (-s, -s), r2 = (r, r).
+__device__ __forceinline__ float2 quotient2(float2 x, float2 ns2, float2 r2) {
+  const float2 q0 = __fmul2_rn(x, r2);
+  const float2 q1 = __ffma2_rn(__ffma2_rn(q0, ns2, x), r2, q0);
+  const float2 q2 = __ffma2_rn(__ffma2_rn(q1, ns2, x), r2, q1);
+  return make_float2(copysignf(q2.x, x.x), copysignf(q2.y, x.y));
+}
+// ---- INT8 block codec of the state (page "Torch GDN/KDA decode QAT with INT8 recurrent state",
+// its summary): signed INT8 codes, one scale per block of 32; a block is 32 consecutive value
 // columns of one key row; scale = amax / 127 (IEEE divide) with the zero guard; code = nearest
 // integer to x / scale, ties to even, within [-127, 127]; value = code * scale.
 constexpr int kInt8BlockCols = 32;

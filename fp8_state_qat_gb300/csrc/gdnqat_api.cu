@@ -15,8 +15,11 @@ namespace {
 using gdn::ChunkProblem;
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_arch_ok[kMaxDevices];   // 0 = unknown, 1 = sm_103, 2 = other
+std::atomic<int> g_arch_ok[kMaxDevices];   // 0 = unknown, 1 = sm_103, 2 = other (devices >= 64 are probed every call)
 
+}  // namespace
+
+namespace gdn {
 gdn_status check_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
@@ -37,6 +40,10 @@ gdn_status check_device() {
   if (dev < kMaxDevices) g_arch_ok[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok ? GDN_OK : GDN_ERR_UNSUPPORTED_ARCH;
 }
+}  // namespace gdn
+
+namespace {
+using gdn::check_device;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -365,10 +372,14 @@ gdn_status int8_block_qdq(const float* x, float* y, float* scales, int64_t rows,
 }
 
 gdn_status gdn_check_device_status(const void* workspace, gdn_stream_t stream) {
-  if (!workspace) return GDN_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
   int word = 0;
-  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  if (!workspace) {   // the array behind gdn_chunk_fwd_noalloc on the current device
+    const gdn_status s = gdn::noalloc_status_word(&word);
+    if (s != GDN_OK) return s;
+  } else if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    return GDN_ERR_CUDA;
+  }
   return word == 0 ? GDN_OK : GDN_ERR_DEVICE_TIMEOUT;
 }
 

@@ -5,7 +5,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/gdnqat.h"
+
 namespace gdn {
+
+// The current device is an sm_103 GPU (cached per device ordinal below 64); checked by every
+// entry point before it enqueues anything.
+gdn_status check_device();
+// The status word of the array behind gdn_chunk_fwd_noalloc on the current device (synchronous).
+gdn_status noalloc_status_word(int* word);
 
 struct ChunkProblem {
   const void* q;

@@ -18,26 +18,6 @@ namespace {
 constexpr int kQdqThreads = 256;
 constexpr int kQdqRegF4 = 8;   // float4 per thread on the register path: tiles up to 8192 elements
 
-// fl32(x / s), computed as the round-to-nearest reciprocal r of s plus one FMA correction
-// (Markstein's theorem: with r correctly rounded and q0 = fl32(x r) within an ulp of x / s, the
-// corrected q1 is the correctly rounded quotient, barring a subnormal quotient). Callers use it
-// only for normal s (then 1 / s is finite and normal); a subnormal quotient is below 2^-126,
-// far under half the smallest E4M3 subnormal, so its code is 0 either way -- the E4M3 code of
-// every element is the one the IEEE division gives.
-// The correction turns -0 into +0; x / s with s > 0 always has the sign of x, so it is copied back.
-__device__ __forceinline__ float quotient(float x, float s, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float e = __fmaf_rn(-q0, s, x);
-  return copysignf(__fmaf_rn(e, r, q0), x);
-}
-// The same for two elements with the paired fp32 instructions (each component rounded as the
-// scalar form rounds it): ns2 = (-s, -s), r2 = (r, r).
-__device__ __forceinline__ float2 quotient2(float2 x, float2 ns2, float2 r2) {
-  const float2 q0 = __fmul2_rn(x, r2);
-  const float2 e = __ffma2_rn(q0, ns2, x);
-  const float2 q1 = __ffma2_rn(e, r2, q0);
-  return make_float2(copysignf(q1.x, x.x), copysignf(q1.y, x.y));
-}
 __device__ __forceinline__ float2 qdq_exact2(float a, float b, float s, float r, bool fast) {
   const float2 y = fast ? quotient2(make_float2(a, b), make_float2(-s, -s), make_float2(r, r))
                         : make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
@@ -182,11 +162,11 @@ tile_qdq_kernel(const float* x, float* y, float* __restrict__ scales, int rows, 
   }
 }
 
-// INT8 block codec ("Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 block-32
-// state recipes): one warp per block of one row (block_cols consecutive columns, the last block
-// of a row narrower), amax = max |x| (redux), s = amax / 127 (IEEE divide, zero guard), c =
-// nearest integer to x / s (ties to even) within [-127, 127], y = c * s. x / s is the correctly
-// rounded quotient (the corrected reciprocal above for normal s, else an IEEE divide; a
+// INT8 block codec (page "Torch GDN/KDA decode QAT with INT8 recurrent state", summary: one
+// scale per 32-value block of the state): one warp per block of one row (block_cols consecutive
+// columns, the last block of a row narrower), amax = max |x| (redux), s = amax / 127 (IEEE
+// divide, zero guard), c = nearest integer to x / s (ties to even) within [-127, 127], y = c * s.
+// x / s is the correctly rounded quotient (common.cuh's corrected reciprocal for normal s, else an IEEE divide; a
 // subnormal quotient rounds to 0 either way), so the result is bit-for-bit the fp32 definition.
 // HBM-bound: 4 bytes read + 4 written per element; with 32-column blocks a warp moves 128
 // contiguous bytes each way.

@@ -65,9 +65,15 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Polls a pipeline wait makes before it gives up. The library uses the default; the test suite
+// compiles a copy of the chunk kernels with 0 to drive every kernel's give-up path (the waits that
+// drain copies in flight while a CTA winds down pass their own limits and keep them).
+#ifndef GDN_WAIT_LIMIT
+#define GDN_WAIT_LIMIT (1u << 22)
+#endif
 // Bounded wait: gives up after `limit` polls (each poll may itself suspend briefly) and
 // returns false; callers record the failure in the device status word and wind down.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint32_t limit = (1u << 22)) {
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint32_t limit = GDN_WAIT_LIMIT) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(addr, parity)) return true;
   return false;

@@ -408,5 +408,8 @@ def int8_block_qdq(x, block_cols=32, *, y=None, scales=True, stream=None):
 
 
 def gdn_check_device_status(workspace, stream=None):
-    st = load().gdn_check_device_status(_ptr(workspace), _stream(stream, workspace.device))
+    """Raise GdnError if a kernel that used `workspace` gave up a bounded wait. workspace None:
+    the library array behind gdn_chunk_fwd_noalloc on the current device."""
+    dev = workspace.device if workspace is not None else torch.device("cuda", torch.cuda.current_device())
+    st = load().gdn_check_device_status(_ptr(workspace), _stream(stream, dev))
     _check("gdn_check_device_status", st)

@@ -15,8 +15,8 @@
  *      per-key-channel retention, with causal pairwise decays from prefix differences.
  *  [R] "Add experimental GDN/KDA decode and replay QAT", "What does this PR do?":
  *      per-token FP8 state writes.
- *  [I] "Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 state recipes with
- *      block-32 and signed INT8 state; "Add experimental GDN/KDA decode and replay QAT": codec
+ *  [I] "Torch GDN/KDA decode QAT with INT8 recurrent state", summary: a signed INT8 state
+ *      codec with one scale per 32-value block; "Add experimental GDN/KDA decode and replay QAT": codec
  *      blocks along the value columns of the state.
  *  [H] "Torch GDN/KDA decode QAT with INT8 recurrent state", "Megatron-Core QAT/QAD workflow",
  *      steps 2-3: chunked prefix without internal state QDQ, QDQ at the handoff, then decode
@@ -129,16 +129,18 @@ gdn_status gdn_chunk_fwd(const gdn_chunk_args* args, void* workspace, size_t wor
  * results as gdn_chunk_fwd, minus the workspace: the workspace is a 256-byte array
  * inside the library (static device memory, held by every GPU that loads the library until
  * the process exits). No cudaMalloc, cudaFree or other allocating call is made.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *    with that device current; make that first call before any stream capture.
+ *  - The device is checked first (GDN_ERR_UNSUPPORTED_ARCH on anything but sm_103); then
+ *    every call looks up the array's device address (cudaGetSymbolAddress) with the
+ *    device current. The first call on a device also loads the library's device code
+ *    there; make that first call before any stream capture.
  *  - All calls on a device share the array (its status word is cleared at the start of
  *    each call): calls that may run at the same time on the GPU, e.g. on different
  *    streams, race on it. Serialize them, or use gdn_chunk_fwd with separate workspaces.
  *  - The array holds GDN_CHUNK_MIN_WORKSPACE_BYTES, so dk = 128 always takes the fused
  *    single-kernel path. Returns GDN_ERR_WORKSPACE_TOO_SMALL if a path would need more
  *    workspace than the array holds (none does today).
- *  - A device-side timeout is recorded in the shared array and cannot be queried through
- *    gdn_check_device_status. */
+ *  - A device-side timeout is recorded in the shared array: gdn_check_device_status(NULL,
+ *    stream) reads it for the current device. */
 gdn_status gdn_chunk_fwd_noalloc(const gdn_chunk_args* args, gdn_stream_t stream);
 
 /* Bytes of device workspace for the fastest kda_chunk_fwd path with these arguments; 0 when
@@ -254,7 +256,8 @@ gdn_status int8_block_qdq(const float* x, float* y, float* scales, int64_t rows,
 const char* gdn_status_string(gdn_status status);
 
 /* Synchronizes `stream`, then reads the status word a chunk-forward call left in
- * `workspace`: GDN_OK, or GDN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait. */
+ * `workspace`: GDN_OK, or GDN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait.
+ * workspace == NULL reads the array behind gdn_chunk_fwd_noalloc on the current device. */
 gdn_status gdn_check_device_status(const void* workspace, gdn_stream_t stream);
 
 #ifdef __cplusplus

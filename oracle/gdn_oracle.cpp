@@ -20,8 +20,8 @@
 //        exponentials come from prefix differences of the log decay.
 //   [R]  "Add experimental GDN/KDA decode and replay QAT" (#2509), section "What does
 //        this PR do?": per-token FP8 state writes in decode.
-//   [I]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519): its summary lists
-//        dynamic INT8 state recipes with a block-32 variant; the shipped recipe
+//   [I]  "Torch GDN/KDA decode QAT with INT8 recurrent state" (#2519): its summary names an
+//        INT8 state codec whose scales cover 32-value blocks; the shipped recipe
 //        linear_attention_state_int8_block32_dynamic ("Megatron-Core QAT/QAD workflow" step 1
 //        and "Usage"); the INT8 state is signed; and "Add experimental GDN/KDA decode and replay
 //        QAT" tests state and value tails at codec block sizes 32 and 128. Read as: a block is 32

@@ -12,6 +12,9 @@ scale of its whole tile, and later QDQs carry that difference on ("Add experimen
 GDN/KDA decode and replay QAT": tiny arithmetic differences flip rounding ties and
 accumulate). Per unit we therefore only bound gross errors (UNIT_SANITY) when QDQ is on.
 """
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -19,12 +22,26 @@ TOL_OFF = 1e-3
 TOL_QDQ = 2e-2
 UNIT_SANITY = 0.1
 
+# With GDN_PARITY_LOG=<path>, every measured relative error is appended there as one JSON line
+# (test id, what was measured, value), so the margins of every parity test can be tabulated.
+_LOG = os.environ.get("GDN_PARITY_LOG")
+
+
+def record(kind, value, **extra):
+    if not _LOG:
+        return
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" (")[0]
+    with open(_LOG, "a") as f:
+        f.write(json.dumps({"test": test, "kind": kind, "value": float(value), **extra}) + "\n")
+
 
 def rel(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
     n = np.linalg.norm(b)
-    return float(np.linalg.norm(a - b) / (n if n > 0 else 1.0))
+    r = float(np.linalg.norm(a - b) / (n if n > 0 else 1.0))
+    record("rel", r)
+    return r
 
 
 def to_cuda(x):
@@ -61,6 +78,9 @@ def compare_units(x, units, o_gpu, hT_gpu, o_ref, hT_ref, tol):
         worst = max(worst, rel(hg[-1], hrf[-1]))
     eo = rel(np.concatenate(og), np.concatenate(orf)) if sum(a.size for a in og) else 0.0
     eh = rel(np.concatenate(hg), np.concatenate(hrf))
+    record("o", eo, tol=tol)
+    record("hT", eh, tol=tol)
+    record("worst_unit", worst, tol=tol, units=len(units))
     assert eo <= tol, f"o rel-L2 {eo:.3e} > {tol}"
     assert eh <= tol, f"hT rel-L2 {eh:.3e} > {tol}"
     unit_tol = tol if tol <= TOL_OFF else max(tol, UNIT_SANITY)

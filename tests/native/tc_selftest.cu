@@ -4,9 +4,9 @@
 // memory (A and B staged in the 128-byte-swizzled K-major or MN-major layout, bf16 or tf32
 // values), accumulates in TMEM and writes every TMEM lane (128) x N columns back. The host
 // compares with a CPU product. Every shared-memory access stays inside the 227 KB buffer and
-// the only wait is bounded. Not part of the public API.
-#include "common.cuh"
-#include "tc_common.cuh"
+// the only wait is bounded. Built into the test-only library, not the product library.
+#include "../../fp8_state_qat_gb300/csrc/common.cuh"
+#include "../../fp8_state_qat_gb300/csrc/tc_common.cuh"
 
 namespace gdn {
 namespace {
@@ -69,7 +69,7 @@ tc_selftest_kernel(const float* A, const float* B, float* D, float* D2, int M, i
     }
     tc::mma_commit(tc::smem_u32(&mbar));
   }
-  const bool ok = tc::mbar_wait(tc::smem_u32(&mbar), 0);
+  const bool ok = tc::mbar_wait(tc::smem_u32(&mbar), 0, 1u << 22);   // its own limit: the test library lowers the default
   if (!ok && threadIdx.x == 0) atomicExch(status, 1);
   tc::tc_fence_after();
   if (ok) {

@@ -244,3 +244,20 @@ def test_backward_validation(so):
                             None) == B.GDN_ERR_INVALID_ARG
     if not torch.cuda.is_available():
         assert fn(ctypes.byref(a), ctypes.byref(g), P(FAKE + (7 << 32)), need, None) == B.GDN_ERR_UNSUPPORTED_ARCH
+
+
+def test_testing_library_builds_and_exports():
+    """The test-only library (layout self-test, the chunk kernels with zero-poll waits) builds and
+    exports its two entry points; the product library exports neither."""
+    import native
+    t = native.load()
+    for name in ("gdnqat_internal_tc_selftest", "gdnqat_testing_split_fwd"):
+        assert hasattr(t, name), name
+        assert not hasattr(lib.load(), name), name
+
+
+def test_check_device_status_null_reads_noalloc_array(so):
+    """gdn_check_device_status(NULL) addresses the array behind gdn_chunk_fwd_noalloc; without a
+    device it reports a CUDA error instead of reading anything."""
+    if not torch.cuda.is_available():
+        assert so.gdn_check_device_status(None, None) in (B.GDN_ERR_CUDA, B.GDN_ERR_UNSUPPORTED_ARCH)

@@ -171,7 +171,7 @@ def test_kda_paths_agree_closely(gdn):
 @pytest.mark.parametrize("path", PATHS)
 def test_gdn_b4_h16_t4096_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("gdn_b4_h16_t4096_d128")
-    units = sample_units(4, 16, 6, seed=1)
+    units = sample_units(4, 16, 16, seed=1)
     check(gdn, oracle_mod, x, True, True, units, path=path)        # the benchmarked configuration
     check(gdn, oracle_mod, x, False, False, units, path=path)      # quantizers off: the 1e-3 bound
 
@@ -181,12 +181,12 @@ def test_gdn_varlen8_hqk16_hv32_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("gdn_varlen8_hqk16_hv32_d128")
     lens = np.diff(x.cu_seqlens.numpy())
     longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
-    units = sorted(set(sample_units(8, 32, 6, seed=2) + [(longest, 31), (shortest, 0)]))
+    units = sorted(set(sample_units(8, 32, 16, seed=2) + [(longest, 31), (shortest, 0)]))
     check(gdn, oracle_mod, x, True, False, units, path=path)
 
 
 @pytest.mark.parametrize("path", PATHS)
 def test_kda_b2_h32_t8192_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("kda_b2_h32_t8192_d128")
-    units = sample_units(2, 32, 4, seed=4)
+    units = sample_units(2, 32, 16, seed=4)
     check(gdn, oracle_mod, x, True, True, units, path=path)

@@ -1,7 +1,7 @@
 """The INT8 block state codec on the GPU against the fp64 oracle.
 
-Codec ("Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 block-32 state
-recipes, signed INT8 state): one scale per key row and 32 value columns, amax / 127 with the zero
+Codec (summary of "Torch GDN/KDA decode QAT with INT8 recurrent state"; signed INT8 codes,
+a scale per 32-value block): one scale per key row and 32 value columns, amax / 127 with the zero
 guard, codes = nearest integer (ties to even) within +-127. The standalone op is compared bit for
 bit with the oracle's fp32 definition; the fused uses (chunk carry, decode, handoff) within the
 QDQ bound (rel-L2 <= 2e-2), plus teacher-forced decode steps that take the same decisions.

@@ -1,5 +1,7 @@
 """fp8_tile_qdq on the GPU is bit-for-bit the oracle's fp32 tile QDQ ("GDN state/W QAT
 foundation", "What does this PR do?": one scale per tile, amax / 448, zero guard, E4M3)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -83,3 +85,38 @@ def test_qdq_empty(gdn):
     y, s = gdn.fp8_tile_qdq(x, 64)
     torch.cuda.synchronize()
     assert (s.cpu() == 1.0).all()
+
+
+def test_quotient_matches_ieee_divide_over_all_significands(gdn):
+    """The standalone QDQ ops divide by the tile scale as the rounded reciprocal plus two FMA
+    corrections (common.cuh). Against __fdiv_rn, bit for bit, over (1) every fp32 significand of
+    x at 22 binades (x / s from 2^-13 to 2^10: every E4M3 binade, subnormal codes and saturation)
+    times 256 scale significands, and (2) every significand of s at 4 binades times 256 values of
+    x: the quotient bits, hence the E4M3 codes, must all agree; the paired instruction form must
+    agree with the scalar one. The fused kernels' plain reciprocal product is counted for
+    reference only."""
+    import native
+    from helpers import record
+    lib = native.load()
+    fn = lib.gdnqat_testing_quotient_sweep
+    fn.restype = ctypes.c_int
+    rng = np.random.default_rng(11)
+    sig = lambda n: (1.0 + rng.integers(0, 1 << 23, n) / float(1 << 23)).astype(np.float32)
+    scales = np.concatenate([np.float32([1.0, np.nextafter(np.float32(1), np.float32(2)),
+                                         np.nextafter(np.float32(2), np.float32(1))]), sig(253)])
+    xs = sig(256) * np.float32(2.0) ** rng.integers(-12, 10, 256).astype(np.float32)
+    xs[::2] *= -1
+    for mode, vals, exps in ((0, scales, np.arange(-12, 10)), (1, xs, np.array([-3, 0, 5, 20]))):
+        dv = torch.from_numpy(np.ascontiguousarray(vals, np.float32)).cuda()
+        de = torch.from_numpy(exps.astype(np.int32)).cuda()
+        counts = torch.zeros(4, dtype=torch.int64, device="cuda")
+        first = torch.zeros(3, dtype=torch.int32, device="cuda")
+        rc = fn(ctypes.c_void_p(dv.data_ptr()), len(vals), ctypes.c_void_p(de.data_ptr()), len(exps), mode,
+                ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(first.data_ptr()), None)
+        assert rc == 0
+        torch.cuda.synchronize()
+        c = counts.cpu().tolist()
+        f = first.cpu().numpy().view(np.uint32)
+        record("plain_reciprocal_code_mismatches", c[3], mode=mode, pairs=(1 << 23) * len(vals) * len(exps))
+        assert c[0] == 0 and c[1] == 0, (mode, c, f[:2].view(np.float32))
+        assert c[2] == 0, (mode, c)

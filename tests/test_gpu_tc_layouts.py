@@ -7,6 +7,8 @@ import numpy as np
 import pytest
 import torch
 
+import native
+
 pytestmark = pytest.mark.gpu
 
 
@@ -30,8 +32,7 @@ COMBOS = [(0, 0, 0), (0, 0, 1), (0, 1, 0), (0, 1, 1), (1, 0, 0)]
 @pytest.mark.parametrize("M", [128, 64])
 def test_mma_layouts(gdn, kind, a_mn, b_mn, N, K, M):
     """M = 128: row m of D in TMEM lane m. M = 64: row m in lane 32 (m / 16) + m % 16."""
-    lib = gdn.load()
-    fn = lib.gdnqat_internal_tc_selftest
+    fn = native.load().gdnqat_internal_tc_selftest
     fn.restype = ctypes.c_int
     rng = np.random.default_rng(kind * 8 + a_mn * 4 + b_mn * 2 + N + K)
     A = rng.standard_normal((M, K)).astype(np.float32)
@@ -56,8 +57,7 @@ def test_tmem_16x32bx2_reads_m64_rows(gdn, N):
     """The 16-lane two-half TMEM load on an M = 64 accumulator: thread t of warp w reads row
     16 w + t % 16, columns [c0 + (t / 16) N / 2, + 16). Every row of the product is recovered and
     lanes 16-31 of each quadrant are never touched."""
-    lib = gdn.load()
-    fn = lib.gdnqat_internal_tc_selftest
+    fn = native.load().gdnqat_internal_tc_selftest
     fn.restype = ctypes.c_int
     M, K = 64, 128
     rng = np.random.default_rng(500 + N)

@@ -1,8 +1,8 @@
 """Pins for the oracle's INT8 block state codec (CPU only).
 
-Reading of the pages ("Torch GDN/KDA decode QAT with INT8 recurrent state": dynamic INT8 state
-recipes with block-32, signed INT8 state; "Add experimental GDN/KDA decode and replay QAT": state
-and value tails at codec blocks 32/128): a block is 32 consecutive value columns of one key row
+Reading of the pages (summary of "Torch GDN/KDA decode QAT with INT8 recurrent state": a signed
+INT8 state codec whose scales cover blocks of 32 values; "Add experimental GDN/KDA decode and
+replay QAT": its tests cover tails of the value axis at codec block sizes 32 and 128): a block is 32 consecutive value columns of one key row
 (the last block of a row may be narrower); scale = amax / 127 with the zero guard of the E4M3
 tiles; code = nearest integer to x / scale, ties to even, within [-127, 127]; value = code *
 scale. Checked by hand-worked blocks (exact scales, every tie), invariants, and the state codec
