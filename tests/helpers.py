@@ -10,7 +10,13 @@ The bound applies to the whole tensor (here: all sampled units together). A sing
 (sequence, head) unit can drift further under QDQ: a flipped amax element changes the
 scale of its whole tile, and later QDQs carry that difference on ("Add experimental
 GDN/KDA decode and replay QAT": tiny arithmetic differences flip rounding ties and
-accumulate). Per unit we therefore only bound gross errors (UNIT_SANITY) when QDQ is on.
+accumulate). Measured on GB300 over the whole GPU suite, the worst single unit with QDQ on
+sat at 2.1e-3 (whole tensors <= 1.2e-3) and at 7.4e-6 with the quantizers off, so each unit
+is held to the same 2e-2 bound as the whole tensor (UNIT_SANITY). Paths that quantize the
+state on every token (decode steps, the handoff's decode tokens) carry 64 quantizations per
+64 tokens instead of one; their worst single unit measured 5.4e-2 (handoff) and 3.7e-2
+(64 decode steps), so per unit those are only bounded for gross errors
+(UNIT_SANITY_PER_TOKEN) while the whole sampled tensor keeps the 2e-2 bound.
 """
 import json
 import os
@@ -20,7 +26,8 @@ import torch
 
 TOL_OFF = 1e-3
 TOL_QDQ = 2e-2
-UNIT_SANITY = 0.1
+UNIT_SANITY = 2e-2
+UNIT_SANITY_PER_TOKEN = 0.1
 
 # With GDN_PARITY_LOG=<path>, every measured relative error is appended there as one JSON line
 # (test id, what was measured, value), so the margins of every parity test can be tabulated.

@@ -190,3 +190,23 @@ def test_kda_b2_h32_t8192_d128_sampled(gdn, oracle_mod, path):
     x = workloads.workload("kda_b2_h32_t8192_d128")
     units = sample_units(2, 32, 16, seed=4)
     check(gdn, oracle_mod, x, True, True, units, path=path)
+
+
+def test_gdn_b4_h16_t4096_d128_quantizers_take_effect(gdn, oracle_mod):
+    """The benchmarked configuration is much closer to the oracle with the state and W
+    quantizers on than to the same oracle with them off: the QDQ steps really run (the
+    per-unit errors with QDQ sit near 1e-4 to 1e-3, the quantization itself moves the result by
+    percents)."""
+    from helpers import rel
+    x = workloads.workload("gdn_b4_h16_t4096_d128")
+    units = sample_units(4, 16, 4, seed=8)
+    o, hT = run_gpu(gdn, x, True, True)
+    o, hT = o.cpu().double().numpy(), hT.cpu().double().numpy()
+    on = run_oracle(oracle_mod, x, True, True, units)
+    off = oracle_mod.gdn_chunked(x.q, x.k, x.v, x.g, x.beta, x.h0, None, state_qdq=False, w_qdq=False,
+                                 unit_mask=mask_for(units, 4, 16))
+    ns, hs = (list(t) for t in zip(*units))
+    for got, want_on, want_off in ((o[ns, :, hs], on[0][ns, :, hs], off[0][ns, :, hs]),
+                                   (hT[ns, hs], on[1][ns, hs], off[1][ns, hs])):
+        e_on, e_off = rel(got, want_on), rel(got, want_off)
+        assert e_on <= TOL_QDQ and e_off >= 10 * e_on, (e_on, e_off)

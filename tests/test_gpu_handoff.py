@@ -161,7 +161,7 @@ def test_handoff_full_size_sampled(gdn, oracle_mod):
     states free of gross errors (their decode tokens carry independent quantization noise, see
     check()), and every decode token's step checked teacher forced in
     test_teacher_forced_decode_tokens."""
-    from helpers import UNIT_SANITY, mask_for, sample_units
+    from helpers import UNIT_SANITY_PER_TOKEN, mask_for, sample_units
     x = workloads.workload("handoff_n256_t128_p64_h16_d128")
     c = to_cuda(x)
     o, hT = gdn.gdn_prefill_decode_fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], None, x.prefill_lengths,
@@ -174,5 +174,5 @@ def test_handoff_full_size_sampled(gdn, oracle_mod):
     ns, hs = (list(t) for t in zip(*units))
     assert rel(o[ns, :, hs], oref[ns, :, hs]) <= TOL_QDQ
     for n, h in units:
-        assert rel(hT[n, h], href[n, h]) <= UNIT_SANITY
+        assert rel(hT[n, h], href[n, h]) <= UNIT_SANITY_PER_TOKEN
         assert rel(o[n, :64, h], oref[n, :64, h]) <= TOL_QDQ   # the prefix: W QDQ, no state QDQ
