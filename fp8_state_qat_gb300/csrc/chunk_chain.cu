@@ -1,6 +1,6 @@
 // chunk_chain.cu -- the state-carrying half of the chunked gated-delta-rule forward (dk = 128) on
-// the sm_103a tensor cores, after chunk_prep.cu has staged every chunk's W^T, T'' and gate vectors
-// in the workspace.
+// the sm_103a tensor cores, after chunk_prep.cu has staged every chunk's W^T, T'', P and gate
+// vectors in the workspace.
 //
 // One CTA (256 threads) per (sequence n, v-head h, 64-column value slab); the slab is one
 // state-QDQ tile (all 128 key rows x 64 value columns), so its amax is CTA-local ("GDN state/W QAT
@@ -10,13 +10,13 @@
 //                       S1 = Gam_63 S0 + C, QDQ(S1) at a 64-token boundary -> the next chunk.
 //                       Only this loop is serial from chunk to chunk. It also refills the W^T
 //                       buffer and the Q/K stages once their last readers are done.
-//   output (warps 0-3)  U = T'' V (and the next T'' / V load), G = Q K^T -> P (exp(gam_r - gam_i)
-//                       G, i <= r), Y = Q S0, P Delta, o = scale (Gam Y + P Delta); U and G of the
-//                       next chunk are issued right after P Delta, ahead of the chain's next X.
+//   output (warps 0-3)  U = T'' V (and the next T'' / V / P load), Y = Q S0, P Delta (P staged by
+//                       the prep, double-buffered), o = scale (Gam Y + P Delta); U of the next
+//                       chunk is issued right after P Delta, ahead of the chain's next X.
 // The state S0 (fp32) lives in the chain's registers (one key row of the slab per thread) and, as
 // the MMA operand, in shared memory as bf16 hi + lo, or as exact E4M3 codes once QDQ'd (the scale
 // is applied in the epilogues). W arrives as codes
-// (exact in bf16) with W QDQ, else as bf16 hi + lo; T'' as hi + lo; Delta, Dt and P are split
+// (exact in bf16) with W QDQ, else as bf16 hi + lo; T'' and P as hi + lo; Delta and Dt are split
 // into hi + lo before their MMAs.
 //
 // Hand-offs are mbarriers (TMA transactions, MMA commits, and three one-arrival signals from the
@@ -57,22 +57,21 @@ constexpr uint32_t OFF_V = 84 * KB;     // V slab [64 tok][64 j]
 constexpr uint32_t OFF_WT = 92 * KB;    // W^T codes [128 c][64 r] (or hi | lo, 16 KB apart)
 constexpr uint32_t OFF_SHI = 124 * KB;  // S0 operand [128 c][64 j] MN-major; lo at +16 KB
 constexpr uint32_t OFF_DL = 156 * KB;   // Delta hi, lo, Dt hi, lo ([i][j] MN-major, 8 KB each)
-constexpr uint32_t OFF_P = 188 * KB;    // P hi | lo ([r][i] K-major)
-constexpr uint32_t OFF_MISC = 204 * KB; // S0 scale [2], S0-is-codes [2], partial maxima [4], abort flag
+constexpr uint32_t OFF_P = 188 * KB;    // P hi | lo ([r][i] K-major), two buffers by chunk parity
+constexpr uint32_t OFF_MISC = 220 * KB; // S0 scale [2], S0-is-codes [2], partial maxima [4], abort flag
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + slack to align the base
 
 // TMEM columns (M = 64 results sit in lanes 16 w .. 16 w + 15 of quadrant w)
-constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128, TM_C = 192, TM_GP = 256, TM_PD = 320;
+constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128, TM_C = 192, TM_PD = 256;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // T'' (K) x V (MN)
 constexpr uint32_t IDESC_X = tc::make_idesc(tc::kKindBF16, 64, 64, true, true);     // W^T (MN) x S0 (MN)
 constexpr uint32_t IDESC_Y = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // Q (K) x S0 (MN)
 constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);    // K^T (MN) x Dt (MN)
-constexpr uint32_t IDESC_GP = tc::make_idesc(tc::kKindBF16, 64, 64, false, false);  // Q (K) x K (K)
 constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);   // P (K) x Delta (MN)
 
-enum : int { B_QK0 = 0, B_QK1, B_TV, B_WC, B_U, B_GP, B_X, B_Y, B_C, B_PD, B_SRDY, B_DRDY, B_UFREE, kNumBars };
+enum : int { B_QK0 = 0, B_QK1, B_TV, B_WC, B_U, B_X, B_Y, B_C, B_PD, B_SRDY, B_DRDY, B_UFREE, kNumBars };
 
 struct ChainParams {
   const int32_t* order;   // chain order of the sequences, or null (natural order)
@@ -104,7 +103,8 @@ __device__ __forceinline__ bool wg_any(int id, bool pred) {
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap twt,
-                   const __grid_constant__ CUtensorMap ttt, const ChainParams p) {
+                   const __grid_constant__ CUtensorMap ttt, const __grid_constant__ CUtensorMap tpp,
+                   const ChainParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_slot;
@@ -154,6 +154,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tc::tma_prefetch_desc(&tv);
     tc::tma_prefetch_desc(&twt);
     tc::tma_prefetch_desc(&ttt);
+    tc::tma_prefetch_desc(&tpp);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
   tc::tc_fence_before();
@@ -182,10 +183,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tc::tma_load_3d(base + SK0 + 16 * KB, &tk, b, 64, hq, tok);
     tc::bulk_load(base + SVEC, p.vec + item(cj) * 256, 1024, b);
   };
-  auto tma_tv = [&](int64_t cj) {   // T'' hi | lo and the V slab of chunk cj
-    tc::mbar_expect_tx(bar(B_TV), 24 * KB);
+  auto tma_tv = [&](int64_t cj) {   // T'' hi | lo, the V slab and P hi | lo (buffer cj & 1) of chunk cj
+    tc::mbar_expect_tx(bar(B_TV), 40 * KB);
     tc::tma_load_2d(sbase + OFF_TT, &ttt, bar(B_TV), 0, (int)(item(cj) * 128));
     tc::tma_load_3d(sbase + OFF_V, &tv, bar(B_TV), slab * 64, h, (int)(t0 + cj * 64));
+    tc::tma_load_2d(sbase + OFF_P + (uint32_t)(cj & 1) * 16 * KB, &tpp, bar(B_TV), 0, (int)(item(cj) * 128));
   };
   auto tma_wc = [&](int64_t cj) {   // W^T of chunk cj
     if (p.w_qdq) {
@@ -220,8 +222,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if (warp < 4) {
     // ================================ output warpgroup ================================
-    // U and G of chunk c + 1 are issued right after P Delta of chunk c, so that they are through
-    // the tensor pipe before the chain issues its next X.
+    // U of chunk c + 1 is issued right after P Delta of chunk c, so that it is through the tensor
+    // pipe before the chain issues its next X.
     auto issue_u = [&]() {   // U = T'' V (T'' hi + lo)
       tc::tc_fence_after();
 #pragma unroll
@@ -231,20 +233,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           tc::mma_bf16(tmem + TM_U, dadv(dTT, part * 8 * KB + ks * 32), dadv(dV, ks * 2048), IDESC_U, (part | ks) != 0);
       tc::mma_commit(bar(B_U));
     };
-    auto issue_gp = [&](uint32_t stg) {   // G = Q K^T
-      tc::tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = stg + (ks >> 2) * 16 * KB + (ks & 3) * 32;
-        tc::mma_bf16(tmem + TM_GP, dadv(dStgK, SQ0 + koff), dadv(dStgK, SK0 + koff), IDESC_GP, ks > 0);
-      }
-      tc::mma_commit(bar(B_GP));
-    };
     if (nchunks > 0) {
       wait(B_TV, 0);
       if (tid == kOutIssuer && live()) issue_u();
-      wait(B_QK0, 0);
-      if (tid == kOutIssuer && live()) issue_gp(0);
     }
     for (int64_t c = 0; c < nchunks; ++c) {
       const int s = (int)(c & 1);
@@ -252,39 +243,15 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const uint32_t par = (uint32_t)(c & 1);
       const uint32_t stg = (uint32_t)s * kStage;
       const float* vg = reinterpret_cast<const float*>(sm + stg + SVEC);
-      // T'' / V are free once U has read them: fetch the next chunk's (a whole chunk ahead)
+      // the row's Gam, read before Y is issued: the chain refills the stage once Y and C are done
+      wait(B_QK0 + s, (uint32_t)((c >> 1) & 1));
+      const float egam_r = vg[64 + row64];
+      // T'' / V and the other P buffer are free once U (issued after the previous P Delta by the
+      // same thread) has completed: fetch the next chunk's, a whole chunk ahead
       if (warp == kOutIssuer / 32) {
         wait(B_U, par);
         if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_tv(c + 1);
       }
-      // ---- P = exp(gam_r - gam_i) G for i <= r -> bf16 hi | lo, K-major [r][i] ----
-      float egam_r;
-      wait(B_GP, par);
-      tc::tc_fence_after();
-      {
-        float v[32];
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_GP), v);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_GP + 16), v + 16);
-        tc::tmem_ld_wait();
-        const float gr = vg[row64];
-        egam_r = vg[64 + row64];   // kept for the output epilogue: the stage is refilled once Y is done
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {   // the exponent is clamped so both select inputs are finite
-          const int i = half * 32 + j;
-          const float e = __expf(fminf(gr - vg[i], 0.f)) * v[j];
-          v[j] = i <= row64 ? e : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 h16, l16;
-          split8(v + 8 * q, h16, l16);
-          const uint32_t off = tc::sw128(row64, 2 * (half * 32 + 8 * q));
-          st16(sm, OFF_P + off, h16);
-          st16(sm, OFF_P + 8 * KB + off, l16);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
       if (wg_any(1, !live())) break;
       // ---- Y = Q S0 once the chain has stored S0 for this chunk ----
       wait(B_SRDY, par);
@@ -303,21 +270,20 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       wait(B_DRDY, par);
       if (tid == kOutIssuer && live()) {
         tc::tc_fence_after();
+        const uint32_t pb = (uint32_t)s * 16 * KB;
 #pragma unroll
         for (int q = 0; q < 3; ++q)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + TM_PD, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32),
+            tc::mma_bf16(tmem + TM_PD, dadv(dP, pb + (q == 2 ? 8 * KB : 0) + ks * 32),
                          dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048), IDESC_PD, (q | ks) != 0);
         tc::mma_commit(bar(B_PD));
       }
-      // ---- the next chunk's U (once the chain has read this one) and G ----
+      // ---- the next chunk's U (once the chain has read this one) ----
       if (c + 1 < nchunks) {
         wait(B_TV, par ^ 1u);
         wait(B_UFREE, par);
         if (tid == kOutIssuer && live()) issue_u();
-        wait(B_QK0 + (s ^ 1), (uint32_t)(((c + 1) >> 1) & 1));
-        if (tid == kOutIssuer && live()) issue_gp(stg ^ kStage);
       }
       // ---- o = scale (Gam Y + P Delta), rows r < L ----
       wait(B_Y, par);
@@ -537,8 +503,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (ctid == 0) {
         tc::mbar_arrive(bar(B_SRDY));   // S0 of chunk c + 1 is stored
       }
-      // stage s is free: C and Y (committed after G) have read it, and the output warpgroup read its
-      // gate vectors before issuing Y -- fetch chunk c + 2 into it
+      // stage s is free: C and Y have read it (both waited for above), and the output warpgroup read
+      // its gate vector before issuing Y -- fetch chunk c + 2 into it
       if (ctid == kChainIssuer && c + 2 < nchunks && live()) tma_qk(c + 2);
     }
     if (live() && p.hT) {
@@ -591,7 +557,8 @@ SplitLayout chunk_split_layout(const ChunkProblem& p) {
   auto up = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
   l.off_wt = up(kStatusBytes);
   l.off_tt = up(l.off_wt + (size_t)l.items * l.wt_item_bytes);
-  l.off_vec = up(l.off_tt + (size_t)l.items * 16 * KB);
+  l.off_p = up(l.off_tt + (size_t)l.items * 16 * KB);
+  l.off_vec = up(l.off_p + (size_t)l.items * 16 * KB);
   l.off_order = up(l.off_vec + (size_t)l.items * 1024);
   l.total = l.off_order + (size_t)p.N * 4;
   return l;
@@ -623,11 +590,12 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   if (blocks == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)p.B * p.T;
   const int64_t tmap = tokens > 0 ? tokens : 1;   // an empty batch still needs valid maps (never loaded)
-  CUtensorMap tq, tk, tv, twt, ttt;
+  CUtensorMap tq, tk, tv, twt, ttt, tpp;
   if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap) ||
       !make_bf16_map(&tv, p.v, p.dv, p.Hv, tmap) ||
       !make_bf16_rows_map(&twt, w + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 128) ||
-      !make_bf16_rows_map(&ttt, w + lay.off_tt, lay.items * 128, 128))
+      !make_bf16_rows_map(&ttt, w + lay.off_tt, lay.items * 128, 128) ||
+      !make_bf16_rows_map(&tpp, w + lay.off_p, lay.items * 128, 128))
     return cudaErrorInvalidValue;
   const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
   if (e != cudaSuccess) return e;
@@ -636,7 +604,7 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   cp.sscale = p.state_scales;
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, twt, ttt, cp);
+  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, twt, ttt, tpp, cp);
   return cudaGetLastError();
 }
 

@@ -66,11 +66,12 @@ bool make_bf16_rows_map(CUtensorMap* map, const void* base, int64_t rows, int bo
 //   W^T  bf16 [128 c][64 r]: the chunk's W transposed -- E4M3 codes (exact in bf16) with W QDQ,
 //        else the bf16 hi part followed by the lo part ([2][128][64]);
 //   T''  bf16 [2][64 r][64 i]: hi and lo parts of T diag(beta) (U = T'' V in the chain);
+//   P    bf16 [2][64 r][64 i]: hi and lo parts of exp(gam_r - gam_i) (q_r . k_i), i <= r < L;
 //   vec  fp32 [256]: gam [64], Gam = exp(gam) [64], exp(gam_63 - gam) [64], W scale (index 192).
 struct SplitLayout {
   int64_t slots, items;
   size_t wt_item_bytes;            // 16 KB with W QDQ, 32 KB without
-  size_t off_wt, off_tt, off_vec;  // byte offsets inside the workspace
+  size_t off_wt, off_tt, off_p, off_vec;  // byte offsets inside the workspace
   size_t off_order;                // N int32: sequences by decreasing length (varlen chain order)
   size_t total;                    // workspace bytes, status word included
 };

@@ -104,9 +104,9 @@ typedef struct {
 /* Bytes of device workspace for the fastest path with these arguments; 0 when the arguments
  * are invalid. For dk = 128 (GDN) that is the status word plus the staging of the two-kernel
  * path: per 64-token chunk slot and v-head, the chunk's W (transposed; E4M3 codes in bf16
- * with GDN_FLAG_W_QDQ, else bf16 hi + lo), T diag(beta) as bf16 hi + lo and its gate vectors
- * -- 33 KB (49 KB without W QDQ) for each of (B T / 64 + N) x Hv slots. Otherwise
- * GDN_CHUNK_MIN_WORKSPACE_BYTES. */
+ * with GDN_FLAG_W_QDQ, else bf16 hi + lo), T diag(beta) and the decay-weighted Q K^T (both
+ * bf16 hi + lo) and its gate vectors -- 49 KB (65 KB without W QDQ) for each of
+ * (B T / 64 + N) x Hv slots. Otherwise GDN_CHUNK_MIN_WORKSPACE_BYTES. */
 size_t gdn_chunk_fwd_workspace_size(const gdn_chunk_args* args);
 
 /* Chunked GDN forward ([F]): per 64-token chunk, decay-weighted K.K^T, WY solve (W, U),

@@ -100,13 +100,14 @@ def test_workspace_checks(so):
 
 def test_workspace_size_covers_the_two_kernel_staging(so):
     """dk = 128: status word + per (chunk slot, v-head) W^T (16 KB with W QDQ, 32 KB without),
-    T'' hi + lo (16 KB) and the gate vectors (1 KB), slots = B T / 64 + N. dk = 64: the minimum."""
+    T'' hi + lo (16 KB), P hi + lo (16 KB) and the gate vectors (1 KB), slots = B T / 64 + N.
+    dk = 64: the minimum."""
     for flags, wt in ((B.GDN_FLAG_STATE_QDQ | B.GDN_FLAG_W_QDQ, 16), (B.GDN_FLAG_STATE_QDQ, 32)):
         a = good_args(flags=flags)
         items = (a.B * a.T // 64 + a.N) * a.Hv
         need = so.gdn_chunk_fwd_workspace_size(ctypes.byref(a))
-        assert need >= MIN_WS + items * (wt + 16 + 1) * 1024
-        assert need <= MIN_WS + items * (wt + 16 + 1) * 1024 + 4 * 1024
+        assert need >= MIN_WS + items * (wt + 16 + 16 + 1) * 1024
+        assert need <= MIN_WS + items * (wt + 16 + 16 + 1) * 1024 + 5 * 1024
     assert so.gdn_chunk_fwd_workspace_size(ctypes.byref(good_args(dk=64))) == MIN_WS
 
 
