@@ -1,26 +1,30 @@
 // chunk_chain.cu -- the state-carrying half of the chunked gated-delta-rule forward (dk = 128) on
-// the sm_103a tensor cores, after chunk_prep.cu has staged every chunk's W^T, T'', P and gate
+// the sm_103a tensor cores, after chunk_prep.cu has staged every chunk's W, T'', P and gate
 // vectors in the workspace.
 //
 // One CTA (256 threads) per (sequence n, v-head h, 64-column value slab); the slab is one
 // state-QDQ tile (all 128 key rows x 64 value columns), so its amax is CTA-local ("GDN state/W QAT
 // foundation", "What does this PR do?"); with the INT8 codec each thread's key row holds its two
-// 32-column blocks, and the QDQ'd state is carried as bf16 hi + lo. Two warpgroups split each 64-token chunk:
-//   chain  (warps 4-7)  X = W S0 -> Delta = U - X, Dt = exp(gam_63 - gam) Delta -> C = K^T Dt ->
-//                       S1 = Gam_63 S0 + C, QDQ(S1) at a 64-token boundary -> the next chunk.
-//                       Only this loop is serial from chunk to chunk. It also refills the W^T
-//                       buffer and the Q/K stages once their last readers are done.
-//   output (warps 0-3)  U = T'' V (and the next T'' / V / P load), Y = Q S0, P Delta (P staged by
-//                       the prep, double-buffered), o = scale (Gam Y + P Delta); U of the next
-//                       chunk is issued right after P Delta, ahead of the chain's next X.
+// 32-column blocks, and the QDQ'd state is carried as bf16 hi + lo. Two warpgroups split each chunk:
+//   chain  (warps 4-7)  [X; Y] = [W; Q] S0 -> Delta = U - X, Dt = exp(gam_63 - gam) Delta ->
+//                       C = K^T Dt -> S1 = Gam_63 S0 + C, QDQ(S1) at a 64-token boundary -> the
+//                       next chunk. Only this loop is serial from chunk to chunk. X and Y come
+//                       from one M = 128 product whose A rows interleave W and Q in 16-row groups,
+//                       so X lands in TMEM lanes 0-15 and Y in lanes 16-31 of each quadrant (the
+//                       M = 64 row layout) and Y costs no separate MMA or wait. It also refills
+//                       the stages (W, Q, K, gate vectors) once their last readers are done.
+//   output (warps 0-3)  U = T'' V (and the next T'' / V load), P Delta (P staged by the prep),
+//                       o = scale (Gam Y + P Delta) through a shared-memory tile and one TMA store
+//                       per chunk; U of the next chunk is issued right after P Delta, ahead of the
+//                       chain's next [X; Y].
 // The state S0 (fp32) lives in the chain's registers (one key row of the slab per thread) and, as
 // the MMA operand, in shared memory as bf16 hi + lo, or as exact E4M3 codes once QDQ'd (the scale
-// is applied in the epilogues). W arrives as codes
-// (exact in bf16) with W QDQ, else as bf16 hi + lo; T'' and P as hi + lo; Delta and Dt are split
-// into hi + lo before their MMAs.
+// is applied in the epilogues). W arrives as codes (exact in bf16) with W QDQ, else as bf16 hi +
+// lo (the lo part as a separate M = 64 product accumulating onto X); T'' and P as hi + lo; Delta
+// and Dt are split into hi + lo before their MMAs.
 //
-// Hand-offs are mbarriers (TMA transactions, MMA commits, and three one-arrival signals from the
-// chain: "U consumed", "Delta stored", "S0 of the next chunk stored"). Every wait is bounded; a
+// Hand-offs are mbarriers (TMA transactions, MMA commits, and one-arrival signals: "U consumed"
+// and "Delta stored" from the chain, "Y read" from the output warpgroup). Every wait is bounded; a
 // warp whose wait gives up raises a CTA-wide abort flag, both warpgroups leave their loops at
 // their next checked barrier, TMA in flight is waited for (bounded), TMEM is freed.
 #include <algorithm>
@@ -50,28 +54,37 @@ constexpr int kThreads = 256;
 constexpr int kOutIssuer = GDN_OUT_ISSUER, kChainIssuer = GDN_CHAIN_ISSUER;
 constexpr uint32_t KB = 1024;
 // shared memory map (byte offsets from a 1024-byte aligned base)
-constexpr uint32_t kStage = 34 * KB;   // two stages: Q0 | K0 | Q1 | K1 (8 KB each, key columns 0-63 | 64-127) | vec
-constexpr uint32_t SQ0 = 0, SK0 = 8 * KB, SQ1 = 16 * KB, SVEC = 32 * KB;
-constexpr uint32_t OFF_TT = 68 * KB;    // T'' hi | lo, [64 r][64 i] K-major
-constexpr uint32_t OFF_V = 84 * KB;     // V slab [64 tok][64 j]
-constexpr uint32_t OFF_WT = 92 * KB;    // W^T codes [128 c][64 r] (or hi | lo, 16 KB apart)
-constexpr uint32_t OFF_SHI = 124 * KB;  // S0 operand [128 c][64 j] MN-major; lo at +16 KB
-constexpr uint32_t OFF_DL = 156 * KB;   // Delta hi, lo, Dt hi, lo ([i][j] MN-major, 8 KB each)
-constexpr uint32_t OFF_P = 188 * KB;    // P hi | lo ([r][i] K-major), two buffers by chunk parity
-constexpr uint32_t OFF_MISC = 220 * KB; // S0 scale [2], S0-is-codes [2], partial maxima [4], abort flag
+//   stage s (two, by chunk parity) at s * kStage: A0 | A1 (16 KB each: key columns 0-63 | 64-127 of
+//   the [W; Q] operand, 128 rows; rows 32 g .. 32 g + 15 are W rows 16 g .. 16 g + 15, rows 32 g +
+//   16 .. 32 g + 31 the Q rows 16 g .. 16 g + 15), then K0 | K1 (8 KB each, [64 tok][64])
+constexpr uint32_t kStage = 50 * KB;
+constexpr uint32_t SA0 = 0, SK0 = 32 * KB;
+constexpr uint32_t OFF_VEC = 100 * KB;  // gate vectors of chunk c in slot c mod 4 (1 KB each)
+constexpr uint32_t OFF_WLO = 104 * KB;  // W lo without W QDQ: key block 0 | 1, [64 r][64 c] K-major
+constexpr uint32_t OFF_TT = 120 * KB;   // T'' hi | lo, [64 r][64 i] K-major
+constexpr uint32_t OFF_V = 136 * KB;    // V slab [64 tok][64 j]
+constexpr uint32_t OFF_SHI = 144 * KB;  // S0 operand [128 c][64 j] MN-major; lo at +16 KB
+constexpr uint32_t OFF_DL = 176 * KB;   // Delta hi, lo, Dt hi, lo ([i][j] MN-major, 8 KB each)
+constexpr uint32_t OFF_PO = 208 * KB;   // P hi | lo ([r][i] K-major); once P Delta is done, the o tile
+                                        // (two [64 tok][32 j] fp32 halves, 128-byte swizzled rows)
+constexpr uint32_t OFF_MISC = 224 * KB; // S0 scales [4] by chunk mod 4, partial maxima [4], abort flag
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + slack to align the base
+static_assert(kSmemBytes <= 227 * KB, "shared memory map exceeds the per-CTA limit");
 
-// TMEM columns (M = 64 results sit in lanes 16 w .. 16 w + 15 of quadrant w)
-constexpr uint32_t TM_U = 0, TM_X = 64, TM_Y = 128, TM_C = 192, TM_PD = 256;
+// TMEM columns: [X; Y] of chunk c at TM_XY + 64 (c & 1) (M = 128: X in lanes 0-15, Y in lanes
+// 16-31 of each quadrant); U and P Delta are M = 64 results (lanes 0-15 of each quadrant)
+constexpr uint32_t TM_XY = 0, TM_U = 128, TM_C = 192, TM_PD = 256;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // T'' (K) x V (MN)
-constexpr uint32_t IDESC_X = tc::make_idesc(tc::kKindBF16, 64, 64, true, true);     // W^T (MN) x S0 (MN)
-constexpr uint32_t IDESC_Y = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // Q (K) x S0 (MN)
-constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);    // K^T (MN) x Dt (MN)
-constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);   // P (K) x Delta (MN)
+constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);     // T'' (K) x V (MN)
+constexpr uint32_t IDESC_XY = tc::make_idesc(tc::kKindBF16, 128, 64, false, true);   // [W; Q] (K) x S0 (MN)
+constexpr uint32_t IDESC_WLO = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);   // W lo (K) x S0 (MN)
+constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);     // K^T (MN) x Dt (MN)
+constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // P (K) x Delta (MN)
 
-enum : int { B_QK0 = 0, B_QK1, B_TV, B_WC, B_U, B_X, B_Y, B_C, B_PD, B_SRDY, B_DRDY, B_UFREE, kNumBars };
+enum : int {
+  B_QK0 = 0, B_QK1, B_TV, B_P, B_WLO, B_U, B_XY0, B_XY1, B_C, B_PD, B_DRDY, B_UFREE, B_OD0, B_OD1, kNumBars
+};
 
 struct ChainParams {
   const int32_t* order;   // chain order of the sequences, or null (natural order)
@@ -101,9 +114,10 @@ __device__ __forceinline__ bool wg_any(int id, bool pred) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap twt,
-                   const __grid_constant__ CUtensorMap ttt, const __grid_constant__ CUtensorMap tpp,
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tw16,
+                   const __grid_constant__ CUtensorMap tw64, const __grid_constant__ CUtensorMap ttt,
+                   const __grid_constant__ CUtensorMap tpp, const __grid_constant__ CUtensorMap tout,
                    const ChainParams p) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
@@ -137,10 +151,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const int64_t slot0 = t0 / 64 + n;   // workspace slot of chunk 0
   auto item = [&](int64_t cj) { return (slot0 + cj) * p.Hv + h; };
   auto chunk_len = [&](int64_t cj) { return (len - cj * 64) < 64 ? (int)(len - cj * 64) : 64; };
+  auto vecs = [&](int64_t cj) { return reinterpret_cast<const float*>(sm + OFF_VEC + (uint32_t)(cj & 3) * KB); };
 
   float* const misc = reinterpret_cast<float*>(sm + OFF_MISC);
-  float* const s_scale_slot = misc;                                       // [2], by chunk parity
-  int* const s_exact_slot = reinterpret_cast<int*>(misc + 2);             // [2]
+  float* const s_scale_slot = misc;                                       // [4], by chunk mod 4
   float* const red = misc + 4;                                            // [4]
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 8);
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
@@ -149,12 +163,14 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), 1);
     *abort_flag = 0;
     tc::mbar_fence_init();
-    tc::tma_prefetch_desc(&tq);
+    tc::tma_prefetch_desc(&tq16);
     tc::tma_prefetch_desc(&tk);
     tc::tma_prefetch_desc(&tv);
-    tc::tma_prefetch_desc(&twt);
+    tc::tma_prefetch_desc(&tw16);
+    tc::tma_prefetch_desc(&tw64);
     tc::tma_prefetch_desc(&ttt);
     tc::tma_prefetch_desc(&tpp);
+    tc::tma_prefetch_desc(&tout);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_slot), kTmemCols);
   tc::tc_fence_before();
@@ -163,46 +179,53 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t tmem = tmem_slot;
 
   // operand descriptors (128-byte swizzle, 8-row groups 1024 bytes apart)
-  const uint64_t dStgK = tc::make_sdesc(sbase, 16, 1024);        // K-major Q / K of stage 0
-  const uint64_t dStgM = tc::make_sdesc(sbase, 16 * KB, 1024);   // MN-major K^T of stage 0
+  const uint64_t dStgA = tc::make_sdesc(sbase + SA0, 16, 1024);       // K-major [W; Q] of stage 0
+  const uint64_t dStgM = tc::make_sdesc(sbase + SK0, 8 * KB, 1024);   // MN-major K^T of stage 0
+  const uint64_t dWlo = tc::make_sdesc(sbase + OFF_WLO, 16, 1024);
   const uint64_t dTT = tc::make_sdesc(sbase + OFF_TT, 16, 1024);
   const uint64_t dV = tc::make_sdesc(sbase + OFF_V, 8 * KB, 1024);
-  const uint64_t dWT = tc::make_sdesc(sbase + OFF_WT, 16 * KB, 1024);
   const uint64_t dS = tc::make_sdesc(sbase + OFF_SHI, 16 * KB, 1024);
   const uint64_t dDl = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);
-  const uint64_t dP = tc::make_sdesc(sbase + OFF_P, 16, 1024);
+  const uint64_t dP = tc::make_sdesc(sbase + OFF_PO, 16, 1024);
 
-  auto tma_qk = [&](int64_t cj) {   // Q, K tiles and gate vectors of chunk cj into stage cj & 1
+  const int64_t wrows = p.w_qdq ? 128 : 256;   // staged W rows per item: codes, or hi then lo
+  auto tma_qk = [&](int64_t cj) {   // [W; Q], K tiles and gate vectors of chunk cj into stage cj & 1
     const int s = (int)(cj & 1);
     const uint32_t base = sbase + (uint32_t)s * kStage, b = bar(B_QK0 + s);
-    tc::mbar_expect_tx(b, 32 * KB + 1024);
+    tc::mbar_expect_tx(b, 48 * KB + 1024);
     const int tok = (int)(t0 + cj * 64);
-    tc::tma_load_3d(base + SQ0, &tq, b, 0, hq, tok);
+    const int wr = (int)(item(cj) * wrows);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t dst = base + SA0 + (uint32_t)kb * 16 * KB + (uint32_t)g * 4 * KB;
+        tc::tma_load_2d(dst, &tw16, b, 0, wr + kb * 64 + 16 * g);
+        tc::tma_load_3d(dst + 2 * KB, &tq16, b, kb * 64, hq, tok + 16 * g);
+      }
     tc::tma_load_3d(base + SK0, &tk, b, 0, hq, tok);
-    tc::tma_load_3d(base + SQ1, &tq, b, 64, hq, tok);
-    tc::tma_load_3d(base + SK0 + 16 * KB, &tk, b, 64, hq, tok);
-    tc::bulk_load(base + SVEC, p.vec + item(cj) * 256, 1024, b);
+    tc::tma_load_3d(base + SK0 + 8 * KB, &tk, b, 64, hq, tok);
+    tc::bulk_load(sbase + OFF_VEC + (uint32_t)(cj & 3) * KB, p.vec + item(cj) * 256, 1024, b);
   };
-  auto tma_tv = [&](int64_t cj) {   // T'' hi | lo, the V slab and P hi | lo (buffer cj & 1) of chunk cj
-    tc::mbar_expect_tx(bar(B_TV), 40 * KB);
+  auto tma_wlo = [&](int64_t cj) {  // W lo (without W QDQ) of chunk cj
+    tc::mbar_expect_tx(bar(B_WLO), 16 * KB);
+    tc::tma_load_2d(sbase + OFF_WLO, &tw64, bar(B_WLO), 0, (int)(item(cj) * 256 + 128));
+    tc::tma_load_2d(sbase + OFF_WLO + 8 * KB, &tw64, bar(B_WLO), 0, (int)(item(cj) * 256 + 192));
+  };
+  auto tma_tv = [&](int64_t cj) {   // T'' hi | lo and the V slab of chunk cj
+    tc::mbar_expect_tx(bar(B_TV), 24 * KB);
     tc::tma_load_2d(sbase + OFF_TT, &ttt, bar(B_TV), 0, (int)(item(cj) * 128));
     tc::tma_load_3d(sbase + OFF_V, &tv, bar(B_TV), slab * 64, h, (int)(t0 + cj * 64));
-    tc::tma_load_2d(sbase + OFF_P + (uint32_t)(cj & 1) * 16 * KB, &tpp, bar(B_TV), 0, (int)(item(cj) * 128));
   };
-  auto tma_wc = [&](int64_t cj) {   // W^T of chunk cj
-    if (p.w_qdq) {
-      tc::mbar_expect_tx(bar(B_WC), 16 * KB);
-      tc::tma_load_2d(sbase + OFF_WT, &twt, bar(B_WC), 0, (int)(item(cj) * 128));
-    } else {
-      tc::mbar_expect_tx(bar(B_WC), 32 * KB);
-      tc::tma_load_2d(sbase + OFF_WT, &twt, bar(B_WC), 0, (int)(item(cj) * 256));
-      tc::tma_load_2d(sbase + OFF_WT + 16 * KB, &twt, bar(B_WC), 0, (int)(item(cj) * 256 + 128));
-    }
+  auto tma_p = [&](int64_t cj) {    // P hi | lo of chunk cj
+    tc::mbar_expect_tx(bar(B_P), 16 * KB);
+    tc::tma_load_2d(sbase + OFF_PO, &tpp, bar(B_P), 0, (int)(item(cj) * 128));
   };
   if (tid == 0 && nchunks > 0) {
     tma_qk(0);
     tma_tv(0);
-    tma_wc(0);
+    tma_p(0);
+    if (!p.w_qdq) tma_wlo(0);
     if (nchunks > 1) tma_qk(1);
   }
 
@@ -222,8 +245,6 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if (warp < 4) {
     // ================================ output warpgroup ================================
-    // U of chunk c + 1 is issued right after P Delta of chunk c, so that it is through the tensor
-    // pipe before the chain issues its next X.
     auto issue_u = [&]() {   // U = T'' V (T'' hi + lo)
       tc::tc_fence_after();
 #pragma unroll
@@ -241,41 +262,24 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int s = (int)(c & 1);
       const int L = chunk_len(c);
       const uint32_t par = (uint32_t)(c & 1);
-      const uint32_t stg = (uint32_t)s * kStage;
-      const float* vg = reinterpret_cast<const float*>(sm + stg + SVEC);
-      // the row's Gam, read before Y is issued: the chain refills the stage once Y and C are done
-      wait(B_QK0 + s, (uint32_t)((c >> 1) & 1));
-      const float egam_r = vg[64 + row64];
-      // T'' / V and the other P buffer are free once U (issued after the previous P Delta by the
-      // same thread) has completed: fetch the next chunk's, a whole chunk ahead
+      // T'' / V are free once U has completed: fetch the next chunk's, a whole chunk ahead
       if (warp == kOutIssuer / 32) {
         wait(B_U, par);
         if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_tv(c + 1);
       }
-      if (wg_any(1, !live())) break;
-      // ---- Y = Q S0 once the chain has stored S0 for this chunk ----
-      wait(B_SRDY, par);
-      const float y_scale = s_scale_slot[s];
-      if (tid == kOutIssuer && live()) {
-        tc::tc_fence_after();
-        const int ny = s_exact_slot[s] ? 1 : 2;
-        for (int q = 0; q < ny; ++q)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tmem + TM_Y, dadv(dStgK, SQ0 + stg + (ks >> 2) * 16 * KB + (ks & 3) * 32),
-                         dadv(dS, q * 16 * KB + ks * 2048), IDESC_Y, (q | ks) != 0);
-        tc::mma_commit(bar(B_Y));
-      }
       // ---- P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi once the chain has stored Delta ----
       wait(B_DRDY, par);
+      // S0's scale and the row's Gam: written / landed before the chain stored Delta
+      const float y_scale = s_scale_slot[c & 3];
+      const float egam_r = vecs(c)[64 + row64];
+      wait(B_P, par);
       if (tid == kOutIssuer && live()) {
         tc::tc_fence_after();
-        const uint32_t pb = (uint32_t)s * 16 * KB;
 #pragma unroll
         for (int q = 0; q < 3; ++q)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + TM_PD, dadv(dP, pb + (q == 2 ? 8 * KB : 0) + ks * 32),
+            tc::mma_bf16(tmem + TM_PD, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32),
                          dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048), IDESC_PD, (q | ks) != 0);
         tc::mma_commit(bar(B_PD));
       }
@@ -286,28 +290,45 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (tid == kOutIssuer && live()) issue_u();
       }
       // ---- o = scale (Gam Y + P Delta), rows r < L ----
-      wait(B_Y, par);
+      wait(B_XY0 + s, (uint32_t)((c >> 1) & 1));
       wait(B_PD, par);
       tc::tc_fence_after();
       {
         float yv[32], pv[32];
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_Y), yv);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_Y + 16), yv + 16);
+        const uint32_t ty = TM_XY + (uint32_t)s * 64;
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, ty), yv);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, ty + 16), yv + 16);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD), pv);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 16), pv + 16);
         tc::tmem_ld_wait();
-        if (row64 < L) {
-          const float e2 = egam_r * y_scale;
+        const float e2 = egam_r * y_scale;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) yv[j] = p.scale * fmaf(e2, yv[j], pv[j]);
+        if (L == 64) {   // row row64, columns [32 half, +32): one 128-byte row of half-tile `half`
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(sm + OFF_PO + (uint32_t)half * 8 * KB + tc::sw128(row64, 16 * q)) =
+                make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
+          tc::fence_proxy_async_smem();
+        } else if (row64 < L) {   // a sequence's last chunk: rows past its end belong to others
           float4* out = reinterpret_cast<float4*>(p.o + ((t0 + c * 64 + row64) * p.Hv + h) * (int64_t)p.dv +
                                                   slab * 64 + half * 32);
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            out[j >> 2] = make_float4(p.scale * fmaf(e2, yv[j], pv[j]), p.scale * fmaf(e2, yv[j + 1], pv[j + 1]),
-                                      p.scale * fmaf(e2, yv[j + 2], pv[j + 2]), p.scale * fmaf(e2, yv[j + 3], pv[j + 3]));
+          for (int j = 0; j < 32; j += 4) out[j >> 2] = make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
         }
       }
       tc::tc_fence_before();
       if (wg_any(1, !live())) break;
+      if (tid == 0) tc::mbar_arrive(bar(B_OD0 + s));   // Y of chunk c has been read
+      if (tid == kOutIssuer) {
+        if (L == 64) {   // the tile is complete: one store, read back before the region is reused
+          tc::tma_store_3d(&tout, sbase + OFF_PO, slab * 64, h, (int)(t0 + c * 64));
+          tc::tma_store_3d(&tout, sbase + OFF_PO + 8 * KB, slab * 64 + 32, h, (int)(t0 + c * 64));
+          tc::bulk_commit();
+          tc::bulk_wait_read();
+        }
+        if (c + 1 < nchunks && live()) tma_p(c + 1);   // needed after the chain's next Delta
+      }
     }
   } else {
     // ================================ chain warpgroup ================================
@@ -334,14 +355,10 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       st16(sm, OFF_SHI + off, h16);
       st16(sm, OFF_SHI + 16 * KB + off, l16);
     }
-    if (ctid == 0) {
-      s_scale_slot[0] = 1.f;
-      s_exact_slot[0] = 0;
-    }
+    if (ctid == 0) s_scale_slot[0] = 1.f;
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     wg_sync(2);
-    if (ctid == 0) tc::mbar_arrive(bar(B_SRDY));
     bool s_exact = false;   // S0 operand holds exact codes with scale s_scale
     float s_scale = 1.f;
     float i8s[2] = {0.f, 0.f};   // INT8: this row's two block scales of the last QDQ'd state
@@ -350,32 +367,36 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int L = chunk_len(c);
       const uint32_t par = (uint32_t)(c & 1);
       const uint32_t stg = (uint32_t)s * kStage;
-      const float* vg = reinterpret_cast<const float*>(sm + stg + SVEC);
       wait(B_QK0 + s, (uint32_t)((c >> 1) & 1));
+      const float* vg = vecs(c);
       const float dr = vg[128 + row64], el = vg[64 + 63];
       const float f = vg[192] * s_scale;   // X = W S0 holds codes x codes: W scale x S0 scale
-      // ---- X = W S0 ----
-      wait(B_WC, par);
+      if (!p.w_qdq) wait(B_WLO, par);
+      if (c >= 2) wait(B_OD0 + s, (uint32_t)(((c - 2) >> 1) & 1));   // Y of chunk c - 2 has been read
+      // ---- [X; Y] = [W; Q] S0 ----
+      const uint32_t txy = TM_XY + (uint32_t)s * 64;
       if (ctid == kChainIssuer && live()) {
         tc::tc_fence_after();
-        // (W codes or W hi) x (S codes or S hi) [+ W x S lo] [+ W lo x S hi]
+        // [W codes or W hi; Q] x (S codes or S hi) [+ [W; Q] x S lo] [+ W lo x S hi]
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tmem + TM_X, dadv(dWT, ks * 2048), dadv(dS, ks * 2048), IDESC_X, ks > 0);
+          tc::mma_bf16(tmem + txy, dadv(dStgA, stg + (ks >> 2) * 16 * KB + (ks & 3) * 32), dadv(dS, ks * 2048),
+                       IDESC_XY, ks > 0);
         if (!s_exact) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tmem + TM_X, dadv(dWT, ks * 2048), dadv(dS, 16 * KB + ks * 2048), IDESC_X, 1);
+            tc::mma_bf16(tmem + txy, dadv(dStgA, stg + (ks >> 2) * 16 * KB + (ks & 3) * 32),
+                         dadv(dS, 16 * KB + ks * 2048), IDESC_XY, 1);
         }
         if (!p.w_qdq) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_bf16(tmem + TM_X, dadv(dWT, 16 * KB + ks * 2048), dadv(dS, ks * 2048), IDESC_X, 1);
+            tc::mma_bf16(tmem + txy, dadv(dWlo, (ks >> 2) * 8 * KB + (ks & 3) * 32), dadv(dS, ks * 2048), IDESC_WLO, 1);
         }
-        tc::mma_commit(bar(B_X));
+        tc::mma_commit(bar(B_XY0 + s));
       }
-      wait(B_X, par);
-      if (ctid == kChainIssuer && c + 1 < nchunks && live()) tma_wc(c + 1);   // W^T is free once X has read it
+      wait(B_XY0 + s, (uint32_t)((c >> 1) & 1));
+      if (ctid == kChainIssuer && !p.w_qdq && c + 1 < nchunks && live()) tma_wlo(c + 1);   // W lo has been read
       // ---- Delta = U - f X, Dt = exp(gam_63 - gam_r) Delta ----
       wait(B_U, par);
       if (c > 0) wait(B_PD, (uint32_t)((c - 1) & 1));   // the previous P Delta has read Delta
@@ -383,8 +404,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       float d[32];
       {
         float xv[32], uv[32];
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_X), xv);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_X + 16), xv + 16);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, txy), xv);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, txy + 16), xv + 16);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_U), uv);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_U + 16), uv + 16);
         tc::tmem_ld_wait();
@@ -414,7 +435,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + TM_C, dadv(dStgM, stg + SK0 + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
+            tc::mma_bf16(tmem + TM_C, dadv(dStgM, stg + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
                          IDESC_C, (part | ks) != 0);
         tc::mma_commit(bar(B_C));
       }
@@ -430,9 +451,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tc::fence_proxy_async_smem();
       if (wg_any(2, !live())) break;
       if (ctid == 0) tc::mbar_arrive(bar(B_DRDY));
-      // ---- S1 = Gam_63 S0 + C; QDQ at the 64-token boundary (after Y has read S0) ----
+      // ---- S1 = Gam_63 S0 + C; QDQ at the 64-token boundary (Y read S0 with X, waited above) ----
       wait(B_C, par);
-      wait(B_Y, par);
       tc::tc_fence_after();
       {
         float* const s1 = S;
@@ -493,18 +513,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           s_scale = 1.f;
         }
       }
-      if (ctid == 0) {
-        s_scale_slot[s ^ 1] = s_scale;
-        s_exact_slot[s ^ 1] = s_exact ? 1 : 0;
-      }
+      if (ctid == 0) s_scale_slot[(c + 1) & 3] = s_scale;
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
-      if (ctid == 0) {
-        tc::mbar_arrive(bar(B_SRDY));   // S0 of chunk c + 1 is stored
-      }
-      // stage s is free: C and Y have read it (both waited for above), and the output warpgroup read
-      // its gate vector before issuing Y -- fetch chunk c + 2 into it
+      // stage s is free: [X; Y] and C (committed after it by the same thread) have read it -- fetch
+      // chunk c + 2 into it
       if (ctid == kChainIssuer && c + 2 < nchunks && live()) tma_qk(c + 2);
     }
     if (live() && p.hT) {
@@ -531,8 +545,8 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       atomicExch(p.status, 1);
       // TMA loads may still be landing in this CTA's shared memory: wait for each barrier's
       // current phase (one of the two parities returns at once), bounded
-      const int tx_bars[4] = {B_QK0, B_QK1, B_TV, B_WC};
-      for (int i = 0; i < 4; ++i) {
+      const int tx_bars[5] = {B_QK0, B_QK1, B_TV, B_P, B_WLO};
+      for (int i = 0; i < 5; ++i) {
         tc::mbar_wait(bar(tx_bars[i]), 0, 1u << 14);
         tc::mbar_wait(bar(tx_bars[i]), 1, 1u << 14);
       }
@@ -590,12 +604,14 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   if (blocks == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)p.B * p.T;
   const int64_t tmap = tokens > 0 ? tokens : 1;   // an empty batch still needs valid maps (never loaded)
-  CUtensorMap tq, tk, tv, twt, ttt, tpp;
-  if (!make_bf16_map(&tq, p.q, 128, p.Hqk, tmap) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap) ||
-      !make_bf16_map(&tv, p.v, p.dv, p.Hv, tmap) ||
-      !make_bf16_rows_map(&twt, w + lay.off_wt, lay.items * (p.w_qdq ? 128 : 256), 128) ||
+  CUtensorMap tq16, tk, tv, tw16, tw64, ttt, tpp, tout;
+  const int64_t wrows = lay.items * (p.w_qdq ? 128 : 256);
+  if (!make_bf16_map(&tq16, p.q, 128, p.Hqk, tmap, 16) || !make_bf16_map(&tk, p.k, 128, p.Hqk, tmap) ||
+      !make_bf16_map(&tv, p.v, p.dv, p.Hv, tmap) || !make_bf16_rows_map(&tw16, w + lay.off_wt, wrows, 16) ||
+      !make_bf16_rows_map(&tw64, w + lay.off_wt, wrows, 64) ||
       !make_bf16_rows_map(&ttt, w + lay.off_tt, lay.items * 128, 128) ||
-      !make_bf16_rows_map(&tpp, w + lay.off_p, lay.items * 128, 128))
+      !make_bf16_rows_map(&tpp, w + lay.off_p, lay.items * 128, 128) ||
+      !make_f32_out_map(&tout, p.o, p.dv, p.Hv, tmap))
     return cudaErrorInvalidValue;
   const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
   if (e != cudaSuccess) return e;
@@ -604,7 +620,7 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   cp.sscale = p.state_scales;
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, twt, ttt, tpp, cp);
+  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq16, tk, tv, tw16, tw64, ttt, tpp, tout, cp);
   return cudaGetLastError();
 }
 

@@ -53,24 +53,27 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const flo
 bool chunk_tc_supported(const ChunkProblem& p);
 cudaError_t launch_chunk_tc(const ChunkProblem& p, int* status, cudaStream_t stream);
 
-// TMA descriptor of a head-last bf16 tensor [tokens, heads, D] with 64 x 1 x 64 boxes
+// TMA descriptor of a head-last bf16 tensor [tokens, heads, D] with 64 x 1 x box_tokens boxes
 // (128-byte swizzle). Host only; false when the driver entry point is unavailable.
-bool make_bf16_map(CUtensorMap* map, const void* base, int D, int heads, int64_t tokens);
+bool make_bf16_map(CUtensorMap* map, const void* base, int D, int heads, int64_t tokens, int box_tokens = 64);
 // TMA descriptor of a bf16 matrix [rows][64] with 64 x box_rows boxes (128-byte swizzle).
 bool make_bf16_rows_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows);
+// TMA descriptor of a head-last fp32 output [tokens, heads, D] with 32 x 1 x 64 boxes (128-byte swizzle).
+bool make_f32_out_map(CUtensorMap* map, void* base, int D, int heads, int64_t tokens);
 
 // ---- split tensor-core path: a parallel prep kernel, then the state-carrying chain kernel ----
 // Work items are (slot, v-head); slot(n, c) = floor(cu[n] / 64) + n + c for chunk c of sequence n
 // (cu[n] = n T without cu_seqlens). The slots of different sequences never collide, and there
 // are at most floor(tokens / 64) + N of them. Per item the prep kernel stores, in the workspace:
-//   W^T  bf16 [128 c][64 r]: the chunk's W transposed -- E4M3 codes (exact in bf16) with W QDQ,
-//        else the bf16 hi part followed by the lo part ([2][128][64]);
+//   W    bf16 [2 key blocks][64 r][64 c]: the chunk's W, key columns 0-63 then 64-127 -- E4M3
+//        codes (exact in bf16) with W QDQ, else the bf16 hi part followed by the lo part
+//        ([2][2][64][64]);
 //   T''  bf16 [2][64 r][64 i]: hi and lo parts of T diag(beta) (U = T'' V in the chain);
 //   P    bf16 [2][64 r][64 i]: hi and lo parts of exp(gam_r - gam_i) (q_r . k_i), i <= r < L;
 //   vec  fp32 [256]: gam [64], Gam = exp(gam) [64], exp(gam_63 - gam) [64], W scale (index 192).
 struct SplitLayout {
   int64_t slots, items;
-  size_t wt_item_bytes;            // 16 KB with W QDQ, 32 KB without
+  size_t wt_item_bytes;            // W: 16 KB with W QDQ, 32 KB without
   size_t off_wt, off_tt, off_p, off_vec;  // byte offsets inside the workspace
   size_t off_order;                // N int32: sequences by decreasing length (varlen chain order)
   size_t total;                    // workspace bytes, status word included

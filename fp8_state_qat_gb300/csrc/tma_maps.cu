@@ -26,13 +26,13 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// 3-D map over a head-last bf16 tensor [tokens, heads, D]: dims (D, heads, tokens), box 64 x 1 x 64
-bool make_bf16_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens) {
+// 3-D map over a head-last bf16 tensor [tokens, heads, D]: dims (D, heads, tokens), box 64 x 1 x box_tokens
+bool make_bf16_map(CUtensorMap* m, const void* base, int D, int heads, int64_t tokens, int box_tokens) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_tokens};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -50,6 +50,20 @@ bool make_bf16_rows_map(CUtensorMap* m, const void* base, int64_t rows, int box_
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over a head-last fp32 output [tokens, heads, D]: dims (D, heads, tokens), box 32 x 1 x 64
+// (one 128-byte swizzled row of 32 values per token)
+bool make_f32_out_map(CUtensorMap* m, void* base, int D, int heads, int64_t tokens) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)heads * D * 4};
+  const cuuint32_t box[3] = {32, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 }  // namespace gdn

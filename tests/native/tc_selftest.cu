@@ -81,16 +81,20 @@ tc_selftest_kernel(const float* A, const float* B, float* D, float* D2, int M, i
 #pragma unroll
       for (int j = 0; j < 16; ++j) D[lane * N + c0 + j] = v[j];
     }
-    if (D2) {   // the same accumulator read with the 16-lane two-half shape (split = N / 2)
-      const int t = threadIdx.x & 31, row = warp * 32 + (t & 15);
-      for (int c0 = 0; c0 < N / 2; c0 += 16) {
-        float v[16];
-        if (N == 128) tc::tmem_ld16x2<64>(tc::tmem_addr(tmem, warp * 32, c0), v);
-        else tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, warp * 32, c0), v);
-        tc::tmem_ld_wait();
-        const int col = c0 + (t >> 4) * (N / 2);
+    if (D2) {   // the same accumulator read with the 16-lane two-half shape (split = N / 2); with
+                // M = 128 also the upper 16 lanes of each quadrant (lane offset 16)
+      const int t = threadIdx.x & 31;
+      for (int lo16 = 0; lo16 < (M == 128 ? 32 : 16); lo16 += 16) {
+        const int row = warp * 32 + lo16 + (t & 15);
+        for (int c0 = 0; c0 < N / 2; c0 += 16) {
+          float v[16];
+          if (N == 128) tc::tmem_ld16x2<64>(tc::tmem_addr(tmem, warp * 32 + lo16, c0), v);
+          else tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, warp * 32 + lo16, c0), v);
+          tc::tmem_ld_wait();
+          const int col = c0 + (t >> 4) * (N / 2);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) D2[row * N + col + j] = v[j];
+          for (int j = 0; j < 16; ++j) D2[row * N + col + j] = v[j];
+        }
       }
     }
   }
@@ -104,7 +108,8 @@ tc_selftest_kernel(const float* A, const float* B, float* D, float* D2, int M, i
 
 // Internal: D [128 lanes x N] from A [M x K] and B [K x N] (device fp32, row-major) with the
 // requested operand kind (0 bf16, 1 tf32) and majors; status (device int) set on a timeout.
-// D2 (nullable): the accumulator read again with the 16x32bx2 TMEM load shape.
+// D2 (nullable): the accumulator read again with the 16x32bx2 TMEM load shape (M = 128: both
+// 16-lane halves of every quadrant).
 extern "C" int gdnqat_internal_tc_selftest(const float* A, const float* B, float* D, float* D2, int M, int N, int K,
                                            int kind, int a_mn, int b_mn, int* status, cudaStream_t stream) {
   if ((M != 64 && M != 128) || (N != 64 && N != 128) || (K != 64 && K != 128)) return 1;

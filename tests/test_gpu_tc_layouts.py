@@ -78,3 +78,27 @@ def test_tmem_16x32bx2_reads_m64_rows(gdn, N):
     np.testing.assert_allclose(got[rows], want, rtol=1e-4, atol=1e-4 * np.abs(want).max())
     untouched = [l for l in range(128) if l not in rows]
     assert np.isnan(got[untouched]).all()
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_tmem_16x32bx2_upper_half_lanes_m128(gdn, N):
+    """An M = 128 accumulator read with the 16-lane two-half shape at lane offsets 0 and 16 of
+    each quadrant: every row comes back (the chain kernel reads X from lanes 0-15 and Y from
+    lanes 16-31 of one M = 128 product whose A rows interleave W and Q in 16-row groups)."""
+    fn = native.load().gdnqat_internal_tc_selftest
+    fn.restype = ctypes.c_int
+    M, K = 128, 128
+    rng = np.random.default_rng(600 + N)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dD = torch.full((128, N), float("nan"), device="cuda")
+    dD2 = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = fn(ctypes.c_void_p(dA.data_ptr()), ctypes.c_void_p(dB.data_ptr()), ctypes.c_void_p(dD.data_ptr()),
+            ctypes.c_void_p(dD2.data_ptr()), M, N, K, 0, 0, 0, ctypes.c_void_p(st.data_ptr()), None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "bounded wait gave up"
+    want = rounded(A, 0) @ rounded(B, 0)
+    np.testing.assert_allclose(dD2.cpu().double().numpy(), want, rtol=1e-4, atol=1e-4 * np.abs(want).max())
