@@ -13,18 +13,20 @@
 //                       so X lands in TMEM lanes 0-15 and Y in lanes 16-31 of each quadrant (the
 //                       M = 64 row layout) and Y costs no separate MMA or wait. It also refills
 //                       the stages (W, Q, K, gate vectors) once their last readers are done.
-//   output (warps 0-3)  U = T'' V (and the next T'' / V load), P Delta (P staged by the prep),
-//                       o = scale (Gam Y + P Delta) through a shared-memory tile and one TMA store
-//                       per chunk; U of the next chunk is issued right after P Delta, ahead of the
-//                       chain's next [X; Y].
+//   output (warps 0-3)  U = T'' V, P Delta (P staged by the prep), o = scale (Gam Y + P Delta)
+//                       through a shared-memory tile and one TMA store per chunk; U of the next
+//                       chunk is issued right after P Delta, ahead of the chain's next [X; Y].
+//                       Its warps also issue every TMA copy of the CTA (stage refills once the
+//                       chain signals a stage free, T'' / V, P, the o store), so that neither MMA
+//                       issuer issues anything but MMAs.
 // The state S0 (fp32) lives in the chain's registers (one key row of the slab per thread) and, as
 // the MMA operand, in shared memory as bf16 hi + lo, or as exact E4M3 codes once QDQ'd (the scale
 // is applied in the epilogues). W arrives as codes (exact in bf16) with W QDQ, else as bf16 hi +
 // lo (the lo part as a separate M = 64 product accumulating onto X); T'' and P as hi + lo; Delta
 // and Dt are split into hi + lo before their MMAs.
 //
-// Hand-offs are mbarriers (TMA transactions, MMA commits, and one-arrival signals: "U consumed"
-// and "Delta stored" from the chain, "Y read" from the output warpgroup). Every wait is bounded; a
+// Hand-offs are mbarriers (TMA transactions, MMA commits, and one-arrival signals: "U consumed",
+// "Delta stored" and "stage free" from the chain, "Y read" from the output warpgroup). Every wait is bounded; a
 // warp whose wait gives up raises a CTA-wide abort flag, both warpgroups leave their loops at
 // their next checked barrier, TMA in flight is waited for (bounded), TMEM is freed.
 #include <algorithm>
@@ -61,30 +63,39 @@ constexpr uint32_t kStage = 50 * KB;
 constexpr uint32_t SA0 = 0, SK0 = 32 * KB;
 constexpr uint32_t OFF_VEC = 100 * KB;  // gate vectors of chunk c in slot c mod 4 (1 KB each)
 constexpr uint32_t OFF_WLO = 104 * KB;  // W lo without W QDQ: key block 0 | 1, [64 r][64 c] K-major
-constexpr uint32_t OFF_TT = 120 * KB;   // T'' hi | lo, [64 r][64 i] K-major
+constexpr uint32_t OFF_TT = 120 * KB;   // T'' hi | lo rows interleaved, [128][64 i] K-major
 constexpr uint32_t OFF_V = 136 * KB;    // V slab [64 tok][64 j]
 constexpr uint32_t OFF_SHI = 144 * KB;  // S0 operand [128 c][64 j] MN-major; lo at +16 KB
 constexpr uint32_t OFF_DL = 176 * KB;   // Delta hi, lo, Dt hi, lo ([i][j] MN-major, 8 KB each)
-constexpr uint32_t OFF_PO = 208 * KB;   // P hi | lo ([r][i] K-major); once P Delta is done, the o tile
+constexpr uint32_t OFF_PO = 208 * KB;   // P hi | lo rows interleaved ([128][i] K-major); once P Delta is done, the o tile
                                         // (two [64 tok][32 j] fp32 halves, 128-byte swizzled rows)
 constexpr uint32_t OFF_MISC = 224 * KB; // S0 scales [4] by chunk mod 4, partial maxima [4], abort flag
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + slack to align the base
 static_assert(kSmemBytes <= 227 * KB, "shared memory map exceeds the per-CTA limit");
 
-// TMEM columns: [X; Y] of chunk c at TM_XY + 64 (c & 1) (M = 128: X in lanes 0-15, Y in lanes
-// 16-31 of each quadrant); U and P Delta are M = 64 results (lanes 0-15 of each quadrant)
-constexpr uint32_t TM_XY = 0, TM_U = 128, TM_C = 192, TM_PD = 256;
+// TMEM columns. M = 128 products whose A rows interleave two 64-row matrices in 16-row groups put
+// the first one's result in lanes 0-15 and the second's in lanes 16-31 of each quadrant (the M = 64
+// row layout, row 16 q + i in lane 32 q + i):
+//   [X; Y] of chunk c   TM_XY + 64 (c & 1)   [W; Q] S0
+//   U                   TM_U                 [T''_hi; T''_lo] V         (U = the two halves summed)
+//   C                   TM_C (128 columns)   K^T [Dt_hi | Dt_lo]        (C = left + right)
+//   P Delta             TM_PD (128 columns)  [P_hi; P_lo] [D_hi | D_lo] (P Delta = the four parts summed)
+constexpr uint32_t TM_XY = 0, TM_U = 128, TM_C = 192, TM_PD = 320;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);     // T'' (K) x V (MN)
+constexpr uint32_t IDESC_U = tc::make_idesc(tc::kKindBF16, 128, 64, false, true);    // [T''hi; T''lo] (K) x V (MN)
 constexpr uint32_t IDESC_XY = tc::make_idesc(tc::kKindBF16, 128, 64, false, true);   // [W; Q] (K) x S0 (MN)
 constexpr uint32_t IDESC_WLO = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);   // W lo (K) x S0 (MN)
-constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 64, true, true);     // K^T (MN) x Dt (MN)
-constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 64, 64, false, true);    // P (K) x Delta (MN)
+constexpr uint32_t IDESC_C = tc::make_idesc(tc::kKindBF16, 128, 128, true, true);    // K^T (MN) x [Dt hi | lo] (MN)
+constexpr uint32_t IDESC_PD = tc::make_idesc(tc::kKindBF16, 128, 128, false, true);  // [P hi; lo] (K) x [D hi | lo] (MN)
 
 enum : int {
-  B_QK0 = 0, B_QK1, B_TV, B_P, B_WLO, B_U, B_XY0, B_XY1, B_C, B_PD, B_DRDY, B_UFREE, B_OD0, B_OD1, kNumBars
+  B_QK0 = 0, B_QK1, B_TV, B_P, B_WLO, B_U, B_XY0, B_XY1, B_C, B_PD, B_DRDY, B_OD0, B_OD1, B_SF0, B_SF1, kNumBars
 };
+// Threads that issue TMA copies. The MMA issuers issue nothing else: a thread's tcgen05.mma queues
+// behind the bulk copies it issued before, so refills from an issuer sit on the chain's path.
+constexpr int kTvLoader = 32;     // warp 1: T'' / V
+constexpr int kStageLoader = 96;  // warp 3: stage refills, the o store and P
 
 struct ChainParams {
   const int32_t* order;   // chain order of the sequences, or null (natural order)
@@ -185,7 +196,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
   const uint64_t dTT = tc::make_sdesc(sbase + OFF_TT, 16, 1024);
   const uint64_t dV = tc::make_sdesc(sbase + OFF_V, 8 * KB, 1024);
   const uint64_t dS = tc::make_sdesc(sbase + OFF_SHI, 16 * KB, 1024);
-  const uint64_t dDl = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);
+  const uint64_t dDl = tc::make_sdesc(sbase + OFF_DL, 8 * KB, 1024);   // [D hi | D lo], then [Dt hi | Dt lo] at +16 KB
   const uint64_t dP = tc::make_sdesc(sbase + OFF_PO, 16, 1024);
 
   const int64_t wrows = p.w_qdq ? 128 : 256;   // staged W rows per item: codes, or hi then lo
@@ -221,6 +232,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
     tc::mbar_expect_tx(bar(B_P), 16 * KB);
     tc::tma_load_2d(sbase + OFF_PO, &tpp, bar(B_P), 0, (int)(item(cj) * 128));
   };
+  // launched as a programmatic dependent of the prep kernel: everything above overlaps its last
+  // wave; its staging is read only after it has completed (a no-op without that launch attribute)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0 && nchunks > 0) {
     tma_qk(0);
     tma_tv(0);
@@ -245,13 +259,11 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
 
   if (warp < 4) {
     // ================================ output warpgroup ================================
-    auto issue_u = [&]() {   // U = T'' V (T'' hi + lo)
+    auto issue_u = [&]() {   // [T''_hi; T''_lo] V
       tc::tc_fence_after();
 #pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + TM_U, dadv(dTT, part * 8 * KB + ks * 32), dadv(dV, ks * 2048), IDESC_U, (part | ks) != 0);
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(tmem + TM_U, dadv(dTT, ks * 32), dadv(dV, ks * 2048), IDESC_U, ks != 0);
       tc::mma_commit(bar(B_U));
     };
     if (nchunks > 0) {
@@ -263,30 +275,28 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
       const int L = chunk_len(c);
       const uint32_t par = (uint32_t)(c & 1);
       // T'' / V are free once U has completed: fetch the next chunk's, a whole chunk ahead
-      if (warp == kOutIssuer / 32) {
+      if (warp == kTvLoader / 32) {
         wait(B_U, par);
-        if (tid == kOutIssuer && c + 1 < nchunks && live()) tma_tv(c + 1);
+        if (tid == kTvLoader && c + 1 < nchunks && live()) tma_tv(c + 1);
       }
-      // ---- P Delta = P_hi D_hi + P_hi D_lo + P_lo D_hi once the chain has stored Delta ----
+      // ---- P Delta and the next U, once the chain's C has completed: they run in the tensor pipe
+      // while the chain carries out its state epilogue, never next to its [X; Y] or C ----
       wait(B_DRDY, par);
       // S0's scale and the row's Gam: written / landed before the chain stored Delta
       const float y_scale = s_scale_slot[c & 3];
       const float egam_r = vecs(c)[64 + row64];
+      wait(B_SF0 + s, (uint32_t)((c >> 1) & 1));   // C has read stage c & 1 and Dt; the chain has read U
+      if (tid == kStageLoader && c + 2 < nchunks && live()) tma_qk(c + 2);
       wait(B_P, par);
       if (tid == kOutIssuer && live()) {
         tc::tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 3; ++q)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + TM_PD, dadv(dP, (q == 2 ? 8 * KB : 0) + ks * 32),
-                         dadv(dDl, (q == 1 ? 8 * KB : 0) + ks * 2048), IDESC_PD, (q | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_PD, dadv(dP, ks * 32), dadv(dDl, ks * 2048), IDESC_PD, ks != 0);
         tc::mma_commit(bar(B_PD));
       }
-      // ---- the next chunk's U (once the chain has read this one) ----
-      if (c + 1 < nchunks) {
+      if (c + 1 < nchunks && warp == kOutIssuer / 32) {
         wait(B_TV, par ^ 1u);
-        wait(B_UFREE, par);
         if (tid == kOutIssuer && live()) issue_u();
       }
       // ---- o = scale (Gam Y + P Delta), rows r < L ----
@@ -294,16 +304,21 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
       wait(B_PD, par);
       tc::tc_fence_after();
       {
-        float yv[32], pv[32];
+        float yv[32];
         const uint32_t ty = TM_XY + (uint32_t)s * 64;
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, ty), yv);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, ty + 16), yv + 16);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD), pv);
-        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 16), pv + 16);
-        tc::tmem_ld_wait();
         const float e2 = egam_r * y_scale;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) yv[j] = p.scale * fmaf(e2, yv[j], pv[j]);
+        for (int k = 0; k < 2; ++k) {   // columns [32 half + 16 k, +16): Y and the four P Delta parts
+          float y16[16], a0[16], a1[16], b0[16], b1[16];
+          tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, ty + 16 * k), y16);
+          tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 16 * k), a0);
+          tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_PD + 64 + 16 * k), a1);
+          tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, TM_PD + 16 * k), b0);
+          tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, TM_PD + 64 + 16 * k), b1);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) yv[16 * k + j] = p.scale * fmaf(e2, y16[j], (a0[j] + a1[j]) + (b0[j] + b1[j]));
+        }
         if (L == 64) {   // row row64, columns [32 half, +32): one 128-byte row of half-tile `half`
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -320,7 +335,7 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
       tc::tc_fence_before();
       if (wg_any(1, !live())) break;
       if (tid == 0) tc::mbar_arrive(bar(B_OD0 + s));   // Y of chunk c has been read
-      if (tid == kOutIssuer) {
+      if (tid == kStageLoader) {
         if (L == 64) {   // the tile is complete: one store, read back before the region is reused
           tc::tma_store_3d(&tout, sbase + OFF_PO, slab * 64, h, (int)(t0 + c * 64));
           tc::tma_store_3d(&tout, sbase + OFF_PO + 8 * KB, slab * 64 + 32, h, (int)(t0 + c * 64));
@@ -361,6 +376,9 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
     wg_sync(2);
     bool s_exact = false;   // S0 operand holds exact codes with scale s_scale
     float s_scale = 1.f;
+    // The registers S hold the state divided by sT: the E4M3 codes after a QDQ (sT = their scale),
+    // plain values otherwise (sT = 1); the scale is folded into the next step's multiplier.
+    float sT = 1.f;
     float i8s[2] = {0.f, 0.f};   // INT8: this row's two block scales of the last QDQ'd state
     for (int64_t c = 0; c < nchunks; ++c) {
       const int s = (int)(c & 1);
@@ -396,19 +414,23 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
         tc::mma_commit(bar(B_XY0 + s));
       }
       wait(B_XY0 + s, (uint32_t)((c >> 1) & 1));
-      if (ctid == kChainIssuer && !p.w_qdq && c + 1 < nchunks && live()) tma_wlo(c + 1);   // W lo has been read
+      if (ctid == 96 && !p.w_qdq && c + 1 < nchunks && live()) tma_wlo(c + 1);   // W lo has been read
       // ---- Delta = U - f X, Dt = exp(gam_63 - gam_r) Delta ----
       wait(B_U, par);
       if (c > 0) wait(B_PD, (uint32_t)((c - 1) & 1));   // the previous P Delta has read Delta
       tc::tc_fence_after();
       float d[32];
       {
-        float xv[32], uv[32];
+        float xv[32], uv[32], ulo[32];   // U = T''_hi V (lanes 0-15) + T''_lo V (lanes 16-31)
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, txy), xv);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, txy + 16), xv + 16);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_U), uv);
         tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0, TM_U + 16), uv + 16);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, TM_U), ulo);
+        tc::tmem_ld16x2<32>(tc::tmem_addr(tmem, lane0 + 16, TM_U + 16), ulo + 16);
         tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) uv[j] += ulo[j];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float dt[8];
@@ -427,16 +449,12 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
-      if (ctid == 0) tc::mbar_arrive(bar(B_UFREE));   // U has been read
       if (ctid == kChainIssuer) {
         tc::tc_fence_after();
-        // C = K^T Dt (Dt hi + lo)
+        // C = K^T [Dt hi | Dt lo] (N = 128: the two parts side by side)
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + TM_C, dadv(dStgM, stg + ks * 2048), dadv(dDl, 16 * KB + part * 8 * KB + ks * 2048),
-                         IDESC_C, (part | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + TM_C, dadv(dStgM, stg + ks * 2048), dadv(dDl, 16 * KB + ks * 2048), IDESC_C, ks != 0);
         tc::mma_commit(bar(B_C));
       }
       // Delta hi | lo for the output warpgroup's P Delta (while C runs)
@@ -453,18 +471,22 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
       if (ctid == 0) tc::mbar_arrive(bar(B_DRDY));
       // ---- S1 = Gam_63 S0 + C; QDQ at the 64-token boundary (Y read S0 with X, waited above) ----
       wait(B_C, par);
+      if (ctid == 0) tc::mbar_arrive(bar(B_SF0 + s));   // [X; Y] and C have read stage s, U has been read
       tc::tc_fence_after();
       {
         float* const s1 = S;
         {
-          float cv[64];
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C), cv);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 16), cv + 16);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 32), cv + 32);
-          tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 48), cv + 48);
-          tc::tmem_ld_wait();
+          const float elt = el * sT;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) s1[j] = fmaf(el, s1[j], cv[j]);
+          for (int k = 0; k < 4; ++k) {   // C = K^T Dt_hi + K^T Dt_lo, 16 columns at a time
+            float ch[16], cl[16];
+            tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 16 * k), ch);
+            tc::tmem_ld16(tc::tmem_addr(tmem, lane0, TM_C + 64 + 16 * k), cl);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s1[16 * k + j] = fmaf(elt, s1[16 * k + j], ch[j] + cl[j]);
+          }
+          sT = 1.f;
         }
         if (p.state_qdq == 1 && L == 64) {
           float m8[8];
@@ -473,21 +495,20 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
 #pragma unroll
           for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], fabsf(s1[j]));
           float mm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          mm = warp_max(mm);
+          mm = warp_absmax(mm);
           if (lt == 0) red[quad] = mm;
           wg_sync(2);
           const float amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
           const float sS = qdq_scale(amax), rS = __frcp_rn(sS);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float cd[8];
+          for (int q = 0; q < 8; ++q) {   // the codes stay in S (dequantized as codes x sS)
 #pragma unroll
-            for (int u = 0; u < 8; u += 2)
-              qdq_pair(s1[8 * q + u], s1[8 * q + u + 1], rS, sS, cd[u], cd[u + 1], s1[8 * q + u], s1[8 * q + u + 1]);
-            st16(sm, OFF_SHI + tc::sw128(lane128, 16 * q), pack8(cd));
+            for (int u = 0; u < 8; u += 2) e4m3_codes2(s1[8 * q + u], s1[8 * q + u + 1], rS, s1[8 * q + u], s1[8 * q + u + 1]);
+            st16(sm, OFF_SHI + tc::sw128(lane128, 16 * q), pack8(s1 + 8 * q));
           }
           s_exact = true;
           s_scale = sS;
+          sT = sS;
         } else {
           if (p.state_qdq == 2 && L == 64) {   // INT8: this row's two 32-column blocks, in registers
 #pragma unroll
@@ -517,14 +538,13 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tq16, const __grid_consta
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (wg_any(2, !live())) break;
-      // stage s is free: [X; Y] and C (committed after it by the same thread) have read it -- fetch
-      // chunk c + 2 into it
-      if (ctid == kChainIssuer && c + 2 < nchunks && live()) tma_qk(c + 2);
     }
-    if (live() && p.hT) {
+    if (live() && p.hT) {   // code x scale: the value the QDQ produced
       float4* out = reinterpret_cast<float4*>(p.hT + sb + (int64_t)lane128 * p.dv);
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) out[j >> 2] = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      for (int j = 0; j < 64; j += 4)
+        out[j >> 2] = make_float4(__fmul_rn(S[j], sT), __fmul_rn(S[j + 1], sT), __fmul_rn(S[j + 2], sT),
+                                  __fmul_rn(S[j + 3], sT));
     }
     if (live() && p.sscale) {   // the final state was QDQ'd iff its last token was a 64th token
       const bool q = len > 0 && len % 64 == 0;
@@ -598,7 +618,11 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
   const SplitLayout lay = chunk_split_layout(p);
   if (lay.items * 256 >= (int64_t)1 << 31) return cudaErrorInvalidValue;   // TMA row coordinates are int32
   unsigned char* w = static_cast<unsigned char*>(ws);
-  cudaError_t e = launch_chunk_prep(p, lay, w, stream);
+  cudaError_t e;
+  // the chain order is staged first, so that the chain kernel directly follows the prep kernel
+  const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
+  if (e != cudaSuccess) return e;
+  e = launch_chunk_prep(p, lay, w, stream);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.N * p.Hv * (p.dv / 64);
   if (blocks == 0) return cudaSuccess;
@@ -613,15 +637,24 @@ cudaError_t launch_chunk_split(const ChunkProblem& p, void* ws, cudaStream_t str
       !make_bf16_rows_map(&tpp, w + lay.off_p, lay.items * 128, 128) ||
       !make_f32_out_map(&tout, p.o, p.dv, p.Hv, tmap))
     return cudaErrorInvalidValue;
-  const int32_t* order = stage_chain_order(p, w, lay.off_order, stream, &e);
-  if (e != cudaSuccess) return e;
   ChainParams cp{order, reinterpret_cast<const float*>(w + lay.off_vec), p.h0, p.cu, p.lens, p.o, p.hT, reinterpret_cast<int*>(ws),
                  p.T, p.Hqk, p.Hv, p.dv, p.scale, p.state_qdq, p.w_qdq};
   cp.sscale = p.state_scales;
   e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  chunk_chain_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(tq16, tk, tv, tw16, tw64, ttt, tpp, tout, cp);
-  return cudaGetLastError();
+  // programmatic dependent launch: the chain's CTAs may become resident while the prep's last
+  // wave runs (griddepcontrol.wait in the kernel holds back every read of the staging)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_chain_kernel, tq16, tk, tv, tw16, tw64, ttt, tpp, tout, cp);
 }
 
 }  // namespace gdn

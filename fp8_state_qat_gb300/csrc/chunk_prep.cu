@@ -5,14 +5,16 @@
 // drop out), with gam = prefix sums of g inside the chunk and Gam = exp(gam):
 //   G      [K; Q] K^T                              tcgen05 bf16, M=128 N=64 K=128 (exact products)
 //   A      A[r][i] = beta_r exp(gam_r - gam_i) (k_r . k_i), i < r          (rows 0-63 of G)
-//   P      P[r][i] = exp(gam_r - gam_i) (q_r . k_i), i <= r < L -> workspace (rows 64-127 of G)
+//   P      P[r][i] = exp(gam_r - gam_i) (q_r . k_i), i <= r < L -> workspace as bf16 hi + lo rows,
+//          interleaved (rows 64-127 of G)
 //          The decays exp(gam_r - gam_i) are exp(gam_r - m) exp(m - gam_i) with m the midpoint of the
 //          chunk's gam range while that range is at most 64 (both factors within e^+-32; 128
 //          exponentials instead of 64 x 64), pairwise otherwise.
 //   T      (I + A)^{-1} by blocked forward substitution: the two 32 x 32 diagonal blocks column by
 //          column in registers (one thread per column, no barriers), then the block below the
 //          diagonal, T10 = -T11 (A10 T00), as two 32 x 32 x 32 products over all threads
-//   T''    T diag(beta)                 -> workspace as bf16 hi + lo (the chain forms U = T'' V)
+//   T''    T diag(beta)                 -> workspace as bf16 hi + lo rows, interleaved (the chain
+//          forms U = T'' V)
 //   W      T' K,  T' = T diag(beta Gam)            bf16 (T' as hi + lo), M=64 N=128 K=64
 //   W QDQ  one E4M3 scale over the chunk's W; codes -> workspace (exact in bf16)
 //   vec    gam, Gam, exp(gam_63 - gam), the W scale -> workspace
@@ -73,6 +75,12 @@ struct PrepParams {
   int w_qdq;
 };
 
+// Staged hi / lo pairs of 64-row matrices are interleaved in 16-row groups (rows 32 g .. 32 g + 15
+// the hi rows 16 g .., rows 32 g + 16 .. the lo rows), so that the chain's one M = 128 product
+// over both leaves hi . B in TMEM lanes 0-15 and lo . B in lanes 16-31 of each quadrant: the
+// position of hi row r (lo row r: + 16).
+__device__ __forceinline__ int ilv_row(int r) { return 32 * (r >> 4) + (r & 15); }
+
 __device__ __forceinline__ int64_t seq_start(const PrepParams& p, int n) {
   return p.cu ? (int64_t)p.cu[n] : (int64_t)n * p.T;
 }
@@ -85,6 +93,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   __shared__ __align__(8) uint64_t bars[3];
   __shared__ uint32_t tmem_slot;
 
+  // the state chain that follows may start its set-up (it waits for this grid before reading any
+  // of its output)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t item = blockIdx.x;
   const int h = (int)(item % p.Hv);
   const int64_t slot = item / p.Hv;
@@ -227,7 +238,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             dst[j >> 2] = make_float4(c < r ? v[j] : 0.f, c + 1 < r ? v[j + 1] : 0.f, c + 2 < r ? v[j + 2] : 0.f,
                                       c + 3 < r ? v[j + 3] : 0.f);
           }
-        } else {      // lower part with the diagonal, bf16 hi -> Q0, lo -> Q1 (K-major [r][i])
+        } else {      // lower part with the diagonal, bf16 hi | lo rows interleaved (K-major [row][i])
+          const int ah = ilv_row(r), al = ah + 16;
+          const uint32_t rh = (ah < 64 ? OFF_Q0 : OFF_Q1), rl = (al < 64 ? OFF_Q0 : OFF_Q1);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float x8[8];
@@ -235,8 +248,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             for (int u = 0; u < 8; ++u) x8[u] = 32 * hb + 8 * q + u <= r ? v[8 * q + u] : 0.f;
             uint4 h16, l16;
             split8(x8, h16, l16);
-            st16(sm, OFF_Q0 + tc::sw128(r, 64 * hb + 16 * q), h16);
-            st16(sm, OFF_Q1 + tc::sw128(r, 64 * hb + 16 * q), l16);
+            st16(sm, rh + tc::sw128(ah & 63, 64 * hb + 16 * q), h16);
+            st16(sm, rl + tc::sw128(al & 63, 64 * hb + 16 * q), l16);
           }
         }
       }
@@ -343,9 +356,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         uint4 h16, l16;
         const uint32_t off = tc::sw128(r, 2 * i0);
-        split8(t2, h16, l16);
-        st16(sm, OFF_A + off, h16);            // T'' hi rows 0-63, lo rows 64-127 (A is dead)
-        st16(sm, OFF_A + 8 * KB + off, l16);
+        split8(t2, h16, l16);                  // T'' hi | lo rows interleaved in the A region (A is dead)
+        st16(sm, OFF_A + tc::sw128(ilv_row(r), 2 * i0), h16);
+        st16(sm, OFF_A + tc::sw128(ilv_row(r) + 16, 2 * i0), l16);
         split8(t1, h16, l16);
         st16(sm, OFF_Q0 + off, h16);
         st16(sm, OFF_Q1 + off, l16);
@@ -353,9 +366,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 96) {   // not the MMA issuer: its MMAs would queue behind this copy
       tc::tma_store_2d(&ttt, sbase + OFF_A, 0, (int)(item * 128));   // T'' hi | lo
       tc::bulk_commit();
+    }
+    if (tid == 0) {
       tc::tc_fence_after();
       // W = T' K: A = T' hi / lo (K-major [r][i]), B = K (MN-major [i][c], key blocks 16 KB apart)
 #pragma unroll
@@ -429,7 +444,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       if (!k_done) tc::mbar_wait(bar_k, 0, 1u << 16);   // the Q / K tiles may still be landing
     }
   }
-  if (tid == 0 || tid == 64) tc::bulk_wait_read();   // the stores have read their shared-memory sources
+  if (tid == 0 || tid == 64 || tid == 96) tc::bulk_wait_read();   // the stores have read their sources
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);

@@ -14,10 +14,21 @@ constexpr int kChunk = 64;          // chunk length fixed by the method ("GDN st
 constexpr int kStateTileCols = 64;  // state QDQ tile: all dk rows x 64 value columns (same page)
 constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 (fn) magnitude
 
-// Scale of one QDQ tile from its amax: amax / 448 with the zero guard (0 -> 1), in fp32
-// with IEEE round-to-nearest division.
+// Scale of one QDQ tile from its amax: amax / 448 with the zero guard (0 -> 1), in fp32 with
+// round-to-nearest division. The quotient is formed as the rounded reciprocal of 448 plus two FMA
+// corrections (see quotient() below: correctly rounded for a normal quotient), the IEEE divide
+// below 1e-30; equal to __fdiv_rn(amax, 448) for every non-negative finite amax (checked
+// exhaustively on the GPU by the test suite).
 __device__ __forceinline__ float qdq_scale(float amax) {
-  float s = __fdiv_rn(amax, kE4M3Max);
+  float s;
+  if (amax >= 1.0e-30f) {
+    constexpr float r = 1.0f / kE4M3Max;
+    const float q0 = __fmul_rn(amax, r);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, kE4M3Max, amax), r, q0);
+    s = __fmaf_rn(__fmaf_rn(-q1, kE4M3Max, amax), r, q1);
+  } else {
+    s = __fdiv_rn(amax, kE4M3Max);
+  }
   return s == 0.0f ? 1.0f : s;
 }
 

@@ -71,8 +71,10 @@ __device__ __forceinline__ void stage_token(TokenBuf<DK, DV, KDA>& buf, const __
 // QDQ of the state registers: one tile = all DK rows x 64 columns = 4 consecutive warps. The
 // state registers are column pairs (col, col + 1) and (col + 2, col + 3) so that the
 // elementwise work runs as paired fp32 operations (fma / mul .f32x2, each lane rounded like
-// its scalar form).
-template <int DK, int DV>
+// its scalar form). EXACT: x / s as the correctly rounded quotient (the once-per-sequence QDQ at
+// the handoff, bit for bit the fp32 definition); otherwise x times the rounded reciprocal of s
+// (every decode token's QDQ; differs from the IEEE quotient's E4M3 code for ~2 in 10^7 elements).
+template <int DK, int DV, bool EXACT = false>
 __device__ __forceinline__ float qdq_state_regs(float2 (&sa)[DK / 8], float2 (&sb)[DK / 8], float amax, float* wmax,
                                                 int warp, int lane) {
   constexpr int RPT = DK / 8;
@@ -82,10 +84,17 @@ __device__ __forceinline__ float qdq_state_regs(float2 (&sa)[DK / 8], float2 (&s
   const int t0 = (warp / 4) * 4;
   const float tmax = fmaxf(fmaxf(wmax[t0], wmax[t0 + 1]), fmaxf(wmax[t0 + 2], wmax[t0 + 3]));
   const float sc = qdq_scale(tmax), rc = __frcp_rn(sc);
-  const float2 sc2 = make_float2(sc, sc), rc2 = make_float2(rc, rc);
+  const float2 sc2 = make_float2(sc, sc), rc2 = make_float2(rc, rc), nsc2 = make_float2(-sc, -sc);
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const __nv_fp8x2_e4m3 ca(__fmul2_rn(sa[i], rc2)), cb(__fmul2_rn(sb[i], rc2));
+    // a subnormal scale has no finite reciprocal: the IEEE divide then (tmax below ~3e-36)
+    const float2 ya = !EXACT ? __fmul2_rn(sa[i], rc2)
+                             : (sc >= 1.17549435e-38f ? quotient2(sa[i], nsc2, rc2)
+                                                      : make_float2(__fdiv_rn(sa[i].x, sc), __fdiv_rn(sa[i].y, sc)));
+    const float2 yb = !EXACT ? __fmul2_rn(sb[i], rc2)
+                             : (sc >= 1.17549435e-38f ? quotient2(sb[i], nsc2, rc2)
+                                                      : make_float2(__fdiv_rn(sb[i].x, sc), __fdiv_rn(sb[i].y, sc)));
+    const __nv_fp8x2_e4m3 ca(ya), cb(yb);
     sa[i] = __fmul2_rn(static_cast<float2>(ca), sc2);
     sb[i] = __fmul2_rn(static_cast<float2>(cb), sc2);
   }
@@ -187,7 +196,7 @@ handoff_suffix_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   if (state_qdq == 2) {
     int8_state_regs<DK, DV>(sa, sb, rmax, warp, rg, cg, nullptr);   // the handoff (decode tokens follow)
   } else if (state_qdq) {
-    last_tile = qdq_state_regs<DK, DV>(sa, sb, amax, wmax[slot], warp, lane);   // the handoff
+    last_tile = qdq_state_regs<DK, DV, true>(sa, sb, amax, wmax[slot], warp, lane);   // the handoff
     slot ^= 1;
   }
 

@@ -68,8 +68,10 @@ bool make_f32_out_map(CUtensorMap* map, void* base, int D, int heads, int64_t to
 //   W    bf16 [2 key blocks][64 r][64 c]: the chunk's W, key columns 0-63 then 64-127 -- E4M3
 //        codes (exact in bf16) with W QDQ, else the bf16 hi part followed by the lo part
 //        ([2][2][64][64]);
-//   T''  bf16 [2][64 r][64 i]: hi and lo parts of T diag(beta) (U = T'' V in the chain);
-//   P    bf16 [2][64 r][64 i]: hi and lo parts of exp(gam_r - gam_i) (q_r . k_i), i <= r < L;
+//   T''  bf16 [128][64 i]: hi and lo parts of T diag(beta) (U = T'' V in the chain), rows
+//        interleaved in 16-row groups: row 32 g + s is hi row 16 g + s, row 32 g + 16 + s lo row 16 g + s;
+//   P    bf16 [128][64 i]: hi and lo parts of exp(gam_r - gam_i) (q_r . k_i), i <= r < L, rows
+//        interleaved the same way;
 //   vec  fp32 [256]: gam [64], Gam = exp(gam) [64], exp(gam_63 - gam) [64], W scale (index 192).
 struct SplitLayout {
   int64_t slots, items;

@@ -42,6 +42,13 @@ __device__ __forceinline__ void qdq_pair(float a, float b, float rs, float s, fl
   qa = __fmul_rn(cf.x, s);
   qb = __fmul_rn(cf.y, s);
 }
+// E4M3 codes (as fp32) of a pair scaled by the reciprocal of the tile scale
+__device__ __forceinline__ void e4m3_codes2(float a, float b, float rs, float& ca, float& cb) {
+  const __nv_fp8x2_e4m3 c(make_float2(__fmul_rn(a, rs), __fmul_rn(b, rs)));
+  const float2 cf = static_cast<float2>(c);
+  ca = cf.x;
+  cb = cf.y;
+}
 __device__ __forceinline__ void ld32(uint32_t tmem, uint32_t lane0, uint32_t col, float* v) {
   tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col), v);
   tc::tmem_ld16(tc::tmem_addr(tmem, lane0, col + 16), v + 16);

@@ -58,3 +58,27 @@ extern "C" int gdnqat_testing_quotient_sweep(const float* vals, int nvals, const
   sweep_kernel<<<152 * 8, 256, 0, stream>>>(vals, nvals, exps, nexps, mode, counts, first);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
+
+namespace {
+// gdn::qdq_scale(amax) against the IEEE divide with the zero guard, for every non-negative finite
+// fp32 amax (bit patterns 0 .. 0x7f7fffff): mismatches counted in counts[0], the first in first[0].
+__global__ void scale_sweep_kernel(unsigned long long* counts, unsigned int* first) {
+  unsigned long long local = 0;
+  for (unsigned int b = blockIdx.x * blockDim.x + threadIdx.x; b <= 0x7f7fffffu; b += gridDim.x * blockDim.x) {
+    const float x = __uint_as_float(b);
+    float want = __fdiv_rn(x, 448.0f);
+    if (want == 0.0f) want = 1.0f;
+    if (__float_as_uint(gdn::qdq_scale(x)) != __float_as_uint(want)) {
+      ++local;
+      atomicCAS(first, 0u, b);
+    }
+    if (b > 0x7f7fffffu - gridDim.x * blockDim.x) break;   // the next step would wrap around
+  }
+  if (local) atomicAdd(counts, local);
+}
+}  // namespace
+
+extern "C" int gdnqat_testing_scale_sweep(unsigned long long* counts, unsigned int* first, cudaStream_t stream) {
+  scale_sweep_kernel<<<152 * 8, 256, 0, stream>>>(counts, first);
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}

@@ -125,7 +125,9 @@ def test_teacher_forced_decode_tokens(gdn, oracle_mod, kda, dv):
     token), and the result is compared with the GPU's state after t + 1 tokens. Both sides
     then take each QDQ decision on nearly the same input, as in the decode step's own
     teacher-forced test: o of the token within 1e-5, and >= 99.9 % of the stored state the
-    same E4M3 value times the same scale."""
+    same E4M3 value times the same scale. The handoff QDQ (before the first decode token's o)
+    divides exactly on the GPU and is compared with the oracle's fp32 QDQ, so the same codes
+    result; the per-token QDQs after each o use the rounded reciprocal of the scale."""
     L, P = 100, 37
     x = workloads.prefill(1, L, 2, 2, 128, dv, seed=36, kda=kda, h0_std=0.1, state_qdq=True, w_qdq=True)
     c = to_cuda(x)
@@ -142,8 +144,8 @@ def test_teacher_forced_decode_tokens(gdn, oracle_mod, kda, dv):
     for t in range(P, L):
         o_next, S_next = gpu_upto(t + 1)
         start = S
-        if t == P:   # the handoff QDQ
-            start = oracle_mod.tile_qdq_f64(S.reshape(-1, 128, dv), 64)[0].reshape(S.shape)
+        if t == P:   # the handoff QDQ: in fp32 with the IEEE quotient, as the GPU takes it
+            start = oracle_mod.tile_qdq_f32(S.astype(np.float32).reshape(-1, 128, dv), 64)[0].reshape(S.shape)
         step = lambda v: v[:, t:t + 1].transpose(0, 1).contiguous()   # token t as one decode step, N = 1
         oo, so = oracle_mod.gdn_decode(step(x.q), step(x.k), step(x.v), step(x.g), step(x.beta), start, kda=kda,
                                        state_qdq=True)

@@ -120,3 +120,18 @@ def test_quotient_matches_ieee_divide_over_all_significands(gdn):
         record("plain_reciprocal_code_mismatches", c[3], mode=mode, pairs=(1 << 23) * len(vals) * len(exps))
         assert c[0] == 0 and c[1] == 0, (mode, c, f[:2].view(np.float32))
         assert c[2] == 0, (mode, c)
+
+
+def test_tile_scale_matches_ieee_divide_for_every_amax(gdn):
+    """The tile scale amax / 448 (zero guard: 1) every QDQ site uses is computed as the rounded
+    reciprocal of 448 plus two FMA corrections; over every non-negative finite fp32 amax it must
+    equal the IEEE round-to-nearest divide bit for bit."""
+    import native
+    lib = native.load()
+    fn = lib.gdnqat_testing_scale_sweep
+    fn.restype = ctypes.c_int
+    counts = torch.zeros(1, dtype=torch.int64, device="cuda")
+    first = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert fn(ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(first.data_ptr()), None) == 0
+    torch.cuda.synchronize()
+    assert int(counts.item()) == 0, (int(counts.item()), hex(int(first.item()) & 0xffffffff))
